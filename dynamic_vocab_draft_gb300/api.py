@@ -1,0 +1,172 @@
+"""Thin torch-facing binding of the DynaSpec C ABI: argument marshalling only.
+
+Every function takes CUDA tensors (device memory owned by the caller), checks dtype, device
+and contiguity, and calls the library function of the same name on the current (or given)
+CUDA stream.  bf16 tensors may be ``torch.bfloat16`` or raw ``torch.int16``/``uint16`` bits.
+All computation happens in the library's kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+ACT = {"relu": 0, "gelu": 1}
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t, dtypes, name, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtypes and t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+BF16 = (torch.bfloat16, torch.int16, torch.uint16)
+I32 = (torch.int32,)
+F32 = (torch.float32,)
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """Zero-filled scratch of at least `nbytes` (the counters it may hold start at zero)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def router_workspace_bytes(B, Hr):
+    return int(_lib.load().ds_router_workspace_bytes(B, Hr))
+
+
+def shortlist_workspace_bytes(B, M):
+    return int(_lib.load().ds_shortlist_workspace_bytes(B, M))
+
+
+def head_workspace_bytes(rows):
+    return int(_lib.load().ds_head_workspace_bytes(rows))
+
+
+def verify_workspace_bytes(B, gamma, V):
+    return int(_lib.load().ds_verify_workspace_bytes(B, gamma, V))
+
+
+def verify_tree_workspace_bytes(B, D, Wd, V):
+    return int(_lib.load().ds_verify_tree_workspace_bytes(B, D, Wd, V))
+
+
+def vocab_index(csr_off, csr_tok, cluster_of, rank_in_cluster, status, stream=None):
+    M = csr_off.numel() - 1
+    V = csr_tok.numel()
+    _lib.check(_lib.load().ds_vocab_index(
+        _ptr(csr_off, I32, "csr_off"), _ptr(csr_tok, I32, "csr_tok"), M, V,
+        _ptr(cluster_of, I32, "cluster_of"), _ptr(rank_in_cluster, I32, "rank_in_cluster"),
+        _ptr(status, I32, "status"), _stream(stream)), "ds_vocab_index")
+
+
+def router_topk(H, W1, b1, W2, b2, act, budget, pos, scores, cluster_ids, ws, status, stream=None):
+    """budget: host int32 tensor / sequence of clusters kept per draft position."""
+    B, d = H.shape
+    Hr = W1.shape[0]
+    M = W2.shape[0]
+    bud = torch.as_tensor(budget, dtype=torch.int32).contiguous()
+    _lib.check(_lib.load().ds_router_topk(
+        _ptr(H, BF16, "H"), B, d, _ptr(W1, BF16, "W1"), _ptr(b1, BF16, "b1"), Hr,
+        _ptr(W2, BF16, "W2"), _ptr(b2, BF16, "b2"), M, ACT.get(act, act),
+        bud.data_ptr(), bud.numel(), int(pos),
+        _ptr(scores, F32, "scores"), _ptr(cluster_ids, I32, "cluster_ids"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
+        _stream(stream)), "ds_router_topk")
+
+
+def build_shortlist(csr_off, csr_tok, cluster_ids, vs_offsets, vs_ids, cpos, ws, status,
+                    union_ids=None, union_cluster=None, union_count=None, stream=None):
+    M = csr_off.numel() - 1
+    V = csr_tok.numel()
+    B, k = cluster_ids.shape
+    _lib.check(_lib.load().ds_build_shortlist(
+        _ptr(csr_off, I32, "csr_off"), _ptr(csr_tok, I32, "csr_tok"), M, V,
+        _ptr(cluster_ids, I32, "cluster_ids"), B, k,
+        _ptr(vs_offsets, I32, "vs_offsets"), _ptr(vs_ids, I32, "vs_ids"), vs_ids.numel(),
+        _ptr(cpos, I32, "cpos"),
+        _ptr(union_ids, I32, "union_ids", True), _ptr(union_cluster, I32, "union_cluster", True),
+        _ptr(union_count, I32, "union_count", True),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
+        _stream(stream)), "ds_build_shortlist")
+
+
+def gathered_head(H, G, W, vs_offsets, vs_ids, T, seed, pos, logits, token, token_idx, ws, status,
+                  cpos=None, rank_in_cluster=None, union=None, row_max=None, row_sumexp=None,
+                  stream=None):
+    """H [B*G, d]; union = (union_ids, union_cluster, union_count) or None (per-row path)."""
+    R, d = H.shape
+    B = vs_offsets.numel() - 1
+    if R != B * G:
+        raise ValueError(f"H has {R} rows, expected B*G = {B}*{G}")
+    V = W.shape[0]
+    M = cpos.numel() // B if cpos is not None else 0
+    uids, ucl, ucnt = union if union is not None else (None, None, None)
+    _lib.check(_lib.load().ds_gathered_head(
+        _ptr(H, BF16, "H"), B, G, _ptr(W, BF16, "W"), V, d,
+        _ptr(vs_offsets, I32, "vs_offsets"), _ptr(vs_ids, I32, "vs_ids"),
+        _ptr(cpos, I32, "cpos", True), M, _ptr(rank_in_cluster, I32, "rank_in_cluster", True),
+        _ptr(uids, I32, "union_ids", True), _ptr(ucl, I32, "union_cluster", True),
+        _ptr(ucnt, I32, "union_count", True),
+        float(T), int(seed) & 0xFFFFFFFFFFFFFFFF, int(pos),
+        _ptr(logits, F32, "logits"), _ptr(row_max, F32, "row_max", True),
+        _ptr(row_sumexp, F32, "row_sumexp", True),
+        _ptr(token, I32, "token"), _ptr(token_idx, I32, "token_idx"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
+        _stream(stream)), "ds_gathered_head")
+
+
+def verify(p_logits, T, q_logits, vs_offsets, cpos, cluster_of, rank_in_cluster, draft_ids,
+           uniforms, accepted_len, correction, ws, status, stream=None):
+    """p_logits [B, gamma+1, V]; q_logits [gamma, q_stride]; vs_offsets [gamma, B+1];
+    cpos [gamma, B*M]; draft_ids [gamma, B]; uniforms [B, gamma+1]."""
+    B, g1, V = p_logits.shape
+    gamma = g1 - 1
+    M = cpos.shape[-1] // B
+    _lib.check(_lib.load().ds_verify(
+        _ptr(p_logits, F32, "p_logits"), B, gamma, V, float(T),
+        _ptr(q_logits, F32, "q_logits"), q_logits.stride(0),
+        _ptr(vs_offsets, I32, "vs_offsets"), _ptr(cpos, I32, "cpos"), M,
+        _ptr(cluster_of, I32, "cluster_of"), _ptr(rank_in_cluster, I32, "rank_in_cluster"),
+        _ptr(draft_ids, I32, "draft_ids"), _ptr(uniforms, F32, "uniforms"),
+        _ptr(accepted_len, I32, "accepted_len"), _ptr(correction, I32, "correction"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
+        _stream(stream)), "ds_verify")
+
+
+def verify_tree(p_logits, D, Wd, T, parent, q_logits, vs_offsets, cpos, cluster_of,
+                rank_in_cluster, node_tokens, u_node, u_res, accepted_len, correction, path,
+                ws, status, stream=None):
+    """p_logits [B, 1+D*Wd, V]; q_logits [D, q_stride]; node_tokens [D, B*Wd]."""
+    B, n1, V = p_logits.shape
+    M = cpos.shape[-1] // B
+    _lib.check(_lib.load().ds_verify_tree(
+        _ptr(p_logits, F32, "p_logits"), B, D, Wd, V, float(T), _ptr(parent, I32, "parent"),
+        _ptr(q_logits, F32, "q_logits"), q_logits.stride(0),
+        _ptr(vs_offsets, I32, "vs_offsets"), _ptr(cpos, I32, "cpos"), M,
+        _ptr(cluster_of, I32, "cluster_of"), _ptr(rank_in_cluster, I32, "rank_in_cluster"),
+        _ptr(node_tokens, I32, "node_tokens"), _ptr(u_node, F32, "u_node"),
+        _ptr(u_res, F32, "u_res"),
+        _ptr(accepted_len, I32, "accepted_len"), _ptr(correction, I32, "correction"),
+        _ptr(path, I32, "path"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
+        _stream(stream)), "ds_verify_tree")
+
+
+def philox4x32_10(ctr, seed, out, stream=None):
+    n = ctr.shape[0]
+    _lib.check(_lib.load().ds_philox4x32_10(
+        _ptr(ctr, (torch.int32, torch.uint32), "ctr"), int(seed) & 0xFFFFFFFFFFFFFFFF,
+        _ptr(out, (torch.int32, torch.uint32), "out"), n, _stream(stream)), "ds_philox4x32_10")

@@ -1,0 +1,198 @@
+// Shared device helpers of the DynaSpec GB300 kernels: bf16 unpacking, streaming loads,
+// the Philox4x32-10 generator, warp reductions and the softmax/argmax partial-state
+// algebra every head and verify reduction uses.
+#pragma once
+
+#include <cstdint>
+#include <cfloat>
+#include <cuda_runtime.h>
+
+#include "../../include/dynaspec.h"
+
+namespace ds {
+
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------------------------------
+// bf16 <-> fp32.  A bf16 value is the top half of an fp32 word, so widening is a shift.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// Dot product of 8 packed bf16 (one 16-byte vector) with 8 fp32 values.
+__device__ __forceinline__ float dot8(uint4 w, const float4 x0, const float4 x1, float acc)
+{
+    acc = fmaf(bf16lo(w.x), x0.x, acc);
+    acc = fmaf(bf16hi(w.x), x0.y, acc);
+    acc = fmaf(bf16lo(w.y), x0.z, acc);
+    acc = fmaf(bf16hi(w.y), x0.w, acc);
+    acc = fmaf(bf16lo(w.z), x1.x, acc);
+    acc = fmaf(bf16hi(w.z), x1.y, acc);
+    acc = fmaf(bf16lo(w.w), x1.z, acc);
+    acc = fmaf(bf16hi(w.w), x1.w, acc);
+    return acc;
+}
+
+// 16-byte streaming load through the non-coherent path, not kept in L1: LM-head rows are
+// read once per draft position.
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void set_status(int32_t *st, int32_t bit)
+{
+    if (st) atomicOr(st, bit);
+}
+
+// ---------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+// SC'11): ten rounds of two 32x32->64 multiplies whose halves are crossed over the four
+// lanes and xored with a key that advances by the golden-ratio Weyl constants.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// Gumbel noise g = -log(-log u) of full-vocabulary token v for draft position `pos`, head
+// row `row`: counter (v >> 2, pos, row, 0), word v & 3, u = (2 (w >> 9) + 1) 2^-24 in (0, 1).
+__device__ __forceinline__ float gumbel(uint64_t seed, uint32_t v, uint32_t pos, uint32_t row)
+{
+    const uint4 w = philox4x32_10(make_uint4(v >> 2, pos, row, 0u), uint32_t(seed),
+                                  uint32_t(seed >> 32));
+    const uint32_t x = (v & 3u) == 0 ? w.x : (v & 3u) == 1 ? w.y : (v & 3u) == 2 ? w.z : w.w;
+    const float u = float(2u * (x >> 9) + 1u) * 5.9604644775390625e-8f;   // * 2^-24, exact
+    return -logf(-logf(u));
+}
+
+// ---------------------------------------------------------------------------------------
+// Softmax statistics + sampled argmax as one associative partial state.
+//   m, s : running max of x and sum of exp(x - m)  (x = logit / Te)
+//   key  : best sampling key so far, v its full-vocabulary id, j its index in the list;
+//          a larger key wins, equal keys go to the lower v.
+// ---------------------------------------------------------------------------------------
+struct Stat {
+    float m, s, key;
+    int v, j;
+};
+
+__device__ __forceinline__ Stat stat_empty() { return Stat{-INFINITY, 0.f, -INFINITY, -1, -1}; }
+
+__device__ __forceinline__ void stat_add(Stat &a, float x, float key, int v, int j)
+{
+    if (x > a.m) {
+        a.s = a.s * __expf(a.m - x) + 1.f;   // exp(-inf) = 0 for the first element
+        a.m = x;
+    } else {
+        a.s += __expf(x - a.m);
+    }
+    if (key > a.key || (key == a.key && (unsigned)v < (unsigned)a.v)) {
+        a.key = key; a.v = v; a.j = j;
+    }
+}
+
+__device__ __forceinline__ Stat stat_merge(Stat a, const Stat &b)
+{
+    if (b.m > a.m) {
+        a.s = (a.m == -INFINITY ? 0.f : a.s * __expf(a.m - b.m)) + b.s;
+        a.m = b.m;
+    } else if (b.m != -INFINITY) {
+        a.s += b.s * __expf(b.m - a.m);
+    }
+    if (b.v >= 0 && (a.v < 0 || b.key > a.key || (b.key == a.key && b.v < a.v))) {
+        a.key = b.key; a.v = b.v; a.j = b.j;
+    }
+    return a;
+}
+
+__device__ __forceinline__ Stat shfl_xor_stat(const Stat &a, int mask)
+{
+    Stat b;
+    b.m = __shfl_xor_sync(0xFFFFFFFFu, a.m, mask);
+    b.s = __shfl_xor_sync(0xFFFFFFFFu, a.s, mask);
+    b.key = __shfl_xor_sync(0xFFFFFFFFu, a.key, mask);
+    b.v = __shfl_xor_sync(0xFFFFFFFFu, a.v, mask);
+    b.j = __shfl_xor_sync(0xFFFFFFFFu, a.j, mask);
+    return b;
+}
+
+__device__ __forceinline__ float warp_sum(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ float warp_max(float x)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+    return x;
+}
+
+// Read of a value another block of the same grid published before its release fence.
+template <typename T>
+__device__ __forceinline__ T ld_volatile(const T *p) { return *(const volatile T *)p; }
+
+__device__ __forceinline__ Stat ld_stat(const Stat *p)
+{
+    const volatile Stat *q = (const volatile Stat *)p;
+    return Stat{q->m, q->s, q->key, q->v, q->j};
+}
+
+__device__ __forceinline__ void st_stat(Stat *p, const Stat &a)
+{
+    volatile Stat *q = (volatile Stat *)p;
+    q->m = a.m; q->s = a.s; q->key = a.key; q->v = a.v; q->j = a.j;
+}
+
+// "Am I the last block of this group to finish?"  Every block calls it once, after its
+// results are stored; the returning `true` block may read all of them.  The counter is
+// reset for the next launch by the last block.
+__device__ __forceinline__ bool last_block_done(unsigned *counter, unsigned nblocks)
+{
+    __shared__ bool is_last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(counter, 1u);
+        is_last = (prev == nblocks - 1);
+        if (is_last) {
+            *counter = 0u;
+            __threadfence();
+        }
+    }
+    __syncthreads();
+    return is_last;
+}
+
+}  // namespace ds
+
+// ---------------------------------------------------------------------------------------
+// Host-side helpers
+// ---------------------------------------------------------------------------------------
+#define DS_TRY_LAUNCH()                                                 \
+    do {                                                                \
+        if (cudaPeekAtLastError() != cudaSuccess) {                     \
+            (void)cudaGetLastError();                                   \
+            return DS_ERR_CUDA;                                         \
+        }                                                               \
+    } while (0)
+
+namespace ds {
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace ds

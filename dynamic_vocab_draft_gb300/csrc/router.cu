@@ -1,0 +1,246 @@
+// Router MLP and position-aware top-k cluster selection.
+//
+// DynaSpec summary ("DynaSpec: Context-aware Dynamic Speculative Sampling for Large-
+// Vocabulary Language Models"), Technical Details > System Modules "Router (Meta-
+// Classifier)": a 2-layer MLP scoring vocabulary clusters from the drafter hidden state
+// H_{t-1}; Key Hyperparameters: ReLU, and a budget k_c(t) that decays with draft position t;
+// abstract: the shortlist is the union of the top-selected clusters.
+//
+// Both layers are GEMV-shaped and HBM-bound at the batch sizes of drafting (one weight row
+// feeds at most a few dozen hidden states), so they run on CUDA cores: one warp per weight
+// row, 16-byte streaming loads, the hidden states staged once per block in shared memory,
+// warp-shuffle reductions.  Top-k is an exact MSB-first radix select on order-preserving
+// 32-bit keys followed by two block scans (ties to the lower cluster id, output ascending).
+#include "common.cuh"
+#include "block_scan.cuh"
+
+namespace ds {
+namespace {
+
+constexpr int kGemvWarps = 8;          // rows per block
+constexpr int kGemvU = 8;              // 16-byte loads in flight per lane per pass
+constexpr int kGemvBT = 4;             // hidden states per block
+constexpr int kRouterMaxK = 8192;      // inner dimension the staging buffer allows
+
+__device__ __forceinline__ float act_fn(float x, int act)
+{
+    if (act == DS_ACT_RELU) return fmaxf(x, 0.f);
+    if (act == DS_ACT_GELU) return 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+    return x;
+}
+
+template <typename XT> __device__ __forceinline__ float load_x(const XT *p);
+template <> __device__ __forceinline__ float load_x<uint16_t>(const uint16_t *p) { return bf16_to_f32(*p); }
+template <> __device__ __forceinline__ float load_x<float>(const float *p) { return *p; }
+
+// y[b][i] = act(sum_k A[i][k] x[b][k] + bias[i]) for i < N, b < B.
+//   grid.x = ceil(N / kGemvWarps), grid.y = ceil(B / kGemvBT); dynamic smem = BT*K floats.
+template <typename XT>
+__global__ void __launch_bounds__(kGemvWarps * 32)
+gemv_rows_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict__ x, int B,
+                 const uint16_t *__restrict__ bias, int act, float *__restrict__ y)
+{
+    extern __shared__ float4 xs4[];
+    float *xs = reinterpret_cast<float *>(xs4);
+    const int b0 = blockIdx.y * kGemvBT;
+    const int nb = min(kGemvBT, B - b0);
+    for (int e = threadIdx.x; e < kGemvBT * K; e += blockDim.x) {
+        const int bt = e / K, k = e - bt * K;
+        xs[e] = bt < nb ? load_x<XT>(x + size_t(b0 + bt) * K + k) : 0.f;
+    }
+    __syncthreads();
+
+    const int lane = threadIdx.x & 31;
+    const int i = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
+    if (i >= N) return;
+    const uint4 *row = reinterpret_cast<const uint4 *>(A + size_t(i) * K);
+    float acc[kGemvBT];
+#pragma unroll
+    for (int bt = 0; bt < kGemvBT; ++bt) acc[bt] = 0.f;
+
+    for (int k0 = 0; k0 < K; k0 += kGemvU * 256) {
+        uint4 w[kGemvU];
+#pragma unroll
+        for (int u = 0; u < kGemvU; ++u) {
+            const int k = k0 + u * 256 + lane * 8;
+            w[u] = k < K ? ld_stream(row + (k >> 3)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kGemvU; ++u) {
+            const int k = k0 + u * 256 + lane * 8;
+            if (k < K) {
+#pragma unroll
+                for (int bt = 0; bt < kGemvBT; ++bt) {
+                    const float4 *xv = reinterpret_cast<const float4 *>(xs + bt * K + k);
+                    acc[bt] = dot8(w[u], xv[0], xv[1], acc[bt]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int bt = 0; bt < kGemvBT; ++bt) acc[bt] = warp_sum(acc[bt]);
+    if (lane < nb) {
+        float a = acc[0];
+#pragma unroll
+        for (int bt = 1; bt < kGemvBT; ++bt) if (lane == bt) a = acc[bt];
+        y[size_t(b0 + lane) * N + i] = act_fn(a + bf16_to_f32(bias[i]), act);
+    }
+}
+
+// Order-preserving key: a larger float maps to a larger unsigned key; +0 and -0 share a key.
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    if (f == 0.f) f = 0.f;
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+constexpr int kTopkThreads = 1024;
+constexpr int kTopkPerThread = kRouterMaxK / kTopkThreads;
+
+// One block per row: keep the k largest of scores[b][0..M), ties to the lower index, and
+// write their indices in ascending order.
+__global__ void __launch_bounds__(kTopkThreads)
+topk_kernel(const float *__restrict__ scores, int M, int k, int32_t *__restrict__ ids)
+{
+    __shared__ unsigned hist[256];
+    __shared__ int scan_scratch[33];
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_need;
+    const float *s = scores + size_t(blockIdx.x) * M;
+    // thread t owns the contiguous index range [t*E, t*E + E)
+    const int E = (M + kTopkThreads - 1) / kTopkThreads;
+    const int lo = threadIdx.x * E;
+    uint32_t key[kTopkPerThread];
+#pragma unroll
+    for (int e = 0; e < kTopkPerThread; ++e)
+        key[e] = (e < E && lo + e < M) ? order_key(s[lo + e]) : 0u;
+
+    // MSB-first radix select of the k-th largest key, 8 bits per pass.
+    if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; }
+    uint32_t mask = 0u;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        if (threadIdx.x < 256) hist[threadIdx.x] = 0u;
+        __syncthreads();
+        const uint32_t prefix = s_prefix;
+#pragma unroll
+        for (int e = 0; e < kTopkPerThread; ++e)
+            if (e < E && lo + e < M && (key[e] & mask) == prefix)
+                atomicAdd(&hist[(key[e] >> shift) & 255u], 1u);
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            // bins from the top: lane l owns digits 255-8l .. 248-8l
+            const int lane = threadIdx.x;
+            unsigned c[8], tot = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) { c[q] = hist[255 - 8 * lane - q]; tot += c[q]; }
+            unsigned incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                unsigned y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int need = s_need;
+            unsigned before = incl - tot;          // elements in higher digits than my range
+            const bool mine = before < unsigned(need) && unsigned(need) <= incl;
+            if (mine) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    if (before + c[q] >= unsigned(need)) {
+                        s_prefix = prefix | (uint32_t(255 - 8 * lane - q) << shift);
+                        s_need = need - int(before);
+                        break;
+                    }
+                    before += c[q];
+                }
+            }
+        }
+        mask |= 255u << shift;
+        __syncthreads();
+    }
+    const uint32_t theta = s_prefix;      // the k-th largest key
+    const int need_eq = s_need;           // how many of the keys equal to theta to keep
+
+    // Keep keys above theta, and the first need_eq keys equal to theta in index order.
+    int eq = 0;
+#pragma unroll
+    for (int e = 0; e < kTopkPerThread; ++e)
+        if (e < E && lo + e < M && key[e] == theta) ++eq;
+    int tot;
+    int eq_before = block_exclusive_scan(eq, scan_scratch, &tot);
+    bool sel[kTopkPerThread];
+    int nsel = 0;
+#pragma unroll
+    for (int e = 0; e < kTopkPerThread; ++e) {
+        const bool valid = e < E && lo + e < M;
+        bool keep = false;
+        if (valid && key[e] > theta) keep = true;
+        if (valid && key[e] == theta) { keep = eq_before < need_eq; ++eq_before; }
+        sel[e] = keep;
+        nsel += keep;
+    }
+    int out = block_exclusive_scan(nsel, scan_scratch, &tot);
+    int32_t *dst = ids + size_t(blockIdx.x) * k;
+#pragma unroll
+    for (int e = 0; e < kTopkPerThread; ++e)
+        if (sel[e] && out < k) dst[out++] = lo + e;
+}
+
+}  // namespace
+}  // namespace ds
+
+using namespace ds;
+
+extern "C" size_t ds_router_workspace_bytes(int B, int Hr)
+{
+    if (B <= 0 || Hr <= 0) return 0;
+    return align256(size_t(B) * size_t(Hr) * sizeof(float));
+}
+
+extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
+                                    const uint16_t *W1, const uint16_t *b1, int Hr,
+                                    const uint16_t *W2, const uint16_t *b2, int M, int act,
+                                    const int32_t *budget, int n_budget, int pos,
+                                    float *scores, int32_t *cluster_ids,
+                                    void *ws, size_t ws_bytes, int32_t *dev_status,
+                                    cudaStream_t stream)
+{
+    (void)dev_status;
+    if (!H || !W1 || !b1 || !W2 || !b2 || !budget || !scores || !cluster_ids)
+        return DS_ERR_INVALID_ARG;
+    if (B < 1 || B > 4096 || d < 8 || d % 8 || Hr < 8 || Hr % 8 || M < 1 || M > kRouterMaxK)
+        return DS_ERR_INVALID_ARG;
+    if (d > kRouterMaxK || Hr > kRouterMaxK) return DS_ERR_UNSUPPORTED;
+    if (act != DS_ACT_RELU && act != DS_ACT_GELU) return DS_ERR_INVALID_ARG;
+    if (pos < 1 || pos > n_budget) return DS_ERR_INVALID_ARG;
+    const int k = budget[pos - 1];
+    if (k < 1 || k > M) return DS_ERR_INVALID_ARG;
+    if (!aligned16(H) || !aligned16(W1) || !aligned16(W2)) return DS_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < ds_router_workspace_bytes(B, Hr)) return DS_ERR_WORKSPACE;
+
+    float *u = static_cast<float *>(ws);
+    const int by = (B + kGemvBT - 1) / kGemvBT;
+    {
+        const size_t smem = size_t(kGemvBT) * d * sizeof(float);
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(gemv_rows_kernel<uint16_t>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+            return DS_ERR_CUDA;
+        dim3 grid((Hr + kGemvWarps - 1) / kGemvWarps, by);
+        gemv_rows_kernel<uint16_t><<<grid, kGemvWarps * 32, smem, stream>>>(W1, Hr, d, H, B, b1, act, u);
+        DS_TRY_LAUNCH();
+    }
+    {
+        const size_t smem = size_t(kGemvBT) * Hr * sizeof(float);
+        if (smem > 48 * 1024 &&
+            cudaFuncSetAttribute(gemv_rows_kernel<float>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+            return DS_ERR_CUDA;
+        dim3 grid((M + kGemvWarps - 1) / kGemvWarps, by);
+        gemv_rows_kernel<float><<<grid, kGemvWarps * 32, smem, stream>>>(W2, M, Hr, u, B, b2, -1, scores);
+        DS_TRY_LAUNCH();
+    }
+    topk_kernel<<<B, kTopkThreads, 0, stream>>>(scores, M, k, cluster_ids);
+    DS_TRY_LAUNCH();
+    return DS_OK;
+}

@@ -1,0 +1,214 @@
+// Shortlist construction: V_S = the union of the selected clusters' tokens.
+//
+// DynaSpec abstract ("the union of the top-selected clusters defines the drafter's
+// shortlist"); summary, Technical Details > Problem Definition ("Outputs: shortlisted subset
+// V_S").  The clusters partition the vocabulary, so the union is a concatenation: an
+// exclusive scan of the selected clusters' sizes in ascending cluster id gives every
+// cluster's place in the list (cpos), and a copy of the CSR slices fills it.  The same
+// scan over "selected by any list" gives the batch union the batched / tree heads read W
+// through.
+#include "common.cuh"
+#include "block_scan.cuh"
+
+namespace ds {
+namespace {
+
+constexpr int kSlThreads = 1024;
+constexpr int kSlMaxM = 8192;
+constexpr int kSlMaxPer = kSlMaxM / kSlThreads;
+
+// cluster_of[v] = c and rank_in_cluster[v] = position of v in cluster c's list.
+__global__ void vocab_index_kernel(const int32_t *__restrict__ off, const int32_t *__restrict__ tok,
+                                   int M, int V, int32_t *__restrict__ cluster_of,
+                                   int32_t *__restrict__ rank, int32_t *st)
+{
+    const int c = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (c >= M) return;
+    const int lo = off[c], hi = off[c + 1];
+    if (lo < 0 || hi < lo || hi > V) { if ((threadIdx.x & 31) == 0) set_status(st, DS_DEV_BAD_INDEX); return; }
+    for (int r = lo + (threadIdx.x & 31); r < hi; r += 32) {
+        const int v = tok[r];
+        if (v < 0 || v >= V) { set_status(st, DS_DEV_BAD_INDEX); continue; }
+        cluster_of[v] = c;
+        rank[v] = r - lo;
+    }
+}
+
+// One block per list b: cpos[b][c] = exclusive prefix (over ascending c) of the sizes of the
+// clusters b selected, or -1; sizes[b] = |S_b|.
+__global__ void __launch_bounds__(kSlThreads)
+shortlist_scan_kernel(const int32_t *__restrict__ off, int M, const int32_t *__restrict__ ids, int k,
+                      int32_t *__restrict__ cpos, int32_t *__restrict__ sizes, int32_t *st)
+{
+    __shared__ unsigned char flag[kSlMaxM];
+    __shared__ int scratch[33];
+    const int b = blockIdx.x;
+    for (int c = threadIdx.x; c < M; c += blockDim.x) flag[c] = 0;
+    __syncthreads();
+    const int32_t *my = ids + size_t(b) * k;
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+        const int c = my[j];
+        if (c < 0 || c >= M || (j > 0 && my[j - 1] >= c)) { set_status(st, DS_DEV_BAD_INDEX); continue; }
+        flag[c] = 1;
+    }
+    __syncthreads();
+    const int E = (M + kSlThreads - 1) / kSlThreads;
+    const int lo = threadIdx.x * E;
+    int sz[kSlMaxPer];
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < kSlMaxPer; ++e) {
+        const int c = lo + e;
+        sz[e] = (e < E && c < M && flag[c]) ? off[c + 1] - off[c] : 0;
+        sum += sz[e];
+    }
+    int tot;
+    int run = block_exclusive_scan(sum, scratch, &tot);
+    int32_t *dst = cpos + size_t(b) * M;
+#pragma unroll
+    for (int e = 0; e < kSlMaxPer; ++e) {
+        const int c = lo + e;
+        if (e < E && c < M) { dst[c] = flag[c] ? run : -1; run += sz[e]; }
+    }
+    if (threadIdx.x == 0) sizes[b] = tot;
+}
+
+// Single block: vs_offsets = exclusive scan of the list sizes; and, if asked, the batch
+// union (clusters selected by any list) with each cluster's start in it (ustart, -1 if out).
+__global__ void __launch_bounds__(kSlThreads)
+shortlist_offsets_kernel(const int32_t *__restrict__ off, int M, int B,
+                         const int32_t *__restrict__ sizes, const int32_t *__restrict__ cpos,
+                         int32_t *__restrict__ vs_offsets, int64_t capacity,
+                         int32_t *__restrict__ ustart, int32_t *__restrict__ union_count, int32_t *st)
+{
+    __shared__ int scratch[33];
+    {
+        const int E = (B + kSlThreads - 1) / kSlThreads;
+        const int lo = threadIdx.x * E;
+        int sum = 0;
+        for (int e = 0; e < E; ++e) if (lo + e < B) sum += sizes[lo + e];
+        int tot;
+        int run = block_exclusive_scan(sum, scratch, &tot);
+        for (int e = 0; e < E; ++e) if (lo + e < B) { vs_offsets[lo + e] = run; run += sizes[lo + e]; }
+        if (threadIdx.x == 0) {
+            vs_offsets[B] = tot;
+            if (int64_t(tot) > capacity) set_status(st, DS_DEV_CAPACITY);
+        }
+    }
+    if (!ustart) return;
+    const int E = (M + kSlThreads - 1) / kSlThreads;
+    const int lo = threadIdx.x * E;
+    int sz[kSlMaxPer];
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < kSlMaxPer; ++e) {
+        const int c = lo + e;
+        bool any = false;
+        if (e < E && c < M)
+            for (int b = 0; b < B && !any; ++b) any = cpos[size_t(b) * M + c] >= 0;
+        sz[e] = any ? off[c + 1] - off[c] : 0;
+        sum += sz[e];
+    }
+    int tot;
+    int run = block_exclusive_scan(sum, scratch, &tot);
+#pragma unroll
+    for (int e = 0; e < kSlMaxPer; ++e) {
+        const int c = lo + e;
+        if (e < E && c < M) { ustart[c] = sz[e] ? run : -1; run += sz[e]; }
+    }
+    if (threadIdx.x == 0) *union_count = tot;
+}
+
+// One warp per selected cluster of list b: copy its CSR slice into the list.
+__global__ void shortlist_expand_kernel(const int32_t *__restrict__ off, const int32_t *__restrict__ tok,
+                                        int M, int V, const int32_t *__restrict__ ids, int k,
+                                        const int32_t *__restrict__ cpos,
+                                        const int32_t *__restrict__ vs_offsets, int32_t *__restrict__ vs_ids,
+                                        int64_t capacity)
+{
+    const int b = blockIdx.y;
+    const int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (j >= k) return;
+    const int c = ids[size_t(b) * k + j];
+    if (c < 0 || c >= M) return;                          // flagged by the scan kernel
+    const int p = cpos[size_t(b) * M + c];
+    if (p < 0) return;                                    // duplicate / unsorted ids, flagged
+    const int lo = off[c], n = off[c + 1] - lo;
+    if (lo < 0 || n < 0 || lo + n > V) return;
+    const int64_t base = int64_t(vs_offsets[b]) + p;
+    for (int r = threadIdx.x & 31; r < n; r += 32)
+        if (base + r < capacity) vs_ids[base + r] = tok[lo + r];
+}
+
+// One warp per cluster of the batch union.
+__global__ void union_expand_kernel(const int32_t *__restrict__ off, const int32_t *__restrict__ tok,
+                                    int M, int V, const int32_t *__restrict__ ustart,
+                                    int32_t *__restrict__ union_ids, int32_t *__restrict__ union_cluster)
+{
+    const int c = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (c >= M) return;
+    const int u = ustart[c];
+    if (u < 0) return;
+    const int lo = off[c], n = off[c + 1] - lo;
+    if (lo < 0 || n < 0 || lo + n > V || u + n > V) return;
+    for (int r = threadIdx.x & 31; r < n; r += 32) {
+        union_ids[u + r] = tok[lo + r];
+        union_cluster[u + r] = c;
+    }
+}
+
+}  // namespace
+}  // namespace ds
+
+using namespace ds;
+
+extern "C" ds_status ds_vocab_index(const int32_t *csr_off, const int32_t *csr_tok, int M, int V,
+                                    int32_t *cluster_of, int32_t *rank_in_cluster,
+                                    int32_t *dev_status, cudaStream_t stream)
+{
+    if (!csr_off || !csr_tok || !cluster_of || !rank_in_cluster) return DS_ERR_INVALID_ARG;
+    if (M < 1 || V < 1 || M > V) return DS_ERR_INVALID_ARG;
+    vocab_index_kernel<<<(M + 7) / 8, 256, 0, stream>>>(csr_off, csr_tok, M, V, cluster_of,
+                                                       rank_in_cluster, dev_status);
+    DS_TRY_LAUNCH();
+    return DS_OK;
+}
+
+extern "C" size_t ds_shortlist_workspace_bytes(int B, int M)
+{
+    if (B <= 0 || M <= 0) return 0;
+    return align256(size_t(B) * sizeof(int32_t)) + align256(size_t(M) * sizeof(int32_t));
+}
+
+extern "C" ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *csr_tok, int M, int V,
+                                        const int32_t *cluster_ids, int B, int k,
+                                        int32_t *vs_offsets, int32_t *vs_ids, int64_t vs_capacity,
+                                        int32_t *cpos,
+                                        int32_t *union_ids, int32_t *union_cluster, int32_t *union_count,
+                                        void *ws, size_t ws_bytes, int32_t *dev_status,
+                                        cudaStream_t stream)
+{
+    if (!csr_off || !csr_tok || !cluster_ids || !vs_offsets || !vs_ids || !cpos)
+        return DS_ERR_INVALID_ARG;
+    const int nu = (union_ids != nullptr) + (union_cluster != nullptr) + (union_count != nullptr);
+    if (nu != 0 && nu != 3) return DS_ERR_INVALID_ARG;
+    if (M < 1 || M > kSlMaxM || V < M || B < 1 || B > 4096 || k < 1 || k > M || vs_capacity < 0)
+        return DS_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < ds_shortlist_workspace_bytes(B, M)) return DS_ERR_WORKSPACE;
+    int32_t *sizes = static_cast<int32_t *>(ws);
+    int32_t *ustart = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + align256(size_t(B) * 4));
+
+    shortlist_scan_kernel<<<B, kSlThreads, 0, stream>>>(csr_off, M, cluster_ids, k, cpos, sizes, dev_status);
+    DS_TRY_LAUNCH();
+    shortlist_offsets_kernel<<<1, kSlThreads, 0, stream>>>(csr_off, M, B, sizes, cpos, vs_offsets, vs_capacity,
+                                                          nu ? ustart : nullptr, union_count, dev_status);
+    DS_TRY_LAUNCH();
+    shortlist_expand_kernel<<<dim3((k + 7) / 8, B), 256, 0, stream>>>(csr_off, csr_tok, M, V, cluster_ids, k, cpos,
+                                                                     vs_offsets, vs_ids, vs_capacity);
+    DS_TRY_LAUNCH();
+    if (nu) {
+        union_expand_kernel<<<(M + 7) / 8, 256, 0, stream>>>(csr_off, csr_tok, M, V, ustart, union_ids, union_cluster);
+        DS_TRY_LAUNCH();
+    }
+    return DS_OK;
+}

@@ -1,0 +1,231 @@
+"""One DynaSpec speculation step on one GPU, stage by stage through the C ABI.
+
+Pipeline order (DynaSpec summary, Technical Details > Pipeline Flow): router on a parallel
+stream, draft computation on the main stream, a synchronisation, the gathered projection,
+then rejection-sampling verification.  Per draft position t the router and shortlist build
+run on a side stream (Novel Architectural Elements: "Parallel execution of the Router on a
+separate CUDA stream"), an event marks the shortlist ready, and the main stream waits on that
+event before the gathered head.  The routers of later positions therefore run while the
+heads of earlier positions stream W.
+
+Buffers are allocated once per drafter; a step launches kernels only.  ``capture()`` records
+one whole step (both streams) into a CUDA graph that ``replay()`` launches in one call.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import api
+
+
+class _Common:
+    def _setup_vocab(self, csr_off, csr_tok, dev):
+        self.csr_off = csr_off.to(dev, torch.int32).contiguous()
+        self.csr_tok = csr_tok.to(dev, torch.int32).contiguous()
+        self.M = self.csr_off.numel() - 1
+        self.V = self.csr_tok.numel()
+        self.cluster_of = torch.empty(self.V, dtype=torch.int32, device=dev)
+        self.rank = torch.empty(self.V, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        api.vocab_index(self.csr_off, self.csr_tok, self.cluster_of, self.rank, self.status)
+
+    def check_status(self):
+        s = int(self.status.item())
+        if s:
+            from . import _lib
+            raise _lib.DynaSpecError(f"device status {s:#x}: {_lib.load().ds_status_string(s).decode()}")
+
+    def capture(self):
+        """Record one step into a CUDA graph (the step's inputs are the drafter's buffers)."""
+        self.step()                              # warm up: lazy attributes, library state
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step()
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+
+
+class ChainDrafter(_Common):
+    """Chain drafting: B sequences, gamma draft positions, one shortlist per (sequence, position).
+
+    Weights (device tensors, bf16 bits): W [V, d], W1 [Hr, d], b1 [Hr], W2 [M, Hr], b2 [M].
+    Per-step inputs are written into ``self.H`` [gamma+1, B, d] (hidden states; the router at
+    position t reads H[t-1], the head H[t]), ``self.z`` [B, gamma+1, V] (target logits) and
+    ``self.u`` [B, gamma+1] (verification uniforms).
+    """
+
+    def __init__(self, W, W1, b1, W2, b2, csr_off, csr_tok, *, B, gamma, budget, act, T, seed,
+                 union=None):
+        dev = W.device
+        self.dev = dev
+        self.W, self.W1, self.b1, self.W2, self.b2 = W, W1, b1, W2, b2
+        self._setup_vocab(csr_off, csr_tok, dev)
+        self.d = W.shape[1]
+        self.Hr = W1.shape[0]
+        self.B, self.gamma = B, gamma
+        self.budget = torch.tensor(list(budget), dtype=torch.int32)
+        self.act, self.T, self.seed = act, float(T), int(seed)
+        self.union = (B > 1) if union is None else bool(union)
+        V, M = self.V, self.M
+        cap = B * V
+        i32 = dict(dtype=torch.int32, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.H = torch.zeros(gamma + 1, B, self.d, dtype=torch.bfloat16, device=dev)
+        self.z = torch.zeros(B, gamma + 1, V, **f32)
+        self.u = torch.full((B, gamma + 1), 0.5, **f32)
+        self.scores = torch.empty(gamma, B, M, **f32)
+        self.cluster_ids = [torch.empty(B, int(self.budget[t]), **i32) for t in range(gamma)]
+        self.vs_offsets = torch.zeros(gamma, B + 1, **i32)
+        self.vs_ids = torch.zeros(gamma, cap, **i32)
+        self.cpos = torch.empty(gamma, B * M, **i32)
+        if self.union:
+            self.union_ids = torch.empty(gamma, V, **i32)
+            self.union_cluster = torch.empty(gamma, V, **i32)
+            self.union_count = torch.zeros(gamma, 1, **i32)
+        self.logits = torch.zeros(gamma, cap, **f32)
+        self.row_max = torch.empty(gamma, B, **f32)
+        self.row_sumexp = torch.empty(gamma, B, **f32)
+        self.tokens = torch.empty(gamma, B, **i32)
+        self.token_idx = torch.empty(gamma, B, **i32)
+        self.accepted = torch.empty(B, **i32)
+        self.correction = torch.empty(B, **i32)
+        self.ws_router = [api.workspace(api.router_workspace_bytes(B, self.Hr), dev) for _ in range(gamma)]
+        self.ws_short = [api.workspace(api.shortlist_workspace_bytes(B, M), dev) for _ in range(gamma)]
+        self.ws_head = api.workspace(api.head_workspace_bytes(B), dev)
+        self.ws_verify = api.workspace(api.verify_workspace_bytes(B, gamma, V), dev)
+        self.side = torch.cuda.Stream(device=dev)
+        self.ready = [torch.cuda.Event() for _ in range(gamma)]
+        self.graph = None
+
+    def route(self, t, stream=None):
+        """Router + top-k + shortlist of draft position t (0-based) for all sequences."""
+        api.router_topk(self.H[t], self.W1, self.b1, self.W2, self.b2, self.act, self.budget, t + 1,
+                        self.scores[t], self.cluster_ids[t], self.ws_router[t], self.status, stream)
+        un = (self.union_ids[t], self.union_cluster[t], self.union_count[t]) if self.union else (None,) * 3
+        api.build_shortlist(self.csr_off, self.csr_tok, self.cluster_ids[t], self.vs_offsets[t],
+                            self.vs_ids[t], self.cpos[t], self.ws_short[t], self.status,
+                            un[0], un[1], un[2], stream)
+
+    def head(self, t, stream=None):
+        api.gathered_head(self.H[t + 1], 1, self.W, self.vs_offsets[t], self.vs_ids[t], self.T,
+                          self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],
+                          self.ws_head, self.status, cpos=self.cpos[t], rank_in_cluster=self.rank,
+                          union=(self.union_ids[t], self.union_cluster[t], self.union_count[t])
+                          if self.union else None,
+                          row_max=self.row_max[t], row_sumexp=self.row_sumexp[t], stream=stream)
+
+    def verify(self, stream=None):
+        api.verify(self.z, self.T, self.logits, self.vs_offsets, self.cpos, self.cluster_of, self.rank,
+                   self.tokens, self.u, self.accepted, self.correction, self.ws_verify, self.status,
+                   stream)
+
+    def step(self):
+        main = torch.cuda.current_stream(self.dev)
+        self.side.wait_stream(main)
+        for t in range(self.gamma):
+            with torch.cuda.stream(self.side):
+                self.route(t)
+                self.ready[t].record(self.side)
+        for t in range(self.gamma):
+            main.wait_event(self.ready[t])
+            self.head(t)
+        self.verify()
+
+    def launches_per_step(self) -> int:
+        n_router = 3
+        n_short = 4 if self.union else 3
+        n_head = 2 if self.union else 1
+        return self.gamma * (n_router + n_short + n_head) + 2
+
+
+class TreeDrafter(_Common):
+    """Tree drafting: B sequences, D depths of Wd nodes; the Wd nodes of one depth of one
+    sequence share that depth's shortlist, so the head is a dense contraction of B*Wd rows
+    against the union of the B shortlists.
+
+    Per-step inputs: ``self.Hr_h`` [D, B, d] (router hidden state per depth), ``self.Hn``
+    [D, B*Wd, d] (node hidden states), ``self.z`` [B, 1+D*Wd, V], ``self.u_node`` [B, D*Wd],
+    ``self.u_res`` [B, D+1]; ``self.parent`` [D*Wd] the tree's wiring.
+    """
+
+    def __init__(self, W, W1, b1, W2, b2, csr_off, csr_tok, parent, *, B, D, Wd, budget, act, T, seed):
+        dev = W.device
+        self.dev = dev
+        self.W, self.W1, self.b1, self.W2, self.b2 = W, W1, b1, W2, b2
+        self._setup_vocab(csr_off, csr_tok, dev)
+        self.d = W.shape[1]
+        self.Hr = W1.shape[0]
+        self.B, self.D, self.Wd = B, D, Wd
+        self.budget = torch.tensor(list(budget), dtype=torch.int32)
+        self.act, self.T, self.seed = act, float(T), int(seed)
+        V, M, N = self.V, self.M, D * Wd
+        cap = B * V
+        i32 = dict(dtype=torch.int32, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.parent = torch.as_tensor(parent, dtype=torch.int32).to(dev)
+        self.Hr_h = torch.zeros(D, B, self.d, dtype=torch.bfloat16, device=dev)
+        self.Hn = torch.zeros(D, B * Wd, self.d, dtype=torch.bfloat16, device=dev)
+        self.z = torch.zeros(B, 1 + N, V, **f32)
+        self.u_node = torch.full((B, N), 0.5, **f32)
+        self.u_res = torch.full((B, D + 1), 0.5, **f32)
+        self.scores = torch.empty(D, B, M, **f32)
+        self.cluster_ids = [torch.empty(B, int(self.budget[t]), **i32) for t in range(D)]
+        self.vs_offsets = torch.zeros(D, B + 1, **i32)
+        self.vs_ids = torch.zeros(D, cap, **i32)
+        self.cpos = torch.empty(D, B * M, **i32)
+        self.union_ids = torch.empty(D, V, **i32)
+        self.union_cluster = torch.empty(D, V, **i32)
+        self.union_count = torch.zeros(D, 1, **i32)
+        self.logits = torch.zeros(D, cap * Wd, **f32)
+        self.row_max = torch.empty(D, B * Wd, **f32)
+        self.row_sumexp = torch.empty(D, B * Wd, **f32)
+        self.tokens = torch.empty(D, B * Wd, **i32)
+        self.token_idx = torch.empty(D, B * Wd, **i32)
+        self.accepted = torch.empty(B, **i32)
+        self.correction = torch.empty(B, **i32)
+        self.path = torch.empty(B, D, **i32)
+        self.ws_router = [api.workspace(api.router_workspace_bytes(B, self.Hr), dev) for _ in range(D)]
+        self.ws_short = [api.workspace(api.shortlist_workspace_bytes(B, M), dev) for _ in range(D)]
+        self.ws_head = api.workspace(api.head_workspace_bytes(B * Wd), dev)
+        self.ws_verify = api.workspace(api.verify_tree_workspace_bytes(B, D, Wd, V), dev)
+        self.side = torch.cuda.Stream(device=dev)
+        self.ready = [torch.cuda.Event() for _ in range(D)]
+        self.graph = None
+
+    def route(self, t, stream=None):
+        api.router_topk(self.Hr_h[t], self.W1, self.b1, self.W2, self.b2, self.act, self.budget, t + 1,
+                        self.scores[t], self.cluster_ids[t], self.ws_router[t], self.status, stream)
+        api.build_shortlist(self.csr_off, self.csr_tok, self.cluster_ids[t], self.vs_offsets[t],
+                            self.vs_ids[t], self.cpos[t], self.ws_short[t], self.status,
+                            self.union_ids[t], self.union_cluster[t], self.union_count[t], stream)
+
+    def head(self, t, stream=None):
+        api.gathered_head(self.Hn[t], self.Wd, self.W, self.vs_offsets[t], self.vs_ids[t], self.T,
+                          self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],
+                          self.ws_head, self.status, cpos=self.cpos[t], rank_in_cluster=self.rank,
+                          union=(self.union_ids[t], self.union_cluster[t], self.union_count[t]),
+                          row_max=self.row_max[t], row_sumexp=self.row_sumexp[t], stream=stream)
+
+    def verify(self, stream=None):
+        api.verify_tree(self.z, self.D, self.Wd, self.T, self.parent, self.logits, self.vs_offsets,
+                        self.cpos, self.cluster_of, self.rank, self.tokens, self.u_node, self.u_res,
+                        self.accepted, self.correction, self.path, self.ws_verify, self.status, stream)
+
+    def step(self):
+        main = torch.cuda.current_stream(self.dev)
+        self.side.wait_stream(main)
+        for t in range(self.D):
+            with torch.cuda.stream(self.side):
+                self.route(t)
+                self.ready[t].record(self.side)
+        for t in range(self.D):
+            main.wait_event(self.ready[t])
+            self.head(t)
+        self.verify()
+
+    def launches_per_step(self) -> int:
+        return self.D * (3 + 4 + 2) + 2

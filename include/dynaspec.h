@@ -1,0 +1,248 @@
+/*
+ * dynaspec.h -- C ABI of the GB300 (sm_103a) DynaSpec draft head and verifier.
+ *
+ * DynaSpec (arXiv 2510.13847) replaces the drafter's full-vocabulary output projection with
+ * a context-dependent shortlist: a small router scores vocabulary clusters from the drafter
+ * hidden state, the top clusters under a position-aware budget form the shortlist V_S, the
+ * head projects onto the gathered LM-head rows W[V_S] only, and the target model verifies
+ * the drafted tokens over the full vocabulary by rejection sampling (abstract on
+ * mlsanity.com/paper/2510.13847; summary "DynaSpec: Context-aware Dynamic Speculative
+ * Sampling for Large-Vocabulary Language Models", Technical Details > Problem Definition,
+ * Pipeline Flow, System Modules).  The four stages are the four calls below, in the order
+ * of that pipeline:  ds_router_topk -> ds_build_shortlist -> ds_gathered_head -> ds_verify
+ * (ds_verify_tree for tree drafting).
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers owned by the caller unless marked "host".  The library
+ *     never allocates, frees or retains memory and keeps no state between calls.
+ *   - bf16 tensors are passed as their raw 16-bit patterns (uint16_t).  Row-major layouts.
+ *   - Every call is asynchronous on `stream` and returns a ds_status at once.  Errors the
+ *     host can see (NULL pointers, bad sizes, a workspace that is too small, d % 8 != 0)
+ *     are returned before anything is launched.  Errors only the device can see are OR-ed
+ *     into *dev_status (a caller-owned int32 in device memory, which the caller zeroes and
+ *     reads after synchronising); when a bit is set the outputs of that call are undefined.
+ *     No call prints, exits or traps.
+ *   - `ws` is caller-owned scratch of at least the size the matching *_workspace_bytes()
+ *     query returns, 256-byte aligned.  Scratch that holds cross-block completion counters
+ *     must be zero-filled once before its first use; each call leaves those counters at
+ *     zero again.  Two calls that are in flight at the same time must not share a `ws`.
+ */
+#ifndef DYNASPEC_H
+#define DYNASPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t ds_status;
+
+/* Host-side return codes. */
+#define DS_OK               0
+#define DS_ERR_INVALID_ARG  1   /* NULL pointer, size out of range, misaligned row pitch   */
+#define DS_ERR_UNSUPPORTED  2   /* a size beyond what the kernels are built for            */
+#define DS_ERR_CUDA         3   /* a CUDA launch or runtime call failed                     */
+#define DS_ERR_WORKSPACE    4   /* ws NULL or smaller than the *_workspace_bytes() query    */
+
+/* Device-side bits OR-ed into *dev_status. */
+#define DS_DEV_BAD_INDEX    0x10  /* an id outside [0, V) or [0, M), or a draft token that is
+                                     not in its shortlist                                   */
+#define DS_DEV_CAPACITY     0x20  /* a shortlist larger than the capacity the caller gave   */
+#define DS_DEV_TIMEOUT      0x40  /* a bounded wait gave up (reserved; no wait exists yet)  */
+
+/* Router activations (summary, Key Hyperparameters: "2-layer MLP with ReLU"; the Tiny
+ * workload names GELU, taken in its exact erf form). */
+#define DS_ACT_RELU 0
+#define DS_ACT_GELU 1
+
+/* Text for a host-side code or a device-side bit pattern.  Never NULL. */
+const char *ds_status_string(ds_status s);
+
+/* ABI version, bumped on any incompatible change. */
+int ds_version(void);
+
+/* -------------------------------------------------------------------------------------
+ * ds_vocab_index -- per-token inverse of the cluster CSR.
+ * The vocabulary is partitioned into M clusters (summary, Key Novelty: clusters of
+ * LM-head rows), given as CSR: csr_off [M+1] (csr_off[0] = 0, csr_off[M] = V, non-
+ * decreasing) and csr_tok [V] (a permutation of 0..V-1).  Fills cluster_of [V] (the
+ * cluster of token v) and rank_in_cluster [V] (v's position inside its cluster's list).
+ * Run once per clustering; ds_gathered_head and ds_verify look tokens up through it.
+ * Device errors: DS_DEV_BAD_INDEX when a token id is outside [0, V).
+ * ------------------------------------------------------------------------------------- */
+ds_status ds_vocab_index(const int32_t *csr_off, const int32_t *csr_tok, int M, int V,
+                         int32_t *cluster_of, int32_t *rank_in_cluster,
+                         int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * ds_router_topk -- router MLP + position-aware top-k (summary, System Modules "Router
+ * (Meta-Classifier)": a 2-layer MLP predicting relevant clusters from H_{t-1}; Key
+ * Novelty and Key Hyperparameters: the budget k_c(t) shrinks with draft position t;
+ * abstract: "the union of the top-selected clusters").
+ *   H [B, d] bf16          hidden states the router reads (H_{t-1} of each sequence)
+ *   W1 [Hr, d], b1 [Hr]    first layer (out x in), bf16
+ *   W2 [M, Hr], b2 [M]     second layer, bf16
+ *   act                    DS_ACT_RELU or DS_ACT_GELU
+ *   budget (host) [n_budget], pos (1-based draft position): k = budget[pos-1] clusters
+ *   scores [B, M] fp32     out: s = W2 act(W1 h + b1) + b2 (fp32 accumulation; no sigmoid,
+ *                          which would not change the top-k)
+ *   cluster_ids [B, k]     out: the k highest-scoring clusters of each row, ties to the lower
+ *                          id, listed in ascending id
+ * Limits: 1 <= B <= 4096, d % 8 == 0, Hr % 8 == 0, 1 <= k <= M <= 8192.
+ * ws: ds_router_workspace_bytes(B, Hr) bytes (the hidden layer).
+ * ------------------------------------------------------------------------------------- */
+size_t ds_router_workspace_bytes(int B, int Hr);
+ds_status ds_router_topk(const uint16_t *H, int B, int d,
+                         const uint16_t *W1, const uint16_t *b1, int Hr,
+                         const uint16_t *W2, const uint16_t *b2, int M, int act,
+                         const int32_t *budget, int n_budget, int pos,
+                         float *scores, int32_t *cluster_ids,
+                         void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * ds_build_shortlist -- V_S as the union of the selected clusters (abstract; summary,
+ * Problem Definition "Outputs: shortlisted subset V_S").  Clusters partition V, so the union
+ * needs no de-duplication.  Order (the pages fix only the set): selected clusters in
+ * ascending id, each cluster's tokens in CSR order.
+ *   cluster_ids [B, k]     ascending per row (as ds_router_topk writes them)
+ *   vs_offsets [B+1]       out: list b is vs_ids[vs_offsets[b] .. vs_offsets[b+1])
+ *   vs_ids [vs_capacity]   out: shortlisted token ids
+ *   cpos [B, M]            out: index in list b of cluster c's first token, -1 if c is not
+ *                          selected by b (ds_gathered_head and ds_verify use it)
+ *   union_ids, union_cluster [V], union_count [1]: optional (all NULL or all set).  Out:
+ *                          the union over the B lists of the selected clusters' tokens (same
+ *                          canonical order), each token's cluster, and the union's size.
+ *                          Batched and tree heads read W once over this union.
+ * Device errors: DS_DEV_BAD_INDEX (cluster id outside [0, M) or not ascending),
+ * DS_DEV_CAPACITY (sum of list sizes > vs_capacity; nothing past the capacity is written).
+ * Limits: 1 <= B <= 4096, 1 <= k <= M <= 8192.
+ * ws: ds_shortlist_workspace_bytes(B, M) bytes.
+ * ------------------------------------------------------------------------------------- */
+size_t ds_shortlist_workspace_bytes(int B, int M);
+ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *csr_tok, int M, int V,
+                             const int32_t *cluster_ids, int B, int k,
+                             int32_t *vs_offsets, int32_t *vs_ids, int64_t vs_capacity,
+                             int32_t *cpos,
+                             int32_t *union_ids, int32_t *union_cluster, int32_t *union_count,
+                             void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * ds_gathered_head -- logits over the shortlist only, plus the draft draw (summary, System
+ * Modules "Gathered LM Head": a fused index-select + GEMM; Novel Architectural Elements
+ * "Dynamic Vocabulary Head"; Key Novelty: "restricting the drafter's computation to this
+ * dynamic subset").  W[V_S] is never materialised: rows are streamed straight from W.
+ *   H [B*G, d] bf16        head rows; rows b*G .. b*G+G-1 share list b (G = 1 for chain
+ *                          drafting, G = nodes per depth for tree drafting)
+ *   W [V, d] bf16          the LM head
+ *   vs_offsets, vs_ids, cpos, M: from ds_build_shortlist; rank_in_cluster from ds_vocab_index
+ *   union_ids, union_cluster, union_count: all NULL -> each row's list is gathered on its
+ *                          own (batch-1 path); all set -> W is read once over the union
+ *                          of the lists and every row is scored against every union row
+ *                          on the tensor cores, keeping the entries its list selects
+ *   T                      temperature; 0 = greedy
+ *   seed, pos              Gumbel noise key and the draft position (see below)
+ *   logits (out)           row r = b*G+g writes |S_b| fp32 logits l_j = h_r . W[S_b[j]] at
+ *                          logits[vs_offsets[b]*G + g*|S_b| + j]
+ *   row_max, row_sumexp [B*G] (out, optional): m = max_j l_j/Te, s = sum_j exp(l_j/Te - m),
+ *                          Te = T (T > 0) or 1 (T = 0)
+ *   token, token_idx [B*G] (out): the draft token as a full-vocabulary id and its index j in
+ *                          the list.  T = 0: argmax_j l_j.  T > 0: argmax_j (l_j/T + g_j), the
+ *                          Gumbel-max draw from softmax(l/T), g_j = -log(-log u) with u from
+ *                          Philox4x32-10 (key = seed, counter = (v >> 2, pos, r, 0), word v & 3,
+ *                          u = (2 (w >> 9) + 1) 2^-24).  Ties go to the lower token id.  An
+ *                          empty list gives token = token_idx = -1.
+ * Limits: d % 8 == 0, d <= 16384, B*G <= 128 (union path) and G == 1 (per-row path).
+ * ws: ds_head_workspace_bytes(B*G) bytes; holds completion counters (zero it once).
+ * ------------------------------------------------------------------------------------- */
+size_t ds_head_workspace_bytes(int rows);
+ds_status ds_gathered_head(const uint16_t *H, int B, int G,
+                           const uint16_t *W, int V, int d,
+                           const int32_t *vs_offsets, const int32_t *vs_ids,
+                           const int32_t *cpos, int M, const int32_t *rank_in_cluster,
+                           const int32_t *union_ids, const int32_t *union_cluster,
+                           const int32_t *union_count,
+                           float T, uint64_t seed, int pos,
+                           float *logits, float *row_max, float *row_sumexp,
+                           int32_t *token, int32_t *token_idx,
+                           void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * ds_verify -- rejection-sampling verification over the full vocabulary (abstract: "the
+ * target model still verifies over the full vocabulary, preserving exactness"; summary,
+ * Pipeline Flow "Rejection Sampling Verification").  The pages cite Leviathan et al. and
+ * Chen et al. without printing the algorithm; this is its standard statement:
+ *   p_t = softmax(z_t / T) over all V, q_t = softmax(l_t / T) over the shortlist S_t (0
+ *   elsewhere).  For t = 1..gamma in order accept x_t iff u_t q_t(x_t) < p_t(x_t).  At the
+ *   first rejection, accepted_len = t-1 and the correction is drawn from
+ *   norm(max(0, p_t - q_t)); if all gamma are accepted the bonus token is drawn from
+ *   p_{gamma+1}.  Both draws are inverse-CDF in ascending token id with u_{gamma+1}; a
+ *   residual without mass falls back to p_t.  T = 0: accept while x_t = argmax z_t (ties to
+ *   the lower id); the correction / bonus is that argmax.
+ *   p_logits [B, gamma+1, V] fp32 target logits
+ *   q_logits               draft logits of position t (0-based) at q_logits + t*q_stride,
+ *                          laid out as ds_gathered_head writes them with G = 1
+ *   vs_offsets [gamma, B+1], cpos [gamma, B*M]: the lists of each position
+ *   cluster_of, rank_in_cluster [V]: from ds_vocab_index
+ *   draft_ids [gamma, B]   x_t of each sequence (full-vocabulary ids)
+ *   uniforms [B, gamma+1]  u_1..u_gamma for the accept tests, u_{gamma+1} for the draw
+ *   accepted_len [B], correction [B] (out)
+ * Device errors: DS_DEV_BAD_INDEX when a draft token is not in its shortlist.
+ * Limits: 1 <= gamma <= 32, V <= 2^24, M <= 8192.
+ * ws: ds_verify_workspace_bytes(B, gamma, V) bytes; holds completion counters.
+ * ------------------------------------------------------------------------------------- */
+size_t ds_verify_workspace_bytes(int B, int gamma, int V);
+ds_status ds_verify(const float *p_logits, int B, int gamma, int V, float T,
+                    const float *q_logits, int64_t q_stride,
+                    const int32_t *vs_offsets, const int32_t *cpos, int M,
+                    const int32_t *cluster_of, const int32_t *rank_in_cluster,
+                    const int32_t *draft_ids, const float *uniforms,
+                    int32_t *accepted_len, int32_t *correction,
+                    void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * ds_verify_tree -- verification of a draft tree (EAGLE-style trees, which the pages cite;
+ * the pages state no tree verifier).  Reading: sibling-sequential recursive rejection, the
+ * multi-draft form of speculative sampling.  Walking from the root with p = softmax(z/T) of
+ * the current node, the children are tried in index order; child c is accepted iff
+ * u_c q_c(x_c) < p(x_c), where q_c is c's own draft row over its depth's shortlist; after a
+ * rejection p <- norm(max(0, p - q_c)) (unchanged if that has no mass).  On acceptance the
+ * walk moves to c with p = softmax(z_c / T).  When no child is accepted, or at a leaf, the
+ * correction is drawn from the current p by inverse CDF with u_res[depth].  T = 0: accept
+ * the first child whose token is the argmax of the current node's target row.
+ *   D depths of Wd nodes; node n = (dep-1)*Wd + i (depth-major), N = D*Wd
+ *   p_logits [B, 1+N, V]   row 0: target at the root; row 1+n: target after node n
+ *   parent [N] (device)    parent node of n, -1 for the root; parents sit one depth up
+ *   q_logits               depth dep (0-based) at q_logits + dep*q_stride, laid out as
+ *                          ds_gathered_head writes them with G = Wd
+ *   vs_offsets [D, B+1], cpos [D, B*M], cluster_of, rank_in_cluster: as in ds_verify
+ *   node_tokens [D, B*Wd]  token of node (b, dep, i) at [dep-1][b*Wd + i]
+ *   u_node [B, N], u_res [B, D+1]
+ *   accepted_len [B], correction [B], path [B, D] (out; accepted node ids, -1 padded)
+ * Limits: D <= 32, Wd <= 64, V <= 2^24, M <= 8192.
+ * ws: ds_verify_tree_workspace_bytes(B, D, Wd, V) bytes.
+ * ------------------------------------------------------------------------------------- */
+size_t ds_verify_tree_workspace_bytes(int B, int D, int Wd, int V);
+ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd, int V, float T,
+                         const int32_t *parent,
+                         const float *q_logits, int64_t q_stride,
+                         const int32_t *vs_offsets, const int32_t *cpos, int M,
+                         const int32_t *cluster_of, const int32_t *rank_in_cluster,
+                         const int32_t *node_tokens, const float *u_node, const float *u_res,
+                         int32_t *accepted_len, int32_t *correction, int32_t *path,
+                         void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * ds_philox4x32_10 -- the device Philox4x32-10 the head draws its Gumbel noise from
+ * (Salmon, Moraes, Dror, Shaw, SC'11), exposed so that it can be checked on its own.
+ *   ctr [n, 4] counters, out [n, 4] words; key = the two 32-bit halves of `seed`.
+ * ------------------------------------------------------------------------------------- */
+ds_status ds_philox4x32_10(const uint32_t *ctr, uint64_t seed, uint32_t *out, int n,
+                           cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DYNASPEC_H */

@@ -1,0 +1,99 @@
+"""The C-ABI library loads on a machine without a GPU, exports every symbol the header
+declares, answers workspace queries, and rejects bad host-side arguments before it launches
+anything (no compute call reaches a device here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dynaspec.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dynamic_vocab_draft_gb300 import build
+    build.build()
+    from dynamic_vocab_draft_gb300 import _lib
+    return _lib.load()
+
+
+def declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ds_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+    from dynamic_vocab_draft_gb300 import _lib
+    assert set(_lib.SIGNATURES) == set(names)
+
+
+def test_status_strings(lib):
+    for code in (0, 1, 2, 3, 4, 0x10, 0x20, 0x40, 0x30, 12345):
+        s = lib.ds_status_string(code)
+        assert isinstance(s, bytes) and s
+    assert lib.ds_version() == 1
+
+
+def test_workspace_queries(lib):
+    assert lib.ds_router_workspace_bytes(1, 1024) >= 4096
+    assert lib.ds_router_workspace_bytes(0, 1024) == 0
+    assert lib.ds_shortlist_workspace_bytes(32, 1024) >= 32 * 4 + 1024 * 4
+    assert lib.ds_head_workspace_bytes(80) > lib.ds_head_workspace_bytes(1)
+    assert lib.ds_verify_workspace_bytes(1, 6, 128256) > 0
+    assert lib.ds_verify_tree_workspace_bytes(8, 6, 10, 128256) >= 8 * 128256 * 4
+    for q in (lib.ds_router_workspace_bytes(3, 40), lib.ds_head_workspace_bytes(7)):
+        assert q % 256 == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)   # never dereferenced: every call below fails its host checks
+
+
+def test_host_argument_checks(lib):
+    budget = (ctypes.c_int32 * 2)(4, 4)
+    bptr = ctypes.cast(budget, ctypes.c_void_p)
+    # router: NULL H; d not a multiple of 8; pos out of the budget table; k > M; no workspace
+    assert lib.ds_router_topk(None, 1, 64, FAKE, FAKE, 64, FAKE, FAKE, 32, 0, bptr, 2, 1,
+                              FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
+    assert lib.ds_router_topk(FAKE, 1, 60, FAKE, FAKE, 64, FAKE, FAKE, 32, 0, bptr, 2, 1,
+                              FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
+    assert lib.ds_router_topk(FAKE, 1, 64, FAKE, FAKE, 64, FAKE, FAKE, 32, 0, bptr, 2, 3,
+                              FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
+    assert lib.ds_router_topk(FAKE, 1, 64, FAKE, FAKE, 64, FAKE, FAKE, 3, 0, bptr, 2, 1,
+                              FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
+    assert lib.ds_router_topk(FAKE, 1, 64, FAKE, FAKE, 64, FAKE, FAKE, 32, 7, bptr, 2, 1,
+                              FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
+    assert lib.ds_router_topk(FAKE, 1, 64, FAKE, FAKE, 64, FAKE, FAKE, 32, 0, bptr, 2, 1,
+                              FAKE, FAKE, None, 0, None, None) == 4
+    # shortlist: only some of the union outputs; k > M
+    assert lib.ds_build_shortlist(FAKE, FAKE, 32, 4096, FAKE, 1, 4, FAKE, FAKE, 4096, FAKE,
+                                  FAKE, None, None, FAKE, 1 << 20, None, None) == 1
+    assert lib.ds_build_shortlist(FAKE, FAKE, 32, 4096, FAKE, 1, 40, FAKE, FAKE, 4096, FAKE,
+                                  None, None, None, FAKE, 1 << 20, None, None) == 1
+    # head: negative temperature; d % 8; union path needs cpos; per-row path needs G == 1
+    args = [FAKE, 1, 1, FAKE, 4096, 256, FAKE, FAKE, None, 0, None, None, None, None,
+            1.0, 0, 1, FAKE, None, None, FAKE, FAKE, FAKE, 1 << 24, None, None]
+    a = list(args); a[14] = -1.0
+    assert lib.ds_gathered_head(*a) == 1
+    a = list(args); a[5] = 250
+    assert lib.ds_gathered_head(*a) == 1
+    a = list(args); a[11] = FAKE; a[12] = FAKE; a[13] = FAKE
+    assert lib.ds_gathered_head(*a) == 1
+    a = list(args); a[2] = 4
+    assert lib.ds_gathered_head(*a) == 2
+    a = list(args); a[23] = 16
+    assert lib.ds_gathered_head(*a) == 4
+    # verify: gamma beyond the limit; NULL uniforms
+    assert lib.ds_verify(FAKE, 1, 40, 4096, 1.0, FAKE, 4096, FAKE, FAKE, 32, FAKE, FAKE, FAKE, FAKE,
+                         FAKE, FAKE, FAKE, 1 << 24, None, None) == 1
+    assert lib.ds_verify(FAKE, 1, 4, 4096, 1.0, FAKE, 4096, FAKE, FAKE, 32, FAKE, FAKE, FAKE, None,
+                         FAKE, FAKE, FAKE, 1 << 24, None, None) == 1
+    assert lib.ds_verify_tree(FAKE, 1, 3, 65, 4096, 1.0, FAKE, FAKE, 4096, FAKE, FAKE, 32, FAKE, FAKE,
+                              FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 24, None, None) == 1
+    assert lib.ds_philox4x32_10(None, 0, FAKE, 4, None) == 1

@@ -1,0 +1,474 @@
+"""Stage-by-stage parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Each stage is fed the oracle's own upstream result, so a stage is checked on its own: the
+shortlist builder gets the oracle's cluster ids, the head gets the oracle's shortlist, the
+verifier gets the oracle's draft logits (rounded to fp32) and tokens.  Tolerances and
+near-tie excuses are the ones in tests/parity.py.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle                          # noqa: E402
+import workloads as wl                 # noqa: E402
+from parity import (assert_close, topk_same_or_excused, token_same_or_excused,  # noqa: E402
+                    softmax_full, q_dense, icdf_acceptable, accept_margin, TIE)
+import gpu_util as gu                  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ds():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from dynamic_vocab_draft_gb300 import build
+    build.build()
+    import dynamic_vocab_draft_gb300 as pkg
+    pkg.load_library()
+    return pkg.api
+
+
+# ---------------------------------------------------------------------------------------
+def test_device_philox_matches_oracle(ds):
+    rng = np.random.default_rng(0)
+    ctr = rng.integers(0, 1 << 32, size=(2048, 4), dtype=np.uint64).astype(np.uint32)
+    for seed in (0, 0x0123456789ABCDEF, 0xFFFFFFFF00000001):
+        out = torch.zeros(2048, 4, dtype=torch.int32, device=gu.dev())
+        ds.philox4x32_10(gu.i32(ctr.view(np.int32)), seed, out)
+        got = out.cpu().numpy().view(np.uint32)
+        key = [seed & 0xFFFFFFFF, seed >> 32]
+        for i in range(0, 2048, 37):
+            assert np.array_equal(got[i], oracle.philox4x32_10(ctr[i], key)), i
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama_b1"])
+def test_vocab_index(ds, name):
+    inp = gu.chain_inputs(name)
+    off, tok = inp["csr_off"], inp["csr_tok"]
+    V = tok.size
+    cof = torch.empty(V, dtype=torch.int32, device=gu.dev())
+    rk = torch.empty(V, dtype=torch.int32, device=gu.dev())
+    st = gu.status()
+    ds.vocab_index(gu.i32(off), gu.i32(tok), cof, rk, st)
+    ref_c = np.empty(V, np.int32)
+    ref_r = np.empty(V, np.int32)
+    for c in range(off.size - 1):
+        ref_c[tok[off[c]:off[c + 1]]] = c
+        ref_r[tok[off[c]:off[c + 1]]] = np.arange(off[c + 1] - off[c])
+    assert np.array_equal(cof.cpu().numpy(), ref_c)
+    assert np.array_equal(rk.cpu().numpy(), ref_r)
+    assert st.item() == 0
+
+
+# ---------------------------------------------------------------------------------------
+@pytest.mark.parametrize("name,B", [("tiny", 1), ("small_batched", 5), ("llama_b1", 1),
+                                    ("batched", 32), ("large_b1_f5", 1)])
+def test_router_topk(ds, name, B):
+    inp = gu.chain_inputs(name)
+    cfg = inp["cfg"]
+    Hrows = inp["H"][:B, 0] if inp["H"].shape[0] >= B else inp["H"][:, 0]
+    B = Hrows.shape[0]
+    scores_ref, _ = oracle.router(Hrows, inp["W1"], inp["b1"], inp["W2"], inp["b2"], cfg.act)
+    scores = torch.empty(B, cfg.M, dtype=torch.float32, device=gu.dev())
+    st = gu.status()
+    ws = ds.workspace(ds.router_workspace_bytes(B, cfg.Hr), gu.dev())
+    for pos in range(1, cfg.gamma + 1):
+        k = cfg.budget[pos - 1]
+        ids = torch.empty(B, k, dtype=torch.int32, device=gu.dev())
+        ds.router_topk(gu.bf16(Hrows), gu.bf16(inp["W1"]), gu.bf16(inp["b1"]), gu.bf16(inp["W2"]),
+                       gu.bf16(inp["b2"]), cfg.act, cfg.budget, pos, scores, ids, ws, st)
+        torch.cuda.synchronize()
+        assert_close(scores.cpu().numpy(), scores_ref, f"{name} router scores")
+        g = ids.cpu().numpy()
+        for b in range(B):
+            assert np.all(np.diff(g[b]) > 0)
+            topk_same_or_excused(g[b], scores_ref[b], k)
+    assert st.item() == 0
+
+
+def test_topk_exact_ties_and_edges(ds):
+    # scores with exact ties: the GPU must break them to the lower id, like the oracle.
+    M, B = 300, 3
+    rng = np.random.default_rng(1)
+    s = (np.round(rng.standard_normal((B, M)) * 4) / 4).astype(np.float32)
+    s[1] = 0.0
+    s[2, ::2] = -0.0                   # -0 and +0 tie
+    d = 8
+    # a router whose output equals the bias: W2 = 0, b2 = scores (exactly representable)
+    b2 = wl.to_bf16_bits(s[0])
+    for b in range(B):
+        b2 = wl.to_bf16_bits(s[b])
+        assert np.array_equal(wl.bf16_bits_to_f32(b2), s[b])
+        for k in (1, 7, 150, M):
+            scores = torch.empty(1, M, dtype=torch.float32, device=gu.dev())
+            ids = torch.empty(1, k, dtype=torch.int32, device=gu.dev())
+            ws = ds.workspace(ds.router_workspace_bytes(1, 8), gu.dev())
+            ds.router_topk(gu.bf16(np.zeros((1, d), np.uint16)), gu.bf16(np.zeros((8, d), np.uint16)),
+                           gu.bf16(np.zeros(8, np.uint16)), gu.bf16(np.zeros((M, 8), np.uint16)),
+                           gu.bf16(b2), "relu", [k], 1, scores, ids, ws, gu.status())
+            ref = oracle.topk(s[b].astype(np.float64), k)[0]
+            assert np.array_equal(ids.cpu().numpy()[0], ref), (b, k)
+
+
+# ---------------------------------------------------------------------------------------
+def _oracle_lists(inp, B, pos):
+    cfg = inp["cfg"]
+    s, _ = oracle.router(inp["H"][:B, pos - 1], inp["W1"], inp["b1"], inp["W2"], inp["b2"], cfg.act)
+    ids = oracle.topk(s, cfg.budget[pos - 1])
+    lists = [oracle.shortlist(inp["csr_off"], inp["csr_tok"], ids[b]) for b in range(B)]
+    return ids, lists
+
+
+def _gpu_shortlist(ds, inp, ids, union=True, cap=None):
+    cfg = inp["cfg"]
+    B, k = ids.shape
+    V, M = cfg.V, cfg.M
+    cap = B * V if cap is None else cap
+    vs_off = torch.zeros(B + 1, dtype=torch.int32, device=gu.dev())
+    vs_ids = torch.full((cap + 64,), -7, dtype=torch.int32, device=gu.dev())
+    cpos = torch.empty(B * M, dtype=torch.int32, device=gu.dev())
+    un = (torch.empty(V, dtype=torch.int32, device=gu.dev()), torch.empty(V, dtype=torch.int32, device=gu.dev()),
+          torch.zeros(1, dtype=torch.int32, device=gu.dev())) if union else (None, None, None)
+    st = gu.status()
+    ws = ds.workspace(ds.shortlist_workspace_bytes(B, M), gu.dev())
+    ds.build_shortlist(gu.i32(inp["csr_off"]), gu.i32(inp["csr_tok"]), gu.i32(ids), vs_off, vs_ids[:cap],
+                       cpos, ws, st, *un)
+    torch.cuda.synchronize()
+    return vs_off, vs_ids, cpos, un, st
+
+
+@pytest.mark.parametrize("name,B", [("tiny", 1), ("small_batched", 5), ("llama_b1", 1), ("batched", 32)])
+def test_shortlist_matches_oracle(ds, name, B):
+    inp = gu.chain_inputs(name)
+    cfg = inp["cfg"]
+    B = min(B, inp["H"].shape[0])
+    ids, lists = _oracle_lists(inp, B, 1)
+    vs_off, vs_ids, cpos, un, st = _gpu_shortlist(ds, inp, ids)
+    assert st.item() == 0
+    off = vs_off.cpu().numpy()
+    got = vs_ids.cpu().numpy()
+    cp = cpos.cpu().numpy().reshape(B, cfg.M)
+    sizes = np.diff(inp["csr_off"])
+    for b in range(B):
+        assert np.array_equal(got[off[b]:off[b + 1]], lists[b])
+        ref_cpos = np.full(cfg.M, -1)
+        run = 0
+        for c in ids[b]:
+            ref_cpos[c] = run
+            run += sizes[c]
+        assert np.array_equal(cp[b], ref_cpos)
+    assert (got[off[B]:] == -7).all()
+    # batch union: clusters selected by any list, ascending, CSR order inside
+    sel = np.unique(ids.ravel())
+    ref_union = oracle.shortlist(inp["csr_off"], inp["csr_tok"], sel.astype(np.int32))
+    n = int(un[2].item())
+    assert n == ref_union.size
+    assert np.array_equal(un[0].cpu().numpy()[:n], ref_union)
+    ucl = un[1].cpu().numpy()[:n]
+    assert np.array_equal(ucl, np.repeat(sel, sizes[sel]))
+
+
+def test_shortlist_all_and_one_cluster(ds):
+    inp = gu.chain_inputs("tiny")
+    M = inp["cfg"].M
+    for k in (M, 1):
+        ids = np.arange(k, dtype=np.int32)[None] + (0 if k == M else 17)
+        vs_off, vs_ids, _, un, st = _gpu_shortlist(ds, inp, ids)
+        ref = oracle.shortlist(inp["csr_off"], inp["csr_tok"], ids[0])
+        assert np.array_equal(vs_ids.cpu().numpy()[:vs_off[1].item()], ref)
+        assert st.item() == 0
+
+
+def test_shortlist_device_errors(ds):
+    inp = gu.chain_inputs("tiny")
+    ids, lists = _oracle_lists(inp, 1, 1)
+    cap = len(lists[0]) - 10
+    vs_off, vs_ids, _, _, st = _gpu_shortlist(ds, inp, ids, union=False, cap=cap)
+    assert st.item() & 0x20                                    # capacity bit
+    assert (vs_ids.cpu().numpy()[cap:] == -7).all()            # nothing written past the capacity
+    bad = ids.copy()
+    bad[0, -1] = inp["cfg"].M + 3
+    _, _, _, _, st = _gpu_shortlist(ds, inp, bad, union=False)
+    assert st.item() & 0x10                                    # bad-index bit
+
+
+# ---------------------------------------------------------------------------------------
+# Gathered head
+# ---------------------------------------------------------------------------------------
+def _run_head(ds, inp, Hrows, G, ids, T, pos, union):
+    """Head on the GPU for lists built from the oracle's cluster ids; returns host arrays."""
+    cfg = inp["cfg"]
+    B = ids.shape[0]
+    vs_off, vs_ids, cpos, un, st = _gpu_shortlist(ds, inp, ids, union=union)
+    cof = torch.empty(cfg.V, dtype=torch.int32, device=gu.dev())
+    rk = torch.empty(cfg.V, dtype=torch.int32, device=gu.dev())
+    ds.vocab_index(gu.i32(inp["csr_off"]), gu.i32(inp["csr_tok"]), cof, rk, st)
+    R = B * G
+    logits = torch.full((B * cfg.V * G,), float("nan"), dtype=torch.float32, device=gu.dev())
+    tok = torch.empty(R, dtype=torch.int32, device=gu.dev())
+    tix = torch.empty(R, dtype=torch.int32, device=gu.dev())
+    rmax = torch.empty(R, dtype=torch.float32, device=gu.dev())
+    rsum = torch.empty(R, dtype=torch.float32, device=gu.dev())
+    ws = ds.workspace(ds.head_workspace_bytes(R), gu.dev())
+    ds.gathered_head(gu.bf16(Hrows), G, gu.device_head(inp), vs_off, vs_ids, T, inp["gumbel_seed"], pos,
+                     logits, tok, tix, ws, st, cpos=cpos, rank_in_cluster=rk,
+                     union=un if union else None, row_max=rmax, row_sumexp=rsum)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return (vs_off.cpu().numpy(), logits.cpu().numpy(), tok.cpu().numpy(), tix.cpu().numpy(),
+            rmax.cpu().numpy(), rsum.cpu().numpy())
+
+
+def _check_head(inp, Hrows, G, ids, T, pos, out, rows_to_check=None):
+    vs_off, logits, tok, tix, rmax, rsum = out
+    B = ids.shape[0]
+    R = B * G
+    for r in (range(R) if rows_to_check is None else rows_to_check):
+        b, g = divmod(r, G)
+        S = oracle.shortlist(inp["csr_off"], inp["csr_tok"], ids[b])
+        n = S.size
+        l_ref = oracle.head(Hrows[r][None], inp["W"], S)[0]
+        base = vs_off[b] * G + g * n
+        assert_close(logits[base:base + n], l_ref, f"head logits row {r}")
+        rtok, ridx, m, s = oracle.draft_sample(l_ref, S, T, inp["gumbel_seed"], pos, r)
+        assert_close([rmax[r]], [m], "row max")
+        np.testing.assert_allclose(rsum[r], s, rtol=2e-3)
+        if token_same_or_excused(int(tix[r]), ridx, l_ref, S, T, inp["gumbel_seed"], pos, r):
+            assert tok[r] == rtok
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 1.0), ("tiny", 0.0), ("small_batched", 0.8),
+                                    ("llama_b1", 1.0), ("llama_b1", 0.0), ("large_b1_f5", 1.0)])
+def test_head_per_row_path(ds, name, T):
+    inp = gu.chain_inputs(name)
+    cfg = inp["cfg"]
+    for pos in (1, cfg.gamma):
+        ids, _ = _oracle_lists(inp, 1, pos)
+        Hrows = inp["H"][:1, pos]
+        out = _run_head(ds, inp, Hrows, 1, ids, T, pos, union=False)
+        _check_head(inp, Hrows, 1, ids, T, pos, out)
+
+
+def test_head_all_clusters_is_dense_head(ds):
+    inp = gu.chain_inputs("small_batched")
+    cfg = inp["cfg"]
+    ids = np.arange(cfg.M, dtype=np.int32)[None]
+    Hrows = inp["H"][:1, 1]
+    vs_off, logits, *_ = _run_head(ds, inp, Hrows, 1, ids, 1.0, 1, union=False)
+    S = oracle.shortlist(inp["csr_off"], inp["csr_tok"], ids[0])
+    dense = wl.bf16_bits_to_f32(Hrows).astype(np.float64) @ wl.bf16_bits_to_f32(inp["W"]).astype(np.float64).T
+    assert_close(logits[:cfg.V], dense[0, S], "dense equivalence")
+
+
+@pytest.mark.parametrize("name,B,G,T", [("small_batched", 5, 1, 0.8), ("small_batched", 5, 1, 0.0),
+                                        ("tiny", 1, 3, 1.0), ("small_batched", 3, 7, 1.0)])
+def test_head_union_path(ds, name, B, G, T):
+    inp = gu.chain_inputs(name)
+    cfg = inp["cfg"]
+    rng = np.random.default_rng(3)
+    for pos in (1, cfg.gamma):
+        ids, _ = _oracle_lists(inp, min(B, inp["H"].shape[0]), pos)
+        if ids.shape[0] < B:
+            ids = np.concatenate([ids, ids[:B - ids.shape[0]]])
+        Hrows = wl.to_bf16_bits(rng.standard_normal((B * G, cfg.d)).astype(np.float32))
+        out = _run_head(ds, inp, Hrows, G, ids, T, pos, union=True)
+        _check_head(inp, Hrows, G, ids, T, pos, out)
+
+
+@pytest.mark.parametrize("G", [1, 10])
+def test_head_union_full_size_sampled(ds, G):
+    # Llama-3-8B shape, 32 lists (G=1, batched chain) or 8 lists x 10 nodes (tree): every
+    # token / statistic row is checked for a sample of rows, logits of those rows in full.
+    inp = gu.chain_inputs("batched")
+    B = 32 if G == 1 else 8
+    ids, _ = _oracle_lists(inp, B, 1)
+    rng = np.random.default_rng(5)
+    Hrows = inp["H"][:B, 1] if G == 1 else wl.to_bf16_bits(rng.standard_normal((B * G, 4096)).astype(np.float32))
+    out = _run_head(ds, inp, Hrows, G, ids, 0.7, 1, union=True)
+    _check_head(inp, Hrows, G, ids, 0.7, 1, out, rows_to_check=[0, 5, B * G // 2, B * G - 1])
+
+
+# ---------------------------------------------------------------------------------------
+# Verification
+# ---------------------------------------------------------------------------------------
+def _host_cpos(inp, ids):
+    sizes = np.diff(inp["csr_off"])
+    M = inp["cfg"].M
+    out = np.full((ids.shape[0], M), -1, np.int32)
+    for b in range(ids.shape[0]):
+        run = 0
+        for c in ids[b]:
+            out[b, c] = run
+            run += sizes[c]
+    return out
+
+
+def _vocab_index_dev(ds, inp):
+    V = inp["cfg"].V
+    cof = torch.empty(V, dtype=torch.int32, device=gu.dev())
+    rk = torch.empty(V, dtype=torch.int32, device=gu.dev())
+    ds.vocab_index(gu.i32(inp["csr_off"]), gu.i32(inp["csr_tok"]), cof, rk, gu.status())
+    return cof, rk
+
+
+def _chain_oracle(inp, B, T):
+    ref = oracle.chain_step(inp, T=T, seqs=range(B), verify=False)
+    return [ref[b]["positions"] for b in range(B)]
+
+
+def _check_chain_verify(ds, inp, pos_rows, z, u, T):
+    """pos_rows[b][t]: oracle per-position dicts. Runs GPU verify on the oracle's draft data
+    and compares with the oracle's verification of the same data."""
+    cfg = inp["cfg"]
+    B, gamma, V, M = len(pos_rows), cfg.gamma, cfg.V, cfg.M
+    cap = B * V
+    q = np.zeros((gamma, cap), np.float32)
+    offs = np.zeros((gamma, B + 1), np.int32)
+    cpos = np.zeros((gamma, B * M), np.int32)
+    draft = np.zeros((gamma, B), np.int32)
+    for t in range(gamma):
+        run = 0
+        ids = np.stack([pos_rows[b][t]["ids"] for b in range(B)])
+        cpos[t] = _host_cpos(inp, ids).ravel()
+        for b in range(B):
+            l = pos_rows[b][t]["logits"]
+            offs[t, b] = run
+            q[t, run:run + l.size] = l.astype(np.float32)
+            run += l.size
+            draft[t, b] = pos_rows[b][t]["token"]
+        offs[t, B] = run
+    # the oracle verifies the same fp32-rounded draft logits
+    acc_ref, corr_ref = oracle.verify_chain(
+        z, [[q[t, offs[t, b]:offs[t, b + 1]].astype(np.float64) for t in range(gamma)] for b in range(B)],
+        [[pos_rows[b][t]["S"] for t in range(gamma)] for b in range(B)],
+        np.array([[pos_rows[b][t]["idx"] for t in range(gamma)] for b in range(B)]), u, T)
+    cof, rk = _vocab_index_dev(ds, inp)
+    acc = torch.empty(B, dtype=torch.int32, device=gu.dev())
+    corr = torch.empty(B, dtype=torch.int32, device=gu.dev())
+    st = gu.status()
+    ws = ds.workspace(ds.verify_workspace_bytes(B, gamma, V), gu.dev())
+    ds.verify(gu.f32(z), T, gu.f32(q), gu.i32(offs), gu.i32(cpos), cof, rk, gu.i32(draft), gu.f32(u),
+              acc, corr, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    acc, corr = acc.cpu().numpy(), corr.cpu().numpy()
+    n_exact = 0
+    for b in range(B):
+        if acc[b] != acc_ref[b]:
+            t = min(acc[b], acc_ref[b])
+            S = pos_rows[b][t]["S"]
+            lq = q[t, offs[t, b]:offs[t, b + 1]]
+            x = draft[t, b]
+            p = softmax_full(z[b, t], T)[x]
+            qq = q_dense(lq, S, T, V)[x]
+            assert T > 0 and accept_margin(p, qq, u[b, t]) < TIE, (b, acc[b], acc_ref[b])
+            continue
+        if corr[b] == corr_ref[b]:
+            n_exact += 1
+            continue
+        assert T > 0, (b, corr[b], corr_ref[b])
+        t = acc[b]
+        p = softmax_full(z[b, t], T)
+        if t < gamma:
+            S = pos_rows[b][t]["S"]
+            w = np.maximum(p - q_dense(q[t, offs[t, b]:offs[t, b + 1]], S, T, V), 0.0)
+            if w.sum() <= 0:
+                w = p
+        else:
+            w = p
+        assert icdf_acceptable(w, float(u[b, gamma]), int(corr[b])), (b, corr[b], corr_ref[b])
+    return acc, acc_ref, n_exact
+
+
+@pytest.mark.parametrize("name,B,T", [("tiny", 1, 1.0), ("small_batched", 5, 0.8), ("small_batched", 5, 0.0),
+                                      ("llama_b1", 1, 1.0)])
+@pytest.mark.parametrize("mode", ["independent", "aligned", "half"])
+def test_verify_chain(ds, name, B, T, mode):
+    inp = gu.chain_inputs(name)
+    cfg = inp["cfg"]
+    rows = _chain_oracle(inp, B, T)
+    z = inp["z"][:B].copy()
+    rng = np.random.default_rng(11)
+    if mode != "independent":
+        # target rows that agree with the draft on the first positions: p ~ q there
+        upto = cfg.gamma if mode == "aligned" else cfg.gamma // 2
+        for b in range(B):
+            for t in range(upto):
+                S, l = rows[b][t]["S"], rows[b][t]["logits"]
+                z[b, t] = -60.0
+                z[b, t, S] = l.astype(np.float32)
+                if T == 0.0:
+                    z[b, t, rows[b][t]["token"]] += 1.0
+    u = inp["u"][:B].copy()
+    if mode == "half":
+        u[:, :] = wl.open_uniforms(rng, u.shape)
+    for trial in range(3):
+        acc, acc_ref, n_exact = _check_chain_verify(ds, inp, rows, z, u, T)
+        u = wl.open_uniforms(rng, u.shape)
+    if mode == "aligned" and T > 0:
+        assert acc_ref.mean() > 0.5 * cfg.gamma           # the accept path is exercised
+
+
+def test_verify_tree(ds):
+    inp = gu.tree_inputs("tiny_tree")
+    cfg = inp["cfg"]
+    B, D, Wd, V, M = cfg.B, cfg.gamma, cfg.width, cfg.V, cfg.M
+    for mode in ("independent", "aligned"):
+        ref = oracle.tree_step(inp, verify=False)
+        z = inp["z"].copy()
+        if mode == "aligned":
+            for b in range(B):
+                for n in range(-1, D * Wd):      # make each node's target row look like its first child's draft row
+                    dep = n // Wd + 1 if n >= 0 else 0
+                    if dep >= D:
+                        continue
+                    kids = [c for c in range(D * Wd) if inp["parent"][c] == n]
+                    if not kids:
+                        continue
+                    c0 = kids[0]
+                    S = ref[b]["depths"][dep]["S"]
+                    l = ref[b]["depths"][dep]["nodes"][c0 % Wd]["logits"]
+                    z[b, n + 1] = -60.0
+                    z[b, n + 1, S] = l.astype(np.float32)
+        N = D * Wd
+        qfp = [[ref[b]["depths"][n // Wd]["nodes"][n % Wd]["logits"].astype(np.float32) for n in range(N)]
+               for b in range(B)]
+        acc_ref, corr_ref, path_ref = oracle.verify_tree(
+            z, inp["parent"], [[ref[b]["depths"][k]["S"] for k in range(D)] for b in range(B)],
+            [[q.astype(np.float64) for q in qfp[b]] for b in range(B)],
+            np.array([[ref[b]["depths"][n // Wd]["nodes"][n % Wd]["idx"] for n in range(N)] for b in range(B)]),
+            inp["u_node"], inp["u_res"], cfg.T)
+        cap = B * V * Wd
+        q = np.zeros((D, cap), np.float32)
+        offs = np.zeros((D, B + 1), np.int32)
+        cpos = np.zeros((D, B * M), np.int32)
+        ntok = np.zeros((D, B * Wd), np.int32)
+        for k in range(D):
+            ids = np.stack([ref[b]["depths"][k]["ids"] for b in range(B)])
+            cpos[k] = _host_cpos(inp, ids).ravel()
+            run = 0
+            for b in range(B):
+                n_b = ref[b]["depths"][k]["S"].size
+                offs[k, b] = run
+                for i in range(Wd):
+                    q[k, run * Wd + i * n_b: run * Wd + (i + 1) * n_b] = qfp[b][k * Wd + i]
+                    ntok[k, b * Wd + i] = ref[b]["depths"][k]["nodes"][i]["token"]
+                run += n_b
+            offs[k, B] = run
+        cof, rk = _vocab_index_dev(ds, inp)
+        acc = torch.empty(B, dtype=torch.int32, device=gu.dev())
+        corr = torch.empty(B, dtype=torch.int32, device=gu.dev())
+        path = torch.empty(B, D, dtype=torch.int32, device=gu.dev())
+        st = gu.status()
+        ws = ds.workspace(ds.verify_tree_workspace_bytes(B, D, Wd, V), gu.dev())
+        ds.verify_tree(gu.f32(z), D, Wd, cfg.T, gu.i32(inp["parent"]), gu.f32(q), gu.i32(offs), gu.i32(cpos),
+                       cof, rk, gu.i32(ntok), gu.f32(inp["u_node"]), gu.f32(inp["u_res"]), acc, corr, path, ws, st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        assert np.array_equal(acc.cpu().numpy(), acc_ref), (mode, acc.cpu().numpy(), acc_ref)
+        assert np.array_equal(path.cpu().numpy(), path_ref)
+        assert np.array_equal(corr.cpu().numpy(), corr_ref), (mode, corr.cpu().numpy(), corr_ref)
+        if mode == "aligned":
+            assert acc_ref.sum() > 0

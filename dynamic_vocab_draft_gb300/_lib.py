@@ -36,6 +36,7 @@ SIGNATURES = {
     "ds_verify_tree": (ST, [P, I, I, I, I, F, P, P, I64, P, P, I, P, P, P, P, P,
                             P, P, P, P, SZ, P, P]),
     "ds_philox4x32_10": (ST, [P, U64, P, I, P]),
+    "ds_event_record": (ST, [P, P]),
 }
 
 _lib = None

@@ -170,3 +170,11 @@ def philox4x32_10(ctr, seed, out, stream=None):
     _lib.check(_lib.load().ds_philox4x32_10(
         _ptr(ctr, (torch.int32, torch.uint32), "ctr"), int(seed) & 0xFFFFFFFFFFFFFFFF,
         _ptr(out, (torch.int32, torch.uint32), "out"), n, _stream(stream)), "ds_philox4x32_10")
+
+
+def event_record(event, stream=None):
+    """Record a torch.cuda.Event so that it is timeable inside a captured CUDA graph.  The
+    event must already exist (torch creates it on its first ordinary record())."""
+    if not event.cuda_event:
+        raise ValueError("event_record: record the event once outside capture first")
+    _lib.check(_lib.load().ds_event_record(event.cuda_event, _stream(stream)), "ds_event_record")

@@ -41,3 +41,14 @@ extern "C" ds_status ds_philox4x32_10(const uint32_t *ctr, uint64_t seed, uint32
     DS_TRY_LAUNCH();
     return DS_OK;
 }
+
+extern "C" ds_status ds_event_record(cudaEvent_t event, cudaStream_t stream)
+{
+    if (!event) return DS_ERR_INVALID_ARG;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return DS_ERR_CUDA;
+    const cudaError_t e = cs == cudaStreamCaptureStatusActive
+                              ? cudaEventRecordWithFlags(event, stream, cudaEventRecordExternal)
+                              : cudaEventRecord(event, stream);
+    return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}

@@ -100,6 +100,21 @@ class ChainDrafter(_Common):
         self.side = torch.cuda.Stream(device=dev)
         self.ready = [torch.cuda.Event() for _ in range(gamma)]
         self.graph = None
+        # optional [(start, end)] timing events around each position's head launch
+        self.head_events = None
+
+    def enable_head_timing(self):
+        """Time every position's head launch with CUDA events (also inside a captured graph).
+        Call before capture(); read with head_times_ms() after a step or replay."""
+        self.head_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                            for _ in range(self.gamma)]
+        for a, b in self.head_events:          # torch creates the CUDA event on its first record
+            a.record()
+            b.record()
+        torch.cuda.synchronize()
+
+    def head_times_ms(self):
+        return [a.elapsed_time(b) for a, b in self.head_events]
 
     def route(self, t, stream=None):
         """Router + top-k + shortlist of draft position t (0-based) for all sequences."""
@@ -132,7 +147,11 @@ class ChainDrafter(_Common):
                 self.ready[t].record(self.side)
         for t in range(self.gamma):
             main.wait_event(self.ready[t])
+            if self.head_events:
+                api.event_record(self.head_events[t][0])
             self.head(t)
+            if self.head_events:
+                api.event_record(self.head_events[t][1])
         self.verify()
 
     def launches_per_step(self) -> int:

@@ -242,6 +242,14 @@ ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd, int V, flo
 ds_status ds_philox4x32_10(const uint32_t *ctr, uint64_t seed, uint32_t *out, int n,
                            cudaStream_t stream);
 
+/* -------------------------------------------------------------------------------------
+ * ds_event_record -- measurement helper (no counterpart in the method): records `event` on
+ * `stream` as an external event, so that a CUDA event placed between two launches while the
+ * stream is being captured into a graph becomes a real event-record node and can be timed
+ * after each replay.  Outside capture it is a plain event record.
+ * ------------------------------------------------------------------------------------- */
+ds_status ds_event_record(cudaEvent_t event, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -479,3 +479,66 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
     DS_TRY_LAUNCH();
     return DS_OK;
 }
+
+// ---------------------------------------------------------------------------------------
+// ds_gathered_head_noalloc: the same head for callers that cannot give the library any
+// scratch memory.  The cross-block partials and completion counters live in one file-scope
+// device array of fixed size instead of a caller workspace.
+// ---------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr int kNoAllocMaxRows = 32;
+constexpr size_t kNoAllocBytes = 256 + size_t(kNoAllocMaxRows) * kHeadPartialsPerRow * sizeof(Stat);
+static_assert(256 >= kNoAllocMaxRows * sizeof(unsigned), "counter block");
+
+// Held by every GPU that loads the library, for the life of the process.
+static __device__ __align__(256) unsigned char g_head_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_addr[kNoAllocMaxDevices];
+
+// Device address of the scratch array on the current device, looked up once per device.
+// (In host code the array's name is only a host-side stand-in, not a device address.)
+ds_status noalloc_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DS_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return DS_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_head_noalloc_scratch) != cudaSuccess || !p) return DS_ERR_CUDA;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return DS_OK;
+}
+
+}  // namespace
+
+extern "C" ds_status ds_gathered_head_noalloc(const uint16_t *H, int B, int G,
+                                              const uint16_t *W, int V, int d,
+                                              const int32_t *vs_offsets, const int32_t *vs_ids,
+                                              const int32_t *cpos, int M, const int32_t *rank_in_cluster,
+                                              const int32_t *union_ids, const int32_t *union_cluster,
+                                              const int32_t *union_count,
+                                              float T, uint64_t seed, int pos,
+                                              float *logits, float *row_max, float *row_sumexp,
+                                              int32_t *token, int32_t *token_idx,
+                                              int32_t *dev_status, cudaStream_t stream)
+{
+    if (B < 1 || G < 1) return DS_ERR_INVALID_ARG;
+    if (1LL * B * G > kNoAllocMaxRows) return DS_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    const ds_status st = noalloc_scratch(&scratch);
+    if (st != DS_OK) return st;
+    // The counters must start at zero; the array keeps whatever the previous call left.
+    if (cudaMemsetAsync(scratch, 0, 256, stream) != cudaSuccess) return DS_ERR_CUDA;
+    return ds_gathered_head(H, B, G, W, V, d, vs_offsets, vs_ids, cpos, M, rank_in_cluster,
+                            union_ids, union_cluster, union_count, T, seed, pos,
+                            logits, row_max, row_sumexp, token, token_idx,
+                            scratch, kNoAllocBytes, dev_status, stream);
+}

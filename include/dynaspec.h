@@ -170,6 +170,33 @@ ds_status ds_gathered_head(const uint16_t *H, int B, int G,
                            void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
+ * ds_gathered_head_noalloc -- ds_gathered_head without a workspace argument.  The DynaSpec
+ * pages have no counterpart; this entry exists for callers that cannot hand the library any
+ * device memory of its own: code whose device memory is owned by a pool or framework that
+ * may not be grown in the middle of a step, or a plugin interface that passes only inputs
+ * and outputs.  Inputs, outputs, layouts and results are those of ds_gathered_head.
+ *   - Scratch is a fixed device array inside the library (about 640 KB), reserved on every
+ *     GPU that loads the library until the process exits.  No call allocates or frees.
+ *   - At most 32 head rows (B*G <= 32); larger calls return DS_ERR_UNSUPPORTED and launch
+ *     nothing.
+ *   - The first call on a device looks the array's device address up for that device
+ *     (with that device current); make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents; each call clears
+ *     the counters it needs on `stream` before launching.  Calls that overlap on the GPU (on
+ *     different streams, or from several host threads) race on the array: serialise them.
+ * ------------------------------------------------------------------------------------- */
+ds_status ds_gathered_head_noalloc(const uint16_t *H, int B, int G,
+                                   const uint16_t *W, int V, int d,
+                                   const int32_t *vs_offsets, const int32_t *vs_ids,
+                                   const int32_t *cpos, int M, const int32_t *rank_in_cluster,
+                                   const int32_t *union_ids, const int32_t *union_cluster,
+                                   const int32_t *union_count,
+                                   float T, uint64_t seed, int pos,
+                                   float *logits, float *row_max, float *row_sumexp,
+                                   int32_t *token, int32_t *token_idx,
+                                   int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
  * ds_verify -- rejection-sampling verification over the full vocabulary (abstract: "the
  * target model still verifies over the full vocabulary, preserving exactness"; summary,
  * Pipeline Flow "Rejection Sampling Verification").  The pages cite Leviathan et al. and

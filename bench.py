@@ -249,6 +249,7 @@ def run_ours(args):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     head_ms = []
+    breakdown = []                           # (router before the first head, heads span, verify) ms
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -263,6 +264,8 @@ def run_ours(args):
         if i % 16 == 15 or i == K - 1:      # head timings are overwritten by the next replay
             torch.cuda.synchronize()
             head_ms.append(d.head_times_ms())
+            h0, hl = d.head_events[0][0], d.head_events[-1][1]
+            breakdown.append((starts[i].elapsed_time(h0), h0.elapsed_time(hl), hl.elapsed_time(ends[i])))
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()
@@ -317,7 +320,7 @@ def run_ours(args):
         achieved = float(head_bytes.sum() / (hm.mean(axis=0).sum() * 1e-3) / 1e9)
         traffic = committed_traffic()
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic, "kernel": "head_gemv_kernel (gathered head, per-row path)",
+                "traffic": traffic, "kernel": "head_gemv_kernel (gathered head, per-row path, software-pipelined 16-byte loads)",
                 "algorithmic_bytes_per_launch": float(head_bytes.mean()),
                 "avg_launch_us": float(hm.mean() * 1e3), "peak_source": peak_src,
                 "shortlist_sizes": sizes.tolist()}
@@ -348,6 +351,12 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": Ke, "ms_per_step": e2e_ms / Ke},
+            "breakdown_us": {
+                "before_first_head": 1e3 * float(np.median([x[0] for x in breakdown])),
+                "heads_span": 1e3 * float(np.median([x[1] for x in breakdown])),
+                "heads_busy": 1e3 * float(np.median(hm.sum(axis=1))),
+                "after_last_head (verify)": 1e3 * float(np.median([x[2] for x in breakdown])),
+                "per_position_head": [1e3 * float(x) for x in np.median(hm, axis=0)]},
             "gpu_launches": d.launches_per_step() * K,
             "clocks": clk,
             "wall_s_timed_region": t_wall,

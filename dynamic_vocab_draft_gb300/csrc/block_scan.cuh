@@ -38,4 +38,18 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T *scratch, T *total)
     return res;
 }
 
+// Cumulative boundaries for an inverse-CDF search over per-thread masses v >= 0: buf[t] is the
+// exclusive prefix of thread t (parallel scan, fixed order) and buf[blockDim.x] the total.
+// Thread t's interval is [buf[t], buf[t+1]); read both ends from buf.  Consecutive intervals
+// cover [0, total) even where rounding makes the sequence dip, so a target in range falls in at
+// least one of them; take the lowest such thread.  buf holds blockDim.x + 1 floats; scratch 33.
+__device__ __forceinline__ void block_cdf_bounds(float v, float *buf, float *scratch)
+{
+    float tot;
+    const float ex = block_exclusive_scan(v, scratch, &tot);
+    buf[threadIdx.x] = ex;
+    if (threadIdx.x == 0) buf[blockDim.x] = tot;
+    __syncthreads();
+}
+
 }  // namespace ds

@@ -179,6 +179,74 @@ __device__ __forceinline__ bool last_block_done(unsigned *counter, unsigned nblo
     return is_last;
 }
 
+// ---------------------------------------------------------------------------------------
+// mbarrier + bulk-copy (TMA engine) primitives.  Every wait is bounded: a wait that runs
+// past its budget returns false and the caller records DS_DEV_TIMEOUT and winds down.
+// ---------------------------------------------------------------------------------------
+constexpr long long kWaitBudgetCycles = 2000000000LL;    // about one second at 2 GHz
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return done != 0;
+}
+
+// Wait until the phase with the given parity has completed; false after the budget.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity)
+{
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity))
+        if (clock64() - t0 > kWaitBudgetCycles) return false;
+    return true;
+}
+
+// Same, but gives up at an absolute clock64() deadline (one budget shared by several waits).
+__device__ __forceinline__ bool mbar_wait_until(uint64_t *bar, unsigned parity, long long deadline)
+{
+    while (!mbar_test(bar, parity))
+        if (clock64() > deadline) return false;
+    return true;
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) global -> shared,
+// completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, unsigned bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
 }  // namespace ds
 
 // ---------------------------------------------------------------------------------------

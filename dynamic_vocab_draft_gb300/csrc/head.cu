@@ -35,8 +35,8 @@ int num_sms()
 // ---------------------------------------------------------------------------------------
 // Per-row gathered GEMV
 // ---------------------------------------------------------------------------------------
-constexpr int kGvWarps = 8;
-constexpr int kGvU = 16;               // 16-byte loads in flight per lane (one 8 KB row at d = 4096)
+constexpr int kGvWarps = 16;           // one 512-thread block per SM
+constexpr int kHeadSideSms = 8;        // SMs a batch-1 head leaves to the side stream
 constexpr int kGvMaxD = 16384;
 constexpr int kGvMaxBlocks = 1024;     // per list; bounds the partials in the workspace
 
@@ -61,8 +61,48 @@ __device__ __forceinline__ void write_row(const HeadArgs &a, int r, const Stat &
     a.token_idx[r] = s.j;
 }
 
-// grid (gx, B): block (x, b) handles rows j = x*8 + warp, step gx*8, of list b.
-__global__ void __launch_bounds__(kGvWarps * 32, 2)
+// Rows are streamed in groups of kGvG 16-byte loads per lane (4 KB of a row per warp at a
+// time).  The loads of the warp's next group -- the second half of the row, or the first half
+// of its next row -- are issued before the current group is multiplied, so every warp keeps
+// 4-8 KB in flight while it computes; 16 warps per SM hold ~100 KB in flight.  The id of the
+// warp's next row is prefetched one row ahead.
+//
+// grid (gx, B): block (x, b) handles rows j = x*16 + warp, step gx*16, of list b.
+constexpr int kGvG = 8;                // loads per lane per group (256 bf16 per load round)
+
+__device__ __forceinline__ void load_group(uint4 (&buf)[kGvG], const uint16_t *W, int v, int d, int k0, int lane)
+{
+    const uint4 *row = reinterpret_cast<const uint4 *>(W + size_t(v) * d);
+#pragma unroll
+    for (int u = 0; u < kGvG; ++u) {
+        const int k = k0 + (u * 32 + lane) * 8;
+        buf[u] = k < d ? ld_stream(row + (k >> 3)) : make_uint4(0, 0, 0, 0);
+    }
+}
+
+__device__ __forceinline__ void dot_group(const uint4 (&buf)[kGvG], const float *hs, int d, int k0, int lane,
+                                          float &a0, float &a1)
+{
+#pragma unroll
+    for (int u = 0; u < kGvG; ++u) {
+        const int k = k0 + (u * 32 + lane) * 8;
+        if (k < d) {
+            const float4 *xv = reinterpret_cast<const float4 *>(hs + k);
+            const float4 x0 = xv[0], x1 = xv[1];
+            const uint4 w = buf[u];
+            a0 = fmaf(bf16lo(w.x), x0.x, a0);
+            a1 = fmaf(bf16hi(w.x), x0.y, a1);
+            a0 = fmaf(bf16lo(w.y), x0.z, a0);
+            a1 = fmaf(bf16hi(w.y), x0.w, a1);
+            a0 = fmaf(bf16lo(w.z), x1.x, a0);
+            a1 = fmaf(bf16hi(w.z), x1.y, a1);
+            a0 = fmaf(bf16lo(w.w), x1.z, a0);
+            a1 = fmaf(bf16hi(w.w), x1.w, a1);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kGvWarps * 32, 1)
 head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__ counters)
 {
     extern __shared__ float4 hs4[];
@@ -79,40 +119,54 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
     const int n = a.vs_offsets[b + 1] - base;
     const int32_t *ids = a.vs_ids + base;
     float *lout = a.logits + base;
+    const int stride = gridDim.x * kGvWarps;
+    const int ngroups = (d + kGvG * 256 - 1) / (kGvG * 256);     // groups per row
     Stat st = stat_empty();
 
-    for (int j = blockIdx.x * kGvWarps + warp; j < n; j += gridDim.x * kGvWarps) {
-        const int v = ids[j];
-        if (v < 0 || v >= a.V) {
-            if (lane == 0) { set_status(a.status, DS_DEV_BAD_INDEX); lout[j] = 0.f; }
-            continue;
-        }
-        const uint4 *row = reinterpret_cast<const uint4 *>(a.W + size_t(v) * d);
-        float acc = 0.f;
-        float g = 0.f;
-        for (int k0 = 0; k0 < d; k0 += kGvU * 256) {
-            uint4 w[kGvU];
-#pragma unroll
-            for (int u = 0; u < kGvU; ++u) {
-                const int k = k0 + u * 256 + lane * 8;
-                w[u] = k < d ? ld_stream(row + (k >> 3)) : make_uint4(0, 0, 0, 0);
-            }
-            // the row's Gumbel noise is computed while its loads are in flight
-            if (k0 == 0 && a.T > 0.f && lane == 0) g = gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(b));
-#pragma unroll
-            for (int u = 0; u < kGvU; ++u) {
-                const int k = k0 + u * 256 + lane * 8;
-                if (k < d) {
-                    const float4 *xv = reinterpret_cast<const float4 *>(hs + k);
-                    acc = dot8(w[u], xv[0], xv[1], acc);
+    int j = blockIdx.x * kGvWarps + warp;
+    if (j < n) {
+        auto safe = [&](int v) { return (v >= 0 && v < a.V) ? v : 0; };
+        int v = ids[j];
+        int jn = j + stride;
+        int vn = jn < n ? ids[jn] : 0;                              // next row's id, one row ahead
+        uint4 cur[kGvG], nxt[kGvG];
+        load_group(cur, a.W, safe(v), d, 0, lane);
+        int g = 0;
+        float a0 = 0.f, a1 = 0.f;
+        float gum = 0.f;
+        if (a.T > 0.f && lane == 0 && v >= 0 && v < a.V) gum = gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(b));
+        for (;;) {
+            // issue the next group's loads before multiplying the current one
+            const bool more_in_row = g + 1 < ngroups;
+            const bool have_next = more_in_row || jn < n;
+            if (more_in_row) load_group(nxt, a.W, safe(v), d, (g + 1) * kGvG * 256, lane);
+            else if (jn < n) load_group(nxt, a.W, safe(vn), d, 0, lane);
+            dot_group(cur, hs, d, g * kGvG * 256, lane, a0, a1);
+            if (!more_in_row) {
+                const float acc = warp_sum(a0 + a1);
+                if (lane == 0) {
+                    if (v < 0 || v >= a.V) {
+                        set_status(a.status, DS_DEV_BAD_INDEX);
+                        lout[j] = 0.f;
+                    } else {
+                        lout[j] = acc;
+                        const float x = acc * a.inv_te;
+                        stat_add(st, x, a.T > 0.f ? x + gum : acc, v, j);
+                    }
                 }
+                a0 = a1 = 0.f;
+                if (jn >= n) break;
+                j = jn; v = vn;
+                jn = j + stride;
+                vn = jn < n ? ids[jn] : 0;
+                g = 0;
+                if (a.T > 0.f && lane == 0 && v >= 0 && v < a.V) gum = gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(b));
+            } else {
+                ++g;
             }
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) {
-            lout[j] = acc;
-            const float x = acc * a.inv_te;
-            stat_add(st, x, a.T > 0.f ? x + g : acc, v, j);
+            if (!have_next) break;
+#pragma unroll
+            for (int u = 0; u < kGvG; ++u) cur[u] = nxt[u];
         }
     }
     if (lane == 0) warp_stat[warp] = st;
@@ -445,7 +499,9 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
 
     if (nu == 0) {
         if (G != 1) return DS_ERR_UNSUPPORTED;
-        int gx = (2 * num_sms() + B - 1) / B;
+        // One 512-thread block per SM.  At batch 1 a few SMs are left to the side stream, so the
+        // next position's router and shortlist build run while this head streams W.
+        int gx = B == 1 ? num_sms() - kHeadSideSms : (num_sms() + B - 1) / B;
         if (gx < 1) gx = 1;
         if (gx > kGvMaxBlocks) gx = kGvMaxBlocks;
         const size_t smem = size_t(d) * sizeof(float);

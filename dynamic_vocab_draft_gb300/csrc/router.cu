@@ -18,8 +18,8 @@ namespace ds {
 namespace {
 
 constexpr int kGemvWarps = 8;          // rows per block
-constexpr int kGemvU = 8;              // 16-byte loads in flight per lane per pass
-constexpr int kGemvBT = 4;             // hidden states per block
+constexpr int kGemvU = 16;             // 16-byte loads in flight per lane per pass
+constexpr int kGemvBT = 4;             // hidden states per block (batched); 1 at batch 1
 constexpr int kRouterMaxK = 8192;      // inner dimension the staging buffer allows
 
 __device__ __forceinline__ float act_fn(float x, int act)
@@ -34,17 +34,17 @@ template <> __device__ __forceinline__ float load_x<uint16_t>(const uint16_t *p)
 template <> __device__ __forceinline__ float load_x<float>(const float *p) { return *p; }
 
 // y[b][i] = act(sum_k A[i][k] x[b][k] + bias[i]) for i < N, b < B.
-//   grid.x = ceil(N / kGemvWarps), grid.y = ceil(B / kGemvBT); dynamic smem = BT*K floats.
-template <typename XT>
+//   grid.x = ceil(N / kGemvWarps), grid.y = ceil(B / BT); dynamic smem = BT*K floats.
+template <typename XT, int BT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
 gemv_rows_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict__ x, int B,
                  const uint16_t *__restrict__ bias, int act, float *__restrict__ y)
 {
     extern __shared__ float4 xs4[];
     float *xs = reinterpret_cast<float *>(xs4);
-    const int b0 = blockIdx.y * kGemvBT;
-    const int nb = min(kGemvBT, B - b0);
-    for (int e = threadIdx.x; e < kGemvBT * K; e += blockDim.x) {
+    const int b0 = blockIdx.y * BT;
+    const int nb = min(BT, B - b0);
+    for (int e = threadIdx.x; e < BT * K; e += blockDim.x) {
         const int bt = e / K, k = e - bt * K;
         xs[e] = bt < nb ? load_x<XT>(x + size_t(b0 + bt) * K + k) : 0.f;
     }
@@ -54,9 +54,9 @@ gemv_rows_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restr
     const int i = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
     if (i >= N) return;
     const uint4 *row = reinterpret_cast<const uint4 *>(A + size_t(i) * K);
-    float acc[kGemvBT];
+    float acc[BT];
 #pragma unroll
-    for (int bt = 0; bt < kGemvBT; ++bt) acc[bt] = 0.f;
+    for (int bt = 0; bt < BT; ++bt) acc[bt] = 0.f;
 
     for (int k0 = 0; k0 < K; k0 += kGemvU * 256) {
         uint4 w[kGemvU];
@@ -70,7 +70,7 @@ gemv_rows_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restr
             const int k = k0 + u * 256 + lane * 8;
             if (k < K) {
 #pragma unroll
-                for (int bt = 0; bt < kGemvBT; ++bt) {
+                for (int bt = 0; bt < BT; ++bt) {
                     const float4 *xv = reinterpret_cast<const float4 *>(xs + bt * K + k);
                     acc[bt] = dot8(w[u], xv[0], xv[1], acc[bt]);
                 }
@@ -78,11 +78,11 @@ gemv_rows_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restr
         }
     }
 #pragma unroll
-    for (int bt = 0; bt < kGemvBT; ++bt) acc[bt] = warp_sum(acc[bt]);
+    for (int bt = 0; bt < BT; ++bt) acc[bt] = warp_sum(acc[bt]);
     if (lane < nb) {
         float a = acc[0];
 #pragma unroll
-        for (int bt = 1; bt < kGemvBT; ++bt) if (lane == bt) a = acc[bt];
+        for (int bt = 1; bt < BT; ++bt) if (lane == bt) a = acc[bt];
         y[size_t(b0 + lane) * N + i] = act_fn(a + bf16_to_f32(bias[i]), act);
     }
 }
@@ -95,7 +95,7 @@ __device__ __forceinline__ uint32_t order_key(float f)
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 256;
 constexpr int kTopkPerThread = kRouterMaxK / kTopkThreads;
 
 // One block per row: keep the k largest of scores[b][0..M), ties to the lower index, and
@@ -123,10 +123,16 @@ topk_kernel(const float *__restrict__ scores, int M, int k, int32_t *__restrict_
         if (threadIdx.x < 256) hist[threadIdx.x] = 0u;
         __syncthreads();
         const uint32_t prefix = s_prefix;
+        // Scores cluster in a few exponent bytes, so lanes with the same digit are combined
+        // first (one shared-memory atomic per distinct digit per warp).
 #pragma unroll
-        for (int e = 0; e < kTopkPerThread; ++e)
-            if (e < E && lo + e < M && (key[e] & mask) == prefix)
-                atomicAdd(&hist[(key[e] >> shift) & 255u], 1u);
+        for (int e = 0; e < kTopkPerThread; ++e) {
+            if (e >= E) break;                               // E is uniform across the block
+            const bool in = lo + e < M && (key[e] & mask) == prefix;
+            const unsigned digit = in ? (key[e] >> shift) & 255u : 256u;
+            const unsigned same = __match_any_sync(0xFFFFFFFFu, digit);
+            if (in && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&hist[digit], unsigned(__popc(same)));
+        }
         __syncthreads();
         if (threadIdx.x < 32) {
             // bins from the top: lane l owns digits 255-8l .. 248-8l
@@ -186,6 +192,24 @@ topk_kernel(const float *__restrict__ scores, int M, int k, int32_t *__restrict_
         if (sel[e] && out < k) dst[out++] = lo + e;
 }
 
+template <typename XT, int BT>
+ds_status launch_gemv(const uint16_t *A, int N, int K, const XT *x, int B, const uint16_t *bias, int act,
+                      float *y, cudaStream_t stream)
+{
+    const size_t smem = size_t(BT) * K * sizeof(float);
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(gemv_rows_kernel<XT, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(size_t(BT) * kRouterMaxK * sizeof(float))) != cudaSuccess)
+            return DS_ERR_CUDA;
+        attr = true;
+    }
+    dim3 grid((N + kGemvWarps - 1) / kGemvWarps, (B + BT - 1) / BT);
+    gemv_rows_kernel<XT, BT><<<grid, kGemvWarps * 32, smem, stream>>>(A, N, K, x, B, bias, act, y);
+    DS_TRY_LAUNCH();
+    return DS_OK;
+}
+
 }  // namespace
 }  // namespace ds
 
@@ -219,27 +243,12 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
     if (!ws || ws_bytes < ds_router_workspace_bytes(B, Hr)) return DS_ERR_WORKSPACE;
 
     float *u = static_cast<float *>(ws);
-    const int by = (B + kGemvBT - 1) / kGemvBT;
-    {
-        const size_t smem = size_t(kGemvBT) * d * sizeof(float);
-        if (smem > 48 * 1024 &&
-            cudaFuncSetAttribute(gemv_rows_kernel<uint16_t>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-            return DS_ERR_CUDA;
-        dim3 grid((Hr + kGemvWarps - 1) / kGemvWarps, by);
-        gemv_rows_kernel<uint16_t><<<grid, kGemvWarps * 32, smem, stream>>>(W1, Hr, d, H, B, b1, act, u);
-        DS_TRY_LAUNCH();
-    }
-    {
-        const size_t smem = size_t(kGemvBT) * Hr * sizeof(float);
-        if (smem > 48 * 1024 &&
-            cudaFuncSetAttribute(gemv_rows_kernel<float>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-            return DS_ERR_CUDA;
-        dim3 grid((M + kGemvWarps - 1) / kGemvWarps, by);
-        gemv_rows_kernel<float><<<grid, kGemvWarps * 32, smem, stream>>>(W2, M, Hr, u, B, b2, -1, scores);
-        DS_TRY_LAUNCH();
-    }
+    const ds_status s1 = B == 1 ? launch_gemv<uint16_t, 1>(W1, Hr, d, H, B, b1, act, u, stream)
+                                : launch_gemv<uint16_t, kGemvBT>(W1, Hr, d, H, B, b1, act, u, stream);
+    if (s1 != DS_OK) return s1;
+    const ds_status s2 = B == 1 ? launch_gemv<float, 1>(W2, M, Hr, u, B, b2, -1, scores, stream)
+                                : launch_gemv<float, kGemvBT>(W2, M, Hr, u, B, b2, -1, scores, stream);
+    if (s2 != DS_OK) return s2;
     topk_kernel<<<B, kTopkThreads, 0, stream>>>(scores, M, k, cluster_ids);
     DS_TRY_LAUNCH();
     return DS_OK;

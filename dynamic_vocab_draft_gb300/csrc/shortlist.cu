@@ -157,6 +157,52 @@ __global__ void union_expand_kernel(const int32_t *__restrict__ off, const int32
     }
 }
 
+// One list, no union: the scan and the offsets in a single block (the offsets kernel of the
+// batched path would be a launch with nothing to do); the expansion stays a wide kernel.
+__global__ void __launch_bounds__(kSlThreads)
+shortlist_single_scan_kernel(const int32_t *__restrict__ off, int M, int V, const int32_t *__restrict__ ids,
+                             int k, int32_t *__restrict__ cpos, int32_t *__restrict__ vs_offsets,
+                             int64_t capacity, int32_t *st)
+{
+    __shared__ unsigned char flag[kSlMaxM];
+    __shared__ int scratch[33];
+    for (int c = threadIdx.x; c < M; c += blockDim.x) flag[c] = 0;
+    __syncthreads();
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+        const int c = ids[j];
+        if (c < 0 || c >= M || (j > 0 && ids[j - 1] >= c)) { set_status(st, DS_DEV_BAD_INDEX); continue; }
+        flag[c] = 1;
+    }
+    __syncthreads();
+    const int E = (M + kSlThreads - 1) / kSlThreads;
+    const int lo = threadIdx.x * E;
+    int sz[kSlMaxPer];
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < kSlMaxPer; ++e) {
+        const int c = lo + e;
+        int n = 0;
+        if (e < E && c < M && flag[c]) {
+            n = off[c + 1] - off[c];
+            if (off[c] < 0 || n < 0 || off[c + 1] > V) { set_status(st, DS_DEV_BAD_INDEX); n = 0; }
+        }
+        sz[e] = n;
+        sum += n;
+    }
+    int tot;
+    int run = block_exclusive_scan(sum, scratch, &tot);
+#pragma unroll
+    for (int e = 0; e < kSlMaxPer; ++e) {
+        const int c = lo + e;
+        if (e < E && c < M) { cpos[c] = flag[c] ? run : -1; run += sz[e]; }
+    }
+    if (threadIdx.x == 0) {
+        vs_offsets[0] = 0;
+        vs_offsets[1] = tot;
+        if (int64_t(tot) > capacity) set_status(st, DS_DEV_CAPACITY);
+    }
+}
+
 }  // namespace
 }  // namespace ds
 
@@ -198,6 +244,15 @@ extern "C" ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *c
     int32_t *sizes = static_cast<int32_t *>(ws);
     int32_t *ustart = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + align256(size_t(B) * 4));
 
+    if (B == 1 && nu == 0) {
+        shortlist_single_scan_kernel<<<1, kSlThreads, 0, stream>>>(csr_off, M, V, cluster_ids, k, cpos,
+                                                                   vs_offsets, vs_capacity, dev_status);
+        DS_TRY_LAUNCH();
+        shortlist_expand_kernel<<<dim3((k + 7) / 8, 1), 256, 0, stream>>>(csr_off, csr_tok, M, V, cluster_ids, k,
+                                                                         cpos, vs_offsets, vs_ids, vs_capacity);
+        DS_TRY_LAUNCH();
+        return DS_OK;
+    }
     shortlist_scan_kernel<<<B, kSlThreads, 0, stream>>>(csr_off, M, cluster_ids, k, cpos, sizes, dev_status);
     DS_TRY_LAUNCH();
     shortlist_offsets_kernel<<<1, kSlThreads, 0, stream>>>(csr_off, M, B, sizes, cpos, vs_offsets, vs_capacity,

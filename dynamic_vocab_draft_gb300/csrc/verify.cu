@@ -27,8 +27,8 @@ namespace ds {
 namespace {
 
 constexpr int kVThreads = 256;
-constexpr int kVPer = 32;                        // elements per thread per chunk
-constexpr int kVChunk = kVThreads * kVPer;       // 8192
+constexpr int kVPer = 8;                         // elements per thread per chunk
+constexpr int kVChunk = kVThreads * kVPer;       // 2048
 constexpr int kMaxGamma = 32;
 
 struct PStat { float m, s, amax; int aid; };   // target-row chunk: max, sum-exp, argmax
@@ -288,16 +288,17 @@ __global__ void __launch_bounds__(kVThreads)
 verify_residual_kernel(ChainArgs a)
 {
     __shared__ float scratch[kVThreads / 32];
-    __shared__ int s_chunk, s_use_p;
+    __shared__ float sbuf[kVThreads + 1];
+    __shared__ float fscan[33];
+    __shared__ int s_chunk, s_use_p, s_hit, s_last;
     __shared__ float s_target;
-    __shared__ int s_scan[33];
-    __shared__ int s_hit;
     const int b = blockIdx.y, c = blockIdx.x;
     const int tr = __ldcg(&a.decision[b]);
     if (tr < 0) return;                              // greedy: decided already (whole group returns)
     const ResidualRow rr = residual_row(a, b, tr);
     const int base = c * kVChunk + threadIdx.x * kVPer;
     float rs = 0.f, psum = 0.f;
+#pragma unroll
     for (int i = 0; i < kVPer; ++i) {
         const int v = base + i;
         if (v < a.V) { float r, p; residual_weight(a, rr, v, r, p); rs += r; psum += p; }
@@ -307,37 +308,61 @@ verify_residual_kernel(ChainArgs a)
     if (threadIdx.x == 0) { a.rsum[size_t(b) * a.nch + c] = rs; a.psum[size_t(b) * a.nch + c] = psum; }
     if (!last_block_done(&a.cnt2[b], unsigned(a.nch))) return;
 
-    // Locate the chunk where the cumulative mass first exceeds u * total (chunks in order).
+    // Locate the chunk where the cumulative mass first exceeds u * total: thread t sums a
+    // contiguous run of chunk masses, the runs are scanned in thread order, and the thread
+    // whose run crosses walks it.  A residual without mass falls back to p.
     const float u = a.u[size_t(b) * (a.gamma + 1) + a.gamma];
-    if (threadIdx.x == 0) {
-        float tot = 0.f;
-        for (int i = 0; i < a.nch; ++i) tot += __ldcg(&a.rsum[size_t(b) * a.nch + i]);
-        const int use_p = !(tot > 0.f);
-        const float *w = use_p ? a.psum : a.rsum;
-        if (use_p) { tot = 0.f; for (int i = 0; i < a.nch; ++i) tot += __ldcg(&w[size_t(b) * a.nch + i]); }
-        const float target = u * tot;
-        float cum = 0.f;
+    const int E = (a.nch + kVThreads - 1) / kVThreads;
+    const int c0 = threadIdx.x * E, c1 = min(a.nch, c0 + E);
+    float rrun = 0.f, prun = 0.f;
+    for (int i = c0; i < c1; ++i) {
+        rrun += __ldcg(&a.rsum[size_t(b) * a.nch + i]);
+        prun += __ldcg(&a.psum[size_t(b) * a.nch + i]);
+    }
+    block_cdf_bounds(rrun, sbuf, fscan);
+    const float rtot = sbuf[kVThreads];
+    const int use_p = !(rtot > 0.f);
+    if (use_p) block_cdf_bounds(prun, sbuf, fscan);
+    const float *w = use_p ? a.psum : a.rsum;
+    const float target = u * sbuf[kVThreads];
+    const float lo_b = sbuf[threadIdx.x], hi_b = sbuf[threadIdx.x + 1];
+    if (threadIdx.x == 0) { s_hit = 0x7FFFFFFF; s_last = -1; }
+    __syncthreads();
+    if (lo_b <= target && target < hi_b) atomicMin(&s_hit, threadIdx.x);
+    int lastc = -1;
+    for (int i = c0; i < c1; ++i) if (__ldcg(&w[size_t(b) * a.nch + i]) > 0.f) lastc = i;
+    if (lastc >= 0) atomicMax(&s_last, lastc);
+    __syncthreads();
+    if (int(threadIdx.x) == s_hit) {               // the first claimant walks its run of chunks
+        float cum = lo_b;
         int ch = -1;
-        for (int i = 0; i < a.nch; ++i) {
+        for (int i = c0; i < c1; ++i) {
             const float wi = __ldcg(&w[size_t(b) * a.nch + i]);
             if (cum + wi > target) { ch = i; break; }
             cum += wi;
         }
-        if (ch < 0) {                                // rounding: the last chunk with mass
-            for (int i = a.nch - 1; i >= 0; --i) if (__ldcg(&w[size_t(b) * a.nch + i]) > 0.f) { ch = i; break; }
-            s_target = INFINITY;                      // -> the chunk's last positive token
+        if (ch < 0) {                               // rounding inside the run: its last chunk with mass
+            for (int i = c1 - 1; i >= c0; --i) if (__ldcg(&w[size_t(b) * a.nch + i]) > 0.f) { ch = i; break; }
+            s_target = INFINITY;
         } else {
             s_target = target - cum;
         }
-        s_chunk = ch < 0 ? 0 : ch;
-        s_use_p = use_p;
-        s_hit = 0x7FFFFFFF;
+        s_chunk = ch < 0 ? max(s_last, 0) : ch;
     }
     __syncthreads();
+    if (threadIdx.x == 0) {
+        if (s_hit == 0x7FFFFFFF) { s_chunk = max(s_last, 0); s_target = INFINITY; }   // target beyond total
+        s_use_p = use_p;
+        s_hit = 0x7FFFFFFF;
+        s_last = -1;
+    }
+    __syncthreads();
+
     // Scan the chunk: per-thread segment sums, block scan in thread order, then the segment.
     const int lo = s_chunk * kVChunk + threadIdx.x * kVPer;
     float wv[kVPer];
     float seg = 0.f;
+#pragma unroll
     for (int i = 0; i < kVPer; ++i) {
         const int v = lo + i;
         float r = 0.f, p = 0.f;
@@ -345,36 +370,29 @@ verify_residual_kernel(ChainArgs a)
         wv[i] = s_use_p ? p : r;
         seg += wv[i];
     }
-    // exclusive scan of the segment sums in thread order (fixed association)
-    __shared__ float s_fscan[kVThreads];
-    s_fscan[threadIdx.x] = seg;
+    block_cdf_bounds(seg, sbuf, fscan);
+    const float tgt = s_target;
+    const float lo_s = sbuf[threadIdx.x], hi_s = sbuf[threadIdx.x + 1];
+    int last_pos = -1;
+#pragma unroll
+    for (int i = 0; i < kVPer; ++i) if (wv[i] > 0.f) last_pos = lo + i;
+    if (last_pos >= 0) atomicMax(&s_last, last_pos);
+    if (lo_s <= tgt && tgt < hi_s) atomicMin(&s_hit, threadIdx.x);
     __syncthreads();
-    if (threadIdx.x == 0) {
-        float run = 0.f;
-        for (int i = 0; i < kVThreads; ++i) { const float x = s_fscan[i]; s_fscan[i] = run; run += x; }
+    if (int(threadIdx.x) == s_hit) {
+        float cum = lo_s;
+        int v = -1;
+#pragma unroll
+        for (int i = 0; i < kVPer; ++i) {
+            cum += wv[i];
+            if (v < 0 && cum > tgt) v = lo + i;
+        }
+        if (v < 0) v = last_pos;                    // rounding inside the segment
+        a.correction[b] = v >= 0 ? v : s_last;
     }
     __syncthreads();
-    const float target = s_target;
-    float cum = s_fscan[threadIdx.x];
-    int hit = 0x7FFFFFFF, last_pos = -1;
-    for (int i = 0; i < kVPer; ++i) {
-        cum += wv[i];
-        if (wv[i] > 0.f) last_pos = lo + i;
-        if (hit == 0x7FFFFFFF && cum > target) hit = lo + i;
-    }
-    if (hit != 0x7FFFFFFF) atomicMin(&s_hit, hit);
-    __syncthreads();
-    if (s_hit == 0x7FFFFFFF) {                       // no crossing inside the chunk: last positive
-        if (threadIdx.x == 0) s_scan[0] = -1;
-        __syncthreads();
-        if (last_pos >= 0) atomicMax(&s_scan[0], last_pos);
-        __syncthreads();
-        if (threadIdx.x == 0) a.correction[b] = s_scan[0];
-    } else if (threadIdx.x == 0) {
-        a.correction[b] = s_hit;
-    }
+    if (threadIdx.x == 0 && s_hit == 0x7FFFFFFF) a.correction[b] = s_last;   // target beyond the chunk
 }
-
 
 // ---------------------------------------------------------------------------------------
 // Tree verification.  The pages cite EAGLE-style token trees but state no tree verifier;
@@ -468,24 +486,29 @@ __device__ void fold_qstats(const QStat *src, int nch, PStat *out)
 // weight exceeds `target`; if rounding leaves none, the last v with positive weight.  Thread t
 // owns a contiguous segment; segment sums are scanned in thread order.
 template <typename WF>
-__device__ int block_icdf(WF wf, int V, float target, float *fscan_scratch, int *ibuf)
+__device__ int block_icdf(WF wf, int V, float u, float *sbuf, float *scratch, int *ibuf)
 {
     const int E = (V + blockDim.x - 1) / blockDim.x;
     const int lo = threadIdx.x * E, hi = min(V, lo + E);
     float seg = 0.f;
     int last = -1;
     for (int v = lo; v < hi; ++v) { const float w = wf(v); seg += w; if (w > 0.f) last = v; }
-    float tot;
-    const float before = block_exclusive_scan(seg, fscan_scratch, &tot);
-    if (threadIdx.x == 0) { ibuf[0] = 0x7FFFFFFF; ibuf[1] = -1; }
+    block_cdf_bounds(seg, sbuf, scratch);
+    const float target = u * sbuf[blockDim.x];
+    const float lo_b = sbuf[threadIdx.x], hi_b = sbuf[threadIdx.x + 1];
+    if (threadIdx.x == 0) { ibuf[0] = 0x7FFFFFFF; ibuf[1] = -1; ibuf[2] = -1; }
     __syncthreads();
-    if (before + seg > target && before <= target) {
-        float cum = before;
-        for (int v = lo; v < hi; ++v) { cum += wf(v); if (cum > target) { atomicMin(&ibuf[0], v); break; } }
-    }
+    if (lo_b <= target && target < hi_b) atomicMin(&ibuf[0], threadIdx.x);
     if (last >= 0) atomicMax(&ibuf[1], last);
     __syncthreads();
-    const int r = ibuf[0] != 0x7FFFFFFF ? ibuf[0] : ibuf[1];
+    if (int(threadIdx.x) == ibuf[0]) {              // the first claimant walks its segment
+        float cum = lo_b;
+        int hit = -1;
+        for (int v = lo; v < hi; ++v) { cum += wf(v); if (cum > target) { hit = v; break; } }
+        ibuf[2] = hit >= 0 ? hit : last;            // rounding inside the segment: its last positive
+    }
+    __syncthreads();
+    const int r = ibuf[2] >= 0 ? ibuf[2] : ibuf[1];
     __syncthreads();
     return r;
 }
@@ -495,7 +518,8 @@ tree_walk_kernel(TreeArgs a)
 {
     __shared__ PStat s_p, s_q;
     __shared__ float fscr[33];
-    __shared__ int ibuf[2];
+    __shared__ float sbuf[kWalkThreads + 1];
+    __shared__ int ibuf[3];
     __shared__ int s_kids[64];
     __shared__ int s_nkids, s_accept;
     const int b = blockIdx.x;
@@ -533,15 +557,7 @@ tree_walk_kernel(TreeArgs a)
         }
         auto pval = [&](int v) { return __expf(z[v] * a.inv_te - pm) / ps; };
         if (nk == 0) {
-            const float u = a.u_res[size_t(b) * (a.D + 1) + dep];
-            float tot = 0.f;
-            {   // total mass in the same segment order the draw uses
-                const int E = (a.V + blockDim.x - 1) / blockDim.x;
-                float seg = 0.f;
-                for (int v = tid * E; v < min(a.V, tid * E + E); ++v) seg += pval(v);
-                block_exclusive_scan(seg, fscr, &tot);
-            }
-            corr = block_icdf(pval, a.V, u * tot, fscr, ibuf);
+            corr = block_icdf(pval, a.V, a.u_res[size_t(b) * (a.D + 1) + dep], sbuf, fscr, ibuf);
             break;
         }
         // residual state for the children's shared list: O off the list, r_j on it
@@ -596,14 +612,7 @@ tree_walk_kernel(TreeArgs a)
             const int pc = cposL[a.cluster_of[v]];
             return pc < 0 ? pval(v) : r[pc + a.rank[v]];
         };
-        float tot = 0.f;
-        {
-            const int E = (a.V + blockDim.x - 1) / blockDim.x;
-            float seg = 0.f;
-            for (int v = tid * E; v < min(a.V, tid * E + E); ++v) seg += wres(v);
-            block_exclusive_scan(seg, fscr, &tot);
-        }
-        corr = block_icdf(wres, a.V, u * tot, fscr, ibuf);
+        corr = block_icdf(wres, a.V, u, sbuf, fscr, ibuf);
         break;
     }
     if (tid == 0) { a.accepted[b] = A; a.correction[b] = corr; }

@@ -33,7 +33,7 @@ SIGNATURES = {
     "ds_gathered_head_noalloc": (ST, [P, I, I, P, I, I, P, P, P, I, P, P, P, P, F, U64, I,
                                       P, P, P, P, P, P, P]),
     "ds_verify_workspace_bytes": (SZ, [I, I, I]),
-    "ds_verify": (ST, [P, I, I, I, F, P, I64, P, P, I, P, P, P, P, P, P, P, SZ, P, P]),
+    "ds_verify": (ST, [P, I, I, I, F, P, I64, P, P, P, P, I, P, P, P, P, P, P, P, SZ, P, P]),
     "ds_verify_tree_workspace_bytes": (SZ, [I, I, I, I]),
     "ds_verify_tree": (ST, [P, I, I, I, I, F, P, P, I64, P, P, I, P, P, P, P, P,
                             P, P, P, P, SZ, P, P]),

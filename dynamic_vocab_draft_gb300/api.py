@@ -129,15 +129,17 @@ def gathered_head(H, G, W, vs_offsets, vs_ids, T, seed, pos, logits, token, toke
 
 
 def verify(p_logits, T, q_logits, vs_offsets, cpos, cluster_of, rank_in_cluster, draft_ids,
-           uniforms, accepted_len, correction, ws, status, stream=None):
+           uniforms, accepted_len, correction, ws, status, q_max=None, q_sumexp=None, stream=None):
     """p_logits [B, gamma+1, V]; q_logits [gamma, q_stride]; vs_offsets [gamma, B+1];
-    cpos [gamma, B*M]; draft_ids [gamma, B]; uniforms [B, gamma+1]."""
+    cpos [gamma, B*M]; draft_ids [gamma, B]; uniforms [B, gamma+1]; q_max / q_sumexp
+    [gamma, B] optional (the head's row statistics)."""
     B, g1, V = p_logits.shape
     gamma = g1 - 1
     M = cpos.shape[-1] // B
     _lib.check(_lib.load().ds_verify(
         _ptr(p_logits, F32, "p_logits"), B, gamma, V, float(T),
         _ptr(q_logits, F32, "q_logits"), q_logits.stride(0),
+        _ptr(q_max, F32, "q_max", True), _ptr(q_sumexp, F32, "q_sumexp", True),
         _ptr(vs_offsets, I32, "vs_offsets"), _ptr(cpos, I32, "cpos"), M,
         _ptr(cluster_of, I32, "cluster_of"), _ptr(rank_in_cluster, I32, "rank_in_cluster"),
         _ptr(draft_ids, I32, "draft_ids"), _ptr(uniforms, F32, "uniforms"),

@@ -80,24 +80,24 @@ __device__ __forceinline__ void load_group(uint4 (&buf)[kGvG], const uint16_t *W
     }
 }
 
-__device__ __forceinline__ void dot_group(const uint4 (&buf)[kGvG], const float *hs, int d, int k0, int lane,
+// h is kept in shared memory as bf16: one 16-byte load gives the 8 values a W vector meets.
+__device__ __forceinline__ void dot_group(const uint4 (&buf)[kGvG], const uint4 *hs, int d, int k0, int lane,
                                           float &a0, float &a1)
 {
 #pragma unroll
     for (int u = 0; u < kGvG; ++u) {
         const int k = k0 + (u * 32 + lane) * 8;
         if (k < d) {
-            const float4 *xv = reinterpret_cast<const float4 *>(hs + k);
-            const float4 x0 = xv[0], x1 = xv[1];
+            const uint4 x = hs[k >> 3];
             const uint4 w = buf[u];
-            a0 = fmaf(bf16lo(w.x), x0.x, a0);
-            a1 = fmaf(bf16hi(w.x), x0.y, a1);
-            a0 = fmaf(bf16lo(w.y), x0.z, a0);
-            a1 = fmaf(bf16hi(w.y), x0.w, a1);
-            a0 = fmaf(bf16lo(w.z), x1.x, a0);
-            a1 = fmaf(bf16hi(w.z), x1.y, a1);
-            a0 = fmaf(bf16lo(w.w), x1.z, a0);
-            a1 = fmaf(bf16hi(w.w), x1.w, a1);
+            a0 = fmaf(bf16lo(w.x), bf16lo(x.x), a0);
+            a1 = fmaf(bf16hi(w.x), bf16hi(x.x), a1);
+            a0 = fmaf(bf16lo(w.y), bf16lo(x.y), a0);
+            a1 = fmaf(bf16hi(w.y), bf16hi(x.y), a1);
+            a0 = fmaf(bf16lo(w.z), bf16lo(x.z), a0);
+            a1 = fmaf(bf16hi(w.z), bf16hi(x.z), a1);
+            a0 = fmaf(bf16lo(w.w), bf16lo(x.w), a0);
+            a1 = fmaf(bf16hi(w.w), bf16hi(x.w), a1);
         }
     }
 }
@@ -105,13 +105,12 @@ __device__ __forceinline__ void dot_group(const uint4 (&buf)[kGvG], const float 
 __global__ void __launch_bounds__(kGvWarps * 32, 1)
 head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__ counters)
 {
-    extern __shared__ float4 hs4[];
-    float *hs = reinterpret_cast<float *>(hs4);
+    extern __shared__ uint4 hs[];                 // h as bf16, d / 8 vectors
     __shared__ Stat warp_stat[kGvWarps];
     const int b = blockIdx.y;
     const int d = a.d;
-    const uint16_t *h = a.H + size_t(b) * d;
-    for (int k = threadIdx.x; k < d; k += blockDim.x) hs[k] = bf16_to_f32(h[k]);
+    const uint4 *h = reinterpret_cast<const uint4 *>(a.H + size_t(b) * d);
+    for (int k = threadIdx.x; k < d / 8; k += blockDim.x) hs[k] = h[k];
     __syncthreads();
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -504,7 +503,7 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
         int gx = B == 1 ? num_sms() - kHeadSideSms : (num_sms() + B - 1) / B;
         if (gx < 1) gx = 1;
         if (gx > kGvMaxBlocks) gx = kGvMaxBlocks;
-        const size_t smem = size_t(d) * sizeof(float);
+        const size_t smem = size_t(d) * sizeof(uint16_t);
         static bool attr_set = false;
         if (!attr_set) {
             if (cudaFuncSetAttribute(head_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -35,10 +35,15 @@ template <> __device__ __forceinline__ float load_x<float>(const float *p) { ret
 
 // y[b][i] = act(sum_k A[i][k] x[b][k] + bias[i]) for i < N, b < B.
 //   grid.x = ceil(N / kGemvWarps), grid.y = ceil(B / BT); dynamic smem = BT*K floats.
+__device__ void topk_block(const float *__restrict__ s, int M, int k, int32_t *__restrict__ dst);
+
+// With topk_k > 0 the last block of each batch tile to finish (completion counter per tile)
+// also selects the top-k of the tile's finished rows, saving a launch per draft position.
 template <typename XT, int BT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
 gemv_rows_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict__ x, int B,
-                 const uint16_t *__restrict__ bias, int act, float *__restrict__ y)
+                 const uint16_t *__restrict__ bias, int act, float *__restrict__ y,
+                 int topk_k, int32_t *__restrict__ topk_ids, unsigned *__restrict__ counters)
 {
     extern __shared__ float4 xs4[];
     float *xs = reinterpret_cast<float *>(xs4);
@@ -52,7 +57,7 @@ gemv_rows_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restr
 
     const int lane = threadIdx.x & 31;
     const int i = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
-    if (i >= N) return;
+    if (i < N) {
     const uint4 *row = reinterpret_cast<const uint4 *>(A + size_t(i) * K);
     float acc[BT];
 #pragma unroll
@@ -84,6 +89,12 @@ gemv_rows_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restr
 #pragma unroll
         for (int bt = 1; bt < BT; ++bt) if (lane == bt) a = acc[bt];
         y[size_t(b0 + lane) * N + i] = act_fn(a + bf16_to_f32(bias[i]), act);
+        if (topk_k > 0) __threadfence();
+    }
+    }
+    if (topk_k > 0 && last_block_done(&counters[blockIdx.y], gridDim.x)) {
+        for (int bt = 0; bt < nb; ++bt)
+            topk_block(y + size_t(b0 + bt) * N, N, topk_k, topk_ids + size_t(b0 + bt) * topk_k);
     }
 }
 
@@ -100,21 +111,23 @@ constexpr int kTopkPerThread = kRouterMaxK / kTopkThreads;
 
 // One block per row: keep the k largest of scores[b][0..M), ties to the lower index, and
 // write their indices in ascending order.
-__global__ void __launch_bounds__(kTopkThreads)
-topk_kernel(const float *__restrict__ scores, int M, int k, int32_t *__restrict__ ids)
+// Keep the k largest of s[0..M), ties to the lower index, and write their indices to dst in
+// ascending order.  Called by a whole block of kTopkThreads threads; s is read through L2 (other
+// blocks may have written it).
+__device__ void topk_block(const float *__restrict__ s, int M, int k, int32_t *__restrict__ dst)
 {
+    __syncthreads();                          // a previous call in this block is done with its state
     __shared__ unsigned hist[256];
     __shared__ int scan_scratch[33];
     __shared__ uint32_t s_prefix;
     __shared__ int s_need;
-    const float *s = scores + size_t(blockIdx.x) * M;
     // thread t owns the contiguous index range [t*E, t*E + E)
     const int E = (M + kTopkThreads - 1) / kTopkThreads;
     const int lo = threadIdx.x * E;
     uint32_t key[kTopkPerThread];
 #pragma unroll
     for (int e = 0; e < kTopkPerThread; ++e)
-        key[e] = (e < E && lo + e < M) ? order_key(s[lo + e]) : 0u;
+        key[e] = (e < E && lo + e < M) ? order_key(__ldcg(s + lo + e)) : 0u;
 
     // MSB-first radix select of the k-th largest key, 8 bits per pass.
     if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; }
@@ -186,15 +199,79 @@ topk_kernel(const float *__restrict__ scores, int M, int k, int32_t *__restrict_
         nsel += keep;
     }
     int out = block_exclusive_scan(nsel, scan_scratch, &tot);
-    int32_t *dst = ids + size_t(blockIdx.x) * k;
 #pragma unroll
     for (int e = 0; e < kTopkPerThread; ++e)
         if (sel[e] && out < k) dst[out++] = lo + e;
 }
 
+static_assert(kGemvWarps * 32 == kTopkThreads, "the GEMV block runs the top-k epilogue");
+
+// Batch 1: y[i] = act(A[i] . x + bias[i]).  No staging: every lane loads the slice of x its
+// weight vectors meet, next to those weights.  Warps stride over rows, so a small grid covers
+// the matrix in one wave -- the router of a later draft position runs on the few SMs the head
+// leaves free.  Optional top-k epilogue as in gemv_rows_kernel.
+template <typename XT>
+__global__ void __launch_bounds__(kGemvWarps * 32)
+gemv1_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict__ x,
+             const uint16_t *__restrict__ bias, int act, float *__restrict__ y,
+             int topk_k, int32_t *__restrict__ topk_ids, unsigned *__restrict__ counter)
+{
+    const int lane = threadIdx.x & 31;
+    const int nw = gridDim.x * kGemvWarps;
+    for (int i = blockIdx.x * kGemvWarps + (threadIdx.x >> 5); i < N; i += nw) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(A + size_t(i) * K);
+        float a0 = 0.f, a1 = 0.f;
+        for (int k0 = 0; k0 < K; k0 += kGemvU * 256) {
+            uint4 w[kGemvU];
+            float xv[kGemvU][8];
+#pragma unroll
+            for (int u = 0; u < kGemvU; ++u) {
+                const int k = k0 + u * 256 + lane * 8;
+                w[u] = k < K ? ld_stream(row + (k >> 3)) : make_uint4(0, 0, 0, 0);
+                if (k < K) {
+                    if constexpr (sizeof(XT) == 2) {
+                        const uint4 q = *reinterpret_cast<const uint4 *>(x + k);
+                        xv[u][0] = bf16lo(q.x); xv[u][1] = bf16hi(q.x); xv[u][2] = bf16lo(q.y); xv[u][3] = bf16hi(q.y);
+                        xv[u][4] = bf16lo(q.z); xv[u][5] = bf16hi(q.z); xv[u][6] = bf16lo(q.w); xv[u][7] = bf16hi(q.w);
+                    } else {
+                        const float4 q0 = *reinterpret_cast<const float4 *>(x + k);
+                        const float4 q1 = *reinterpret_cast<const float4 *>(x + k + 4);
+                        xv[u][0] = q0.x; xv[u][1] = q0.y; xv[u][2] = q0.z; xv[u][3] = q0.w;
+                        xv[u][4] = q1.x; xv[u][5] = q1.y; xv[u][6] = q1.z; xv[u][7] = q1.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xv[u][e] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kGemvU; ++u) {
+                a0 = fmaf(bf16lo(w[u].x), xv[u][0], a0);
+                a1 = fmaf(bf16hi(w[u].x), xv[u][1], a1);
+                a0 = fmaf(bf16lo(w[u].y), xv[u][2], a0);
+                a1 = fmaf(bf16hi(w[u].y), xv[u][3], a1);
+                a0 = fmaf(bf16lo(w[u].z), xv[u][4], a0);
+                a1 = fmaf(bf16hi(w[u].z), xv[u][5], a1);
+                a0 = fmaf(bf16lo(w[u].w), xv[u][6], a0);
+                a1 = fmaf(bf16hi(w[u].w), xv[u][7], a1);
+            }
+        }
+        const float acc = warp_sum(a0 + a1);
+        if (lane == 0) {
+            y[i] = act_fn(acc + bf16_to_f32(bias[i]), act);
+            if (topk_k > 0) __threadfence();
+        }
+    }
+    if (topk_k > 0 && last_block_done(counter, gridDim.x)) topk_block(y, N, topk_k, topk_ids);
+}
+
+constexpr int kGemv1Blocks = 32;       // 256 warps: one wave on 16 SMs (2 blocks each)
+
+
+
 template <typename XT, int BT>
 ds_status launch_gemv(const uint16_t *A, int N, int K, const XT *x, int B, const uint16_t *bias, int act,
-                      float *y, cudaStream_t stream)
+                      float *y, int topk_k, int32_t *topk_ids, unsigned *counters, cudaStream_t stream)
 {
     const size_t smem = size_t(BT) * K * sizeof(float);
     static bool attr = false;
@@ -205,7 +282,8 @@ ds_status launch_gemv(const uint16_t *A, int N, int K, const XT *x, int B, const
         attr = true;
     }
     dim3 grid((N + kGemvWarps - 1) / kGemvWarps, (B + BT - 1) / BT);
-    gemv_rows_kernel<XT, BT><<<grid, kGemvWarps * 32, smem, stream>>>(A, N, K, x, B, bias, act, y);
+    gemv_rows_kernel<XT, BT><<<grid, kGemvWarps * 32, smem, stream>>>(A, N, K, x, B, bias, act, y,
+                                                                       topk_k, topk_ids, counters);
     DS_TRY_LAUNCH();
     return DS_OK;
 }
@@ -218,7 +296,8 @@ using namespace ds;
 extern "C" size_t ds_router_workspace_bytes(int B, int Hr)
 {
     if (B <= 0 || Hr <= 0) return 0;
-    return align256(size_t(B) * size_t(Hr) * sizeof(float));
+    // hidden layer u [B, Hr] + one completion counter per batch tile of the second layer
+    return align256(size_t(B) * size_t(Hr) * sizeof(float)) + align256(size_t(B) * sizeof(unsigned));
 }
 
 extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
@@ -243,13 +322,20 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
     if (!ws || ws_bytes < ds_router_workspace_bytes(B, Hr)) return DS_ERR_WORKSPACE;
 
     float *u = static_cast<float *>(ws);
-    const ds_status s1 = B == 1 ? launch_gemv<uint16_t, 1>(W1, Hr, d, H, B, b1, act, u, stream)
-                                : launch_gemv<uint16_t, kGemvBT>(W1, Hr, d, H, B, b1, act, u, stream);
+    unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) +
+                                                      align256(size_t(B) * size_t(Hr) * sizeof(float)));
+    if (B == 1) {
+        gemv1_kernel<uint16_t><<<kGemv1Blocks, kGemvWarps * 32, 0, stream>>>(W1, Hr, d, H, b1, act, u, 0,
+                                                                            nullptr, nullptr);
+        DS_TRY_LAUNCH();
+        gemv1_kernel<float><<<kGemv1Blocks, kGemvWarps * 32, 0, stream>>>(W2, M, Hr, u, b2, -1, scores, k,
+                                                                         cluster_ids, counters);
+        DS_TRY_LAUNCH();
+        return DS_OK;
+    }
+    const ds_status s1 = launch_gemv<uint16_t, kGemvBT>(W1, Hr, d, H, B, b1, act, u, 0, nullptr, nullptr, stream);
     if (s1 != DS_OK) return s1;
-    const ds_status s2 = B == 1 ? launch_gemv<float, 1>(W2, M, Hr, u, B, b2, -1, scores, stream)
-                                : launch_gemv<float, kGemvBT>(W2, M, Hr, u, B, b2, -1, scores, stream);
+    const ds_status s2 = launch_gemv<float, kGemvBT>(W2, M, Hr, u, B, b2, -1, scores, k, cluster_ids, counters, stream);
     if (s2 != DS_OK) return s2;
-    topk_kernel<<<B, kTopkThreads, 0, stream>>>(scores, M, k, cluster_ids);
-    DS_TRY_LAUNCH();
     return DS_OK;
 }

@@ -157,20 +157,28 @@ __global__ void union_expand_kernel(const int32_t *__restrict__ off, const int32
     }
 }
 
-// One list, no union: the scan and the offsets in a single block (the offsets kernel of the
-// batched path would be a launch with nothing to do); the expansion stays a wide kernel.
+// One list, no union: scan and expansion in one launch.  Every block recomputes the (tiny)
+// scan of the selected clusters' sizes in shared memory, then copies its share of the selected
+// clusters' CSR slices, one warp per cluster; block 0 also writes cpos and the offsets.
+constexpr int kSlCopyWarps = 1;           // selected clusters per copying warp
+
 __global__ void __launch_bounds__(kSlThreads)
-shortlist_single_scan_kernel(const int32_t *__restrict__ off, int M, int V, const int32_t *__restrict__ ids,
-                             int k, int32_t *__restrict__ cpos, int32_t *__restrict__ vs_offsets,
-                             int64_t capacity, int32_t *st)
+shortlist_single_kernel(const int32_t *__restrict__ off, const int32_t *__restrict__ tok, int M, int V,
+                        const int32_t *__restrict__ ids, int k, int32_t *__restrict__ cpos,
+                        int32_t *__restrict__ vs_offsets, int32_t *__restrict__ vs_ids, int64_t capacity,
+                        int32_t *st)
 {
     __shared__ unsigned char flag[kSlMaxM];
+    __shared__ int spos[kSlMaxM];
     __shared__ int scratch[33];
     for (int c = threadIdx.x; c < M; c += blockDim.x) flag[c] = 0;
     __syncthreads();
     for (int j = threadIdx.x; j < k; j += blockDim.x) {
         const int c = ids[j];
-        if (c < 0 || c >= M || (j > 0 && ids[j - 1] >= c)) { set_status(st, DS_DEV_BAD_INDEX); continue; }
+        if (c < 0 || c >= M || (j > 0 && ids[j - 1] >= c)) {
+            if (blockIdx.x == 0) set_status(st, DS_DEV_BAD_INDEX);
+            continue;
+        }
         flag[c] = 1;
     }
     __syncthreads();
@@ -184,7 +192,10 @@ shortlist_single_scan_kernel(const int32_t *__restrict__ off, int M, int V, cons
         int n = 0;
         if (e < E && c < M && flag[c]) {
             n = off[c + 1] - off[c];
-            if (off[c] < 0 || n < 0 || off[c + 1] > V) { set_status(st, DS_DEV_BAD_INDEX); n = 0; }
+            if (off[c] < 0 || n < 0 || off[c + 1] > V) {
+                if (blockIdx.x == 0) set_status(st, DS_DEV_BAD_INDEX);
+                n = 0;
+            }
         }
         sz[e] = n;
         sum += n;
@@ -194,12 +205,32 @@ shortlist_single_scan_kernel(const int32_t *__restrict__ off, int M, int V, cons
 #pragma unroll
     for (int e = 0; e < kSlMaxPer; ++e) {
         const int c = lo + e;
-        if (e < E && c < M) { cpos[c] = flag[c] ? run : -1; run += sz[e]; }
+        if (e < E && c < M) {
+            const int p = flag[c] ? run : -1;
+            spos[c] = p;
+            if (blockIdx.x == 0) cpos[c] = p;
+            run += sz[e];
+        }
     }
-    if (threadIdx.x == 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
         vs_offsets[0] = 0;
         vs_offsets[1] = tot;
         if (int64_t(tot) > capacity) set_status(st, DS_DEV_CAPACITY);
+    }
+    __syncthreads();
+    // this block's share of the selected clusters, one warp per cluster
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = gridDim.x * (kSlThreads / 32);
+    for (int j = blockIdx.x * (kSlThreads / 32) + warp; j < k; j += nwarps) {
+        const int c = ids[j];
+        if (c < 0 || c >= M) continue;
+        const int p = spos[c];
+        if (p < 0) continue;
+        const int l0 = off[c], n = off[c + 1] - l0;
+        if (l0 < 0 || n < 0 || l0 + n > V) continue;
+#pragma unroll 4
+        for (int r = lane; r < n; r += 32)
+            if (int64_t(p) + r < capacity) vs_ids[p + r] = tok[l0 + r];
     }
 }
 
@@ -245,11 +276,9 @@ extern "C" ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *c
     int32_t *ustart = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + align256(size_t(B) * 4));
 
     if (B == 1 && nu == 0) {
-        shortlist_single_scan_kernel<<<1, kSlThreads, 0, stream>>>(csr_off, M, V, cluster_ids, k, cpos,
-                                                                   vs_offsets, vs_capacity, dev_status);
-        DS_TRY_LAUNCH();
-        shortlist_expand_kernel<<<dim3((k + 7) / 8, 1), 256, 0, stream>>>(csr_off, csr_tok, M, V, cluster_ids, k,
-                                                                         cpos, vs_offsets, vs_ids, vs_capacity);
+        const int blocks = (k + kSlCopyWarps * (kSlThreads / 32) - 1) / (kSlCopyWarps * (kSlThreads / 32));
+        shortlist_single_kernel<<<blocks, kSlThreads, 0, stream>>>(csr_off, csr_tok, M, V, cluster_ids, k, cpos,
+                                                                   vs_offsets, vs_ids, vs_capacity, dev_status);
         DS_TRY_LAUNCH();
         return DS_OK;
     }

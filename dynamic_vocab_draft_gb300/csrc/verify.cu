@@ -30,6 +30,8 @@ constexpr int kVThreads = 256;
 constexpr int kVPer = 8;                         // elements per thread per chunk
 constexpr int kVChunk = kVThreads * kVPer;       // 2048
 constexpr int kMaxGamma = 32;
+constexpr int kRPer = 4;                         // residual pass: elements per thread
+constexpr int kRChunk = kVThreads * kRPer;       // 1024
 
 struct PStat { float m, s, amax; int aid; };   // target-row chunk: max, sum-exp, argmax
 struct QStat { float m, s; };
@@ -60,24 +62,6 @@ __device__ __forceinline__ PStat shfl_xor_pstat(const PStat &a, int o)
                  __shfl_xor_sync(0xFFFFFFFFu, a.amax, o), __shfl_xor_sync(0xFFFFFFFFu, a.aid, o)};
 }
 
-// Block-wide fold of a PStat in a fixed order (lane tree, then warps in order).
-__device__ PStat block_pstat(PStat p, PStat *scratch)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const PStat q = shfl_xor_pstat(p, o);
-        p = (lane & o) ? pstat_merge(q, p) : pstat_merge(p, q);
-    }
-    __syncthreads();
-    if (lane == 0) scratch[warp] = p;
-    __syncthreads();
-    PStat r = scratch[0];
-    for (int w = 1; w < int(blockDim.x >> 5); ++w) r = pstat_merge(r, scratch[w]);
-    __syncthreads();
-    return r;
-}
-
 __device__ float block_sum(float x, float *scratch)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -92,13 +76,12 @@ __device__ float block_sum(float x, float *scratch)
 }
 
 // Statistics of one chunk of a row of length n: max and sum-exp of x = value * inv_te, and the
-// argmax of the raw values (ties to the lower index).
+// argmax of the raw values (ties to the lower index).  Two plain block reductions (the max,
+// then the sum of exp(x - max)); the result is valid in thread 0.
 __device__ PStat chunk_stats(const float *__restrict__ row, int lo, int n, float inv_te, PStat *scratch)
 {
     float vals[kVPer];
     const int base = lo + threadIdx.x * kVPer;
-    float m = -INFINITY, amax = -INFINITY;
-    int aid = -1;
     if (base + kVPer <= n && (reinterpret_cast<uintptr_t>(row + base) & 15) == 0) {
 #pragma unroll
         for (int i = 0; i < kVPer; i += 4) {
@@ -109,18 +92,42 @@ __device__ PStat chunk_stats(const float *__restrict__ row, int lo, int n, float
 #pragma unroll
         for (int i = 0; i < kVPer; ++i) vals[i] = base + i < n ? __ldg(row + base + i) : -INFINITY;
     }
+    float amax = -INFINITY;
+    int aid = -1;
 #pragma unroll
-    for (int i = 0; i < kVPer; ++i) {
+    for (int i = 0; i < kVPer; ++i)
         if (vals[i] > amax) { amax = vals[i]; aid = base + i; }     // first max = lowest index
-        m = fmaxf(m, vals[i] * inv_te);
-    }
-    float s = 0.f;
-    if (m != -INFINITY) {
+    // block max / argmax of the raw values (x = value * inv_te is monotone in the value)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
-        for (int i = 0; i < kVPer; ++i) s += __expf(vals[i] * inv_te - m);
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xFFFFFFFFu, amax, o);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, aid, o);
+        if (oi >= 0 && (aid < 0 || ov > amax || (ov == amax && oi < aid))) { amax = ov; aid = oi; }
     }
-    if (aid < 0) amax = -INFINITY;
-    return block_pstat(PStat{m, s, amax, aid}, scratch);
+    if (lane == 0) { scratch[warp].amax = amax; scratch[warp].aid = aid; }
+    __syncthreads();
+    float bmax = -INFINITY;
+    int bid = -1;
+    for (int w = 0; w < nw; ++w) {
+        const float ov = scratch[w].amax;
+        const int oi = scratch[w].aid;
+        if (oi >= 0 && (bid < 0 || ov > bmax || (ov == bmax && oi < bid))) { bmax = ov; bid = oi; }
+    }
+    const float m = bid >= 0 ? bmax * inv_te : -INFINITY;
+    float sl = 0.f;
+    if (bid >= 0) {
+#pragma unroll
+        for (int i = 0; i < kVPer; ++i) sl += __expf(vals[i] * inv_te - m);
+    }
+    sl = warp_sum(sl);
+    __syncthreads();                                   // everyone has read scratch
+    if (lane == 0) scratch[warp].s = sl;
+    __syncthreads();
+    PStat r{m, 0.f, bmax, bid};
+    if (threadIdx.x == 0) for (int w = 0; w < nw; ++w) r.s += scratch[w].s;
+    __syncthreads();
+    return r;
 }
 
 struct ChainArgs {
@@ -129,6 +136,7 @@ struct ChainArgs {
     float T, inv_te;
     const float *q_logits;
     int64_t q_stride;
+    const float *q_max, *q_sumexp;     // optional [gamma][B] draft-row statistics
     const int32_t *vs_offsets, *cpos;
     int M;
     const int32_t *cluster_of, *rank;
@@ -143,7 +151,8 @@ struct ChainArgs {
     QStat *prow;        // [B][gamma+1] folded target stats
     QStat *qrow;        // [B][gamma]   folded draft stats
     int32_t *decision;  // [B]: -1 done, else the target row to draw from (t* or gamma)
-    float *rsum, *psum; // [B][nch]
+    int nrch;           // residual-pass chunks
+    float *rsum, *psum; // [B][nrch]
 };
 
 // Index of full-vocabulary token v in list (t, b), or -1.
@@ -171,7 +180,7 @@ verify_stats_kernel(ChainArgs a)
         const PStat ps = chunk_stats(row, lo, a.V, a.inv_te, scratch);
         if (threadIdx.x == 0) a.pstat[(size_t(b) * g1 + t) * a.nch + c] = ps;
     }
-    if (t < a.gamma && a.T > 0.f) {
+    if (t < a.gamma && a.T > 0.f && !a.q_max) {
         const int *off = a.vs_offsets + size_t(t) * (a.B + 1);
         const int n = off[b + 1] - off[b];
         QStat q{-INFINITY, 0.f};
@@ -185,7 +194,13 @@ verify_stats_kernel(ChainArgs a)
 
     // Fold the chunk statistics of this sequence's rows: warp w takes rows w, w+8, ...
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nrows = g1 + (a.T > 0.f ? a.gamma : 0);
+    const int nrows = g1 + (a.T > 0.f && !a.q_max ? a.gamma : 0);
+    if (a.T > 0.f && a.q_max && threadIdx.x < a.gamma) {
+        const int tt = threadIdx.x;
+        const QStat q{a.q_max[size_t(tt) * a.B + b], a.q_sumexp[size_t(tt) * a.B + b]};
+        qrows[tt] = q;
+        a.qrow[size_t(b) * a.gamma + tt] = q;
+    }
     for (int r = warp; r < nrows; r += kVThreads / 32) {
         PStat acc{-INFINITY, 0.f, -INFINITY, -1};
         if (r < g1) {
@@ -296,28 +311,28 @@ verify_residual_kernel(ChainArgs a)
     const int tr = __ldcg(&a.decision[b]);
     if (tr < 0) return;                              // greedy: decided already (whole group returns)
     const ResidualRow rr = residual_row(a, b, tr);
-    const int base = c * kVChunk + threadIdx.x * kVPer;
+    const int base = c * kRChunk + threadIdx.x * kRPer;
     float rs = 0.f, psum = 0.f;
 #pragma unroll
-    for (int i = 0; i < kVPer; ++i) {
+    for (int i = 0; i < kRPer; ++i) {
         const int v = base + i;
         if (v < a.V) { float r, p; residual_weight(a, rr, v, r, p); rs += r; psum += p; }
     }
     rs = block_sum(rs, scratch);
     psum = block_sum(psum, scratch);
-    if (threadIdx.x == 0) { a.rsum[size_t(b) * a.nch + c] = rs; a.psum[size_t(b) * a.nch + c] = psum; }
-    if (!last_block_done(&a.cnt2[b], unsigned(a.nch))) return;
+    if (threadIdx.x == 0) { a.rsum[size_t(b) * a.nrch + c] = rs; a.psum[size_t(b) * a.nrch + c] = psum; }
+    if (!last_block_done(&a.cnt2[b], unsigned(a.nrch))) return;
 
     // Locate the chunk where the cumulative mass first exceeds u * total: thread t sums a
     // contiguous run of chunk masses, the runs are scanned in thread order, and the thread
     // whose run crosses walks it.  A residual without mass falls back to p.
     const float u = a.u[size_t(b) * (a.gamma + 1) + a.gamma];
-    const int E = (a.nch + kVThreads - 1) / kVThreads;
-    const int c0 = threadIdx.x * E, c1 = min(a.nch, c0 + E);
+    const int E = (a.nrch + kVThreads - 1) / kVThreads;
+    const int c0 = threadIdx.x * E, c1 = min(a.nrch, c0 + E);
     float rrun = 0.f, prun = 0.f;
     for (int i = c0; i < c1; ++i) {
-        rrun += __ldcg(&a.rsum[size_t(b) * a.nch + i]);
-        prun += __ldcg(&a.psum[size_t(b) * a.nch + i]);
+        rrun += __ldcg(&a.rsum[size_t(b) * a.nrch + i]);
+        prun += __ldcg(&a.psum[size_t(b) * a.nrch + i]);
     }
     block_cdf_bounds(rrun, sbuf, fscan);
     const float rtot = sbuf[kVThreads];
@@ -330,19 +345,19 @@ verify_residual_kernel(ChainArgs a)
     __syncthreads();
     if (lo_b <= target && target < hi_b) atomicMin(&s_hit, threadIdx.x);
     int lastc = -1;
-    for (int i = c0; i < c1; ++i) if (__ldcg(&w[size_t(b) * a.nch + i]) > 0.f) lastc = i;
+    for (int i = c0; i < c1; ++i) if (__ldcg(&w[size_t(b) * a.nrch + i]) > 0.f) lastc = i;
     if (lastc >= 0) atomicMax(&s_last, lastc);
     __syncthreads();
     if (int(threadIdx.x) == s_hit) {               // the first claimant walks its run of chunks
         float cum = lo_b;
         int ch = -1;
         for (int i = c0; i < c1; ++i) {
-            const float wi = __ldcg(&w[size_t(b) * a.nch + i]);
+            const float wi = __ldcg(&w[size_t(b) * a.nrch + i]);
             if (cum + wi > target) { ch = i; break; }
             cum += wi;
         }
         if (ch < 0) {                               // rounding inside the run: its last chunk with mass
-            for (int i = c1 - 1; i >= c0; --i) if (__ldcg(&w[size_t(b) * a.nch + i]) > 0.f) { ch = i; break; }
+            for (int i = c1 - 1; i >= c0; --i) if (__ldcg(&w[size_t(b) * a.nrch + i]) > 0.f) { ch = i; break; }
             s_target = INFINITY;
         } else {
             s_target = target - cum;
@@ -359,11 +374,11 @@ verify_residual_kernel(ChainArgs a)
     __syncthreads();
 
     // Scan the chunk: per-thread segment sums, block scan in thread order, then the segment.
-    const int lo = s_chunk * kVChunk + threadIdx.x * kVPer;
-    float wv[kVPer];
+    const int lo = s_chunk * kRChunk + threadIdx.x * kRPer;
+    float wv[kRPer];
     float seg = 0.f;
 #pragma unroll
-    for (int i = 0; i < kVPer; ++i) {
+    for (int i = 0; i < kRPer; ++i) {
         const int v = lo + i;
         float r = 0.f, p = 0.f;
         if (v < a.V) residual_weight(a, rr, v, r, p);
@@ -375,7 +390,7 @@ verify_residual_kernel(ChainArgs a)
     const float lo_s = sbuf[threadIdx.x], hi_s = sbuf[threadIdx.x + 1];
     int last_pos = -1;
 #pragma unroll
-    for (int i = 0; i < kVPer; ++i) if (wv[i] > 0.f) last_pos = lo + i;
+    for (int i = 0; i < kRPer; ++i) if (wv[i] > 0.f) last_pos = lo + i;
     if (last_pos >= 0) atomicMax(&s_last, last_pos);
     if (lo_s <= tgt && tgt < hi_s) atomicMin(&s_hit, threadIdx.x);
     __syncthreads();
@@ -383,7 +398,7 @@ verify_residual_kernel(ChainArgs a)
         float cum = lo_s;
         int v = -1;
 #pragma unroll
-        for (int i = 0; i < kVPer; ++i) {
+        for (int i = 0; i < kRPer; ++i) {
             cum += wv[i];
             if (v < 0 && cum > tgt) v = lo + i;
         }
@@ -624,6 +639,7 @@ tree_walk_kernel(TreeArgs a)
 using namespace ds;
 
 static int vchunks(int V) { return (V + kVChunk - 1) / kVChunk; }
+static size_t rchunks(int V) { return size_t((V + kRChunk - 1) / kRChunk); }
 
 extern "C" size_t ds_verify_workspace_bytes(int B, int gamma, int V)
 {
@@ -636,11 +652,12 @@ extern "C" size_t ds_verify_workspace_bytes(int B, int gamma, int V)
            align256(size_t(B) * g1 * sizeof(QStat)) +
            align256(size_t(B) * gamma * sizeof(QStat)) +
            align256(size_t(B) * sizeof(int32_t)) +
-           2 * align256(size_t(B) * nch * sizeof(float));
+           2 * align256(size_t(B) * rchunks(V) * sizeof(float));
 }
 
 extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, float T,
                                const float *q_logits, int64_t q_stride,
+                               const float *q_max, const float *q_sumexp,
                                const int32_t *vs_offsets, const int32_t *cpos, int M,
                                const int32_t *cluster_of, const int32_t *rank_in_cluster,
                                const int32_t *draft_ids, const float *uniforms,
@@ -653,12 +670,14 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     if (B < 1 || gamma < 1 || gamma > kMaxGamma || V < 1 || V > (1 << 24) || M < 1 || M > 8192 ||
         !(T >= 0.f) || q_stride < 0)
         return DS_ERR_INVALID_ARG;
+    if ((q_max == nullptr) != (q_sumexp == nullptr)) return DS_ERR_INVALID_ARG;
     if (B > 65535 / (gamma + 1)) return DS_ERR_UNSUPPORTED;
     if (!ws || ws_bytes < ds_verify_workspace_bytes(B, gamma, V)) return DS_ERR_WORKSPACE;
     ChainArgs a;
     a.p_logits = p_logits; a.B = B; a.gamma = gamma; a.V = V; a.nch = vchunks(V);
     a.T = T; a.inv_te = T > 0.f ? 1.f / T : 1.f;
     a.q_logits = q_logits; a.q_stride = q_stride;
+    a.q_max = q_max; a.q_sumexp = q_sumexp;
     a.vs_offsets = vs_offsets; a.cpos = cpos; a.M = M;
     a.cluster_of = cluster_of; a.rank = rank_in_cluster;
     a.draft_ids = draft_ids; a.u = uniforms;
@@ -672,12 +691,13 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     a.prow = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * g1 * sizeof(QStat));
     a.qrow = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * gamma * sizeof(QStat));
     a.decision = reinterpret_cast<int32_t *>(w); w += align256(size_t(B) * sizeof(int32_t));
-    a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * nch * sizeof(float));
+    a.nrch = int(rchunks(V));
+    a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.psum = reinterpret_cast<float *>(w);
 
     verify_stats_kernel<<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
     DS_TRY_LAUNCH();
-    verify_residual_kernel<<<dim3(a.nch, B), kVThreads, 0, stream>>>(a);
+    verify_residual_kernel<<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
     DS_TRY_LAUNCH();
     return DS_OK;
 }

@@ -136,7 +136,7 @@ class ChainDrafter(_Common):
     def verify(self, stream=None):
         api.verify(self.z, self.T, self.logits, self.vs_offsets, self.cpos, self.cluster_of, self.rank,
                    self.tokens, self.u, self.accepted, self.correction, self.ws_verify, self.status,
-                   stream)
+                   q_max=self.row_max, q_sumexp=self.row_sumexp, stream=stream)
 
     def step(self):
         main = torch.cuda.current_stream(self.dev)
@@ -155,7 +155,7 @@ class ChainDrafter(_Common):
         self.verify()
 
     def launches_per_step(self) -> int:
-        n_router = 3
+        n_router = 2
         n_short = 4 if self.union else (2 if self.B == 1 else 3)
         n_head = 2 if self.union else 1
         return self.gamma * (n_router + n_short + n_head) + 2
@@ -247,4 +247,4 @@ class TreeDrafter(_Common):
         self.verify()
 
     def launches_per_step(self) -> int:
-        return self.D * (3 + 4 + 2) + 2
+        return self.D * (2 + 4 + 2) + 2

@@ -92,7 +92,8 @@ ds_status ds_vocab_index(const int32_t *csr_off, const int32_t *csr_tok, int M, 
  *   cluster_ids [B, k]     out: the k highest-scoring clusters of each row, ties to the lower
  *                          id, listed in ascending id
  * Limits: 1 <= B <= 4096, d % 8 == 0, Hr % 8 == 0, 1 <= k <= M <= 8192.
- * ws: ds_router_workspace_bytes(B, Hr) bytes (the hidden layer).
+ * ws: ds_router_workspace_bytes(B, Hr) bytes (the hidden layer and completion counters:
+ *     zero it once before first use).
  * ------------------------------------------------------------------------------------- */
 size_t ds_router_workspace_bytes(int B, int Hr);
 ds_status ds_router_topk(const uint16_t *H, int B, int d,
@@ -211,6 +212,9 @@ ds_status ds_gathered_head_noalloc(const uint16_t *H, int B, int G,
  *   p_logits [B, gamma+1, V] fp32 target logits
  *   q_logits               draft logits of position t (0-based) at q_logits + t*q_stride,
  *                          laid out as ds_gathered_head writes them with G = 1
+ *   q_max, q_sumexp [gamma, B] (optional, both or neither): the draft rows' softmax
+ *                          statistics as ds_gathered_head reports them (row_max, row_sumexp);
+ *                          NULL -> recomputed here from q_logits
  *   vs_offsets [gamma, B+1], cpos [gamma, B*M]: the lists of each position
  *   cluster_of, rank_in_cluster [V]: from ds_vocab_index
  *   draft_ids [gamma, B]   x_t of each sequence (full-vocabulary ids)
@@ -223,6 +227,7 @@ ds_status ds_gathered_head_noalloc(const uint16_t *H, int B, int G,
 size_t ds_verify_workspace_bytes(int B, int gamma, int V);
 ds_status ds_verify(const float *p_logits, int B, int gamma, int V, float T,
                     const float *q_logits, int64_t q_stride,
+                    const float *q_max, const float *q_sumexp,
                     const int32_t *vs_offsets, const int32_t *cpos, int M,
                     const int32_t *cluster_of, const int32_t *rank_in_cluster,
                     const int32_t *draft_ids, const float *uniforms,

@@ -90,9 +90,9 @@ def test_host_argument_checks(lib):
     a = list(args); a[23] = 16
     assert lib.ds_gathered_head(*a) == 4
     # verify: gamma beyond the limit; NULL uniforms
-    assert lib.ds_verify(FAKE, 1, 40, 4096, 1.0, FAKE, 4096, FAKE, FAKE, 32, FAKE, FAKE, FAKE, FAKE,
+    assert lib.ds_verify(FAKE, 1, 40, 4096, 1.0, FAKE, 4096, None, None, FAKE, FAKE, 32, FAKE, FAKE, FAKE, FAKE,
                          FAKE, FAKE, FAKE, 1 << 24, None, None) == 1
-    assert lib.ds_verify(FAKE, 1, 4, 4096, 1.0, FAKE, 4096, FAKE, FAKE, 32, FAKE, FAKE, FAKE, None,
+    assert lib.ds_verify(FAKE, 1, 4, 4096, 1.0, FAKE, 4096, None, None, FAKE, FAKE, 32, FAKE, FAKE, FAKE, None,
                          FAKE, FAKE, FAKE, 1 << 24, None, None) == 1
     assert lib.ds_verify_tree(FAKE, 1, 3, 65, 4096, 1.0, FAKE, FAKE, 4096, FAKE, FAKE, 32, FAKE, FAKE,
                               FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 24, None, None) == 1

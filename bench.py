@@ -54,8 +54,9 @@ def dist_env():
 
 
 def workload_config(cfg):
-    return {"workload": f"{cfg.name}: chain drafting, Llama-3-8B-shaped LM head, "
-                        f"B={cfg.B}, gamma={cfg.gamma}, T={cfg.T}",
+    kind = (f"chain drafting, B={cfg.B}, gamma={cfg.gamma}" if cfg.mode == "chain" else
+            f"tree drafting, B={cfg.B}, depth {cfg.gamma} x {cfg.width} nodes")
+    return {"workload": f"{cfg.name}: {kind}, V={cfg.V}, d={cfg.d}, T={cfg.T}",
             "V": cfg.V, "d": cfg.d, "clusters": cfg.M, "router": f"{cfg.d}->{cfg.Hr}->{cfg.M} {cfg.act}",
             "B": cfg.B, "gamma": cfg.gamma, "budget": list(cfg.budget), "T": cfg.T,
             "sigma_p": cfg.sigma_p, "seed": None,
@@ -96,15 +97,29 @@ def run_reference(args):
     import oracle
     import workloads as wl
     cfg = wl.config(args.config)
-    inp = wl.chain_inputs(cfg, args.seed)
-    value, n, dt = oracle_sample(inp, budget_s=90.0, max_steps=args.steps, warmup=args.warmup)
+    if cfg.mode == "chain":
+        inp = wl.chain_inputs(cfg, args.seed)
+        value, n, dt = oracle_sample(inp, budget_s=90.0, max_steps=args.steps, warmup=args.warmup)
+        sample = (f"{n} oracle draft positions of sequence 0 (router + top-k + shortlist + head + sample; "
+                  f"verification of the whole chain after every {cfg.gamma}th), {dt:.1f} s")
+        ms_per_step = 1e3 * dt / max(n, 1) * cfg.gamma * cfg.B
+    else:
+        inp = wl.tree_inputs(cfg, args.seed)
+        t0 = time.perf_counter()
+        n = 0
+        while n < max(1, min(args.steps, 3)) and time.perf_counter() - t0 < 90.0:
+            oracle.tree_step(inp, seqs=[0])
+            n += 1
+        dt = time.perf_counter() - t0
+        value = n * cfg.gamma * cfg.width / dt
+        sample = f"{n} whole tree steps of sequence 0 ({cfg.gamma * cfg.width} nodes each + verification), {dt:.1f} s"
+        ms_per_step = 1e3 * dt / n * cfg.B
     cores = oracle.get_threads()
-    sample = (f"{n} oracle draft positions of sequence 0 (router + top-k + shortlist + head + sample; "
-              f"verification of the whole chain after every {cfg.gamma}th), {dt:.1f} s")
     cfgd = workload_config(cfg)
     cfgd["seed"] = args.seed
+    cfgd["l2"] = "n/a (host)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": n, "warmup": min(args.warmup, 1), "ms_per_step": 1e3 * dt / max(n, 1) * cfg.gamma,
+            "steps": n, "warmup": min(args.warmup, 1), "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": cfgd,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
@@ -201,6 +216,59 @@ def committed_traffic():
         return None
 
 
+def build_drafter(cfg, inp, dev, pkg, torch):
+    """Drafter + pinned host copies of the per-step inputs (name -> (host, device buffer))."""
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def pinned_bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+
+    common = (bf(inp["W"]), bf(inp["W1"]), bf(inp["b1"]), bf(inp["W2"]), bf(inp["b2"]),
+              torch.as_tensor(inp["csr_off"]), torch.as_tensor(inp["csr_tok"]))
+    if cfg.mode == "chain":
+        d = pkg.pipeline.ChainDrafter(*common, B=cfg.B, gamma=cfg.gamma, budget=cfg.budget, act=cfg.act,
+                                      T=cfg.T, seed=inp["gumbel_seed"])
+        host = {"H": (pinned_bf(inp["H"].transpose(1, 0, 2)), d.H),
+                "z": (torch.from_numpy(inp["z"]).pin_memory(), d.z),
+                "u": (torch.from_numpy(inp["u"]).pin_memory(), d.u)}
+        tokens = cfg.B * cfg.gamma
+    else:
+        d = pkg.pipeline.TreeDrafter(*common, inp["parent"], B=cfg.B, D=cfg.gamma, Wd=cfg.width,
+                                     budget=cfg.budget, act=cfg.act, T=cfg.T, seed=inp["gumbel_seed"])
+        host = {"Hr_h": (pinned_bf(inp["Hr_h"].transpose(1, 0, 2)), d.Hr_h),
+                "Hn": (pinned_bf(inp["Hn"]), d.Hn),
+                "z": (torch.from_numpy(inp["z"]).pin_memory(), d.z),
+                "u_node": (torch.from_numpy(inp["u_node"]).pin_memory(), d.u_node),
+                "u_res": (torch.from_numpy(inp["u_res"]).pin_memory(), d.u_res)}
+        tokens = cfg.B * cfg.gamma * cfg.width
+    for h, dv in host.values():
+        dv.copy_(h)
+    return d, host, tokens
+
+
+def algorithmic_bytes(cfg, d):
+    """Per head launch (list) and per step, counted once per byte the path must move: every W row of
+    the (per-position) union once, the router weights once per position, each target row once, the
+    ids, logits and hidden states once."""
+    V, dd, M, Hr = cfg.V, cfg.d, cfg.M, cfg.Hr
+    G = 1 if cfg.mode == "chain" else cfg.width
+    n_pos = cfg.gamma
+    offs = d.vs_offsets.cpu().numpy()
+    sizes = np.diff(offs, axis=1)                                       # [pos, B]
+    union = d.union_count.cpu().numpy()[:, 0] if getattr(d, "union", True) and hasattr(d, "union_count") else None
+    heads = []
+    for t in range(n_pos):
+        S = float(sizes[t].sum())
+        rows = S if union is None else float(union[t])                   # W rows streamed
+        ids_bytes = 4 * rows if union is None else 8 * rows              # list ids / union ids + clusters
+        heads.append(rows * 2 * dd + ids_bytes + 4 * S * G + cfg.B * G * 2 * dd)
+    router = 2 * (Hr * dd + Hr + M * Hr + M) + cfg.B * (2 * dd + 4 * Hr * 2 + 4 * M)
+    rows_target = cfg.gamma + 1 if cfg.mode == "chain" else 1 + cfg.gamma * cfg.width
+    verify = 4 * cfg.B * rows_target * V
+    return heads, float(sum(heads) + n_pos * router + verify), (union.tolist() if union is not None else None), sizes
+
+
 def run_ours(args):
     import torch
     import workloads as wl
@@ -214,25 +282,9 @@ def run_ours(args):
     dev = torch.device("cuda", local_rank)
     pkg.load_library()
     cfg = wl.config(args.config)
-    assert cfg.mode == "chain"
     seed = args.seed + rank                      # each replica drafts its own sequences
-    inp = wl.chain_inputs(cfg, seed)
-
-    def bf(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    d = pkg.pipeline.ChainDrafter(bf(inp["W"]), bf(inp["W1"]), bf(inp["b1"]), bf(inp["W2"]), bf(inp["b2"]),
-                                  torch.as_tensor(inp["csr_off"]), torch.as_tensor(inp["csr_tok"]),
-                                  B=cfg.B, gamma=cfg.gamma, budget=cfg.budget, act=cfg.act, T=cfg.T,
-                                  seed=inp["gumbel_seed"])
-    # step inputs in pinned host memory (the e2e leg copies them every step)
-    H_host = torch.from_numpy(np.ascontiguousarray(inp["H"].transpose(1, 0, 2)).view(np.int16)) \
-        .view(torch.bfloat16).pin_memory()
-    z_host = torch.from_numpy(inp["z"]).pin_memory()
-    u_host = torch.from_numpy(inp["u"]).pin_memory()
-    d.H.copy_(H_host)
-    d.z.copy_(z_host)
-    d.u.copy_(u_host)
+    inp = wl.chain_inputs(cfg, seed) if cfg.mode == "chain" else wl.tree_inputs(cfg, seed)
+    d, host, tokens_per_step = build_drafter(cfg, inp, dev, pkg, torch)
     d.enable_head_timing()
     d.capture()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -243,7 +295,6 @@ def run_ours(args):
         d.replay()
     torch.cuda.synchronize()
     d.check_status()
-    sizes = np.diff(d.vs_offsets.cpu().numpy(), axis=1)[:, 0] if cfg.B == 1 else None
 
     K = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -276,32 +327,28 @@ def run_ours(args):
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         total_ms = float(t.item())
     d.check_status()
-    tokens_per_step = cfg.B * cfg.gamma
     value = world * tokens_per_step * K / (total_ms * 1e-3)
 
     # e2e through the public API: pinned host inputs -> device, step, results -> host
     Ke = min(K, args.e2e_steps)
-    acc_h = torch.empty(cfg.B, dtype=torch.int32).pin_memory()
-    cor_h = torch.empty(cfg.B, dtype=torch.int32).pin_memory()
-    tok_h = torch.empty(cfg.gamma, cfg.B, dtype=torch.int32).pin_memory()
+    outs = [d.accepted, d.correction, d.tokens] + ([d.path] if cfg.mode == "tree" else [])
+    outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     e2e_ms = 0.0
     for i in range(Ke):
         flush.fill_(i & 0xFF)
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record(main)
-        d.H.copy_(H_host, non_blocking=True)
-        d.z.copy_(z_host, non_blocking=True)
-        d.u.copy_(u_host, non_blocking=True)
+        for h, dv in host.values():
+            dv.copy_(h, non_blocking=True)
         d.replay()
-        acc_h.copy_(d.accepted, non_blocking=True)
-        cor_h.copy_(d.correction, non_blocking=True)
-        tok_h.copy_(d.tokens, non_blocking=True)
+        for oh, o in zip(outs_h, outs):
+            oh.copy_(o, non_blocking=True)
         e.record(main)
         e.synchronize()
         e2e_ms += s.elapsed_time(e)
-    h2d = H_host.numel() * 2 + z_host.numel() * 4 + u_host.numel() * 4
-    d2h = (acc_h.numel() + cor_h.numel() + tok_h.numel()) * 4
+    h2d = sum(h.numel() * h.element_size() for h, _ in host.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs_h)
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -310,42 +357,41 @@ def run_ours(args):
 
     # roofline of the dominant kernel: the gathered head (algorithmic bytes per launch)
     peak, peak_src = load_peak()
-    hm = np.array(head_ms)                               # [samples, gamma] ms
-    if sizes is not None:
-        head_bytes = sizes.astype(np.float64) * (2 * cfg.d + 8) + 2 * cfg.d   # W rows + id + logit, h
-    else:
-        head_bytes = None
-    roof = None
-    if head_bytes is not None:
-        achieved = float(head_bytes.sum() / (hm.mean(axis=0).sum() * 1e-3) / 1e9)
-        traffic = committed_traffic()
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": traffic, "kernel": "head_gemv_kernel (gathered head, per-row path, software-pipelined 16-byte loads)",
-                "algorithmic_bytes_per_launch": float(head_bytes.mean()),
-                "avg_launch_us": float(hm.mean() * 1e3), "peak_source": peak_src,
-                "shortlist_sizes": sizes.tolist()}
-    step_bytes = None
-    if sizes is not None:
-        router_bytes = 2 * (cfg.Hr * cfg.d + cfg.Hr + cfg.M * cfg.Hr + cfg.M) + 4 * cfg.Hr * 2 + 4 * cfg.M * 2
-        verify_bytes = 4 * cfg.B * (cfg.gamma + 1) * cfg.V
-        step_bytes = float(head_bytes.sum() + cfg.gamma * router_bytes + verify_bytes)
+    hm = np.array(head_ms)                               # [samples, positions] ms
+    head_bytes, step_bytes, union, sizes = algorithmic_bytes(cfg, d)
+    per_row = cfg.mode == "chain" and cfg.B == 1
+    achieved = float(sum(head_bytes) / (hm.mean(axis=0).sum() * 1e-3) / 1e9)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": committed_traffic() if per_row and cfg.name == "llama_b1" else None,
+            "kernel": ("head_gemv_kernel (gathered head, per-row path, software-pipelined 16-byte loads)"
+                       if per_row else "head_union_kernel (gathered head over the union of the lists)"),
+            "algorithmic_bytes_per_launch": float(np.mean(head_bytes)),
+            "avg_launch_us": float(hm.mean() * 1e3), "peak_source": peak_src,
+            "shortlist_sizes": sizes.sum(axis=1).tolist(), "union_rows": union}
 
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline:
         import oracle
-        v, n, dt = oracle_sample(inp, budget_s=20.0, max_steps=10 ** 9, warmup=1)
-        cpu = {"value": v, "unit": UNIT, "cores": oracle.get_threads(), "kind": "oracle",
-               "sample": f"{n} oracle draft positions of sequence 0 of this workload "
-                         f"(+ chain verification every {cfg.gamma}th), {dt:.1f} s"}
+        if cfg.mode == "chain":
+            v, n, dt = oracle_sample(inp, budget_s=20.0, max_steps=10 ** 9, warmup=1)
+            sample = (f"{n} oracle draft positions of sequence 0 of this workload "
+                      f"(+ chain verification every {cfg.gamma}th), {dt:.1f} s")
+        else:
+            t0 = time.perf_counter()
+            oracle.tree_step(inp, seqs=[0])
+            dt = time.perf_counter() - t0
+            v = cfg.gamma * cfg.width / dt
+            sample = f"one whole tree step of sequence 0 ({cfg.gamma * cfg.width} nodes + tree verification), {dt:.1f} s"
+        cpu = {"value": v, "unit": UNIT, "cores": oracle.get_threads(), "kind": "oracle", "sample": sample}
     cfgd = workload_config(cfg)
     cfgd["seed"] = args.seed
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": cfgd, "roofline": roof,
-            "step_roofline": None if step_bytes is None else {
+            "step_roofline": {
                 "algorithmic_bytes": step_bytes, "achieved_gbs": step_bytes / (total_ms / K * 1e-3) / 1e9,
                 "frac": step_bytes / (total_ms / K * 1e-3) / 1e9 / peak},
             "cpu_baseline": cpu,

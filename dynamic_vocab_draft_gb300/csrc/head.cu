@@ -189,18 +189,9 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
 }
 
 // ---------------------------------------------------------------------------------------
-// Union path: W read once over the union of the lists, all head rows on the tensor cores.
-//
-// Swap-AB tile: the 128 union rows of W are the MMA's M side (8 warps x 16 rows) and the
-// R = B*G head rows are its N side (NT tiles of 8, R <= 128), K swept in 64-element (128-
-// byte) slabs through a STAGES-deep cp.async ring.  Shared-memory rows are 128 bytes with the
-// 16-byte chunks XOR-swizzled by (row & 7), so ldmatrix reads are bank-conflict free.
+// Helpers of the union path.
 // ---------------------------------------------------------------------------------------
-constexpr int kUnWarps = 8;
-constexpr int kUnRows = 128;            // W rows per tile
-constexpr int kUnBK = 64;               // K elements per slab
-constexpr int kUnStages = 4;
-constexpr int kUnMaxRows = 128;         // head rows (N side)
+constexpr int kUnMaxRows = 128;                 // head rows
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -214,212 +205,305 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int sr
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
 template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N)); }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-
-__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1)
-{
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// byte offset of 16-byte chunk `ch` of row `r` in a 128-byte-row swizzled slab
-__device__ __forceinline__ uint32_t swz(int r, int ch) { return uint32_t(r * 128 + ((ch ^ (r & 7)) << 4)); }
-
 struct UnionArgs {
     HeadArgs h;
     int B, G, R, M;
     const int32_t *cpos, *rank, *union_ids, *union_cluster, *union_count;
 };
 
-template <int NT>
-struct UnionSmem {
-    static constexpr int kA = kUnRows * 128;          // bytes per A slab
-    static constexpr int kB = NT * 8 * 128;           // bytes per B slab
-    static constexpr int kStage = kA + kB;
-    static constexpr size_t kBytes = size_t(kUnStages) * kStage + sizeof(Stat) * kUnWarps * NT * 8
-                                     + 3 * kUnRows * sizeof(int32_t) + 128;
+// ---------------------------------------------------------------------------------------
+// Union path on the 5th-generation tensor cores (tcgen05, accumulator in tensor memory).
+//
+// Block tile: 128 union rows of W (the MMA's M side) x all head rows (N = 16*MT) x the full
+// depth d, swept in stages of kTcAtoms * 64 columns.  Every stage holds, in shared memory, the
+// 128 W rows and the N head rows for those columns in the 128-byte-swizzled K-major layout the
+// MMA descriptors describe (8-row x 128-byte atoms, 16-byte chunk c of row r at c ^ (r & 7));
+// each row contributes kTcAtoms * 128 contiguous bytes per stage.  All threads fill a stage with
+// cp.async; one thread issues the stage's MMAs (M=128, N=16*MT, K=16 each) and commits them
+// to the stage's mbarrier, which gates the stage's reuse.  The 128 x N fp32 accumulator lives
+// in tensor memory; the epilogue reads it with tcgen05.ld (warps 0-3 and 4-7 split the
+// columns, each warp its 32 lanes = W rows) and scatters the selected logits.
+// ---------------------------------------------------------------------------------------
+constexpr int kTcRows = 128;
+constexpr int kTcThreads = 256;
+
+template <int MT> struct TcCfg {
+    static constexpr int N = 16 * MT;
+    static constexpr int kAtoms = MT <= 5 ? 4 : 2;              // 64-column atoms per stage
+    static constexpr int kStages = MT <= 5 ? 2 : 3;
+    static constexpr int kABytes = kAtoms * kTcRows * 128;      // W part of a stage
+    static constexpr int kBBytes = kAtoms * N * 128;            // H part of a stage
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kTmemCols = N <= 32 ? 32 : N <= 64 ? 64 : 128;
+    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 /* align */ +
+                                    3 * kTcRows * sizeof(int32_t) + 64;
 };
 
-template <int NT>
-__global__ void __launch_bounds__(kUnWarps * 32, 1)
-head_union_kernel(UnionArgs a, Stat *__restrict__ partials)
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr)
 {
-    extern __shared__ __align__(128) unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    using L = UnionSmem<NT>;
-    Stat *s_stat = reinterpret_cast<Stat *>(smem + kUnStages * L::kStage);       // [warp][NT*8]
-    int32_t *s_uid = reinterpret_cast<int32_t *>(s_stat + kUnWarps * NT * 8);    // [128]
-    int32_t *s_ucl = s_uid + kUnRows;
-    int32_t *s_rnk = s_ucl + kUnRows;
-    const uint32_t s_base = smem_u32(smem);
+    uint64_t d = 0;
+    d |= uint64_t((saddr >> 4) & 0x3FFFu);             // start address
+    d |= uint64_t(1) << 16;                             // leading byte offset (unused, K-major SW128)
+    d |= uint64_t((1024u >> 4) & 0x3FFFu) << 32;        // stride byte offset: next 8-row group
+    d |= uint64_t(1) << 46;                             // descriptor version
+    d |= uint64_t(2) << 61;                             // 128-byte swizzle
+    return d;
+}
 
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void proxy_fence_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kTcThreads, 1)
+head_union_tc_kernel(UnionArgs a)
+{
+    using C = TcCfg<MT>;
+    extern __shared__ __align__(1024) unsigned char tc_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
+    int32_t *s_v = reinterpret_cast<int32_t *>(sm + size_t(C::kStages) * C::kStageBytes);
+    int32_t *s_c = s_v + kTcRows;
+    int32_t *s_rk = s_c + kTcRows;
+    __shared__ uint64_t mma_done[4];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_fail;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d = a.h.d, R = a.R, G = a.G, M = a.M;
-    const int nU = min(*a.union_count, a.h.V);
-    const int ntiles = (nU + kUnRows - 1) / kUnRows;
-    const int KT = (d + kUnBK - 1) / kUnBK;
+    const int d = a.h.d, R = a.R, G = a.G, M = a.M, V = a.h.V;
+    const int nU = min(*a.union_count, V);
+    const int ntiles = (nU + kTcRows - 1) / kTcRows;
+    const int kstage = C::kAtoms * 64;
+    const int nks = (d + kstage - 1) / kstage;                  // stages per tile
+    constexpr uint32_t idesc = umma_idesc_bf16(kTcRows, C::N);
 
-    for (int i = tid; i < kUnWarps * NT * 8; i += blockDim.x) s_stat[i] = stat_empty();
+    if (tid == 0) {
+        for (int i = 0; i < C::kStages; ++i) mbar_init(&mma_done[i], 1);
+        mbar_fence_init();
+        s_fail = 0;
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_addr(&s_tmem)), "r"(uint32_t(C::kTmemCols)) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    unsigned uses[4] = {0, 0, 0, 0};                            // completed commits per stage slot
+
+    // cp.async fill of stage slot `slot` with columns [ks*kstage, ...) of this tile
+    auto fill = [&](int slot, int ks) {
+        unsigned char *A = sm + size_t(slot) * C::kStageBytes;
+        unsigned char *Bm = A + C::kABytes;
+        const int k0 = ks * kstage;
+        // A: kTcRows rows x kAtoms atoms x 8 chunks
+        for (int q = tid; q < kTcRows * C::kAtoms * 8; q += kTcThreads) {
+            const int r = q / (C::kAtoms * 8), rem = q - r * (C::kAtoms * 8);
+            const int at = rem >> 3, ch = rem & 7;
+            const int k = k0 + at * 64 + ch * 8;
+            const int v = s_v[r];
+            const bool ok = v >= 0 && k < d;
+            const uint16_t *src = ok ? a.h.W + size_t(v) * d + k : a.h.W;
+            cp_async16(smem_u32(A + at * (kTcRows * 128) + r * 128 + ((ch ^ (r & 7)) << 4)), src, ok ? 16 : 0);
+        }
+        for (int q = tid; q < C::N * C::kAtoms * 8; q += kTcThreads) {
+            const int r = q / (C::kAtoms * 8), rem = q - r * (C::kAtoms * 8);
+            const int at = rem >> 3, ch = rem & 7;
+            const int k = k0 + at * 64 + ch * 8;
+            const bool ok = r < R && k < d;
+            const uint16_t *src = ok ? a.h.H + size_t(r) * d + k : a.h.H;
+            cp_async16(smem_u32(Bm + at * (C::N * 128) + r * 128 + ((ch ^ (r & 7)) << 4)), src, ok ? 16 : 0);
+        }
+        cp_async_commit();
+    };
+    // wait until the MMAs that last read stage slot `slot` are done (bounded)
+    auto slot_free = [&](int slot) -> bool {
+        if (uses[slot] == 0) return true;
+        return mbar_wait(&mma_done[slot], (uses[slot] - 1) & 1u);
+    };
 
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        __syncthreads();                    // previous tile's epilogue is done with s_uid
-        for (int r = tid; r < kUnRows; r += blockDim.x) {
-            const int u = tile * kUnRows + r;
+        __syncthreads();
+        if (s_fail) break;                              // read after a barrier: uniform
+        for (int q = tid; q < kTcRows; q += kTcThreads) {
+            const int u = tile * kTcRows + q;
             int v = -1, c = -1, rk = 0;
             if (u < nU) {
                 v = a.union_ids[u];
                 c = a.union_cluster[u];
-                if (v < 0 || v >= a.h.V || c < 0 || c >= M) { set_status(a.h.status, DS_DEV_BAD_INDEX); v = -1; }
+                if (v < 0 || v >= V || c < 0 || c >= M) { set_status(a.h.status, DS_DEV_BAD_INDEX); v = -1; }
                 else rk = a.rank[v];
             }
-            s_uid[r] = v; s_ucl[r] = c; s_rnk[r] = rk;
+            s_v[q] = v; s_c[q] = c; s_rk[q] = rk;
         }
         __syncthreads();
-
-        auto load_slab = [&](int stage, int kt) {
-            const uint32_t sa = s_base + stage * L::kStage;
-            const uint32_t sb = sa + L::kA;
-            const int k0 = kt * kUnBK;
-            // A: 128 rows x 8 chunks
-#pragma unroll
-            for (int i = 0; i < (kUnRows * 8) / (kUnWarps * 32); ++i) {
-                const int q = tid + i * kUnWarps * 32;
-                const int r = q >> 3, ch = q & 7;
-                const int k = k0 + ch * 8;
-                const int v = s_uid[r];
-                const bool ok = v >= 0 && k < d;
-                const uint16_t *src = ok ? a.h.W + size_t(v) * d + k : a.h.W;
-                cp_async16(sa + swz(r, ch), src, ok ? 16 : 0);
+        // prologue: the first kStages - 1 stages
+        for (int s = 0; s < C::kStages - 1; ++s) {
+            if (s < nks) {
+                if (!slot_free(s)) { s_fail = 1; set_status(a.h.status, DS_DEV_TIMEOUT); }
+                fill(s, s);
+            } else {
+                cp_async_commit();
             }
-            // B: NT*8 head rows x 8 chunks
-            for (int q = tid; q < NT * 8 * 8; q += kUnWarps * 32) {
-                const int r = q >> 3, ch = q & 7;
-                const int k = k0 + ch * 8;
-                const bool ok = r < R && k < d;
-                const uint16_t *src = ok ? a.h.H + size_t(r) * d + k : a.h.H;
-                cp_async16(sb + swz(r, ch), src, ok ? 16 : 0);
-            }
-        };
-
-        float acc[NT][4];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-#pragma unroll
-        for (int s = 0; s < kUnStages - 1; ++s) {
-            if (s < KT) load_slab(s, s);
-            cp_async_commit();
         }
-        for (int kt = 0; kt < KT; ++kt) {
-            cp_async_wait<kUnStages - 2>();
+        for (int ks = 0; ks < nks; ++ks) {
+            const int slot = ks % C::kStages;
+            // refill the slot the stage kStages-1 ahead will use
+            const int nk = ks + C::kStages - 1;
+            if (nk < nks) {
+                const int ns = nk % C::kStages;
+                if (!slot_free(ns)) { s_fail = 1; set_status(a.h.status, DS_DEV_TIMEOUT); }
+                fill(ns, nk);
+            } else {
+                cp_async_commit();
+            }
+            cp_async_wait<C::kStages - 1>();            // stage ks has landed (this thread's part)
+            proxy_fence_async();                         // make it visible to the tensor cores
             __syncthreads();
-            const int nk = kt + kUnStages - 1;
-            if (nk < KT) load_slab(nk % kUnStages, nk);
-            cp_async_commit();
-            const uint32_t sa = s_base + (kt % kUnStages) * L::kStage;
-            const uint32_t sb = sa + L::kA;
+            if (s_fail) break;                           // uniform: read after the barrier
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t A = smem_u32(sm + size_t(slot) * C::kStageBytes);
+                const uint32_t Bm = A + C::kABytes;
 #pragma unroll
-            for (int ks = 0; ks < kUnBK / 16; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                {
-                    const int r = warp * 16 + (lane & 15);
-                    const int ch = ks * 2 + (lane >> 4);
-                    ldsm_x4(sa + swz(r, ch), a0, a1, a2, a3);
-                }
+                for (int at = 0; at < C::kAtoms; ++at) {
 #pragma unroll
-                for (int j = 0; j + 1 < NT; j += 2) {
-                    uint32_t b0, b1, b2, b3;
-                    const int r = (j + (lane >> 4)) * 8 + (lane & 7);
-                    const int ch = ks * 2 + ((lane >> 3) & 1);
-                    ldsm_x4(sb + swz(r, ch), b0, b1, b2, b3);
-                    mma_bf16(acc[j], a0, a1, a2, a3, b0, b1);
-                    mma_bf16(acc[j + 1], a0, a1, a2, a3, b2, b3);
-                }
-                if (NT & 1) {
-                    uint32_t b0, b1;
-                    const int r = (NT - 1) * 8 + (lane & 7);
-                    const int ch = ks * 2 + ((lane >> 3) & 1);
-                    ldsm_x2(sb + swz(r, ch), b0, b1);
-                    mma_bf16(acc[NT - 1], a0, a1, a2, a3, b0, b1);
-                }
-            }
-        }
-        cp_async_wait<0>();
-
-        // Epilogue: keep (W row, head row) pairs whose list selects the row's cluster.
-        const int rl0 = warp * 16 + (lane >> 2);
-        int vv[2], cc[2], rk[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) { vv[e] = s_uid[rl0 + 8 * e]; cc[e] = s_ucl[rl0 + 8 * e]; rk[e] = s_rnk[rl0 + 8 * e]; }
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int n = j * 8 + (lane & 3) * 2 + q;      // head row
-                Stat st = stat_empty();
-                if (n < R) {
-                    const int b = n / G, gi = n - b * G;
-                    const int off = a.h.vs_offsets[b];
-                    const int nb = a.h.vs_offsets[b + 1] - off;
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        if (vv[e] < 0) continue;
-                        const int p = a.cpos[size_t(b) * M + cc[e]];
-                        if (p < 0) continue;
-                        const int jj = p + rk[e];
-                        const float l = acc[j][2 * e + q];
-                        a.h.logits[int64_t(off) * G + int64_t(gi) * nb + jj] = l;
-                        const float x = l * a.h.inv_te;
-                        const float key = a.h.T > 0.f ? x + gumbel(a.h.seed, uint32_t(vv[e]), uint32_t(a.h.pos), uint32_t(n)) : l;
-                        stat_add(st, x, key, vv[e], jj);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = umma_desc_sw128(A + at * (kTcRows * 128) + kk * 32);
+                        const uint64_t bd = umma_desc_sw128(Bm + at * (C::N * 128) + kk * 32);
+                        tc_mma(tmem, ad, bd, idesc, (ks > 0 || at > 0 || kk > 0) ? 1u : 0u);
                     }
                 }
-                // combine the 8 lanes that hold this column (lane bits 2..4), in lane order
+                tc_commit(&mma_done[slot]);
+            }
+            uses[slot] += 1;
+        }
+        // epilogue: wait for the tile's last MMAs, read the accumulator, scatter selected logits
+        const int last = (nks - 1) % C::kStages;
+        if (!s_fail && !mbar_wait(&mma_done[last], (uses[last] - 1) & 1u)) {
+            s_fail = 1;
+            set_status(a.h.status, DS_DEV_TIMEOUT);
+        }
+        __syncthreads();
+        if (s_fail) break;
+        tc_fence_after();
+        {
+            const int wq = warp & 3;                         // TMEM lane quarter this warp may read
+            const int row = wq * 32 + lane;                  // W row of the tile
+            const int v = s_v[row];
+            const int c = s_c[row], rk = s_rk[row];
+            for (int cb = (warp >> 2) * 16; cb < C::N; cb += 32) {
+                uint32_t r16[16];
+                tc_ld16(tmem + (uint32_t(wq * 32) << 16) + uint32_t(cb), r16);
+                if (v < 0) continue;
 #pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    const Stat other = shfl_xor_stat(st, o);
-                    st = (lane & o) ? stat_merge(other, st) : stat_merge(st, other);
-                }
-                if (lane < 4 && n < R) {
-                    Stat &dst = s_stat[warp * NT * 8 + n];
-                    dst = stat_merge(dst, st);
+                for (int e = 0; e < 16; ++e) {
+                    const int r = cb + e;
+                    if (r >= R) break;
+                    const int b = r / G, gi = r - b * G;
+                    const int pc = a.cpos[size_t(b) * M + c];
+                    if (pc < 0) continue;
+                    const int off = a.h.vs_offsets[b];
+                    const int nb = a.h.vs_offsets[b + 1] - off;
+                    a.h.logits[int64_t(off) * G + int64_t(gi) * nb + pc + rk] = __uint_as_float(r16[e]);
                 }
             }
         }
+        tc_fence_before();
     }
+    cp_async_wait<0>();
+    // all MMAs must be complete before the accumulator is released
+    if (tid == 0) {
+        const long long deadline = clock64() + kWaitBudgetCycles;
+        for (int i = 0; i < C::kStages; ++i)
+            if (uses[i]) (void)mbar_wait_until(&mma_done[i], (uses[i] - 1) & 1u, deadline);
+    }
+    tc_fence_before();
     __syncthreads();
-    for (int n = tid; n < R; n += blockDim.x) {
-        Stat c = s_stat[n];
-        for (int w = 1; w < kUnWarps; ++w) c = stat_merge(c, s_stat[w * NT * 8 + n]);
-        partials[size_t(n) * gridDim.x + blockIdx.x] = c;
-    }
+    tc_fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem), "r"(uint32_t(C::kTmemCols)) : "memory");
 }
 
-// One warp per head row: fold the union kernel's per-block partials in a fixed order.
-__global__ void head_union_finalize_kernel(HeadArgs a, int R, int nblocks, const Stat *__restrict__ partials)
+// Softmax statistics and the draft draw of every head row from its stored logits.
+// grid (chunks, R): block (x, r) folds elements [x*kRsChunk, ...) of row r; the last block of the
+// row combines the partials in a fixed order.
+constexpr int kRsPer = 16;
+constexpr int kRsChunk = 256 * kRsPer;
+
+__global__ void __launch_bounds__(256)
+head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *__restrict__ counters)
 {
-    const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (n >= R) return;
+    __shared__ Stat ws[8];
+    const int r = blockIdx.y, b = r / G, gi = r - b * G;
+    const int off = a.vs_offsets[b];
+    const int n = a.vs_offsets[b + 1] - off;
+    const float *l = a.logits + int64_t(off) * G + int64_t(gi) * n;
+    const int32_t *ids = a.vs_ids + off;
+    Stat st = stat_empty();
+    const int j0 = blockIdx.x * kRsChunk + threadIdx.x * kRsPer;
+    for (int e = 0; e < kRsPer; ++e) {
+        const int j = j0 + e;
+        if (j >= n) break;
+        const float lj = l[j];
+        const int v = ids[j];
+        const float x = lj * a.inv_te;
+        const float key = a.T > 0.f ? x + gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(r)) : lj;
+        stat_add(st, x, key, v, j);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const Stat other = shfl_xor_stat(st, o);
+        st = (lane & o) ? stat_merge(other, st) : stat_merge(st, other);
+    }
+    if (lane == 0) ws[warp] = st;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        Stat c = ws[0];
+        for (int w = 1; w < 8; ++w) c = stat_merge(c, ws[w]);
+        st_stat(&partials[size_t(r) * kGvMaxBlocks + blockIdx.x], c);
+    }
+    if (!last_block_done(&counters[r], gridDim.x)) return;
+    if (warp != 0) return;
     Stat c = stat_empty();
-    for (int i = lane; i < nblocks; i += 32) c = stat_merge(c, partials[size_t(n) * nblocks + i]);
+    for (int i = lane; i < int(gridDim.x); i += 32) c = stat_merge(c, ld_stat(&partials[size_t(r) * kGvMaxBlocks + i]));
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const Stat other = shfl_xor_stat(c, o);
         c = (lane & o) ? stat_merge(other, c) : stat_merge(c, other);
     }
-    if (lane == 0) write_row(a, n, c);
+    if (lane == 0) write_row(a, r, c);
 }
 
 }  // namespace
@@ -431,25 +515,19 @@ namespace {
 
 constexpr size_t kHeadPartialsPerRow = 1024;   // >= kGvMaxBlocks and >= any union grid
 
-template <int NT>
-ds_status launch_union(const UnionArgs &ua, Stat *partials, cudaStream_t stream, int *grid_out)
+template <int MT>
+ds_status launch_union(const UnionArgs &ua, cudaStream_t stream)
 {
-    const size_t smem = UnionSmem<NT>::kBytes;
-    static int occ = -1;
-    if (occ < 0) {
-        if (cudaFuncSetAttribute(head_union_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = TcCfg<MT>::kSmem;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(head_union_tc_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(smem)) != cudaSuccess)
             return DS_ERR_CUDA;
-        int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, head_union_kernel<NT>, kUnWarps * 32, smem) != cudaSuccess)
-            return DS_ERR_CUDA;
-        occ = o > 0 ? o : 1;
+        attr = true;
     }
-    int grid = num_sms() * occ;
-    if (grid > int(kHeadPartialsPerRow)) grid = int(kHeadPartialsPerRow);
-    head_union_kernel<NT><<<grid, kUnWarps * 32, smem, stream>>>(ua, partials);
+    head_union_tc_kernel<MT><<<num_sms(), kTcThreads, smem, stream>>>(ua);
     DS_TRY_LAUNCH();
-    *grid_out = grid;
     return DS_OK;
 }
 
@@ -518,19 +596,21 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
 
     if (!cpos || !rank_in_cluster || M < 1) return DS_ERR_INVALID_ARG;
     if (rows > kUnMaxRows) return DS_ERR_UNSUPPORTED;
+    if ((V + kRsChunk - 1) / kRsChunk > kGvMaxBlocks) return DS_ERR_UNSUPPORTED;
     UnionArgs ua;
     ua.h = a; ua.B = B; ua.G = G; ua.R = int(rows); ua.M = M;
     ua.cpos = cpos; ua.rank = rank_in_cluster;
     ua.union_ids = union_ids; ua.union_cluster = union_cluster; ua.union_count = union_count;
-    int grid = 0;
     ds_status st;
-    if (rows <= 16) st = launch_union<2>(ua, partials, stream, &grid);
-    else if (rows <= 32) st = launch_union<4>(ua, partials, stream, &grid);
-    else if (rows <= 64) st = launch_union<8>(ua, partials, stream, &grid);
-    else if (rows <= 80) st = launch_union<10>(ua, partials, stream, &grid);
-    else st = launch_union<16>(ua, partials, stream, &grid);
+    if (rows <= 16) st = launch_union<1>(ua, stream);
+    else if (rows <= 32) st = launch_union<2>(ua, stream);
+    else if (rows <= 48) st = launch_union<3>(ua, stream);
+    else if (rows <= 64) st = launch_union<4>(ua, stream);
+    else if (rows <= 80) st = launch_union<5>(ua, stream);
+    else st = launch_union<8>(ua, stream);
     if (st != DS_OK) return st;
-    head_union_finalize_kernel<<<(int(rows) + 7) / 8, 256, 0, stream>>>(a, int(rows), grid, partials);
+    const int chunks = (V + kRsChunk - 1) / kRsChunk;
+    head_rowstats_kernel<<<dim3(chunks, unsigned(rows)), 256, 0, stream>>>(a, G, partials, counters);
     DS_TRY_LAUNCH();
     return DS_OK;
 }

@@ -48,6 +48,20 @@ class _Common:
     def replay(self):
         self.graph.replay()
 
+    def enable_head_timing(self):
+        """Time every position's head launch with CUDA events (also inside a captured graph).
+        Call before capture(); read with head_times_ms() after a step or replay."""
+        self.head_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                            for _ in range(self.n_heads())]
+        for a, b in self.head_events:          # torch creates the CUDA event on its first record
+            a.record()
+            b.record()
+        torch.cuda.synchronize()
+
+    def head_times_ms(self):
+        return [a.elapsed_time(b) for a, b in self.head_events]
+
+
 
 class ChainDrafter(_Common):
     """Chain drafting: B sequences, gamma draft positions, one shortlist per (sequence, position).
@@ -103,19 +117,6 @@ class ChainDrafter(_Common):
         # optional [(start, end)] timing events around each position's head launch
         self.head_events = None
 
-    def enable_head_timing(self):
-        """Time every position's head launch with CUDA events (also inside a captured graph).
-        Call before capture(); read with head_times_ms() after a step or replay."""
-        self.head_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                            for _ in range(self.gamma)]
-        for a, b in self.head_events:          # torch creates the CUDA event on its first record
-            a.record()
-            b.record()
-        torch.cuda.synchronize()
-
-    def head_times_ms(self):
-        return [a.elapsed_time(b) for a, b in self.head_events]
-
     def route(self, t, stream=None):
         """Router + top-k + shortlist of draft position t (0-based) for all sequences."""
         api.router_topk(self.H[t], self.W1, self.b1, self.W2, self.b2, self.act, self.budget, t + 1,
@@ -153,6 +154,9 @@ class ChainDrafter(_Common):
             if self.head_events:
                 api.event_record(self.head_events[t][1])
         self.verify()
+
+    def n_heads(self) -> int:
+        return self.gamma
 
     def launches_per_step(self) -> int:
         n_router = 2
@@ -214,6 +218,7 @@ class TreeDrafter(_Common):
         self.side = torch.cuda.Stream(device=dev)
         self.ready = [torch.cuda.Event() for _ in range(D)]
         self.graph = None
+        self.head_events = None
 
     def route(self, t, stream=None):
         api.router_topk(self.Hr_h[t], self.W1, self.b1, self.W2, self.b2, self.act, self.budget, t + 1,
@@ -243,8 +248,15 @@ class TreeDrafter(_Common):
                 self.ready[t].record(self.side)
         for t in range(self.D):
             main.wait_event(self.ready[t])
+            if self.head_events:
+                api.event_record(self.head_events[t][0])
             self.head(t)
+            if self.head_events:
+                api.event_record(self.head_events[t][1])
         self.verify()
+
+    def n_heads(self) -> int:
+        return self.D
 
     def launches_per_step(self) -> int:
         return self.D * (2 + 4 + 2) + 2

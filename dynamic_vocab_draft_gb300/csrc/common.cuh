@@ -180,7 +180,7 @@ __device__ __forceinline__ bool last_block_done(unsigned *counter, unsigned nblo
 }
 
 // ---------------------------------------------------------------------------------------
-// mbarrier + bulk-copy (TMA engine) primitives.  Every wait is bounded: a wait that runs
+// mbarrier primitives.  Every wait is bounded: a wait that runs
 // past its budget returns false and the caller records DS_DEV_TIMEOUT and winds down.
 // ---------------------------------------------------------------------------------------
 constexpr long long kWaitBudgetCycles = 2000000000LL;    // about one second at 2 GHz
@@ -198,17 +198,6 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count)
 __device__ __forceinline__ void mbar_fence_init()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
-                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity)
@@ -237,14 +226,6 @@ __device__ __forceinline__ bool mbar_wait_until(uint64_t *bar, unsigned parity, 
     while (!mbar_test(bar, parity))
         if (clock64() > deadline) return false;
     return true;
-}
-
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) global -> shared,
-// completing as transaction bytes on `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, unsigned bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 :: "r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
 }
 
 }  // namespace ds

@@ -51,7 +51,7 @@ typedef int32_t ds_status;
 #define DS_DEV_BAD_INDEX    0x10  /* an id outside [0, V) or [0, M), or a draft token that is
                                      not in its shortlist                                   */
 #define DS_DEV_CAPACITY     0x20  /* a shortlist larger than the capacity the caller gave   */
-#define DS_DEV_TIMEOUT      0x40  /* a bounded wait gave up (reserved; no wait exists yet)  */
+#define DS_DEV_TIMEOUT      0x40  /* a bounded wait inside a kernel gave up (about 1 s)     */
 
 /* Router activations (summary, Key Hyperparameters: "2-layer MLP with ReLU"; the Tiny
  * workload names GELU, taken in its exact erf form). */
@@ -176,7 +176,7 @@ ds_status ds_gathered_head(const uint16_t *H, int B, int G,
  * device memory of its own: code whose device memory is owned by a pool or framework that
  * may not be grown in the middle of a step, or a plugin interface that passes only inputs
  * and outputs.  Inputs, outputs, layouts and results are those of ds_gathered_head.
- *   - Scratch is a fixed device array inside the library (about 640 KB), reserved on every
+ *   - Scratch is a fixed device array inside the library (about 6 MB), reserved on every
  *     GPU that loads the library until the process exits.  No call allocates or frees.
  *   - At most 32 head rows (B*G <= 32); larger calls return DS_ERR_UNSUPPORTED and launch
  *     nothing.

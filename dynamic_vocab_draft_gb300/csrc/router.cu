@@ -13,6 +13,7 @@
 // 32-bit keys followed by two block scans (ties to the lower cluster id, output ascending).
 #include "common.cuh"
 #include "block_scan.cuh"
+#include "tc_gemm.cuh"
 
 namespace ds {
 namespace {
@@ -267,7 +268,114 @@ gemv1_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict_
 
 constexpr int kGemv1Blocks = 32;       // 256 warps: one wave on 16 SMs (2 blocks each)
 
+// One block per row: the top-k of scores[b][0..M).
+__global__ void __launch_bounds__(kTopkThreads)
+topk_rows_kernel(const float *__restrict__ scores, int M, int k, int32_t *__restrict__ ids)
+{
+    topk_block(scores + size_t(blockIdx.x) * M, M, k, ids + size_t(blockIdx.x) * k);
+}
 
+// ---------------------------------------------------------------------------------------
+// Batched router (2 <= B <= 64) on the tensor cores, through the gathered-row GEMM with every
+// weight row picked in order.  Layer 1 multiplies W1 by the B bf16 hidden states; its
+// epilogue adds b1, applies the activation and stores the fp32 result u as a pair of bf16
+// values, hi = bf16(u) and lo = bf16(u - hi), which together carry about 16 significant bits
+// (the relative error of hi + lo is below 2^-16).  Layer 2 multiplies W2 by the 2B vectors
+// (hi_0, lo_0, hi_1, lo_1, ...) and adds each pair of columns, so the scores see u almost as
+// the fp32 path does while both layers run as bf16 MMAs with fp32 accumulation.
+// ---------------------------------------------------------------------------------------
+constexpr int kRouterTcMaxB = 64;                 // 2B vectors fit one 128-column accumulator
+constexpr int kRouterMaxTiles = kRouterMaxK / tc::kRows;
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    return uint16_t((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);      // finite inputs
+}
+
+struct DenseRows {
+    int n;
+    __device__ int n_rows() const { return n; }
+    __device__ void pick(int u, int &v, int &c) const { v = u; c = 0; }
+    __device__ void col_info(int r, int &i, long long &l) const { i = r; l = 0; }
+};
+
+// Layer 1: hid2[(2b) * Hr + i] = hi, hid2[(2b+1) * Hr + i] = lo of act(W1[i] . h_b + b1[i]).
+struct Layer1Ep : DenseRows {
+    const uint16_t *bias;
+    uint16_t *hid2;
+    int Hr, act;
+    __device__ int row_aux(int v) const { return v >= 0 ? __float_as_int(bf16_to_f32(bias[v])) : 0; }
+    __device__ void emit(const float (&x)[16], int cb, int v, int, int aux, const int32_t *s_i, const long long *) const
+    {
+        if (v < 0) return;
+        const float bv = __int_as_float(aux);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int b = s_i[cb + e];
+            if (b < 0) continue;
+            const float u = act_fn(x[e] + bv, act);
+            const uint16_t hi = f32_to_bf16_rne(u);
+            const uint16_t lo = f32_to_bf16_rne(u - bf16_to_f32(hi));
+            hid2[size_t(2 * b) * Hr + v] = hi;
+            hid2[size_t(2 * b + 1) * Hr + v] = lo;
+        }
+    }
+};
+
+// Layer 2: scores[b][c] = (W2[c] . hi_b + W2[c] . lo_b) + b2[c].
+struct Layer2Ep : DenseRows {
+    const uint16_t *bias;
+    float *scores;
+    int M, B;
+    __device__ int row_aux(int v) const { return v >= 0 ? __float_as_int(bf16_to_f32(bias[v])) : 0; }
+    __device__ void emit(const float (&x)[16], int cb, int v, int, int aux, const int32_t *, const long long *) const
+    {
+        if (v < 0) return;
+        const float bv = __int_as_float(aux);
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+            const int b = (cb + e) >> 1;
+            if (b < B) scores[size_t(b) * M + v] = (x[e] + x[e + 1]) + bv;
+        }
+    }
+};
+
+struct RouterTcWs {
+    size_t hid2, tile_cnt, parts, total;
+};
+RouterTcWs router_tc_layout(int B, int Hr)
+{
+    RouterTcWs w;
+    w.hid2 = 0;
+    w.tile_cnt = align256(size_t(2) * B * Hr * sizeof(uint16_t));
+    w.parts = w.tile_cnt + align256(size_t(kRouterMaxTiles) * sizeof(unsigned));
+    w.total = w.parts + align256(tc::parts_bytes(2 * B, tc::kMaxGrid));
+    return w;
+}
+
+int router_num_sms()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    }
+    return n;
+}
+
+// CTAs of a router GEMM: the first draft position's router runs before any head and takes the
+// whole GPU; a later position's router runs beside the batched head, which leaves
+// kRouterSideSms SMs free for it, and must fit there.
+constexpr int kRouterSideSms = 8;
+int router_grid(int pos, int units)
+{
+    int g = pos == 1 ? router_num_sms() : kRouterSideSms;
+    if (g > tc::kMaxGrid) g = tc::kMaxGrid;
+    if (g > units) g = units;
+    return g < 1 ? 1 : g;
+}
 
 template <typename XT, int BT>
 ds_status launch_gemv(const uint16_t *A, int N, int K, const XT *x, int B, const uint16_t *bias, int act,
@@ -296,6 +404,7 @@ using namespace ds;
 extern "C" size_t ds_router_workspace_bytes(int B, int Hr)
 {
     if (B <= 0 || Hr <= 0) return 0;
+    if (B >= 2 && B <= kRouterTcMaxB) return router_tc_layout(B, Hr).total;
     // hidden layer u [B, Hr] + one completion counter per batch tile of the second layer
     return align256(size_t(B) * size_t(Hr) * sizeof(float)) + align256(size_t(B) * sizeof(unsigned));
 }
@@ -308,7 +417,6 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
                                     void *ws, size_t ws_bytes, int32_t *dev_status,
                                     cudaStream_t stream)
 {
-    (void)dev_status;
     if (!H || !W1 || !b1 || !W2 || !b2 || !budget || !scores || !cluster_ids)
         return DS_ERR_INVALID_ARG;
     if (B < 1 || B > 4096 || d < 8 || d % 8 || Hr < 8 || Hr % 8 || M < 1 || M > kRouterMaxK)
@@ -330,6 +438,28 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
         DS_TRY_LAUNCH();
         gemv1_kernel<float><<<kGemv1Blocks, kGemvWarps * 32, 0, stream>>>(W2, M, Hr, u, b2, -1, scores, k,
                                                                          cluster_ids, counters);
+        DS_TRY_LAUNCH();
+        return DS_OK;
+    }
+    if (B <= kRouterTcMaxB) {
+        const RouterTcWs lay = router_tc_layout(B, Hr);
+        char *w = static_cast<char *>(ws);
+        uint16_t *hid2 = reinterpret_cast<uint16_t *>(w + lay.hid2);
+        unsigned *tile_cnt = reinterpret_cast<unsigned *>(w + lay.tile_cnt);
+        float *parts = reinterpret_cast<float *>(w + lay.parts);
+        Layer1Ep e1;
+        e1.n = Hr; e1.bias = b1; e1.hid2 = hid2; e1.Hr = Hr; e1.act = act;
+        const tc::Operands op1{W1, H, d, B, dev_status};
+        const int u1 = ((Hr + tc::kRows - 1) / tc::kRows) * ((d + 127) / 128);
+        ds_status st = tc::launch_for(op1, e1, parts, tile_cnt, router_grid(pos, u1), stream);
+        if (st != DS_OK) return st;
+        Layer2Ep e2;
+        e2.n = M; e2.bias = b2; e2.scores = scores; e2.M = M; e2.B = B;
+        const tc::Operands op2{W2, hid2, Hr, 2 * B, dev_status};
+        const int u2 = ((M + tc::kRows - 1) / tc::kRows) * ((Hr + 127) / 128);
+        st = tc::launch_for(op2, e2, parts, tile_cnt, router_grid(pos, u2), stream);
+        if (st != DS_OK) return st;
+        topk_rows_kernel<<<B, kTopkThreads, 0, stream>>>(scores, M, k, cluster_ids);
         DS_TRY_LAUNCH();
         return DS_OK;
     }

@@ -104,8 +104,18 @@ shortlist_offsets_kernel(const int32_t *__restrict__ off, int M, int B,
     for (int e = 0; e < kSlMaxPer; ++e) {
         const int c = lo + e;
         bool any = false;
-        if (e < E && c < M)
-            for (int b = 0; b < B && !any; ++b) any = cpos[size_t(b) * M + c] >= 0;
+        if (e < E && c < M) {
+            // eight independent loads per round instead of a dependent chain over b
+            int b = 0;
+            for (; b + 8 <= B && !any; b += 8) {
+                int q[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) q[j] = cpos[size_t(b + j) * M + c];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) any |= q[j] >= 0;
+            }
+            for (; b < B && !any; ++b) any = cpos[size_t(b) * M + c] >= 0;
+        }
         sz[e] = any ? off[c + 1] - off[c] : 0;
         sum += sz[e];
     }

@@ -1,0 +1,429 @@
+// Gathered-row GEMM on the 5th-generation tensor cores (tcgen05, accumulator in tensor memory).
+//
+//   out[u][r] = sum_k A[row(u)][k] * Bop[r][k]      u < n_rows (a list of rows of A), r < R
+//
+// A is a row-major bf16 matrix whose rows are picked through a list (the union of the
+// shortlists for the gathered head, or simply 0..n-1 for the router layers); Bop holds the R
+// bf16 vectors every picked row is scored against.  A policy object (`Ep`) names the picked
+// rows and consumes finished accumulator columns, so the same kernel serves the head (which
+// scatters logits into per-list positions) and the router layers (bias, activation, dense
+// output).  Accumulation is fp32 in tensor memory.
+//
+// Work: tiles of 128 picked rows (the MMA's M side) x all R vectors (N = 16*MT, zero padded) x
+// the full depth d, each tile swept in k-stages of kCols columns.  The (tile, k-stage) units,
+// in tile order, are split into equal contiguous ranges, one per CTA of a persistent grid (a
+// stream-K split), so every SM streams the same number of A bytes whatever the list size; a
+// tile whose stages fall into several CTAs is finished by the last of them, which adds the
+// parts in k order (so results do not depend on timing).
+//
+// Per CTA one software pipeline runs across its tiles: kStages shared-memory slots, loads
+// kLook stages ahead of the stage being multiplied, and the MMAs of stage i are waited for
+// only when their slot is refilled two stages later, so the loads never wait on the tensor
+// core.  A slot holds the 128 A rows and the N B rows for its columns in the 128-byte-swizzled
+// K-major layout the MMA descriptors describe (8-row x 128-byte atoms, 16-byte chunk c of row
+// r at c ^ (r & 7)).  Each of the 512 threads copies one fixed 16-byte column chunk of a fixed
+// set of rows with cp.async, so a stage costs a handful of instructions per thread; one thread
+// issues the MMAs (M=128, N=16*MT, K=16 each) and commits them to the slot's mbarrier.  At a
+// tile's end the epilogue reads the 128 x N accumulator with tcgen05.ld (the four warps of
+// each TMEM lane quarter split the columns, each warp its 32 lanes = A rows) while the next
+// stages' loads are in flight.
+//
+// Every wait on an mbarrier is bounded; a wait that gives up sets DS_DEV_TIMEOUT, the CTA
+// stops, waits (bounded) for its MMAs in flight and frees its tensor memory.
+#pragma once
+#include "common.cuh"
+
+namespace ds {
+namespace tc {
+
+constexpr int kRows = 128;                  // A rows per tile (MMA M)
+constexpr int kThreads = 512;
+constexpr int kMaxGrid = 160;               // CTAs of one launch (<= SMs in use)
+
+__host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+// MT = N / 16 for R vectors: 16, 32, 48, 64, 80 or 128 columns.
+__host__ __device__ constexpr int mt_for(int R)
+{
+    return R <= 16 ? 1 : R <= 32 ? 2 : R <= 48 ? 3 : R <= 64 ? 4 : R <= 80 ? 5 : 8;
+}
+
+template <int MT> struct Cfg {
+    static constexpr int N = 16 * MT;
+    static constexpr int kAtoms = MT >= 8 ? 1 : 2;             // 64-column atoms per stage
+    static constexpr int kCols = kAtoms * 64;                  // columns of d per stage
+    static constexpr int kABytes = kAtoms * kRows * 128;       // A part of a stage
+    static constexpr int kBBytes = kAtoms * N * 128;           // B part of a stage
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = cmin(6, (210 * 1024) / kStageBytes);
+    static constexpr int kLook = kStages - 2;                  // stages loaded ahead
+    static constexpr int kMeta = kLook + 2;                    // tiles whose row ids are held
+    static constexpr int kTmemCols = N <= 32 ? 32 : N <= 64 ? 64 : 128;
+    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 /* align */ +
+                                    size_t(kMeta) * 2 * kRows * sizeof(int32_t);
+    static_assert(kStages >= 3, "the pipeline needs three slots");
+};
+
+// Bytes of the partial-tile buffer a launch with `grid` CTAs and R vectors needs (two 128 x N
+// fp32 parts per CTA: its first and its last tile).
+inline size_t parts_bytes(int R, int grid)
+{
+    return size_t(2) * size_t(grid) * kRows * size_t(16 * mt_for(R)) * sizeof(float);
+}
+
+struct Operands {
+    const uint16_t *A;       // [*, d] bf16, rows picked by the policy
+    const uint16_t *B;       // [R, d] bf16
+    int d, R;
+    int32_t *status;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N)); }
+
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= uint64_t((saddr >> 4) & 0x3FFFu);             // start address
+    d |= uint64_t(1) << 16;                             // leading byte offset (unused, K-major SW128)
+    d |= uint64_t((1024u >> 4) & 0x3FFFu) << 32;        // stride byte offset: next 8-row group
+    d |= uint64_t(1) << 46;                             // descriptor version
+    d |= uint64_t(2) << 61;                             // 128-byte swizzle
+    return d;
+}
+
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
+}
+
+__device__ __forceinline__ void commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void proxy_fence_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Policy interface (all device, const):
+//   int n_rows()                          picked rows (read once per CTA)
+//   void pick(int u, int &v, int &c)      A row of list entry u (-1: none) and a tag c
+//   void col_info(int r, int &i, long long &l)  per-vector values the epilogue keeps in smem
+//   int row_aux(int v)                    per-row value loaded at the tile's epilogue
+//   void emit(x[16], cb, v, c, aux, s_i, s_l)   accumulator row of A row v, columns cb..cb+15
+template <int MT, class Ep>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict__ tile_cnt)
+{
+    using C = Cfg<MT>;
+    constexpr int STG = C::kStages, L = C::kLook;
+    constexpr int CPR = C::kAtoms * 8;                         // 16-byte chunks per row per stage
+    constexpr int RPP = kThreads / CPR;                        // rows per pass of all threads
+    constexpr int APASS = kRows / RPP;                         // A-row passes per stage
+    constexpr int BPASS = (C::N + RPP - 1) / RPP;              // B-row passes per stage
+    static_assert(kRows % RPP == 0 && RPP % 8 == 0, "row passes share their swizzle phase");
+    extern __shared__ __align__(1024) unsigned char tc_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
+    int32_t *s_meta = reinterpret_cast<int32_t *>(sm + size_t(STG) * C::kStageBytes);   // [kMeta][v | c][128]
+    __shared__ uint64_t mma_done[STG];
+    __shared__ int32_t s_ci[C::N];
+    __shared__ long long s_cl[C::N];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_fail, s_first_owner, s_last_owner;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d = op.d, R = op.R;
+    const int nU = ep.n_rows();
+    const int ntiles = (nU + kRows - 1) / kRows;
+    const int nks = (d + C::kCols - 1) / C::kCols;             // stages per tile
+    const long long total = 1LL * ntiles * nks;                // < 2^31 by the host's limits
+    const int grid = gridDim.x, bid = blockIdx.x;
+    const int g0 = int(total * bid / grid), g1 = int(total * (bid + 1) / grid);
+    if (g0 >= g1) return;                                      // uniform: no stage for this CTA
+    constexpr uint32_t idesc = umma_idesc_bf16(kRows, C::N);
+    // the CTA whose range holds unit i, the first tile of CTA c, and the owner of the unit
+    // after CTA c's range (CTAs with empty ranges own nothing)
+    auto cta_of = [&](long long i) { return int(((i + 1) * grid - 1) / total); };
+    auto first_tile = [&](int c) { return int((total * c / grid) / nks); };
+    auto next_owner = [&](int c) { return cta_of(total * (c + 1) / grid); };
+
+    if (tid == 0) {
+        for (int i = 0; i < STG; ++i) mbar_init(&mma_done[i], 1);
+        mbar_fence_init();
+        s_fail = 0;
+    }
+    for (int r = tid; r < C::N; r += kThreads) {
+        int ci = -1;
+        long long cl = 0;
+        if (r < R) ep.col_info(r, ci, cl);
+        s_ci[r] = ci;
+        s_cl[r] = cl;
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&s_tmem)), "r"(uint32_t(C::kTmemCols)) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = s_tmem;
+
+    // Every thread copies one fixed 16-byte column chunk `ch` of rows prow + RPP*j.  Its shared-
+    // memory destinations are the same in every stage (up to the slot base); its sources move
+    // by kCols columns per stage.
+    const int ch = tid % CPR, prow = tid / CPR;
+    const int coff = (ch >> 3) * 64 + (ch & 7) * 8;            // column of the chunk inside a stage
+    const uint32_t dst0 = uint32_t((ch >> 3) * (kRows * 128) + prow * 128 + (((ch & 7) ^ (prow & 7)) << 4));
+    const uint32_t bdst0 = uint32_t((ch >> 3) * (C::N * 128) + prow * 128 + (((ch & 7) ^ (prow & 7)) << 4));
+    const uint16_t *bsrc[BPASS];
+#pragma unroll
+    for (int j = 0; j < BPASS; ++j) {
+        const int r = prow + RPP * j;
+        bsrc[j] = r < R ? op.B + size_t(r) * d + coff : nullptr;
+    }
+    const uint16_t *asrc[APASS];                               // rows of the tile being filled
+    const uint32_t smem0 = smem_u32(sm);
+
+    // Row ids and tags of tile t into ring slot t % kMeta, and this thread's row pointers for
+    // it.  Tiles arrive in increasing order; every thread calls this with the same t.
+    int meta_tile = -1;
+    auto ensure_meta = [&](int t) {
+        if (t == meta_tile) return;
+        int32_t *mv = s_meta + (t % C::kMeta) * (2 * kRows);
+        for (int q = tid; q < kRows; q += kThreads) {
+            const int u = t * kRows + q;
+            int v = -1, c = -1;
+            if (u < nU) ep.pick(u, v, c);
+            mv[q] = v;
+            mv[kRows + q] = c;
+        }
+        meta_tile = t;
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < APASS; ++j) {
+            const int v = mv[prow + RPP * j];
+            asrc[j] = v >= 0 ? op.A + size_t(v) * d + coff : nullptr;
+        }
+    };
+    // cp.async fill of slot `slot` with k-stage ks of the tile ensure_meta last prepared
+    auto fill = [&](int slot, int ks) {
+        const int k0 = ks * C::kCols;
+        const bool kin = k0 + coff < d;
+        const uint32_t As = smem0 + uint32_t(slot * C::kStageBytes);
+        const uint32_t Bs = As + C::kABytes;
+#pragma unroll
+        for (int j = 0; j < APASS; ++j) {
+            const bool ok = kin && asrc[j] != nullptr;
+            cp_async16(As + dst0 + uint32_t(j * RPP * 128), ok ? asrc[j] + k0 : op.A, ok ? 16 : 0);
+        }
+#pragma unroll
+        for (int j = 0; j < BPASS; ++j) {
+            if (prow + RPP * j < C::N) {
+                const bool ok = kin && bsrc[j] != nullptr;
+                cp_async16(Bs + bdst0 + uint32_t(j * RPP * 128), ok ? bsrc[j] + k0 : op.B, ok ? 16 : 0);
+            }
+        }
+    };
+
+    // (tile, k-stage) of the stage being multiplied and of the next stage to load
+    int t = g0 / nks, ks = g0 - t * nks;
+    int ft = t, fks = ks, fslot = 0;
+    for (int p = 0; p < L; ++p) {                              // prologue: the first L stages
+        if (g0 + p < g1) {
+            ensure_meta(ft);
+            fill(fslot, fks);
+            if (++fks == nks) { fks = 0; ++ft; }
+            if (++fslot == STG) fslot = 0;
+        }
+        cp_async_commit();
+    }
+    int issued = 0;                                            // stages whose MMAs were issued
+    int slot = 0;                                              // slot of stage li
+    for (int i = g0; i < g1; ++i) {
+        const int li = i - g0;
+        // refill: stage li + L goes into the slot of stage li - 2, whose MMAs were issued two
+        // iterations ago
+        if (i + L < g1) {
+            const int lf = li + L;
+            if (lf >= STG && !mbar_wait(&mma_done[fslot], unsigned(lf / STG - 1) & 1u)) {
+                s_fail = 1;
+                set_status(op.status, DS_DEV_TIMEOUT);
+            }
+            ensure_meta(ft);
+            fill(fslot, fks);
+            if (++fks == nks) { fks = 0; ++ft; }
+            if (++fslot == STG) fslot = 0;
+        }
+        cp_async_commit();
+        cp_async_wait<L>();                                    // stage li has landed (this thread's part)
+        proxy_fence_async();                                   // make it visible to the tensor cores
+        __syncthreads();
+        if (s_fail) break;                                     // uniform: read after the barrier
+        const bool first = ks == 0 || i == g0;
+        if (tid == 0) {
+            fence_after();
+            const uint32_t As = smem0 + uint32_t(slot * C::kStageBytes);
+            const uint32_t Bs = As + C::kABytes;
+#pragma unroll
+            for (int at = 0; at < C::kAtoms; ++at) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = umma_desc_sw128(As + at * (kRows * 128) + kk * 32);
+                    const uint64_t bd = umma_desc_sw128(Bs + at * (C::N * 128) + kk * 32);
+                    mma(tmem, ad, bd, idesc, (first && at == 0 && kk == 0) ? 0u : 1u);
+                }
+            }
+            commit(&mma_done[slot]);
+        }
+        ++issued;
+        const int cur_slot = slot;
+        if (++slot == STG) slot = 0;
+        const bool tile_end = ks == nks - 1 || i == g1 - 1;
+        const int tt = t;
+        if (++ks == nks) { ks = 0; ++t; }
+        if (!tile_end) continue;
+        // this CTA's part of tile tt is in the accumulator
+        if (!mbar_wait(&mma_done[cur_slot], unsigned(li / STG) & 1u)) {
+            s_fail = 1;
+            set_status(op.status, DS_DEV_TIMEOUT);
+        }
+        fence_after();
+        const int wq = warp & 3;                               // TMEM lane quarter this warp may read
+        const int row = wq * 32 + lane;                        // A row of the tile
+        const int32_t *mv = s_meta + (tt % C::kMeta) * (2 * kRows);
+        const int v = mv[row], c = mv[kRows + row];
+        const int aux = ep.row_aux(v);
+        const uint32_t taddr = tmem + (uint32_t(wq * 32) << 16);
+        const bool whole = 1LL * tt * nks >= g0 && 1LL * (tt + 1) * nks <= g1;
+        constexpr int kColStep = 16 * (kThreads / 128);        // warps sharing a lane quarter split the columns
+        if (whole) {
+            for (int cb = (warp >> 2) * 16; cb < C::N; cb += kColStep) {
+                uint32_t r16[16];
+                ld16(taddr + uint32_t(cb), r16);
+                float x[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(r16[e]);
+                ep.emit(x, cb, v, c, aux, s_ci, s_cl);
+            }
+        } else {
+            // store this part; the last CTA of the tile adds the parts in k (= CTA) order
+            const int mine = 2 * bid + (tt == first_tile(bid) ? 0 : 1);
+            for (int cb = (warp >> 2) * 16; cb < C::N; cb += kColStep) {
+                uint32_t r16[16];
+                ld16(taddr + uint32_t(cb), r16);
+                float4 *dst = reinterpret_cast<float4 *>(parts + (size_t(mine) * kRows + row) * C::N + cb);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    __stcg(dst + e, make_float4(__uint_as_float(r16[4 * e]), __uint_as_float(r16[4 * e + 1]),
+                                                __uint_as_float(r16[4 * e + 2]), __uint_as_float(r16[4 * e + 3])));
+            }
+            __threadfence();
+            if (tid == 0) {
+                s_first_owner = cta_of(1LL * tt * nks);
+                s_last_owner = cta_of(1LL * (tt + 1) * nks - 1);
+            }
+            __syncthreads();
+            const int cf = s_first_owner, cl = s_last_owner;
+            int nparts = 1;                                    // CTAs that own stages of tile tt
+            for (int cc = cf; cc != cl; cc = next_owner(cc)) ++nparts;
+            if (last_block_done(&tile_cnt[tt], unsigned(nparts))) {
+                for (int cb = (warp >> 2) * 16; cb < C::N; cb += kColStep) {
+                    float x[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) x[e] = 0.f;
+                    for (int cc = cf;; cc = next_owner(cc)) {
+                        const int pslot = 2 * cc + (tt == first_tile(cc) ? 0 : 1);
+                        const float4 *src = reinterpret_cast<const float4 *>(parts + (size_t(pslot) * kRows + row) * C::N + cb);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 p = __ldcg(src + e);
+                            x[4 * e] += p.x; x[4 * e + 1] += p.y; x[4 * e + 2] += p.z; x[4 * e + 3] += p.w;
+                        }
+                        if (cc == cl) break;
+                    }
+                    ep.emit(x, cb, v, c, aux, s_ci, s_cl);
+                }
+            }
+        }
+        fence_before();
+        __syncthreads();                                       // the accumulator may be overwritten
+        if (s_fail) break;
+    }
+    cp_async_wait<0>();
+    // every issued MMA must be complete before the accumulator is released
+    if (tid == 0) {
+        const long long deadline = clock64() + kWaitBudgetCycles;
+        for (int li = max(0, issued - STG); li < issued; ++li)
+            (void)mbar_wait_until(&mma_done[li % STG], unsigned(li / STG) & 1u, deadline);
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     :: "r"(tmem), "r"(uint32_t(C::kTmemCols)) : "memory");
+}
+
+// Host: launch gemm_kernel<MT, Ep> on `grid` CTAs (sets the shared-memory attribute once per
+// instantiation).  `parts` holds parts_bytes(R, grid) bytes; `tile_cnt` one zeroed counter per
+// tile (left zero).
+template <int MT, class Ep>
+ds_status launch(const Operands &op, const Ep &ep, float *parts, unsigned *tile_cnt, int grid, cudaStream_t stream)
+{
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(gemm_kernel<MT, Ep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(Cfg<MT>::kSmem)) != cudaSuccess)
+            return DS_ERR_CUDA;
+        attr = true;
+    }
+    gemm_kernel<MT, Ep><<<grid, kThreads, Cfg<MT>::kSmem, stream>>>(op, ep, parts, tile_cnt);
+    DS_TRY_LAUNCH();
+    return DS_OK;
+}
+
+// Dispatch on the number of B vectors.
+template <class Ep>
+ds_status launch_for(const Operands &op, const Ep &ep, float *parts, unsigned *tile_cnt, int grid, cudaStream_t stream)
+{
+    switch (mt_for(op.R)) {
+    case 1: return launch<1>(op, ep, parts, tile_cnt, grid, stream);
+    case 2: return launch<2>(op, ep, parts, tile_cnt, grid, stream);
+    case 3: return launch<3>(op, ep, parts, tile_cnt, grid, stream);
+    case 4: return launch<4>(op, ep, parts, tile_cnt, grid, stream);
+    case 5: return launch<5>(op, ep, parts, tile_cnt, grid, stream);
+    default: return launch<8>(op, ep, parts, tile_cnt, grid, stream);
+    }
+}
+
+}  // namespace tc
+}  // namespace ds

@@ -64,11 +64,15 @@ def test_vocab_index(ds, name):
 
 # ---------------------------------------------------------------------------------------
 @pytest.mark.parametrize("name,B", [("tiny", 1), ("small_batched", 5), ("llama_b1", 1),
-                                    ("batched", 32), ("large_b1_f5", 1)])
+                                    ("batched", 32), ("large_b1_f5", 1), ("large_b8_f10", 8),
+                                    ("large_b64_f100", 64), ("large_b64_f100", 2), ("large_b64_f100", 100)])
 def test_router_topk(ds, name, B):
+    # B = 1: CUDA-core GEMV; 2 <= B <= 64: tensor-core layers; B > 64: CUDA-core batched GEMV.
+    # B larger than the configuration's batch stacks the hidden states of several positions.
     inp = gu.chain_inputs(name)
     cfg = inp["cfg"]
-    Hrows = inp["H"][:B, 0] if inp["H"].shape[0] >= B else inp["H"][:, 0]
+    H = inp["H"]
+    Hrows = np.concatenate([H[:, t] for t in range(H.shape[1])])[:B]
     B = Hrows.shape[0]
     scores_ref, _ = oracle.router(Hrows, inp["W1"], inp["b1"], inp["W2"], inp["b2"], cfg.act)
     scores = torch.empty(B, cfg.M, dtype=torch.float32, device=gu.dev())

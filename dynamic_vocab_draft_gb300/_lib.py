@@ -35,7 +35,7 @@ SIGNATURES = {
     "ds_verify_workspace_bytes": (SZ, [I, I, I]),
     "ds_verify": (ST, [P, I, I, I, F, P, I64, P, P, P, P, I, P, P, P, P, P, P, P, SZ, P, P]),
     "ds_verify_tree_workspace_bytes": (SZ, [I, I, I, I]),
-    "ds_verify_tree": (ST, [P, I, I, I, I, F, P, P, I64, P, P, I, P, P, P, P, P,
+    "ds_verify_tree": (ST, [P, I, I, I, I, F, P, P, I64, P, P, P, P, I64, P, I, P, P, P, P, P,
                             P, P, P, P, SZ, P, P]),
     "ds_philox4x32_10": (ST, [P, U64, P, I, P]),
     "ds_event_record": (ST, [P, P]),

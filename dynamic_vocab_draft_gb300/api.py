@@ -148,16 +148,20 @@ def verify(p_logits, T, q_logits, vs_offsets, cpos, cluster_of, rank_in_cluster,
         _stream(stream)), "ds_verify")
 
 
-def verify_tree(p_logits, D, Wd, T, parent, q_logits, vs_offsets, cpos, cluster_of,
+def verify_tree(p_logits, D, Wd, T, parent, q_logits, vs_offsets, vs_ids, cpos, cluster_of,
                 rank_in_cluster, node_tokens, u_node, u_res, accepted_len, correction, path,
-                ws, status, stream=None):
-    """p_logits [B, 1+D*Wd, V]; q_logits [D, q_stride]; node_tokens [D, B*Wd]."""
+                ws, status, q_max=None, q_sumexp=None, stream=None):
+    """p_logits [B, 1+D*Wd, V]; q_logits [D, q_stride]; vs_offsets [D, B+1]; vs_ids [D, vs_stride];
+    cpos [D, B*M]; node_tokens [D, B*Wd]; q_max / q_sumexp [D, B*Wd] optional (the head's row
+    statistics)."""
     B, n1, V = p_logits.shape
     M = cpos.shape[-1] // B
     _lib.check(_lib.load().ds_verify_tree(
         _ptr(p_logits, F32, "p_logits"), B, D, Wd, V, float(T), _ptr(parent, I32, "parent"),
         _ptr(q_logits, F32, "q_logits"), q_logits.stride(0),
-        _ptr(vs_offsets, I32, "vs_offsets"), _ptr(cpos, I32, "cpos"), M,
+        _ptr(q_max, F32, "q_max", True), _ptr(q_sumexp, F32, "q_sumexp", True),
+        _ptr(vs_offsets, I32, "vs_offsets"), _ptr(vs_ids, I32, "vs_ids"), vs_ids.stride(0),
+        _ptr(cpos, I32, "cpos"), M,
         _ptr(cluster_of, I32, "cluster_of"), _ptr(rank_in_cluster, I32, "rank_in_cluster"),
         _ptr(node_tokens, I32, "node_tokens"), _ptr(u_node, F32, "u_node"),
         _ptr(u_res, F32, "u_res"),

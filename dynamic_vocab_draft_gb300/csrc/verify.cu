@@ -299,65 +299,64 @@ __device__ ResidualRow residual_row(const ChainArgs &a, int b, int tr)
     return rr;
 }
 
-__global__ void __launch_bounds__(kVThreads)
-verify_residual_kernel(ChainArgs a)
+// Inverse-CDF draw of one sequence over V weights, run by a grid (chunks of kRChunk, B).
+// Pass 1 (every block): the chunk's mass of the primary weights r and of the fallback weights
+// p.  Pass 2 (the last block of the sequence): locate the chunk where the cumulative mass
+// first exceeds u * total -- thread t sums a contiguous run of chunk masses, the runs are
+// scanned in thread order and the thread whose run crosses walks it -- then scan that chunk
+// the same way.  Weights without mass fall back to p.  The draw is the smallest v whose
+// cumulative weight exceeds the target; if rounding leaves none, the last v with weight.
+// wf(v, r, p) gives both weights of token v.
+template <class WF>
+__device__ void icdf_draw(WF wf, int V, int nrch, float u, float *__restrict__ rsum, float *__restrict__ psum,
+                          unsigned *counter, int32_t *out)
 {
     __shared__ float scratch[kVThreads / 32];
     __shared__ float sbuf[kVThreads + 1];
     __shared__ float fscan[33];
     __shared__ int s_chunk, s_use_p, s_hit, s_last;
     __shared__ float s_target;
-    const int b = blockIdx.y, c = blockIdx.x;
-    const int tr = __ldcg(&a.decision[b]);
-    if (tr < 0) return;                              // greedy: decided already (whole group returns)
-    const ResidualRow rr = residual_row(a, b, tr);
+    const int c = blockIdx.x;
     const int base = c * kRChunk + threadIdx.x * kRPer;
-    float rs = 0.f, psum = 0.f;
+    float rs = 0.f, ps = 0.f;
 #pragma unroll
     for (int i = 0; i < kRPer; ++i) {
         const int v = base + i;
-        if (v < a.V) { float r, p; residual_weight(a, rr, v, r, p); rs += r; psum += p; }
+        if (v < V) { float r, p; wf(v, r, p); rs += r; ps += p; }
     }
     rs = block_sum(rs, scratch);
-    psum = block_sum(psum, scratch);
-    if (threadIdx.x == 0) { a.rsum[size_t(b) * a.nrch + c] = rs; a.psum[size_t(b) * a.nrch + c] = psum; }
-    if (!last_block_done(&a.cnt2[b], unsigned(a.nrch))) return;
+    ps = block_sum(ps, scratch);
+    if (threadIdx.x == 0) { rsum[c] = rs; psum[c] = ps; }
+    if (!last_block_done(counter, unsigned(nrch))) return;
 
-    // Locate the chunk where the cumulative mass first exceeds u * total: thread t sums a
-    // contiguous run of chunk masses, the runs are scanned in thread order, and the thread
-    // whose run crosses walks it.  A residual without mass falls back to p.
-    const float u = a.u[size_t(b) * (a.gamma + 1) + a.gamma];
-    const int E = (a.nrch + kVThreads - 1) / kVThreads;
-    const int c0 = threadIdx.x * E, c1 = min(a.nrch, c0 + E);
+    const int E = (nrch + kVThreads - 1) / kVThreads;
+    const int c0 = threadIdx.x * E, c1 = min(nrch, c0 + E);
     float rrun = 0.f, prun = 0.f;
-    for (int i = c0; i < c1; ++i) {
-        rrun += __ldcg(&a.rsum[size_t(b) * a.nrch + i]);
-        prun += __ldcg(&a.psum[size_t(b) * a.nrch + i]);
-    }
+    for (int i = c0; i < c1; ++i) { rrun += __ldcg(&rsum[i]); prun += __ldcg(&psum[i]); }
     block_cdf_bounds(rrun, sbuf, fscan);
     const float rtot = sbuf[kVThreads];
     const int use_p = !(rtot > 0.f);
     if (use_p) block_cdf_bounds(prun, sbuf, fscan);
-    const float *w = use_p ? a.psum : a.rsum;
+    const float *w = use_p ? psum : rsum;
     const float target = u * sbuf[kVThreads];
     const float lo_b = sbuf[threadIdx.x], hi_b = sbuf[threadIdx.x + 1];
     if (threadIdx.x == 0) { s_hit = 0x7FFFFFFF; s_last = -1; }
     __syncthreads();
     if (lo_b <= target && target < hi_b) atomicMin(&s_hit, threadIdx.x);
     int lastc = -1;
-    for (int i = c0; i < c1; ++i) if (__ldcg(&w[size_t(b) * a.nrch + i]) > 0.f) lastc = i;
+    for (int i = c0; i < c1; ++i) if (__ldcg(&w[i]) > 0.f) lastc = i;
     if (lastc >= 0) atomicMax(&s_last, lastc);
     __syncthreads();
     if (int(threadIdx.x) == s_hit) {               // the first claimant walks its run of chunks
         float cum = lo_b;
         int ch = -1;
         for (int i = c0; i < c1; ++i) {
-            const float wi = __ldcg(&w[size_t(b) * a.nrch + i]);
+            const float wi = __ldcg(&w[i]);
             if (cum + wi > target) { ch = i; break; }
             cum += wi;
         }
         if (ch < 0) {                               // rounding inside the run: its last chunk with mass
-            for (int i = c1 - 1; i >= c0; --i) if (__ldcg(&w[size_t(b) * a.nrch + i]) > 0.f) { ch = i; break; }
+            for (int i = c1 - 1; i >= c0; --i) if (__ldcg(&w[i]) > 0.f) { ch = i; break; }
             s_target = INFINITY;
         } else {
             s_target = target - cum;
@@ -381,7 +380,7 @@ verify_residual_kernel(ChainArgs a)
     for (int i = 0; i < kRPer; ++i) {
         const int v = lo + i;
         float r = 0.f, p = 0.f;
-        if (v < a.V) residual_weight(a, rr, v, r, p);
+        if (v < V) wf(v, r, p);
         wv[i] = s_use_p ? p : r;
         seg += wv[i];
     }
@@ -403,10 +402,22 @@ verify_residual_kernel(ChainArgs a)
             if (v < 0 && cum > tgt) v = lo + i;
         }
         if (v < 0) v = last_pos;                    // rounding inside the segment
-        a.correction[b] = v >= 0 ? v : s_last;
+        *out = v >= 0 ? v : s_last;
     }
     __syncthreads();
-    if (threadIdx.x == 0 && s_hit == 0x7FFFFFFF) a.correction[b] = s_last;   // target beyond the chunk
+    if (threadIdx.x == 0 && s_hit == 0x7FFFFFFF) *out = s_last;   // target beyond the chunk
+}
+
+__global__ void __launch_bounds__(kVThreads)
+verify_residual_kernel(ChainArgs a)
+{
+    const int b = blockIdx.y;
+    const int tr = __ldcg(&a.decision[b]);
+    if (tr < 0) return;                              // greedy: decided already (whole group returns)
+    const ResidualRow rr = residual_row(a, b, tr);
+    auto wf = [&](int v, float &r, float &p) { residual_weight(a, rr, v, r, p); };
+    icdf_draw(wf, a.V, a.nrch, a.u[size_t(b) * (a.gamma + 1) + a.gamma], a.rsum + size_t(b) * a.nrch,
+              a.psum + size_t(b) * a.nrch, &a.cnt2[b], &a.correction[b]);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -415,222 +426,269 @@ verify_residual_kernel(ChainArgs a)
 // sampling).  All nodes of one depth share their sequence's shortlist, so the residual
 // after a rejected sibling differs from the current target only on that shortlist: the walk
 // keeps it as (O = target mass off the list, r_j on the list) and never builds a dense row.
+//
+//   tree_walk_kernel      one 1024-thread block per sequence.  At each visited node one pass
+//                         over the target row gives its max, sum-exp, argmax and the mass
+//                         off the children's list; r_j = p(S_j) is gathered over the list;
+//                         every rejected sibling costs one pass over the list.  Only the
+//                         rows on the walked path are read.
+//   tree_residual_kernel  grid (chunks, B): the inverse-CDF draw of the correction from the
+//                         walk's final state (the residual, or p at a leaf).
 // ---------------------------------------------------------------------------------------
 constexpr int kWalkThreads = 1024;
+constexpr int kWalkMaxM = 8192;
+
+struct WalkState {                 // what the walk leaves for the correction draw
+    int mode;                      // 0: decided (greedy); 1: draw from p of `row`; 2: residual
+    int row, dep, buf;             // target row (0 = root), list depth, residual buffer
+    float m, s;                    // softmax statistics of the target row
+    int pad0, pad1;
+};
 
 struct TreeArgs {
     const float *p_logits;
-    int B, D, Wd, N, V, nch;
+    int B, D, Wd, N, V;
     float T, inv_te;
     const int32_t *parent;
     const float *q_logits;
     int64_t q_stride;
-    const int32_t *vs_offsets, *cpos;
+    const float *q_max, *q_sumexp;             // optional [D][B*Wd]
+    const int32_t *vs_offsets, *vs_ids;
+    int64_t vs_stride;
+    const int32_t *cpos;
     int M;
     const int32_t *cluster_of, *rank;
     const int32_t *node_tokens;
     const float *u_node, *u_res;
     int32_t *accepted, *correction, *path;
     int32_t *status;
-    PStat *tpstat;     // [B][1+N][nch]
-    QStat *tqstat;     // [B][N][nch]
-    float *rbuf;       // [B][V]
+    // workspace
+    WalkState *state;                          // [B]
+    float *rbuf;                               // [B][2][V]
+    int nrch;
+    float *rsum, *psum;                        // [B][nrch]
+    unsigned *cnt;                             // [B]
 };
 
-// Node n's draft row: logits, length.
-__device__ __forceinline__ const float *node_row(const TreeArgs &a, int b, int n, int *len)
-{
-    const int dep0 = n / a.Wd, i = n - dep0 * a.Wd;
-    const int *off = a.vs_offsets + size_t(dep0) * (a.B + 1);
-    const int nb = off[b + 1] - off[b];
-    *len = nb;
-    return a.q_logits + size_t(dep0) * a.q_stride + int64_t(off[b]) * a.Wd + int64_t(i) * nb;
-}
+// Online softmax statistics of x = value * inv_te with the raw argmax (ties to the lower
+// index) and the part of the sum-exp over tokens off a list.
+struct RowStat { float m, s, o, amax; int aid; };
 
-__global__ void __launch_bounds__(kVThreads)
-tree_stats_kernel(TreeArgs a)
+__device__ __forceinline__ RowStat rowstat_empty() { return RowStat{-INFINITY, 0.f, 0.f, -INFINITY, -1}; }
+
+__device__ __forceinline__ void rowstat_add(RowStat &a, float z, float x, bool off, int v)
 {
-    __shared__ PStat scratch[kVThreads / 32];
-    const int b = blockIdx.y / (1 + a.N), rr = blockIdx.y % (1 + a.N);
-    const int c = blockIdx.x, lo = c * kVChunk;
-    const PStat ps = chunk_stats(a.p_logits + (size_t(b) * (1 + a.N) + rr) * a.V, lo, a.V, a.inv_te, scratch);
-    if (threadIdx.x == 0) a.tpstat[(size_t(b) * (1 + a.N) + rr) * a.nch + c] = ps;
-    if (rr >= 1 && a.T > 0.f) {
-        int nb;
-        const float *ql = node_row(a, b, rr - 1, &nb);
-        QStat q{-INFINITY, 0.f};
-        if (lo < nb) { const PStat qs = chunk_stats(ql, lo, nb, a.inv_te, scratch); q = QStat{qs.m, qs.s}; }
-        if (threadIdx.x == 0) a.tqstat[(size_t(b) * a.N + (rr - 1)) * a.nch + c] = q;
+    if (x > a.m) {
+        const float sc = a.m == -INFINITY ? 0.f : __expf(a.m - x);
+        a.s = a.s * sc + 1.f;
+        a.o = a.o * sc + (off ? 1.f : 0.f);
+        a.m = x;
+    } else {
+        const float e = __expf(x - a.m);
+        a.s += e;
+        if (off) a.o += e;
     }
+    if (z > a.amax || a.aid < 0) { a.amax = z; a.aid = v; }      // v ascending per thread
 }
 
-// Warp 0 folds `nch` chunk partials (stride 1) in a fixed order; the result lands in *out.
-__device__ void fold_pstats(const PStat *src, int nch, PStat *out)
+__device__ __forceinline__ RowStat rowstat_merge(RowStat a, const RowStat &b)
 {
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        PStat acc{-INFINITY, 0.f, -INFINITY, -1};
-        for (int i = lane; i < nch; i += 32) acc = pstat_merge(acc, ldcg(&src[i]));
+    if (b.m > a.m) {
+        const float sc = a.m == -INFINITY ? 0.f : __expf(a.m - b.m);
+        a.s = a.s * sc + b.s;
+        a.o = a.o * sc + b.o;
+        a.m = b.m;
+    } else if (b.m != -INFINITY) {
+        const float sc = __expf(b.m - a.m);
+        a.s += b.s * sc;
+        a.o += b.o * sc;
+    }
+    if (b.aid >= 0 && (a.aid < 0 || b.amax > a.amax || (b.amax == a.amax && b.aid < a.aid))) { a.amax = b.amax; a.aid = b.aid; }
+    return a;
+}
+
+__device__ __forceinline__ RowStat shfl_xor_rowstat(const RowStat &a, int o)
+{
+    return RowStat{__shfl_xor_sync(0xFFFFFFFFu, a.m, o), __shfl_xor_sync(0xFFFFFFFFu, a.s, o),
+                   __shfl_xor_sync(0xFFFFFFFFu, a.o, o), __shfl_xor_sync(0xFFFFFFFFu, a.amax, o),
+                   __shfl_xor_sync(0xFFFFFFFFu, a.aid, o)};
+}
+
+// Fixed-order block reduction (warp trees, then warp 0 over the warp results); the result is
+// returned to every thread.
+__device__ RowStat block_rowstat(RowStat st, RowStat *ws)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const RowStat q = shfl_xor_rowstat(st, o);
+        st = (lane & o) ? rowstat_merge(q, st) : rowstat_merge(st, q);
+    }
+    __syncthreads();
+    if (lane == 0) ws[warp] = st;
+    __syncthreads();
+    if (warp == 0) {
+        RowStat c = lane < nw ? ws[lane] : rowstat_empty();
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const PStat q = shfl_xor_pstat(acc, o);
-            acc = (lane & o) ? pstat_merge(q, acc) : pstat_merge(acc, q);
+            const RowStat q = shfl_xor_rowstat(c, o);
+            c = (lane & o) ? rowstat_merge(q, c) : rowstat_merge(c, q);
         }
-        if (lane == 0) *out = acc;
+        if (lane == 0) ws[32] = c;
     }
     __syncthreads();
-}
-
-__device__ void fold_qstats(const QStat *src, int nch, PStat *out)
-{
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        PStat acc{-INFINITY, 0.f, -INFINITY, -1};
-        for (int i = lane; i < nch; i += 32) { const QStat q = ldcg(&src[i]); acc = pstat_merge(acc, PStat{q.m, q.s, -INFINITY, -1}); }
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const PStat q = shfl_xor_pstat(acc, o);
-            acc = (lane & o) ? pstat_merge(q, acc) : pstat_merge(acc, q);
-        }
-        if (lane == 0) *out = acc;
-    }
-    __syncthreads();
-}
-
-// Inverse-CDF draw over weights w(v), v = 0..V-1 ascending: the smallest v whose cumulative
-// weight exceeds `target`; if rounding leaves none, the last v with positive weight.  Thread t
-// owns a contiguous segment; segment sums are scanned in thread order.
-template <typename WF>
-__device__ int block_icdf(WF wf, int V, float u, float *sbuf, float *scratch, int *ibuf)
-{
-    const int E = (V + blockDim.x - 1) / blockDim.x;
-    const int lo = threadIdx.x * E, hi = min(V, lo + E);
-    float seg = 0.f;
-    int last = -1;
-    for (int v = lo; v < hi; ++v) { const float w = wf(v); seg += w; if (w > 0.f) last = v; }
-    block_cdf_bounds(seg, sbuf, scratch);
-    const float target = u * sbuf[blockDim.x];
-    const float lo_b = sbuf[threadIdx.x], hi_b = sbuf[threadIdx.x + 1];
-    if (threadIdx.x == 0) { ibuf[0] = 0x7FFFFFFF; ibuf[1] = -1; ibuf[2] = -1; }
-    __syncthreads();
-    if (lo_b <= target && target < hi_b) atomicMin(&ibuf[0], threadIdx.x);
-    if (last >= 0) atomicMax(&ibuf[1], last);
-    __syncthreads();
-    if (int(threadIdx.x) == ibuf[0]) {              // the first claimant walks its segment
-        float cum = lo_b;
-        int hit = -1;
-        for (int v = lo; v < hi; ++v) { cum += wf(v); if (cum > target) { hit = v; break; } }
-        ibuf[2] = hit >= 0 ? hit : last;            // rounding inside the segment: its last positive
-    }
-    __syncthreads();
-    const int r = ibuf[2] >= 0 ? ibuf[2] : ibuf[1];
-    __syncthreads();
-    return r;
+    return ws[32];
 }
 
 __global__ void __launch_bounds__(kWalkThreads)
 tree_walk_kernel(TreeArgs a)
 {
-    __shared__ PStat s_p, s_q;
+    __shared__ int s_cpos[kWalkMaxM];           // cpos of the children's list
+    __shared__ RowStat s_red[33];
     __shared__ float fscr[33];
-    __shared__ float sbuf[kWalkThreads + 1];
-    __shared__ int ibuf[3];
     __shared__ int s_kids[64];
     __shared__ int s_nkids, s_accept;
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
-    float *r = a.rbuf + size_t(b) * a.V;
     if (tid < a.D) a.path[size_t(b) * a.D + tid] = -1;
     int cur = -1, dep = 0, A = 0, corr = -1;
+    WalkState ws{0, 0, 0, 0, 0.f, 1.f, 0, 0};
+    int cb = 0;                                  // which residual buffer holds r
     for (int guard = 0; guard <= a.D; ++guard) {
-        fold_pstats(a.tpstat + (size_t(b) * (1 + a.N) + (cur + 1)) * a.nch, a.nch, &s_p);
-        const float *z = a.p_logits + (size_t(b) * (1 + a.N) + (cur + 1)) * a.V;
-        const float pm = s_p.m, ps = s_p.s;
+        const int rr = cur + 1;
+        const float *z = a.p_logits + (size_t(b) * (1 + a.N) + rr) * a.V;
+        const bool has_list = dep < a.D;
         if (tid == 0) {
             int nk = 0;
-            if (dep < a.D)
+            if (has_list)
                 for (int i = 0; i < a.Wd; ++i) {
                     const int n = dep * a.Wd + i;
                     if (a.parent[n] == cur) s_kids[nk++] = n;
                 }
             s_nkids = nk;
         }
+        if (has_list) {
+            const int32_t *cp = a.cpos + (size_t(dep) * a.B + b) * a.M;
+            for (int c = tid; c < a.M; c += blockDim.x) s_cpos[c] = cp[c];
+        }
         __syncthreads();
         const int nk = s_nkids;
-        const int32_t *cposL = a.cpos + (size_t(dep < a.D ? dep : 0) * a.B + b) * a.M;
+        // one pass over the target row
+        RowStat st = rowstat_empty();
+        for (int v = tid; v < a.V; v += blockDim.x) {
+            const float zv = z[v];
+            const int c = a.cluster_of[v];
+            const bool off = has_list && (unsigned(c) >= unsigned(a.M) || s_cpos[c] < 0);
+            rowstat_add(st, zv, zv * a.inv_te, off, v);
+        }
+        const RowStat row = block_rowstat(st, s_red);
         if (a.T == 0.f) {
-            const int am = s_p.aid;
+            const int am = row.aid;
             int next = -1;
             for (int k = 0; k < nk; ++k) {
                 const int n = s_kids[k];
                 if (a.node_tokens[size_t(dep) * a.B * a.Wd + size_t(b) * a.Wd + (n - dep * a.Wd)] == am) { next = n; break; }
             }
-            if (next < 0) { corr = am; break; }
+            if (next < 0) { corr = am; ws.mode = 0; break; }
             if (tid == 0) a.path[size_t(b) * a.D + A] = next;
             ++A; cur = next; ++dep;
             continue;
         }
-        auto pval = [&](int v) { return __expf(z[v] * a.inv_te - pm) / ps; };
-        if (nk == 0) {
-            corr = block_icdf(pval, a.V, a.u_res[size_t(b) * (a.D + 1) + dep], sbuf, fscr, ibuf);
-            break;
+        ws.row = rr; ws.dep = dep; ws.m = row.m; ws.s = row.s;
+        if (nk == 0) { ws.mode = 1; break; }
+        // the children's list and r_j = p(S_j) on it
+        const int *off = a.vs_offsets + size_t(dep) * (a.B + 1);
+        const int lo = off[b];
+        int nb = off[b + 1] - lo;
+        if (lo < 0 || nb < 0 || nb > a.V) { if (tid == 0) set_status(a.status, DS_DEV_BAD_INDEX); nb = 0; }
+        const int32_t *ids = a.vs_ids + size_t(dep) * a.vs_stride + lo;
+        float *r = a.rbuf + (size_t(b) * 2 + cb) * a.V;
+        float on = 0.f;
+        for (int j = tid; j < nb; j += blockDim.x) {
+            const int v = ids[j];
+            const float pj = (v >= 0 && v < a.V) ? __expf(z[v] * a.inv_te - row.m) / row.s : 0.f;
+            r[j] = pj;
+            on += pj;
         }
-        // residual state for the children's shared list: O off the list, r_j on it
-        float off_mass = 0.f, on_mass = 0.f;
-        for (int v = tid; v < a.V; v += blockDim.x) {
-            const float p = pval(v);
-            const int pc = cposL[a.cluster_of[v]];
-            if (pc < 0) off_mass += p;
-            else { r[pc + a.rank[v]] = p; on_mass += p; }
-        }
-        const float O = block_sum(off_mass, fscr);
-        float R = O + block_sum(on_mass, fscr);
+        const float O = row.o / row.s;
+        float R = O + block_sum(on, fscr);
         int next = -1;
         for (int k = 0; k < nk; ++k) {
             const int n = s_kids[k];
-            int nb;
-            const float *ql = node_row(a, b, n, &nb);
-            fold_qstats(a.tqstat + (size_t(b) * a.N + n) * a.nch, a.nch, &s_q);
-            const float qm = s_q.m, qs = s_q.s;
+            const int i = n - dep * a.Wd, hr = b * a.Wd + i;
+            const float *ql = a.q_logits + size_t(dep) * a.q_stride + int64_t(lo) * a.Wd + int64_t(i) * nb;
+            float qm, qs;
+            if (a.q_max) {
+                qm = a.q_max[size_t(dep) * a.B * a.Wd + hr];
+                qs = a.q_sumexp[size_t(dep) * a.B * a.Wd + hr];
+            } else {
+                RowStat q = rowstat_empty();
+                for (int j = tid; j < nb; j += blockDim.x) rowstat_add(q, ql[j], ql[j] * a.inv_te, false, j);
+                q = block_rowstat(q, s_red);
+                qm = q.m; qs = q.s;
+            }
             if (tid == 0) {
-                const int x = a.node_tokens[size_t(dep) * a.B * a.Wd + size_t(b) * a.Wd + (n - dep * a.Wd)];
+                const int x = a.node_tokens[size_t(dep) * a.B * a.Wd + hr];
                 int j = -1;
-                if (x >= 0 && x < a.V) { const int pc = cposL[a.cluster_of[x]]; if (pc >= 0) j = pc + a.rank[x]; }
-                int acc = 0;
-                if (j < 0) set_status(a.status, DS_DEV_BAD_INDEX);
-                else {
-                    const float q = __expf(ql[j] * a.inv_te - qm) / qs;
-                    acc = a.u_node[size_t(b) * a.N + n] * q < r[j] / R;
+                if (x >= 0 && x < a.V) {
+                    const int c = a.cluster_of[x];
+                    const int pc = unsigned(c) < unsigned(a.M) ? s_cpos[c] : -1;
+                    if (pc >= 0) j = pc + a.rank[x];
                 }
+                int acc = 0;
+                if (j < 0 || j >= nb) set_status(a.status, DS_DEV_BAD_INDEX);
+                else acc = a.u_node[size_t(b) * a.N + n] * (__expf(ql[j] * a.inv_te - qm) / qs) < r[j] / R;
                 s_accept = acc;
             }
             __syncthreads();
             if (s_accept) { next = n; break; }
+            // rejected: r <- max(r - R q, 0) into the other buffer, kept if it has mass
+            float *rn = a.rbuf + (size_t(b) * 2 + (cb ^ 1)) * a.V;
             float part = 0.f;
-            for (int j = tid; j < nb; j += blockDim.x)
-                part += fmaxf(r[j] - R * (__expf(ql[j] * a.inv_te - qm) / qs), 0.f);
-            const float Rn = O + block_sum(part, fscr);
-            if (Rn > 0.f) {
-                for (int j = tid; j < nb; j += blockDim.x)
-                    r[j] = fmaxf(r[j] - R * (__expf(ql[j] * a.inv_te - qm) / qs), 0.f);
-                R = Rn;
+            for (int j = tid; j < nb; j += blockDim.x) {
+                const float w = fmaxf(r[j] - R * (__expf(ql[j] * a.inv_te - qm) / qs), 0.f);
+                rn[j] = w;
+                part += w;
             }
-            __syncthreads();
+            const float Rn = O + block_sum(part, fscr);
+            if (Rn > 0.f) { cb ^= 1; r = rn; R = Rn; }
         }
         if (next >= 0) {
             if (tid == 0) a.path[size_t(b) * a.D + A] = next;
             ++A; cur = next; ++dep;
             continue;
         }
-        const float u = a.u_res[size_t(b) * (a.D + 1) + dep];
-        auto wres = [&](int v) {
-            const int pc = cposL[a.cluster_of[v]];
-            return pc < 0 ? pval(v) : r[pc + a.rank[v]];
-        };
-        corr = block_icdf(wres, a.V, u, sbuf, fscr, ibuf);
+        ws.mode = 2; ws.buf = cb;
         break;
     }
-    if (tid == 0) { a.accepted[b] = A; a.correction[b] = corr; }
+    if (tid == 0) {
+        a.accepted[b] = A;
+        if (ws.mode == 0) a.correction[b] = corr;
+        a.state[b] = ws;
+    }
+}
+
+__global__ void __launch_bounds__(kVThreads)
+tree_residual_kernel(TreeArgs a)
+{
+    const int b = blockIdx.y;
+    const WalkState ws = a.state[b];              // written by the previous launch
+    if (ws.mode == 0) return;                     // whole group returns
+    const float *z = a.p_logits + (size_t(b) * (1 + a.N) + ws.row) * a.V;
+    const float *r = a.rbuf + (size_t(b) * 2 + ws.buf) * a.V;
+    const int32_t *cp = a.cpos + (size_t(ws.dep) * a.B + b) * a.M;
+    const bool resid = ws.mode == 2;
+    auto wf = [&](int v, float &w, float &p) {
+        p = __expf(z[v] * a.inv_te - ws.m) / ws.s;
+        w = p;
+        if (resid) {
+            const int c = a.cluster_of[v];
+            const int pc = unsigned(c) < unsigned(a.M) ? cp[c] : -1;
+            if (pc >= 0) { const int j = pc + a.rank[v]; w = unsigned(j) < unsigned(a.V) ? r[j] : 0.f; }
+        }
+    };
+    icdf_draw(wf, a.V, a.nrch, a.u_res[size_t(b) * (a.D + 1) + ws.dep], a.rsum + size_t(b) * a.nrch,
+              a.psum + size_t(b) * a.nrch, &a.cnt[b], &a.correction[b]);
 }
 
 }  // namespace
@@ -705,46 +763,52 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
 extern "C" size_t ds_verify_tree_workspace_bytes(int B, int D, int Wd, int V)
 {
     if (B <= 0 || D <= 0 || Wd <= 0 || V <= 0) return 0;
-    const size_t nch = size_t(vchunks(V)), N = size_t(D) * Wd;
-    return align256(size_t(B) * (1 + N) * nch * sizeof(PStat)) +
-           align256(size_t(B) * N * nch * sizeof(QStat)) +
-           align256(size_t(B) * size_t(V) * sizeof(float));
+    return align256(size_t(B) * sizeof(WalkState)) +
+           align256(size_t(B) * 2 * size_t(V) * sizeof(float)) +
+           2 * align256(size_t(B) * rchunks(V) * sizeof(float)) +
+           align256(size_t(B) * sizeof(unsigned));
 }
 
 extern "C" ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd, int V, float T,
                                     const int32_t *parent,
                                     const float *q_logits, int64_t q_stride,
-                                    const int32_t *vs_offsets, const int32_t *cpos, int M,
+                                    const float *q_max, const float *q_sumexp,
+                                    const int32_t *vs_offsets, const int32_t *vs_ids, int64_t vs_stride,
+                                    const int32_t *cpos, int M,
                                     const int32_t *cluster_of, const int32_t *rank_in_cluster,
                                     const int32_t *node_tokens, const float *u_node, const float *u_res,
                                     int32_t *accepted_len, int32_t *correction, int32_t *path,
                                     void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream)
 {
-    if (!p_logits || !parent || !q_logits || !vs_offsets || !cpos || !cluster_of || !rank_in_cluster ||
-        !node_tokens || !u_node || !u_res || !accepted_len || !correction || !path)
+    if (!p_logits || !parent || !q_logits || !vs_offsets || !vs_ids || !cpos || !cluster_of ||
+        !rank_in_cluster || !node_tokens || !u_node || !u_res || !accepted_len || !correction || !path)
         return DS_ERR_INVALID_ARG;
     if (B < 1 || D < 1 || D > kMaxGamma || Wd < 1 || Wd > 64 || V < 1 || V > (1 << 24) || M < 1 ||
-        M > 8192 || !(T >= 0.f) || q_stride < 0)
+        M > kWalkMaxM || !(T >= 0.f) || q_stride < 0 || vs_stride < 0)
         return DS_ERR_INVALID_ARG;
-    const int N = D * Wd;
-    if (size_t(B) * (1 + N) > 65535) return DS_ERR_UNSUPPORTED;
+    if ((q_max == nullptr) != (q_sumexp == nullptr)) return DS_ERR_INVALID_ARG;
+    if (B > 65535) return DS_ERR_UNSUPPORTED;
     if (!ws || ws_bytes < ds_verify_tree_workspace_bytes(B, D, Wd, V)) return DS_ERR_WORKSPACE;
     TreeArgs a;
-    a.p_logits = p_logits; a.B = B; a.D = D; a.Wd = Wd; a.N = N; a.V = V; a.nch = vchunks(V);
+    a.p_logits = p_logits; a.B = B; a.D = D; a.Wd = Wd; a.N = D * Wd; a.V = V;
     a.T = T; a.inv_te = T > 0.f ? 1.f / T : 1.f;
     a.parent = parent; a.q_logits = q_logits; a.q_stride = q_stride;
-    a.vs_offsets = vs_offsets; a.cpos = cpos; a.M = M;
+    a.q_max = q_max; a.q_sumexp = q_sumexp;
+    a.vs_offsets = vs_offsets; a.vs_ids = vs_ids; a.vs_stride = vs_stride;
+    a.cpos = cpos; a.M = M;
     a.cluster_of = cluster_of; a.rank = rank_in_cluster;
     a.node_tokens = node_tokens; a.u_node = u_node; a.u_res = u_res;
     a.accepted = accepted_len; a.correction = correction; a.path = path; a.status = dev_status;
     char *w = static_cast<char *>(ws);
-    const size_t nch = size_t(a.nch);
-    a.tpstat = reinterpret_cast<PStat *>(w); w += align256(size_t(B) * (1 + N) * nch * sizeof(PStat));
-    a.tqstat = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * N * nch * sizeof(QStat));
-    a.rbuf = reinterpret_cast<float *>(w);
-    tree_stats_kernel<<<dim3(a.nch, B * (1 + N)), kVThreads, 0, stream>>>(a);
-    DS_TRY_LAUNCH();
+    a.state = reinterpret_cast<WalkState *>(w); w += align256(size_t(B) * sizeof(WalkState));
+    a.rbuf = reinterpret_cast<float *>(w); w += align256(size_t(B) * 2 * size_t(V) * sizeof(float));
+    a.nrch = int(rchunks(V));
+    a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
+    a.psum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
+    a.cnt = reinterpret_cast<unsigned *>(w);
     tree_walk_kernel<<<B, kWalkThreads, 0, stream>>>(a);
+    DS_TRY_LAUNCH();
+    tree_residual_kernel<<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
     DS_TRY_LAUNCH();
     return DS_OK;
 }

@@ -18,6 +18,12 @@ import torch
 from . import api
 
 
+def router_launches(B: int) -> int:
+    """Kernels one ds_router_topk call launches: two GEMVs at B = 1 or B > 64; two tensor-core
+    layers and a top-k in between."""
+    return 2 if B == 1 or B > 64 else 3
+
+
 class _Common:
     def _setup_vocab(self, csr_off, csr_tok, dev):
         self.csr_off = csr_off.to(dev, torch.int32).contiguous()
@@ -159,7 +165,7 @@ class ChainDrafter(_Common):
         return self.gamma
 
     def launches_per_step(self) -> int:
-        n_router = 2
+        n_router = router_launches(self.B)
         n_short = 4 if self.union else (2 if self.B == 1 else 3)
         n_head = 2 if self.union else 1
         return self.gamma * (n_router + n_short + n_head) + 2
@@ -236,8 +242,9 @@ class TreeDrafter(_Common):
 
     def verify(self, stream=None):
         api.verify_tree(self.z, self.D, self.Wd, self.T, self.parent, self.logits, self.vs_offsets,
-                        self.cpos, self.cluster_of, self.rank, self.tokens, self.u_node, self.u_res,
-                        self.accepted, self.correction, self.path, self.ws_verify, self.status, stream)
+                        self.vs_ids, self.cpos, self.cluster_of, self.rank, self.tokens, self.u_node,
+                        self.u_res, self.accepted, self.correction, self.path, self.ws_verify,
+                        self.status, q_max=self.row_max, q_sumexp=self.row_sumexp, stream=stream)
 
     def step(self):
         main = torch.cuda.current_stream(self.dev)
@@ -259,4 +266,4 @@ class TreeDrafter(_Common):
         return self.D
 
     def launches_per_step(self) -> int:
-        return self.D * (2 + 4 + 2) + 2
+        return self.D * (router_launches(self.B) + 4 + 2) + 2

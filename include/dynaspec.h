@@ -243,24 +243,31 @@ ds_status ds_verify(const float *p_logits, int B, int gamma, int V, float T,
  * rejection p <- norm(max(0, p - q_c)) (unchanged if that has no mass).  On acceptance the
  * walk moves to c with p = softmax(z_c / T).  When no child is accepted, or at a leaf, the
  * correction is drawn from the current p by inverse CDF with u_res[depth].  T = 0: accept
- * the first child whose token is the argmax of the current node's target row.
+ * the first child whose token is the argmax of the current node's target row.  Only the
+ * target rows on the walked path are read.
  *   D depths of Wd nodes; node n = (dep-1)*Wd + i (depth-major), N = D*Wd
  *   p_logits [B, 1+N, V]   row 0: target at the root; row 1+n: target after node n
  *   parent [N] (device)    parent node of n, -1 for the root; parents sit one depth up
  *   q_logits               depth dep (0-based) at q_logits + dep*q_stride, laid out as
  *                          ds_gathered_head writes them with G = Wd
- *   vs_offsets [D, B+1], cpos [D, B*M], cluster_of, rank_in_cluster: as in ds_verify
+ *   q_max, q_sumexp [D, B*Wd] (optional, both or neither): the node rows' softmax statistics
+ *                          as ds_gathered_head reports them; NULL -> recomputed here
+ *   vs_offsets [D, B+1]    the lists of each depth; list (dep, b) holds the tokens
+ *   vs_ids                 vs_ids[dep*vs_stride + vs_offsets[dep][b] + j]
+ *   cpos [D, B*M], cluster_of, rank_in_cluster: as in ds_verify
  *   node_tokens [D, B*Wd]  token of node (b, dep, i) at [dep-1][b*Wd + i]
  *   u_node [B, N], u_res [B, D+1]
  *   accepted_len [B], correction [B], path [B, D] (out; accepted node ids, -1 padded)
  * Limits: D <= 32, Wd <= 64, V <= 2^24, M <= 8192.
- * ws: ds_verify_tree_workspace_bytes(B, D, Wd, V) bytes.
+ * ws: ds_verify_tree_workspace_bytes(B, D, Wd, V) bytes (completion counters: zero it once).
  * ------------------------------------------------------------------------------------- */
 size_t ds_verify_tree_workspace_bytes(int B, int D, int Wd, int V);
 ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd, int V, float T,
                          const int32_t *parent,
                          const float *q_logits, int64_t q_stride,
-                         const int32_t *vs_offsets, const int32_t *cpos, int M,
+                         const float *q_max, const float *q_sumexp,
+                         const int32_t *vs_offsets, const int32_t *vs_ids, int64_t vs_stride,
+                         const int32_t *cpos, int M,
                          const int32_t *cluster_of, const int32_t *rank_in_cluster,
                          const int32_t *node_tokens, const float *u_node, const float *u_res,
                          int32_t *accepted_len, int32_t *correction, int32_t *path,

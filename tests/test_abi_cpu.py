@@ -94,6 +94,15 @@ def test_host_argument_checks(lib):
                          FAKE, FAKE, FAKE, 1 << 24, None, None) == 1
     assert lib.ds_verify(FAKE, 1, 4, 4096, 1.0, FAKE, 4096, None, None, FAKE, FAKE, 32, FAKE, FAKE, FAKE, None,
                          FAKE, FAKE, FAKE, 1 << 24, None, None) == 1
-    assert lib.ds_verify_tree(FAKE, 1, 3, 65, 4096, 1.0, FAKE, FAKE, 4096, FAKE, FAKE, 32, FAKE, FAKE,
-                              FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 24, None, None) == 1
+    # tree verify: Wd beyond the limit; only one of q_max / q_sumexp; NULL vs_ids
+    tree = [FAKE, 1, 3, 4, 4096, 1.0, FAKE, FAKE, 4096, None, None, FAKE, FAKE, 4096, FAKE, 32, FAKE, FAKE,
+            FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 26, None, None]
+    t = list(tree); t[3] = 65
+    assert lib.ds_verify_tree(*t) == 1
+    t = list(tree); t[9] = FAKE
+    assert lib.ds_verify_tree(*t) == 1
+    t = list(tree); t[12] = None
+    assert lib.ds_verify_tree(*t) == 1
+    t = list(tree); t[25] = 16
+    assert lib.ds_verify_tree(*t) == 4
     assert lib.ds_philox4x32_10(None, 0, FAKE, 4, None) == 1

@@ -12,7 +12,7 @@ torch = pytest.importorskip("torch")
 
 import oracle                          # noqa: E402
 import workloads as wl                 # noqa: E402
-from parity import (assert_close, topk_same_or_excused, token_same_or_excused,  # noqa: E402
+from parity import (ICDF_TOL, assert_close, topk_same_or_excused, token_same_or_excused,  # noqa: E402
                     softmax_full, q_dense, icdf_acceptable, accept_margin, TIE)
 import gpu_util as gu                  # noqa: E402
 
@@ -415,64 +415,137 @@ def test_verify_chain(ds, name, B, T, mode):
         assert acc_ref.mean() > 0.5 * cfg.gamma           # the accept path is exercised
 
 
-def test_verify_tree(ds):
+def _run_tree_verify(ds, V, M, csr_off, csr_tok, parent, D, Wd, ids, S, qfp, didx, z, u_node, u_res, T,
+                     with_stats):
+    """GPU tree verification on host-built draft data against the oracle's.  ids[k] [B, k_c]
+    cluster ids of depth k+1; S[b][k] the lists; qfp[b][n] node n's fp32 draft logits;
+    didx [B, N] each node's token index in its list."""
+    B = z.shape[0]
+    acc_ref, corr_ref, path_ref = oracle.verify_tree(
+        z, parent, S, [[q.astype(np.float64) for q in qfp[b]] for b in range(B)], didx, u_node, u_res, T)
+    cap = max(sum(S[b][k].size for b in range(B)) for k in range(D))
+    q = np.zeros((D, cap * Wd), np.float32)
+    ids_dev = np.zeros((D, cap), np.int32)
+    offs = np.zeros((D, B + 1), np.int32)
+    cpos = np.zeros((D, B * M), np.int32)
+    ntok = np.zeros((D, B * Wd), np.int32)
+    qmax = np.zeros((D, B * Wd), np.float32)
+    qsum = np.zeros((D, B * Wd), np.float32)
+    sizes = np.diff(csr_off)
+    for k in range(D):
+        run = 0
+        for b in range(B):
+            n_b = S[b][k].size
+            offs[k, b] = run
+            ids_dev[k, run:run + n_b] = S[b][k]
+            row = np.full(M, -1, np.int32)
+            pos = 0
+            for c in ids[k][b]:
+                row[c] = pos
+                pos += sizes[c]
+            cpos[k, b * M:(b + 1) * M] = row
+            for i in range(Wd):
+                l = qfp[b][k * Wd + i]
+                q[k, run * Wd + i * n_b: run * Wd + (i + 1) * n_b] = l
+                ntok[k, b * Wd + i] = S[b][k][didx[b, k * Wd + i]]
+                if T > 0:
+                    x = l.astype(np.float64) / T
+                    qmax[k, b * Wd + i] = np.float32(x.max())
+                    qsum[k, b * Wd + i] = np.float32(np.exp(x - x.max()).sum())
+            run += n_b
+        offs[k, B] = run
+    cof = torch.empty(V, dtype=torch.int32, device=gu.dev())
+    rk = torch.empty(V, dtype=torch.int32, device=gu.dev())
+    ds.vocab_index(gu.i32(csr_off), gu.i32(csr_tok), cof, rk, gu.status())
+    acc = torch.empty(B, dtype=torch.int32, device=gu.dev())
+    corr = torch.empty(B, dtype=torch.int32, device=gu.dev())
+    path = torch.empty(B, D, dtype=torch.int32, device=gu.dev())
+    st = gu.status()
+    ws = ds.workspace(ds.verify_tree_workspace_bytes(B, D, Wd, V), gu.dev())
+    stats = dict(q_max=gu.f32(qmax), q_sumexp=gu.f32(qsum)) if with_stats and T > 0 else {}
+    ds.verify_tree(gu.f32(z), D, Wd, T, gu.i32(parent), gu.f32(q), gu.i32(offs), gu.i32(ids_dev), gu.i32(cpos),
+                   cof, rk, gu.i32(ntok), gu.f32(u_node), gu.f32(u_res), acc, corr, path, ws, st, **stats)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(acc.cpu().numpy(), acc_ref), (acc.cpu().numpy(), acc_ref)
+    assert np.array_equal(path.cpu().numpy(), path_ref)
+    corr_gpu = corr.cpu().numpy()
+    if not np.array_equal(corr_gpu, corr_ref):
+        # inverse-CDF near-tie (fp32 vs fp64 cumulative sums): the GPU's token must lie between
+        # the oracle's draws at u_res -/+ ICDF_TOL (the draw is monotone in u)
+        assert T > 0
+        qd = [[q.astype(np.float64) for q in qfp[b]] for b in range(B)]
+        lo = oracle.verify_tree(z, parent, S, qd, didx, u_node, np.clip(u_res - ICDF_TOL, 0, 1).astype(np.float32), T)
+        hi = oracle.verify_tree(z, parent, S, qd, didx, u_node, np.clip(u_res + ICDF_TOL, 0, 1).astype(np.float32), T)
+        for b in np.nonzero(corr_gpu != corr_ref)[0]:
+            assert lo[0][b] == acc_ref[b] and hi[0][b] == acc_ref[b]
+            assert lo[1][b] <= corr_gpu[b] <= hi[1][b], (b, corr_gpu[b], corr_ref[b], lo[1][b], hi[1][b])
+    return acc_ref
+
+
+def _align_targets(z, parent, S, qfp, D, Wd, upto=None):
+    """Make each node's target row look like its first child's draft row (the accept path),
+    for nodes above depth `upto` (all by default)."""
+    z = z.copy()
+    upto = D if upto is None else upto
+    for b in range(z.shape[0]):
+        for n in range(-1, D * Wd):
+            dep = n // Wd + 1 if n >= 0 else 0
+            if dep >= upto:
+                continue
+            kids = [c for c in range(D * Wd) if parent[c] == n]
+            if not kids:
+                continue
+            z[b, n + 1] = -60.0
+            z[b, n + 1, S[b][dep]] = qfp[b][kids[0]]
+    return z
+
+
+@pytest.mark.parametrize("with_stats", [False, True])
+def test_verify_tree(ds, with_stats):
     inp = gu.tree_inputs("tiny_tree")
     cfg = inp["cfg"]
     B, D, Wd, V, M = cfg.B, cfg.gamma, cfg.width, cfg.V, cfg.M
+    N = D * Wd
+    ref = oracle.tree_step(inp, verify=False)
+    S = [[ref[b]["depths"][k]["S"] for k in range(D)] for b in range(B)]
+    ids = [np.stack([ref[b]["depths"][k]["ids"] for b in range(B)]) for k in range(D)]
+    qfp = [[ref[b]["depths"][n // Wd]["nodes"][n % Wd]["logits"].astype(np.float32) for n in range(N)]
+           for b in range(B)]
+    didx = np.array([[ref[b]["depths"][n // Wd]["nodes"][n % Wd]["idx"] for n in range(N)] for b in range(B)])
     for mode in ("independent", "aligned"):
-        ref = oracle.tree_step(inp, verify=False)
-        z = inp["z"].copy()
-        if mode == "aligned":
-            for b in range(B):
-                for n in range(-1, D * Wd):      # make each node's target row look like its first child's draft row
-                    dep = n // Wd + 1 if n >= 0 else 0
-                    if dep >= D:
-                        continue
-                    kids = [c for c in range(D * Wd) if inp["parent"][c] == n]
-                    if not kids:
-                        continue
-                    c0 = kids[0]
-                    S = ref[b]["depths"][dep]["S"]
-                    l = ref[b]["depths"][dep]["nodes"][c0 % Wd]["logits"]
-                    z[b, n + 1] = -60.0
-                    z[b, n + 1, S] = l.astype(np.float32)
-        N = D * Wd
-        qfp = [[ref[b]["depths"][n // Wd]["nodes"][n % Wd]["logits"].astype(np.float32) for n in range(N)]
-               for b in range(B)]
-        acc_ref, corr_ref, path_ref = oracle.verify_tree(
-            z, inp["parent"], [[ref[b]["depths"][k]["S"] for k in range(D)] for b in range(B)],
-            [[q.astype(np.float64) for q in qfp[b]] for b in range(B)],
-            np.array([[ref[b]["depths"][n // Wd]["nodes"][n % Wd]["idx"] for n in range(N)] for b in range(B)]),
-            inp["u_node"], inp["u_res"], cfg.T)
-        cap = B * V * Wd
-        q = np.zeros((D, cap), np.float32)
-        offs = np.zeros((D, B + 1), np.int32)
-        cpos = np.zeros((D, B * M), np.int32)
-        ntok = np.zeros((D, B * Wd), np.int32)
-        for k in range(D):
-            ids = np.stack([ref[b]["depths"][k]["ids"] for b in range(B)])
-            cpos[k] = _host_cpos(inp, ids).ravel()
-            run = 0
-            for b in range(B):
-                n_b = ref[b]["depths"][k]["S"].size
-                offs[k, b] = run
-                for i in range(Wd):
-                    q[k, run * Wd + i * n_b: run * Wd + (i + 1) * n_b] = qfp[b][k * Wd + i]
-                    ntok[k, b * Wd + i] = ref[b]["depths"][k]["nodes"][i]["token"]
-                run += n_b
-            offs[k, B] = run
-        cof, rk = _vocab_index_dev(ds, inp)
-        acc = torch.empty(B, dtype=torch.int32, device=gu.dev())
-        corr = torch.empty(B, dtype=torch.int32, device=gu.dev())
-        path = torch.empty(B, D, dtype=torch.int32, device=gu.dev())
-        st = gu.status()
-        ws = ds.workspace(ds.verify_tree_workspace_bytes(B, D, Wd, V), gu.dev())
-        ds.verify_tree(gu.f32(z), D, Wd, cfg.T, gu.i32(inp["parent"]), gu.f32(q), gu.i32(offs), gu.i32(cpos),
-                       cof, rk, gu.i32(ntok), gu.f32(inp["u_node"]), gu.f32(inp["u_res"]), acc, corr, path, ws, st)
-        torch.cuda.synchronize()
-        assert st.item() == 0
-        assert np.array_equal(acc.cpu().numpy(), acc_ref), (mode, acc.cpu().numpy(), acc_ref)
-        assert np.array_equal(path.cpu().numpy(), path_ref)
-        assert np.array_equal(corr.cpu().numpy(), corr_ref), (mode, corr.cpu().numpy(), corr_ref)
+        z = inp["z"] if mode == "independent" else _align_targets(inp["z"], inp["parent"], S, qfp, D, Wd)
+        acc_ref = _run_tree_verify(ds, V, M, inp["csr_off"], inp["csr_tok"], inp["parent"], D, Wd, ids, S, qfp,
+                                   didx, z, inp["u_node"], inp["u_res"], cfg.T, with_stats)
         if mode == "aligned":
             assert acc_ref.sum() > 0
+
+
+@pytest.mark.parametrize("T", [0.8, 0.0])
+def test_verify_tree_full_size(ds, T):
+    # The tree workload's sizes (V = 128256, M = 1024, B = 8, 6 depths x 10 nodes) with seeded
+    # host-built lists and draft rows; the aligned variant walks deep.
+    cfg = wl.config("tree")
+    B, D, Wd, V, M = cfg.B, cfg.gamma, cfg.width, cfg.V, cfg.M
+    N = D * Wd
+    csr_off, csr_tok = wl.cluster_partition(cfg, 0)
+    parent = wl.tree_parents(D, Wd)
+    rng = np.random.default_rng(7)
+    ids = [np.sort(np.stack([rng.choice(M, cfg.budget[k], replace=False) for _ in range(B)]), axis=1)
+           for k in range(D)]
+    S = [[oracle.shortlist(csr_off, csr_tok, ids[k][b]) for k in range(D)] for b in range(B)]
+    qfp = [[(rng.standard_normal(S[b][n // Wd].size) * 2.0).astype(np.float32) for n in range(N)]
+           for b in range(B)]
+    didx = np.array([[int(np.argmax(qfp[b][n])) for n in range(N)] for b in range(B)])
+    u_node = rng.random((B, N)).astype(np.float32)
+    u_res = rng.random((B, D + 1)).astype(np.float32)
+    z0 = (rng.standard_normal((B, 1 + N, V)) * 3.0).astype(np.float32)
+    for mode in ("independent", "aligned", "partial"):
+        z = z0 if mode == "independent" else _align_targets(z0, parent, S, qfp, D, Wd,
+                                                            upto=3 if mode == "partial" else None)
+        acc_ref = _run_tree_verify(ds, V, M, csr_off, csr_tok, parent, D, Wd, ids, S, qfp, didx, z,
+                                   u_node, u_res, T, with_stats=True)
+        if mode == "aligned":
+            assert acc_ref.sum() >= B
+        if mode == "partial":
+            assert (acc_ref >= 1).all() and (acc_ref < D).all()

@@ -20,8 +20,12 @@
 //   2. verify_residual_kernel grid (chunks, B): per-chunk mass of the residual (or of p for
 //      the bonus draw); the last block of a sequence locates the inverse-CDF crossing chunk
 //      and scans it.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "block_scan.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace ds {
 namespace {
@@ -427,7 +431,7 @@ verify_residual_kernel(ChainArgs a)
 // after a rejected sibling differs from the current target only on that shortlist: the walk
 // keeps it as (O = target mass off the list, r_j on the list) and never builds a dense row.
 //
-//   tree_walk_kernel      one 1024-thread block per sequence.  At each visited node one pass
+//   tree_walk_kernel      one cluster of up to 8 CTAs per sequence.  At each visited node one pass
 //                         over the target row gives its max, sum-exp, argmax and the mass
 //                         off the children's list; r_j = p(S_j) is gathered over the list;
 //                         every rejected sibling costs one pass over the list.  Only the
@@ -437,6 +441,7 @@ verify_residual_kernel(ChainArgs a)
 // ---------------------------------------------------------------------------------------
 constexpr int kWalkThreads = 1024;
 constexpr int kWalkMaxM = 8192;
+constexpr int kWalkMaxCluster = 8;              // CTAs per sequence (portable cluster size)
 
 struct WalkState {                 // what the walk leaves for the correction draw
     int mode;                      // 0: decided (greedy); 1: draw from p of `row`; 2: residual
@@ -540,17 +545,73 @@ __device__ RowStat block_rowstat(RowStat st, RowStat *ws)
     return ws[32];
 }
 
+// Cluster-wide reductions.  Every CTA reduces its own threads, publishes the result in its
+// shared memory, and after a cluster barrier each CTA merges all CTAs' results in rank order,
+// so every thread of the cluster holds the same bits and takes the same decisions.  Two
+// publication slots alternate: a CTA rewrites a slot only after the barrier of the next
+// reduction, which every other CTA reaches only once it has finished reading that slot.
+struct ClusterRed {
+    RowStat stat[2];
+    float sum[2];
+    int k;                                       // reductions so far (per thread, uniform)
+};
+
+__device__ RowStat cluster_rowstat(RowStat st, RowStat *red, ClusterRed &cr, int &k)
+{
+    cg::cluster_group cl = cg::this_cluster();
+    const RowStat mine = block_rowstat(st, red);
+    const int slot = k & 1;
+    if (threadIdx.x == 0) cr.stat[slot] = mine;
+    cl.sync();
+    if (threadIdx.x == 0) {
+        RowStat m = rowstat_empty();
+        for (unsigned r = 0; r < cl.num_blocks(); ++r) m = rowstat_merge(m, cl.map_shared_rank(&cr, r)->stat[slot]);
+        red[32] = m;
+    }
+    __syncthreads();
+    const RowStat out = red[32];
+    ++k;
+    return out;
+}
+
+__device__ float cluster_sum(float x, float *scratch, ClusterRed &cr, int &k)
+{
+    cg::cluster_group cl = cg::this_cluster();
+    const float mine = block_sum(x, scratch);
+    const int slot = k & 1;
+    if (threadIdx.x == 0) cr.sum[slot] = mine;
+    cl.sync();
+    if (threadIdx.x == 0) {
+        float s = 0.f;
+        for (unsigned r = 0; r < cl.num_blocks(); ++r) s += cl.map_shared_rank(&cr, r)->sum[slot];
+        scratch[32] = s;
+    }
+    __syncthreads();
+    const float out = scratch[32];
+    __syncthreads();
+    ++k;
+    return out;
+}
+
+// One thread-block cluster per sequence (grid = B clusters of CL CTAs): every pass over the
+// target row or the list is split over all CL * 1024 threads of the cluster.
 __global__ void __launch_bounds__(kWalkThreads)
 tree_walk_kernel(TreeArgs a)
 {
     __shared__ int s_cpos[kWalkMaxM];           // cpos of the children's list
     __shared__ RowStat s_red[33];
     __shared__ float fscr[33];
+    __shared__ ClusterRed s_cr;
     __shared__ int s_kids[64];
     __shared__ int s_nkids, s_accept;
-    const int b = blockIdx.x;
+    cg::cluster_group cl = cg::this_cluster();
+    const int CL = int(cl.num_blocks()), crank = int(cl.block_rank());
+    const int b = blockIdx.x / CL;
     const int tid = threadIdx.x;
-    if (tid < a.D) a.path[size_t(b) * a.D + tid] = -1;
+    const int gt = crank * blockDim.x + tid, GT = CL * blockDim.x;
+    const bool lead = crank == 0 && tid == 0;
+    int nred = 0;
+    if (crank == 0 && tid < a.D) a.path[size_t(b) * a.D + tid] = -1;
     int cur = -1, dep = 0, A = 0, corr = -1;
     WalkState ws{0, 0, 0, 0, 0.f, 1.f, 0, 0};
     int cb = 0;                                  // which residual buffer holds r
@@ -575,13 +636,13 @@ tree_walk_kernel(TreeArgs a)
         const int nk = s_nkids;
         // one pass over the target row
         RowStat st = rowstat_empty();
-        for (int v = tid; v < a.V; v += blockDim.x) {
+        for (int v = gt; v < a.V; v += GT) {
             const float zv = z[v];
             const int c = a.cluster_of[v];
             const bool off = has_list && (unsigned(c) >= unsigned(a.M) || s_cpos[c] < 0);
             rowstat_add(st, zv, zv * a.inv_te, off, v);
         }
-        const RowStat row = block_rowstat(st, s_red);
+        const RowStat row = cluster_rowstat(st, s_red, s_cr, nred);
         if (a.T == 0.f) {
             const int am = row.aid;
             int next = -1;
@@ -590,7 +651,7 @@ tree_walk_kernel(TreeArgs a)
                 if (a.node_tokens[size_t(dep) * a.B * a.Wd + size_t(b) * a.Wd + (n - dep * a.Wd)] == am) { next = n; break; }
             }
             if (next < 0) { corr = am; ws.mode = 0; break; }
-            if (tid == 0) a.path[size_t(b) * a.D + A] = next;
+            if (lead) a.path[size_t(b) * a.D + A] = next;
             ++A; cur = next; ++dep;
             continue;
         }
@@ -604,14 +665,15 @@ tree_walk_kernel(TreeArgs a)
         const int32_t *ids = a.vs_ids + size_t(dep) * a.vs_stride + lo;
         float *r = a.rbuf + (size_t(b) * 2 + cb) * a.V;
         float on = 0.f;
-        for (int j = tid; j < nb; j += blockDim.x) {
+        for (int j = gt; j < nb; j += GT) {
             const int v = ids[j];
             const float pj = (v >= 0 && v < a.V) ? __expf(z[v] * a.inv_te - row.m) / row.s : 0.f;
             r[j] = pj;
             on += pj;
         }
+        __threadfence();                         // r is read across the cluster after the barrier
         const float O = row.o / row.s;
-        float R = O + block_sum(on, fscr);
+        float R = O + cluster_sum(on, fscr, s_cr, nred);
         int next = -1;
         for (int k = 0; k < nk; ++k) {
             const int n = s_kids[k];
@@ -623,11 +685,11 @@ tree_walk_kernel(TreeArgs a)
                 qs = a.q_sumexp[size_t(dep) * a.B * a.Wd + hr];
             } else {
                 RowStat q = rowstat_empty();
-                for (int j = tid; j < nb; j += blockDim.x) rowstat_add(q, ql[j], ql[j] * a.inv_te, false, j);
-                q = block_rowstat(q, s_red);
+                for (int j = gt; j < nb; j += GT) rowstat_add(q, ql[j], ql[j] * a.inv_te, false, j);
+                q = cluster_rowstat(q, s_red, s_cr, nred);
                 qm = q.m; qs = q.s;
             }
-            if (tid == 0) {
+            if (tid == 0) {                      // every CTA takes the same test on the same data
                 const int x = a.node_tokens[size_t(dep) * a.B * a.Wd + hr];
                 int j = -1;
                 if (x >= 0 && x < a.V) {
@@ -637,7 +699,7 @@ tree_walk_kernel(TreeArgs a)
                 }
                 int acc = 0;
                 if (j < 0 || j >= nb) set_status(a.status, DS_DEV_BAD_INDEX);
-                else acc = a.u_node[size_t(b) * a.N + n] * (__expf(ql[j] * a.inv_te - qm) / qs) < r[j] / R;
+                else acc = a.u_node[size_t(b) * a.N + n] * (__expf(ql[j] * a.inv_te - qm) / qs) < __ldcg(&r[j]) / R;
                 s_accept = acc;
             }
             __syncthreads();
@@ -645,27 +707,29 @@ tree_walk_kernel(TreeArgs a)
             // rejected: r <- max(r - R q, 0) into the other buffer, kept if it has mass
             float *rn = a.rbuf + (size_t(b) * 2 + (cb ^ 1)) * a.V;
             float part = 0.f;
-            for (int j = tid; j < nb; j += blockDim.x) {
+            for (int j = gt; j < nb; j += GT) {
                 const float w = fmaxf(r[j] - R * (__expf(ql[j] * a.inv_te - qm) / qs), 0.f);
                 rn[j] = w;
                 part += w;
             }
-            const float Rn = O + block_sum(part, fscr);
+            __threadfence();
+            const float Rn = O + cluster_sum(part, fscr, s_cr, nred);
             if (Rn > 0.f) { cb ^= 1; r = rn; R = Rn; }
         }
         if (next >= 0) {
-            if (tid == 0) a.path[size_t(b) * a.D + A] = next;
+            if (lead) a.path[size_t(b) * a.D + A] = next;
             ++A; cur = next; ++dep;
             continue;
         }
         ws.mode = 2; ws.buf = cb;
         break;
     }
-    if (tid == 0) {
+    if (lead) {
         a.accepted[b] = A;
         if (ws.mode == 0) a.correction[b] = corr;
         a.state[b] = ws;
     }
+    cl.sync();                                   // no CTA leaves while others may read its slots
 }
 
 __global__ void __launch_bounds__(kVThreads)
@@ -806,8 +870,26 @@ extern "C" ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd,
     a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.psum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.cnt = reinterpret_cast<unsigned *>(w);
-    tree_walk_kernel<<<B, kWalkThreads, 0, stream>>>(a);
-    DS_TRY_LAUNCH();
+    // one cluster of CL CTAs per sequence, CL = 8, 4, 2 or 1 so that the clusters fit the GPU
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return DS_ERR_CUDA;
+    int CL = kWalkMaxCluster;
+    while (CL > 1 && long(B) * CL > sms) CL >>= 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(B * CL));
+    cfg.blockDim = dim3(kWalkThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(CL);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, tree_walk_kernel, a) != cudaSuccess) { (void)cudaGetLastError(); return DS_ERR_CUDA; }
     tree_residual_kernel<<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
     DS_TRY_LAUNCH();
     return DS_OK;

@@ -200,6 +200,11 @@ __device__ __forceinline__ void mbar_fence_init()
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity)
 {
     uint32_t done;

@@ -295,6 +295,8 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f)
 
 struct DenseRows {
     int n;
+    using State = tc::NoState;
+    __device__ void finish(State &) const {}
     __device__ int n_rows() const { return n; }
     __device__ void pick(int u, int &v, int &c) const { v = u; c = 0; }
     __device__ void col_info(int r, int &i, long long &l) const { i = r; l = 0; }
@@ -306,7 +308,8 @@ struct Layer1Ep : DenseRows {
     uint16_t *hid2;
     int Hr, act;
     __device__ int row_aux(int v) const { return v >= 0 ? __float_as_int(bf16_to_f32(bias[v])) : 0; }
-    __device__ void emit(const float (&x)[16], int cb, int v, int, int aux, const int32_t *s_i, const long long *) const
+    __device__ void emit(State &, const float (&x)[16], int cb, int v, int, int aux, const int32_t *s_i,
+                         const long long *) const
     {
         if (v < 0) return;
         const float bv = __int_as_float(aux);
@@ -329,7 +332,8 @@ struct Layer2Ep : DenseRows {
     float *scores;
     int M, B;
     __device__ int row_aux(int v) const { return v >= 0 ? __float_as_int(bf16_to_f32(bias[v])) : 0; }
-    __device__ void emit(const float (&x)[16], int cb, int v, int, int aux, const int32_t *, const long long *) const
+    __device__ void emit(State &, const float (&x)[16], int cb, int v, int, int aux, const int32_t *,
+                         const long long *) const
     {
         if (v < 0) return;
         const float bv = __int_as_float(aux);

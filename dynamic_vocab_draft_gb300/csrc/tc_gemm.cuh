@@ -16,20 +16,23 @@
 // tile whose stages fall into several CTAs is finished by the last of them, which adds the
 // parts in k order (so results do not depend on timing).
 //
-// Per CTA one software pipeline runs across its tiles: kStages shared-memory slots, loads
-// kLook stages ahead of the stage being multiplied, and the MMAs of stage i are waited for
-// only when their slot is refilled two stages later, so the loads never wait on the tensor
-// core.  A slot holds the 128 A rows and the N B rows for its columns in the 128-byte-swizzled
+// Per CTA the work is split between warp roles that meet only at mbarriers (no CTA-wide
+// barrier inside the main loop):
+//   * producers (8 warps) copy each stage into one of kStages shared-memory slots with
+//     cp.async, every thread a fixed 16-byte column chunk of a fixed set of rows, and arrive
+//     on the slot's `full` barrier when their copies land (cp.async.mbarrier.arrive);
+//   * one thread issues the stage's MMAs (M=128, N=16*MT, K=16 each) into one of two tensor-
+//     memory accumulators and commits them to the slot's `empty` barrier, and at a tile's end
+//     to the accumulator's `full` barrier;
+//   * epilogue warps (8) read a finished accumulator with tcgen05.ld, release it, and hand
+//     the values to the policy while the next tile is being multiplied into the other one.
+// A slot holds the 128 A rows and the N B rows for its columns in the 128-byte-swizzled
 // K-major layout the MMA descriptors describe (8-row x 128-byte atoms, 16-byte chunk c of row
-// r at c ^ (r & 7)).  Each of the 512 threads copies one fixed 16-byte column chunk of a fixed
-// set of rows with cp.async, so a stage costs a handful of instructions per thread; one thread
-// issues the MMAs (M=128, N=16*MT, K=16 each) and commits them to the slot's mbarrier.  At a
-// tile's end the epilogue reads the 128 x N accumulator with tcgen05.ld (the four warps of
-// each TMEM lane quarter split the columns, each warp its 32 lanes = A rows) while the next
-// stages' loads are in flight.
+// r at c ^ (r & 7)).
 //
-// Every wait on an mbarrier is bounded; a wait that gives up sets DS_DEV_TIMEOUT, the CTA
-// stops, waits (bounded) for its MMAs in flight and frees its tensor memory.
+// Every wait on an mbarrier is bounded and also gives up when another role has failed; a wait
+// that gives up sets DS_DEV_TIMEOUT.  Producers leave no copy in flight, the MMA thread waits
+// (bounded) for its MMAs to finish, and the tensor memory is freed after a final barrier.
 #pragma once
 #include "common.cuh"
 
@@ -37,7 +40,7 @@ namespace ds {
 namespace tc {
 
 constexpr int kRows = 128;                  // A rows per tile (MMA M)
-constexpr int kThreads = 512;
+constexpr int kThreads = 544;               // 8 epilogue warps, 8 producer warps, 1 MMA warp
 constexpr int kMaxGrid = 160;               // CTAs of one launch (<= SMs in use)
 
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
@@ -55,13 +58,12 @@ template <int MT> struct Cfg {
     static constexpr int kABytes = kAtoms * kRows * 128;       // A part of a stage
     static constexpr int kBBytes = kAtoms * N * 128;           // B part of a stage
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = cmin(6, (210 * 1024) / kStageBytes);
-    static constexpr int kLook = kStages - 2;                  // stages loaded ahead
-    static constexpr int kMeta = kLook + 2;                    // tiles whose row ids are held
-    static constexpr int kTmemCols = N <= 32 ? 32 : N <= 64 ? 64 : 128;
-    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 /* align */ +
-                                    size_t(kMeta) * 2 * kRows * sizeof(int32_t);
+    static constexpr int kStages = cmin(8, (220 * 1024) / kStageBytes);
+    // two accumulators of N columns (the epilogue drains one while the MMAs fill the other)
+    static constexpr int kTmemCols = 2 * N <= 32 ? 32 : 2 * N <= 64 ? 64 : 2 * N <= 128 ? 128 : 256;
+    static constexpr size_t kSmem = size_t(kStages) * kStageBytes + 1024 /* align */;
     static_assert(kStages >= 3, "the pipeline needs three slots");
+    static_assert(kSmem + 2560 <= 232448, "dynamic + static shared memory per CTA");
 };
 
 // Bytes of the partial-tile buffer a launch with `grid` CTAs and R vectors needs (two 128 x N
@@ -139,26 +141,59 @@ __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16])
 //   void pick(int u, int &v, int &c)      A row of list entry u (-1: none) and a tag c
 //   void col_info(int r, int &i, long long &l)  per-vector values the epilogue keeps in smem
 //   int row_aux(int v)                    per-row value loaded at the tile's epilogue
-//   void emit(x[16], cb, v, c, aux, s_i, s_l)   accumulator row of A row v, columns cb..cb+15
+//   State                                 per-thread epilogue state, value-initialised
+//   void emit(st, x[16], cb, v, c, aux, s_i, s_l)  accumulator row of A row v, columns cb..cb+15
+//   void finish(st)                       called once by every thread of every CTA at the end
+//                                         (also by CTAs without work), e.g. to fold st
+// NoState is the State of policies that keep none.
+struct NoState {};
+// Warp roles.  Warps 0-7: epilogue (warp w reads TMEM lanes 32(w%4) .. +31 = A rows of the
+// tile, and every other 16-column group starting at 16(w/4)).  Warps 8-15: producers (256
+// threads of cp.async).  Warp 16: TMEM owner and MMA issuer (one thread).
+constexpr int kEpiWarps = 8;
+constexpr int kProdBase = 256;                  // first producer thread
+constexpr int kProducers = 256;
+constexpr int kMmaWarp = 16;
+static_assert(kThreads == kProdBase + kProducers + 32, "warp roles");
+
+// Wait for a phase of an mbarrier, giving up after the budget or when another role failed.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, unsigned parity, volatile int *fail)
+{
+    if (mbar_test(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity)) {
+        if (*fail) return false;
+        if (clock64() - t0 > kWaitBudgetCycles) return false;
+    }
+    return true;
+}
+
+// Arrive on `bar` once all of this thread's earlier cp.async copies have landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" :: "n"(kEpiWarps * 32) : "memory"); }
+
 template <int MT, class Ep>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict__ tile_cnt)
 {
     using C = Cfg<MT>;
-    constexpr int STG = C::kStages, L = C::kLook;
+    constexpr int STG = C::kStages;
     constexpr int CPR = C::kAtoms * 8;                         // 16-byte chunks per row per stage
-    constexpr int RPP = kThreads / CPR;                        // rows per pass of all threads
+    constexpr int RPP = kProducers / CPR;                      // rows per pass of the producers
     constexpr int APASS = kRows / RPP;                         // A-row passes per stage
     constexpr int BPASS = (C::N + RPP - 1) / RPP;              // B-row passes per stage
     static_assert(kRows % RPP == 0 && RPP % 8 == 0, "row passes share their swizzle phase");
     extern __shared__ __align__(1024) unsigned char tc_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
-    int32_t *s_meta = reinterpret_cast<int32_t *>(sm + size_t(STG) * C::kStageBytes);   // [kMeta][v | c][128]
-    __shared__ uint64_t mma_done[STG];
+    __shared__ uint64_t full[STG], empty[STG], acc_full[2], acc_empty[2], mma_idle;
     __shared__ int32_t s_ci[C::N];
     __shared__ long long s_cl[C::N];
     __shared__ uint32_t s_tmem;
-    __shared__ int s_fail, s_first_owner, s_last_owner;
+    __shared__ int s_fail, s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = op.d, R = op.R;
     const int nU = ep.n_rows();
@@ -167,7 +202,8 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
     const long long total = 1LL * ntiles * nks;                // < 2^31 by the host's limits
     const int grid = gridDim.x, bid = blockIdx.x;
     const int g0 = int(total * bid / grid), g1 = int(total * (bid + 1) / grid);
-    if (g0 >= g1) return;                                      // uniform: no stage for this CTA
+    typename Ep::State est{};
+    if (g0 >= g1) { ep.finish(est); return; }                  // uniform: no stage for this CTA
     constexpr uint32_t idesc = umma_idesc_bf16(kRows, C::N);
     // the CTA whose range holds unit i, the first tile of CTA c, and the owner of the unit
     // after CTA c's range (CTAs with empty ranges own nothing)
@@ -176,7 +212,9 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
     auto next_owner = [&](int c) { return cta_of(total * (c + 1) / grid); };
 
     if (tid == 0) {
-        for (int i = 0; i < STG; ++i) mbar_init(&mma_done[i], 1);
+        for (int i = 0; i < STG; ++i) { mbar_init(&full[i], kProducers); mbar_init(&empty[i], 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&acc_full[i], 1); mbar_init(&acc_empty[i], kEpiWarps); }
+        mbar_init(&mma_idle, 1);
         mbar_fence_init();
         s_fail = 0;
     }
@@ -187,7 +225,7 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
         s_ci[r] = ci;
         s_cl[r] = cl;
     }
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      :: "r"(smem_u32(&s_tmem)), "r"(uint32_t(C::kTmemCols)) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -196,201 +234,183 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
     __syncthreads();
     fence_after();
     const uint32_t tmem = s_tmem;
-
-    // Every thread copies one fixed 16-byte column chunk `ch` of rows prow + RPP*j.  Its shared-
-    // memory destinations are the same in every stage (up to the slot base); its sources move
-    // by kCols columns per stage.
-    const int ch = tid % CPR, prow = tid / CPR;
-    const int coff = (ch >> 3) * 64 + (ch & 7) * 8;            // column of the chunk inside a stage
-    const uint32_t dst0 = uint32_t((ch >> 3) * (kRows * 128) + prow * 128 + (((ch & 7) ^ (prow & 7)) << 4));
-    const uint32_t bdst0 = uint32_t((ch >> 3) * (C::N * 128) + prow * 128 + (((ch & 7) ^ (prow & 7)) << 4));
-    const uint16_t *bsrc[BPASS];
-#pragma unroll
-    for (int j = 0; j < BPASS; ++j) {
-        const int r = prow + RPP * j;
-        bsrc[j] = r < R ? op.B + size_t(r) * d + coff : nullptr;
-    }
-    const uint16_t *asrc[APASS];                               // rows of the tile being filled
+    volatile int *fail = &s_fail;
     const uint32_t smem0 = smem_u32(sm);
 
-    // Row ids and tags of tile t into ring slot t % kMeta, and this thread's row pointers for
-    // it.  Tiles arrive in increasing order; every thread calls this with the same t.
-    int meta_tile = -1;
-    auto ensure_meta = [&](int t) {
-        if (t == meta_tile) return;
-        int32_t *mv = s_meta + (t % C::kMeta) * (2 * kRows);
-        for (int q = tid; q < kRows; q += kThreads) {
-            const int u = t * kRows + q;
-            int v = -1, c = -1;
-            if (u < nU) ep.pick(u, v, c);
-            mv[q] = v;
-            mv[kRows + q] = c;
-        }
-        meta_tile = t;
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < APASS; ++j) {
-            const int v = mv[prow + RPP * j];
-            asrc[j] = v >= 0 ? op.A + size_t(v) * d + coff : nullptr;
-        }
-    };
-    // cp.async fill of slot `slot` with k-stage ks of the tile ensure_meta last prepared
-    auto fill = [&](int slot, int ks) {
-        const int k0 = ks * C::kCols;
-        const bool kin = k0 + coff < d;
-        const uint32_t As = smem0 + uint32_t(slot * C::kStageBytes);
-        const uint32_t Bs = As + C::kABytes;
-#pragma unroll
-        for (int j = 0; j < APASS; ++j) {
-            const bool ok = kin && asrc[j] != nullptr;
-            cp_async16(As + dst0 + uint32_t(j * RPP * 128), ok ? asrc[j] + k0 : op.A, ok ? 16 : 0);
-        }
+    if (tid >= kProdBase && tid < kProdBase + kProducers) {
+        // ---------------- producers: fill slot li % STG with stage i, then arrive on full[]
+        const int p = tid - kProdBase;
+        const int ch = p % CPR, prow = p / CPR;
+        const int coff = (ch >> 3) * 64 + (ch & 7) * 8;        // column of the chunk inside a stage
+        const uint32_t dst0 = uint32_t((ch >> 3) * (kRows * 128) + prow * 128 + (((ch & 7) ^ (prow & 7)) << 4));
+        const uint32_t bdst0 = uint32_t((ch >> 3) * (C::N * 128) + prow * 128 + (((ch & 7) ^ (prow & 7)) << 4));
+        const uint16_t *bsrc[BPASS];
 #pragma unroll
         for (int j = 0; j < BPASS; ++j) {
-            if (prow + RPP * j < C::N) {
-                const bool ok = kin && bsrc[j] != nullptr;
-                cp_async16(Bs + bdst0 + uint32_t(j * RPP * 128), ok ? bsrc[j] + k0 : op.B, ok ? 16 : 0);
-            }
+            const int r = prow + RPP * j;
+            bsrc[j] = r < R ? op.B + size_t(r) * d + coff : nullptr;
         }
-    };
-
-    // (tile, k-stage) of the stage being multiplied and of the next stage to load
-    int t = g0 / nks, ks = g0 - t * nks;
-    int ft = t, fks = ks, fslot = 0;
-    for (int p = 0; p < L; ++p) {                              // prologue: the first L stages
-        if (g0 + p < g1) {
-            ensure_meta(ft);
-            fill(fslot, fks);
-            if (++fks == nks) { fks = 0; ++ft; }
-            if (++fslot == STG) fslot = 0;
-        }
-        cp_async_commit();
-    }
-    int issued = 0;                                            // stages whose MMAs were issued
-    int slot = 0;                                              // slot of stage li
-    for (int i = g0; i < g1; ++i) {
-        const int li = i - g0;
-        // refill: stage li + L goes into the slot of stage li - 2, whose MMAs were issued two
-        // iterations ago
-        if (i + L < g1) {
-            const int lf = li + L;
-            if (lf >= STG && !mbar_wait(&mma_done[fslot], unsigned(lf / STG - 1) & 1u)) {
+        const uint16_t *asrc[APASS];
+        int t = g0 / nks, ks = g0 - t * nks, slot = 0, use = 0, cur_t = -1;
+        for (int i = g0; i < g1; ++i) {
+            if (use > 0 && !wait_phase(&empty[slot], unsigned(use - 1) & 1u, fail)) {
                 s_fail = 1;
                 set_status(op.status, DS_DEV_TIMEOUT);
+                break;
             }
-            ensure_meta(ft);
-            fill(fslot, fks);
-            if (++fks == nks) { fks = 0; ++ft; }
-            if (++fslot == STG) fslot = 0;
-        }
-        cp_async_commit();
-        cp_async_wait<L>();                                    // stage li has landed (this thread's part)
-        proxy_fence_async();                                   // make it visible to the tensor cores
-        __syncthreads();
-        if (s_fail) break;                                     // uniform: read after the barrier
-        const bool first = ks == 0 || i == g0;
-        if (tid == 0) {
-            fence_after();
+            if (t != cur_t) {                                  // this thread's rows of tile t
+#pragma unroll
+                for (int j = 0; j < APASS; ++j) {
+                    const int u = t * kRows + prow + RPP * j;
+                    int v = -1, c = -1;
+                    if (u < nU) ep.pick(u, v, c);
+                    asrc[j] = v >= 0 ? op.A + size_t(v) * d + coff : nullptr;
+                }
+                cur_t = t;
+            }
+            const int k0 = ks * C::kCols;
+            const bool kin = k0 + coff < d;
             const uint32_t As = smem0 + uint32_t(slot * C::kStageBytes);
             const uint32_t Bs = As + C::kABytes;
 #pragma unroll
-            for (int at = 0; at < C::kAtoms; ++at) {
+            for (int j = 0; j < APASS; ++j) {
+                const bool ok = kin && asrc[j] != nullptr;
+                cp_async16(As + dst0 + uint32_t(j * RPP * 128), ok ? asrc[j] + k0 : op.A, ok ? 16 : 0);
+            }
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t ad = umma_desc_sw128(As + at * (kRows * 128) + kk * 32);
-                    const uint64_t bd = umma_desc_sw128(Bs + at * (C::N * 128) + kk * 32);
-                    mma(tmem, ad, bd, idesc, (first && at == 0 && kk == 0) ? 0u : 1u);
+            for (int j = 0; j < BPASS; ++j) {
+                if (prow + RPP * j < C::N) {
+                    const bool ok = kin && bsrc[j] != nullptr;
+                    cp_async16(Bs + bdst0 + uint32_t(j * RPP * 128), ok ? bsrc[j] + k0 : op.B, ok ? 16 : 0);
                 }
             }
-            commit(&mma_done[slot]);
+            cp_async_arrive(&full[slot]);
+            if (++slot == STG) { slot = 0; ++use; }
+            if (++ks == nks) { ks = 0; ++t; }
         }
-        ++issued;
-        const int cur_slot = slot;
-        if (++slot == STG) slot = 0;
-        const bool tile_end = ks == nks - 1 || i == g1 - 1;
-        const int tt = t;
-        if (++ks == nks) { ks = 0; ++t; }
-        if (!tile_end) continue;
-        // this CTA's part of tile tt is in the accumulator
-        if (!mbar_wait(&mma_done[cur_slot], unsigned(li / STG) & 1u)) {
-            s_fail = 1;
-            set_status(op.status, DS_DEV_TIMEOUT);
-        }
-        fence_after();
-        const int wq = warp & 3;                               // TMEM lane quarter this warp may read
-        const int row = wq * 32 + lane;                        // A row of the tile
-        const int32_t *mv = s_meta + (tt % C::kMeta) * (2 * kRows);
-        const int v = mv[row], c = mv[kRows + row];
-        const int aux = ep.row_aux(v);
-        const uint32_t taddr = tmem + (uint32_t(wq * 32) << 16);
-        const bool whole = 1LL * tt * nks >= g0 && 1LL * (tt + 1) * nks <= g1;
-        constexpr int kColStep = 16 * (kThreads / 128);        // warps sharing a lane quarter split the columns
-        if (whole) {
-            for (int cb = (warp >> 2) * 16; cb < C::N; cb += kColStep) {
-                uint32_t r16[16];
-                ld16(taddr + uint32_t(cb), r16);
-                float x[16];
+        cp_async_wait<0>();                                    // nothing in flight when the role ends
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issuer: one thread
+        if (lane == 0) {
+            int t = g0 / nks, ks = g0 - t * nks, slot = 0, use = 0, lt = 0;
+            bool ok = true;
+            for (int i = g0; i < g1 && ok; ++i) {
+                const bool first = ks == 0 || i == g0;
+                const int buf = lt & 1;
+                if (first && lt >= 2 && !wait_phase(&acc_empty[buf], unsigned(lt / 2 - 1) & 1u, fail)) { ok = false; break; }
+                if (!wait_phase(&full[slot], unsigned(use) & 1u, fail)) { ok = false; break; }
+                proxy_fence_async();                           // the producers' copies -> tensor core
+                fence_after();
+                const uint32_t As = smem0 + uint32_t(slot * C::kStageBytes);
+                const uint32_t Bs = As + C::kABytes;
+                const uint32_t dacc = tmem + uint32_t(buf * C::N);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(r16[e]);
-                ep.emit(x, cb, v, c, aux, s_ci, s_cl);
-            }
-        } else {
-            // store this part; the last CTA of the tile adds the parts in k (= CTA) order
-            const int mine = 2 * bid + (tt == first_tile(bid) ? 0 : 1);
-            for (int cb = (warp >> 2) * 16; cb < C::N; cb += kColStep) {
-                uint32_t r16[16];
-                ld16(taddr + uint32_t(cb), r16);
-                float4 *dst = reinterpret_cast<float4 *>(parts + (size_t(mine) * kRows + row) * C::N + cb);
+                for (int at = 0; at < C::kAtoms; ++at) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    __stcg(dst + e, make_float4(__uint_as_float(r16[4 * e]), __uint_as_float(r16[4 * e + 1]),
-                                                __uint_as_float(r16[4 * e + 2]), __uint_as_float(r16[4 * e + 3])));
-            }
-            __threadfence();
-            if (tid == 0) {
-                s_first_owner = cta_of(1LL * tt * nks);
-                s_last_owner = cta_of(1LL * (tt + 1) * nks - 1);
-            }
-            __syncthreads();
-            const int cf = s_first_owner, cl = s_last_owner;
-            int nparts = 1;                                    // CTAs that own stages of tile tt
-            for (int cc = cf; cc != cl; cc = next_owner(cc)) ++nparts;
-            if (last_block_done(&tile_cnt[tt], unsigned(nparts))) {
-                for (int cb = (warp >> 2) * 16; cb < C::N; cb += kColStep) {
-                    float x[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) x[e] = 0.f;
-                    for (int cc = cf;; cc = next_owner(cc)) {
-                        const int pslot = 2 * cc + (tt == first_tile(cc) ? 0 : 1);
-                        const float4 *src = reinterpret_cast<const float4 *>(parts + (size_t(pslot) * kRows + row) * C::N + cb);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float4 p = __ldcg(src + e);
-                            x[4 * e] += p.x; x[4 * e + 1] += p.y; x[4 * e + 2] += p.z; x[4 * e + 3] += p.w;
-                        }
-                        if (cc == cl) break;
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = umma_desc_sw128(As + at * (kRows * 128) + kk * 32);
+                        const uint64_t bd = umma_desc_sw128(Bs + at * (C::N * 128) + kk * 32);
+                        mma(dacc, ad, bd, idesc, (first && at == 0 && kk == 0) ? 0u : 1u);
                     }
-                    ep.emit(x, cb, v, c, aux, s_ci, s_cl);
+                }
+                commit(&empty[slot]);                          // frees the slot when these MMAs finish
+                if (ks == nks - 1 || i == g1 - 1) { commit(&acc_full[buf]); ++lt; }
+                if (++slot == STG) { slot = 0; ++use; }
+                if (++ks == nks) { ks = 0; ++t; }
+            }
+            if (!ok) { s_fail = 1; set_status(op.status, DS_DEV_TIMEOUT); }
+            commit(&mma_idle);                                 // completes once every MMA issued has
+            if (!wait_phase(&mma_idle, 0u, fail) && !ok) { /* already failing */ }
+        }
+        __syncwarp();
+    } else if (warp < kEpiWarps) {
+        // ---------------- epilogue: a TMEM lane quarter and every other 16-column group per warp
+        const int wq = warp & 3;
+        const int row = wq * 32 + lane;                        // A row of the tile
+        const uint32_t tq = tmem + (uint32_t(wq * 32) << 16);
+        const int cb0 = (warp >> 2) * 16;
+        int t = g0 / nks, lt = 0;
+        for (;;) {
+            const long long ts = 1LL * t * nks;                // the tile's first unit
+            if (ts >= g1) break;
+            const bool whole = ts >= g0 && ts + nks <= g1;
+            const int buf = lt & 1;
+            int v = -1, c = -1;
+            const int u = t * kRows + row;
+            if (u < nU) ep.pick(u, v, c);
+            const int aux = ep.row_aux(v);
+            if (!wait_phase(&acc_full[buf], unsigned(lt / 2) & 1u, fail)) {
+                s_fail = 1;
+                set_status(op.status, DS_DEV_TIMEOUT);
+                break;
+            }
+            fence_after();
+            const int mine = 2 * bid + (t == first_tile(bid) ? 0 : 1);
+            // 16 columns at a time: emit them (whole tile) or store them as this CTA's part
+#pragma unroll 1
+            for (int cb = cb0; cb < C::N; cb += 32) {
+                uint32_t r16[16];
+                ld16(tq + uint32_t(buf * C::N + cb), r16);
+                float xs[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) xs[e] = __uint_as_float(r16[e]);
+                if (whole) {
+                    ep.emit(est, xs, cb, v, c, aux, s_ci, s_cl);
+                } else {
+                    float4 *dst = reinterpret_cast<float4 *>(parts + (size_t(mine) * kRows + row) * C::N + cb);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        __stcg(dst + e, make_float4(xs[4 * e], xs[4 * e + 1], xs[4 * e + 2], xs[4 * e + 3]));
                 }
             }
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);      // the MMA may reuse this buffer
+            if (!whole) {
+                // the last CTA of the tile adds the parts in k (= CTA) order
+                __threadfence();
+                epi_sync();
+                const int cf = cta_of(ts), cl = cta_of(ts + nks - 1);
+                if (tid == 0) {
+                    int nparts = 1;                            // CTAs that own stages of tile t
+                    for (int cc = cf; cc != cl; cc = next_owner(cc)) ++nparts;
+                    const unsigned prev = atomicAdd(&tile_cnt[t], 1u);
+                    s_last = prev == unsigned(nparts - 1);
+                    if (s_last) { tile_cnt[t] = 0u; __threadfence(); }
+                }
+                epi_sync();
+                if (s_last) {
+#pragma unroll 1
+                    for (int cb = cb0; cb < C::N; cb += 32) {
+                        float xs[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) xs[e] = 0.f;
+                        for (int cc = cf;; cc = next_owner(cc)) {
+                            const int pslot = 2 * cc + (t == first_tile(cc) ? 0 : 1);
+                            const float4 *src = reinterpret_cast<const float4 *>(parts + (size_t(pslot) * kRows + row) * C::N + cb);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 pv = __ldcg(src + e);
+                                xs[4 * e] += pv.x; xs[4 * e + 1] += pv.y; xs[4 * e + 2] += pv.z; xs[4 * e + 3] += pv.w;
+                            }
+                            if (cc == cl) break;
+                        }
+                        ep.emit(est, xs, cb, v, c, aux, s_ci, s_cl);
+                    }
+                }
+                epi_sync();                                    // s_last is read before the next tile
+            }
+            ++lt;
+            ++t;
         }
-        fence_before();
-        __syncthreads();                                       // the accumulator may be overwritten
-        if (s_fail) break;
-    }
-    cp_async_wait<0>();
-    // every issued MMA must be complete before the accumulator is released
-    if (tid == 0) {
-        const long long deadline = clock64() + kWaitBudgetCycles;
-        for (int li = max(0, issued - STG); li < issued; ++li)
-            (void)mbar_wait_until(&mma_done[li % STG], unsigned(li / STG) & 1u, deadline);
     }
     fence_before();
     __syncthreads();
     fence_after();
-    if (warp == 0)
+    if (warp == kMmaWarp)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
                      :: "r"(tmem), "r"(uint32_t(C::kTmemCols)) : "memory");
+    ep.finish(est);
 }
 
 // Host: launch gemm_kernel<MT, Ep> on `grid` CTAs (sets the shared-memory attribute once per

@@ -62,46 +62,16 @@ __device__ __forceinline__ void write_row(const HeadArgs &a, int r, const Stat &
     a.token_idx[r] = s.j;
 }
 
-// Rows are streamed in groups of kGvG 16-byte loads per lane (4 KB of a row per warp at a
-// time).  The loads of the warp's next group -- the second half of the row, or the first half
-// of its next row -- are issued before the current group is multiplied, so every warp keeps
-// 4-8 KB in flight while it computes; 16 warps per SM hold ~100 KB in flight.  The id of the
-// warp's next row is prefetched one row ahead.
+// A warp takes whole rows: the 16 16-byte loads per lane that cover 4096 columns of its row
+// are issued together (8 KB of one row in flight per warp, ~128 KB per SM with 16 warps), then
+// multiplied against h, which sits in shared memory as bf16 (one 16-byte load gives the 8
+// values a W vector meets).  The id of the warp's next row is loaded one row ahead and lane 0
+// computes the row's Gumbel noise while the loads are in flight.  Rows longer than 4096
+// columns take several such rounds.
 //
 // grid (gx, B): block (x, b) handles rows j = x*16 + warp, step gx*16, of list b.
-constexpr int kGvG = 8;                // loads per lane per group (256 bf16 per load round)
-
-__device__ __forceinline__ void load_group(uint4 (&buf)[kGvG], const uint16_t *W, int v, int d, int k0, int lane)
-{
-    const uint4 *row = reinterpret_cast<const uint4 *>(W + size_t(v) * d);
-#pragma unroll
-    for (int u = 0; u < kGvG; ++u) {
-        const int k = k0 + (u * 32 + lane) * 8;
-        buf[u] = k < d ? ld_stream(row + (k >> 3)) : make_uint4(0, 0, 0, 0);
-    }
-}
-
-// h is kept in shared memory as bf16: one 16-byte load gives the 8 values a W vector meets.
-__device__ __forceinline__ void dot_group(const uint4 (&buf)[kGvG], const uint4 *hs, int d, int k0, int lane,
-                                          float &a0, float &a1)
-{
-#pragma unroll
-    for (int u = 0; u < kGvG; ++u) {
-        const int k = k0 + (u * 32 + lane) * 8;
-        if (k < d) {
-            const uint4 x = hs[k >> 3];
-            const uint4 w = buf[u];
-            a0 = fmaf(bf16lo(w.x), bf16lo(x.x), a0);
-            a1 = fmaf(bf16hi(w.x), bf16hi(x.x), a1);
-            a0 = fmaf(bf16lo(w.y), bf16lo(x.y), a0);
-            a1 = fmaf(bf16hi(w.y), bf16hi(x.y), a1);
-            a0 = fmaf(bf16lo(w.z), bf16lo(x.z), a0);
-            a1 = fmaf(bf16hi(w.z), bf16hi(x.z), a1);
-            a0 = fmaf(bf16lo(w.w), bf16lo(x.w), a0);
-            a1 = fmaf(bf16hi(w.w), bf16hi(x.w), a1);
-        }
-    }
-}
+constexpr int kGvU = 16;               // loads per lane per round (4096 bf16)
+constexpr int kGvRound = kGvU * 256;
 
 __global__ void __launch_bounds__(kGvWarps * 32, 1)
 head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__ counters)
@@ -110,64 +80,76 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
     __shared__ Stat warp_stat[kGvWarps];
     const int b = blockIdx.y;
     const int d = a.d;
-    const uint4 *h = reinterpret_cast<const uint4 *>(a.H + size_t(b) * d);
-    for (int k = threadIdx.x; k < d / 8; k += blockDim.x) hs[k] = h[k];
-    __syncthreads();
-
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int base = a.vs_offsets[b];
     const int n = a.vs_offsets[b + 1] - base;
     const int32_t *ids = a.vs_ids + base;
     float *lout = a.logits + base;
     const int stride = gridDim.x * kGvWarps;
-    const int ngroups = (d + kGvG * 256 - 1) / (kGvG * 256);     // groups per row
     Stat st = stat_empty();
 
+    // the first row's first round is requested before h is staged, so the two latencies overlap
+    auto load_round = [&](uint4 (&w)[kGvU], const uint4 *row, int k0) {
+#pragma unroll
+        for (int u = 0; u < kGvU; ++u) {
+            const int k = k0 + (u * 32 + lane) * 8;
+            w[u] = k < d ? ld_stream(row + (k >> 3)) : make_uint4(0, 0, 0, 0);
+        }
+    };
     int j = blockIdx.x * kGvWarps + warp;
+    int v = j < n ? ids[j] : 0;
+    uint4 w[kGvU];
+    bool preloaded = false;
     if (j < n) {
-        auto safe = [&](int v) { return (v >= 0 && v < a.V) ? v : 0; };
-        int v = ids[j];
-        int jn = j + stride;
-        int vn = jn < n ? ids[jn] : 0;                              // next row's id, one row ahead
-        uint4 cur[kGvG], nxt[kGvG];
-        load_group(cur, a.W, safe(v), d, 0, lane);
-        int g = 0;
+        const bool ok = v >= 0 && v < a.V;
+        load_round(w, reinterpret_cast<const uint4 *>(a.W + size_t(ok ? v : 0) * d), 0);
+        preloaded = true;
+    }
+    const uint4 *h = reinterpret_cast<const uint4 *>(a.H + size_t(b) * d);
+    for (int k = threadIdx.x; k < d / 8; k += blockDim.x) hs[k] = h[k];
+    __syncthreads();
+
+    while (j < n) {
+        const int jn = j + stride;
+        const int vn = jn < n ? ids[jn] : 0;      // next row's id, one row ahead
+        const bool ok = v >= 0 && v < a.V;
+        const uint4 *row = reinterpret_cast<const uint4 *>(a.W + size_t(ok ? v : 0) * d);
         float a0 = 0.f, a1 = 0.f;
         float gum = 0.f;
-        if (a.T > 0.f && lane == 0 && v >= 0 && v < a.V) gum = gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(b));
-        for (;;) {
-            // issue the next group's loads before multiplying the current one
-            const bool more_in_row = g + 1 < ngroups;
-            const bool have_next = more_in_row || jn < n;
-            if (more_in_row) load_group(nxt, a.W, safe(v), d, (g + 1) * kGvG * 256, lane);
-            else if (jn < n) load_group(nxt, a.W, safe(vn), d, 0, lane);
-            dot_group(cur, hs, d, g * kGvG * 256, lane, a0, a1);
-            if (!more_in_row) {
-                const float acc = warp_sum(a0 + a1);
-                if (lane == 0) {
-                    if (v < 0 || v >= a.V) {
-                        set_status(a.status, DS_DEV_BAD_INDEX);
-                        lout[j] = 0.f;
-                    } else {
-                        lout[j] = acc;
-                        const float x = acc * a.inv_te;
-                        stat_add(st, x, a.T > 0.f ? x + gum : acc, v, j);
-                    }
-                }
-                a0 = a1 = 0.f;
-                if (jn >= n) break;
-                j = jn; v = vn;
-                jn = j + stride;
-                vn = jn < n ? ids[jn] : 0;
-                g = 0;
-                if (a.T > 0.f && lane == 0 && v >= 0 && v < a.V) gum = gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(b));
-            } else {
-                ++g;
-            }
-            if (!have_next) break;
+        for (int k0 = 0; k0 < d; k0 += kGvRound) {
+            if (!preloaded) load_round(w, row, k0);
+            preloaded = false;
+            if (k0 == 0 && a.T > 0.f && lane == 0 && ok)
+                gum = gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(b));
 #pragma unroll
-            for (int u = 0; u < kGvG; ++u) cur[u] = nxt[u];
+            for (int u = 0; u < kGvU; ++u) {
+                const int k = k0 + (u * 32 + lane) * 8;
+                if (k < d) {
+                    const uint4 x = hs[k >> 3];
+                    a0 = fmaf(bf16lo(w[u].x), bf16lo(x.x), a0);
+                    a1 = fmaf(bf16hi(w[u].x), bf16hi(x.x), a1);
+                    a0 = fmaf(bf16lo(w[u].y), bf16lo(x.y), a0);
+                    a1 = fmaf(bf16hi(w[u].y), bf16hi(x.y), a1);
+                    a0 = fmaf(bf16lo(w[u].z), bf16lo(x.z), a0);
+                    a1 = fmaf(bf16hi(w[u].z), bf16hi(x.z), a1);
+                    a0 = fmaf(bf16lo(w[u].w), bf16lo(x.w), a0);
+                    a1 = fmaf(bf16hi(w[u].w), bf16hi(x.w), a1);
+                }
+            }
         }
+        const float acc = warp_sum(a0 + a1);
+        if (lane == 0) {
+            if (!ok) {
+                set_status(a.status, DS_DEV_BAD_INDEX);
+                lout[j] = 0.f;
+            } else {
+                lout[j] = acc;
+                const float x = acc * a.inv_te;
+                stat_add(st, x, a.T > 0.f ? x + gum : acc, v, j);
+            }
+        }
+        j = jn;
+        v = vn;
     }
     if (lane == 0) warp_stat[warp] = st;
     __syncthreads();

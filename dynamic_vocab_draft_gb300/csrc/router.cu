@@ -437,11 +437,17 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
     unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) +
                                                       align256(size_t(B) * size_t(Hr) * sizeof(float)));
     if (B == 1) {
-        gemv1_kernel<uint16_t><<<kGemv1Blocks, kGemvWarps * 32, 0, stream>>>(W1, Hr, d, H, b1, act, u, 0,
-                                                                            nullptr, nullptr);
+        // the first position's router has the GPU to itself: one warp per weight row
+        auto grid1 = [&](int rows) {
+            if (pos != 1) return kGemv1Blocks;
+            const int g = (rows + kGemvWarps - 1) / kGemvWarps;
+            return g < router_num_sms() ? g : router_num_sms();
+        };
+        gemv1_kernel<uint16_t><<<grid1(Hr), kGemvWarps * 32, 0, stream>>>(W1, Hr, d, H, b1, act, u, 0,
+                                                                         nullptr, nullptr);
         DS_TRY_LAUNCH();
-        gemv1_kernel<float><<<kGemv1Blocks, kGemvWarps * 32, 0, stream>>>(W2, M, Hr, u, b2, -1, scores, k,
-                                                                         cluster_ids, counters);
+        gemv1_kernel<float><<<grid1(M), kGemvWarps * 32, 0, stream>>>(W2, M, Hr, u, b2, -1, scores, k,
+                                                                      cluster_ids, counters);
         DS_TRY_LAUNCH();
         return DS_OK;
     }

@@ -42,17 +42,26 @@ class _Common:
             raise _lib.DynaSpecError(f"device status {s:#x}: {_lib.load().ds_status_string(s).decode()}")
 
     def capture(self):
-        """Record one step into a CUDA graph (the step's inputs are the drafter's buffers)."""
+        """Record one step into a CUDA graph (the step's inputs are the drafter's buffers).  With
+        head timing enabled a second graph, with the timing events, is recorded as well."""
+        events, self.head_events = self.head_events, None
         self.step()                              # warm up: lazy attributes, library state
         torch.cuda.synchronize()
+        self.graph = self._record()
+        self.head_events = events
+        self.graph_timed = self._record() if events else None
+        return self.graph
+
+    def _record(self):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self.step()
-        self.graph = g
         return g
 
-    def replay(self):
-        self.graph.replay()
+    def replay(self, timed=False):
+        """Launch the captured step; timed=True launches the graph that also records the
+        per-head timing events."""
+        (self.graph_timed if timed else self.graph).replay()
 
     def enable_head_timing(self):
         """Time every position's head launch with CUDA events (also inside a captured graph).

@@ -193,7 +193,7 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
     __shared__ int32_t s_ci[C::N];
     __shared__ long long s_cl[C::N];
     __shared__ uint32_t s_tmem;
-    __shared__ int s_fail, s_last;
+    __shared__ int s_fail, s_last, s_stop;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d = op.d, R = op.R;
     const int nU = ep.n_rows();
@@ -342,8 +342,13 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
             if (!wait_phase(&acc_full[buf], unsigned(lt / 2) & 1u, fail)) {
                 s_fail = 1;
                 set_status(op.status, DS_DEV_TIMEOUT);
-                break;
             }
+            // the epilogue warps meet at named barriers, so they stop together: every warp has
+            // waited (or given up) before thread 0 takes one snapshot of the failure flag
+            epi_sync();
+            if (tid == 0) s_stop = *fail;
+            epi_sync();
+            if (s_stop) break;
             fence_after();
             const int mine = 2 * bid + (t == first_tile(bid) ? 0 : 1);
             // 16 columns at a time: emit them (whole tile) or store them as this CTA's part

@@ -380,8 +380,9 @@ def run_ours(args):
     achieved = float(sum(head_bytes) / (hm.mean(axis=0).sum() * 1e-3) / 1e9)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": committed_traffic() if per_row and cfg.name == "llama_b1" else None,
-            "kernel": ("head_gemv_kernel (gathered head, per-row path, software-pipelined 16-byte loads)"
-                       if per_row else "head_union_kernel (gathered head over the union of the lists)"),
+            "kernel": ("head_gemv_kernel (gathered head, per-row path: one warp per W row, 8 KB in flight)"
+                       if per_row else "tc::gemm_kernel<MT, UnionEp> + head_rowstats_kernel (gathered head "
+                       "over the union of the lists on tcgen05, then the row statistics and draws)"),
             "algorithmic_bytes_per_launch": float(np.mean(head_bytes)),
             "avg_launch_us": float(hm.mean() * 1e3), "peak_source": peak_src,
             "shortlist_sizes": sizes.sum(axis=1).tolist(), "union_rows": union}

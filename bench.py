@@ -55,6 +55,23 @@ def dist_env():
         int(os.environ.get("WORLD_SIZE", "1"))
 
 
+def max_over_ranks(ms, device=None):
+    """The slowest rank's time: every replica ran the same number of steps on its own
+    sequences, so the job's time is the maximum (all_reduce MAX; identity for one process)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_step, steps, job_ms):
+    """Units per second over all ranks: each of `world` replicas did units_per_step * steps."""
+    return world * units_per_step * steps / (job_ms * 1e-3)
+
+
 def workload_config(cfg):
     kind = (f"chain drafting, B={cfg.B}, gamma={cfg.gamma}" if cfg.mode == "chain" else
             f"tree drafting, B={cfg.B}, depth {cfg.gamma} x {cfg.width} nodes")
@@ -338,13 +355,9 @@ def run_ours(args):
         h0, hl = d.head_events[0][0], d.head_events[-1][1]
         breakdown.append((s0.elapsed_time(h0), h0.elapsed_time(hl), hl.elapsed_time(s1)))
     step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     d.check_status()
-    value = world * tokens_per_step * K / (total_ms * 1e-3)
+    value = whole_job_rate(world, tokens_per_step, K, total_ms)
 
     # e2e through the public API: pinned host inputs -> device, step, results -> host
     Ke = min(K, args.e2e_steps)
@@ -366,11 +379,8 @@ def run_ours(args):
         e2e_ms += s.elapsed_time(e)
     h2d = sum(h.numel() * h.element_size() for h, _ in host.values())
     d2h = sum(o.numel() * o.element_size() for o in outs_h)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * tokens_per_step * Ke / (e2e_ms * 1e-3)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_value = whole_job_rate(world, tokens_per_step, Ke, e2e_ms)
 
     # roofline of the dominant kernel: the gathered head (algorithmic bytes per launch)
     peak, peak_src = load_peak()

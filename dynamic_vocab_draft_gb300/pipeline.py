@@ -175,7 +175,7 @@ class ChainDrafter(_Common):
 
     def launches_per_step(self) -> int:
         n_router = router_launches(self.B)
-        n_short = 4 if self.union else (2 if self.B == 1 else 3)
+        n_short = 4 if self.union else (1 if self.B == 1 else 3)
         n_head = 2 if self.union else 1
         return self.gamma * (n_router + n_short + n_head) + 2
 

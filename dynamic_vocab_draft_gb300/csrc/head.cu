@@ -302,14 +302,17 @@ head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *_
     const int32_t *ids = a.vs_ids + off;
     Stat st = stat_empty();
     const int j0 = blockIdx.x * kRsChunk + threadIdx.x * kRsPer;
+    // unrolled by four so the independent noise computations of neighbouring elements overlap
+#pragma unroll 4
     for (int e = 0; e < kRsPer; ++e) {
         const int j = j0 + e;
-        if (j >= n) break;
-        const float lj = l[j];
-        const int v = ids[j];
-        const float x = lj * a.inv_te;
-        const float key = a.T > 0.f ? x + gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(r)) : lj;
-        stat_add(st, x, key, v, j);
+        if (j < n) {
+            const float lj = l[j];
+            const int v = ids[j];
+            const float x = lj * a.inv_te;
+            const float key = a.T > 0.f ? x + gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(r)) : lj;
+            stat_add(st, x, key, v, j);
+        }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll

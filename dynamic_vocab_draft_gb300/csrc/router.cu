@@ -369,13 +369,17 @@ int router_num_sms()
     return n;
 }
 
-// CTAs of a router GEMM: the first draft position's router runs before any head and takes the
-// whole GPU; a later position's router runs beside the batched head, which leaves
-// kRouterSideSms SMs free for it, and must fit there.
+// CTAs of a router GEMM: the first draft position's router runs before any head and may use
+// the whole GPU, but a router layer is only a few hundred (tile, k-stage) units, and a tile
+// split between many CTAs pays for storing and adding its parts, so each CTA takes at least
+// 8 units; a later position's router runs beside the batched head, which leaves kRouterSideSms
+// SMs free for it, and must fit there.
 constexpr int kRouterSideSms = 8;
+constexpr int kRouterMinUnits = 8;
 int router_grid(int pos, int units)
 {
-    int g = pos == 1 ? router_num_sms() : kRouterSideSms;
+    int g = pos == 1 ? (units + kRouterMinUnits - 1) / kRouterMinUnits : kRouterSideSms;
+    if (g > router_num_sms()) g = router_num_sms();
     if (g > tc::kMaxGrid) g = tc::kMaxGrid;
     if (g > units) g = units;
     return g < 1 ? 1 : g;

@@ -31,11 +31,14 @@ namespace ds {
 namespace {
 
 constexpr int kVThreads = 256;
-constexpr int kVPer = 8;                         // elements per thread per chunk
-constexpr int kVChunk = kVThreads * kVPer;       // 2048
+// Statistics chunks: 8192 elements (32 per thread, 8 float4 loads in flight) when that still
+// gives the GPU at least two blocks per SM, else 2048 (few rows: more, smaller blocks).
+constexpr int kVPerBig = 32, kVPerSmall = 8;
+constexpr int kVChunkMin = kVThreads * kVPerSmall;   // sizes the workspace
 constexpr int kMaxGamma = 32;
-constexpr int kRPer = 4;                         // residual pass: elements per thread
-constexpr int kRChunk = kVThreads * kRPer;       // 1024
+// Residual chunks: 2048 elements (8 per thread) under the same rule, else 1024.
+constexpr int kRPerBig = 8, kRPerSmall = 4;
+constexpr int kRChunkMin = kVThreads * kRPerSmall;
 
 struct PStat { float m, s, amax; int aid; };   // target-row chunk: max, sum-exp, argmax
 struct QStat { float m, s; };
@@ -82,25 +85,31 @@ __device__ float block_sum(float x, float *scratch)
 // Statistics of one chunk of a row of length n: max and sum-exp of x = value * inv_te, and the
 // argmax of the raw values (ties to the lower index).  Two plain block reductions (the max,
 // then the sum of exp(x - max)); the result is valid in thread 0.
+template <int kVPer>
 __device__ PStat chunk_stats(const float *__restrict__ row, int lo, int n, float inv_te, PStat *scratch)
 {
+    // thread t holds the 4-element groups lo + 1024 k + 4 t, k = 0..7: every round of loads is
+    // one contiguous 4 KB of the row, and all eight rounds are in flight together
     float vals[kVPer];
-    const int base = lo + threadIdx.x * kVPer;
-    if (base + kVPer <= n && (reinterpret_cast<uintptr_t>(row + base) & 15) == 0) {
+    constexpr int kStride = kVThreads * 4;
 #pragma unroll
-        for (int i = 0; i < kVPer; i += 4) {
-            const float4 f = __ldg(reinterpret_cast<const float4 *>(row + base + i));
-            vals[i] = f.x; vals[i + 1] = f.y; vals[i + 2] = f.z; vals[i + 3] = f.w;
+    for (int k = 0; k < kVPer / 4; ++k) {
+        const int g = lo + k * kStride + threadIdx.x * 4;
+        if (g + 4 <= n && (reinterpret_cast<uintptr_t>(row + g) & 15) == 0) {
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(row + g));
+            vals[4 * k] = f.x; vals[4 * k + 1] = f.y; vals[4 * k + 2] = f.z; vals[4 * k + 3] = f.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) vals[4 * k + e] = g + e < n ? __ldg(row + g + e) : -INFINITY;
         }
-    } else {
-#pragma unroll
-        for (int i = 0; i < kVPer; ++i) vals[i] = base + i < n ? __ldg(row + base + i) : -INFINITY;
     }
     float amax = -INFINITY;
     int aid = -1;
 #pragma unroll
-    for (int i = 0; i < kVPer; ++i)
-        if (vals[i] > amax) { amax = vals[i]; aid = base + i; }     // first max = lowest index
+    for (int i = 0; i < kVPer; ++i) {                  // indices rise with i: first max = lowest index
+        const int idx = lo + (i >> 2) * kStride + threadIdx.x * 4 + (i & 3);
+        if (vals[i] > amax) { amax = vals[i]; aid = idx; }
+    }
     // block max / argmax of the raw values (x = value * inv_te is monotone in the value)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
@@ -168,6 +177,7 @@ __device__ __forceinline__ int list_index(const ChainArgs &a, int t, int b, int 
     return p < 0 ? -1 : p + a.rank[v];
 }
 
+template <int kVPer>
 __global__ void __launch_bounds__(kVThreads)
 verify_stats_kernel(ChainArgs a)
 {
@@ -178,10 +188,10 @@ verify_stats_kernel(ChainArgs a)
     const int g1 = a.gamma + 1;
     const int b = blockIdx.y / g1, t = blockIdx.y % g1;
     const int c = blockIdx.x;
-    const int lo = c * kVChunk;
+    const int lo = c * kVThreads * kVPer;
     {
         const float *row = a.p_logits + (size_t(b) * g1 + t) * a.V;
-        const PStat ps = chunk_stats(row, lo, a.V, a.inv_te, scratch);
+        const PStat ps = chunk_stats<kVPer>(row, lo, a.V, a.inv_te, scratch);
         if (threadIdx.x == 0) a.pstat[(size_t(b) * g1 + t) * a.nch + c] = ps;
     }
     if (t < a.gamma && a.T > 0.f && !a.q_max) {
@@ -189,7 +199,7 @@ verify_stats_kernel(ChainArgs a)
         const int n = off[b + 1] - off[b];
         QStat q{-INFINITY, 0.f};
         if (lo < n) {
-            const PStat qs = chunk_stats(a.q_logits + size_t(t) * a.q_stride + off[b], lo, n, a.inv_te, scratch);
+            const PStat qs = chunk_stats<kVPer>(a.q_logits + size_t(t) * a.q_stride + off[b], lo, n, a.inv_te, scratch);
             q = QStat{qs.m, qs.s};
         }
         if (threadIdx.x == 0) a.qstat[(size_t(b) * a.gamma + t) * a.nch + c] = q;
@@ -311,7 +321,7 @@ __device__ ResidualRow residual_row(const ChainArgs &a, int b, int tr)
 // the same way.  Weights without mass fall back to p.  The draw is the smallest v whose
 // cumulative weight exceeds the target; if rounding leaves none, the last v with weight.
 // wf(v, r, p) gives both weights of token v.
-template <class WF>
+template <int kRPer, class WF>
 __device__ void icdf_draw(WF wf, int V, int nrch, float u, float *__restrict__ rsum, float *__restrict__ psum,
                           unsigned *counter, int32_t *out)
 {
@@ -321,6 +331,7 @@ __device__ void icdf_draw(WF wf, int V, int nrch, float u, float *__restrict__ r
     __shared__ int s_chunk, s_use_p, s_hit, s_last;
     __shared__ float s_target;
     const int c = blockIdx.x;
+    constexpr int kRChunk = kVThreads * kRPer;
     const int base = c * kRChunk + threadIdx.x * kRPer;
     float rs = 0.f, ps = 0.f;
 #pragma unroll
@@ -412,6 +423,7 @@ __device__ void icdf_draw(WF wf, int V, int nrch, float u, float *__restrict__ r
     if (threadIdx.x == 0 && s_hit == 0x7FFFFFFF) *out = s_last;   // target beyond the chunk
 }
 
+template <int kRPer>
 __global__ void __launch_bounds__(kVThreads)
 verify_residual_kernel(ChainArgs a)
 {
@@ -420,7 +432,7 @@ verify_residual_kernel(ChainArgs a)
     if (tr < 0) return;                              // greedy: decided already (whole group returns)
     const ResidualRow rr = residual_row(a, b, tr);
     auto wf = [&](int v, float &r, float &p) { residual_weight(a, rr, v, r, p); };
-    icdf_draw(wf, a.V, a.nrch, a.u[size_t(b) * (a.gamma + 1) + a.gamma], a.rsum + size_t(b) * a.nrch,
+    icdf_draw<kRPer>(wf, a.V, a.nrch, a.u[size_t(b) * (a.gamma + 1) + a.gamma], a.rsum + size_t(b) * a.nrch,
               a.psum + size_t(b) * a.nrch, &a.cnt2[b], &a.correction[b]);
 }
 
@@ -732,6 +744,7 @@ tree_walk_kernel(TreeArgs a)
     cl.sync();                                   // no CTA leaves while others may read its slots
 }
 
+template <int kRPer>
 __global__ void __launch_bounds__(kVThreads)
 tree_residual_kernel(TreeArgs a)
 {
@@ -751,7 +764,7 @@ tree_residual_kernel(TreeArgs a)
             if (pc >= 0) { const int j = pc + a.rank[v]; w = unsigned(j) < unsigned(a.V) ? r[j] : 0.f; }
         }
     };
-    icdf_draw(wf, a.V, a.nrch, a.u_res[size_t(b) * (a.D + 1) + ws.dep], a.rsum + size_t(b) * a.nrch,
+    icdf_draw<kRPer>(wf, a.V, a.nrch, a.u_res[size_t(b) * (a.D + 1) + ws.dep], a.rsum + size_t(b) * a.nrch,
               a.psum + size_t(b) * a.nrch, &a.cnt[b], &a.correction[b]);
 }
 
@@ -760,8 +773,25 @@ tree_residual_kernel(TreeArgs a)
 
 using namespace ds;
 
-static int vchunks(int V) { return (V + kVChunk - 1) / kVChunk; }
-static size_t rchunks(int V) { return size_t((V + kRChunk - 1) / kRChunk); }
+static int vchunks(int V) { return (V + kVChunkMin - 1) / kVChunkMin; }     // the most chunks
+static size_t rchunks(int V) { return size_t((V + kRChunkMin - 1) / kRChunkMin); }
+
+static int verify_sms()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+    }
+    return n;
+}
+
+// The larger chunks when rows * chunks still covers every SM twice.
+static bool big_chunks(long long rows, int V, int chunk)
+{
+    return rows * ((V + chunk - 1) / chunk) >= 2LL * verify_sms();
+}
 
 extern "C" size_t ds_verify_workspace_bytes(int B, int gamma, int V)
 {
@@ -796,7 +826,10 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     if (B > 65535 / (gamma + 1)) return DS_ERR_UNSUPPORTED;
     if (!ws || ws_bytes < ds_verify_workspace_bytes(B, gamma, V)) return DS_ERR_WORKSPACE;
     ChainArgs a;
-    a.p_logits = p_logits; a.B = B; a.gamma = gamma; a.V = V; a.nch = vchunks(V);
+    const bool vbig = big_chunks(1LL * B * (gamma + 1), V, kVThreads * kVPerBig);
+    const bool rbig = big_chunks(B, V, kVThreads * kRPerBig);
+    a.p_logits = p_logits; a.B = B; a.gamma = gamma; a.V = V;
+    a.nch = (V + kVThreads * (vbig ? kVPerBig : kVPerSmall) - 1) / (kVThreads * (vbig ? kVPerBig : kVPerSmall));
     a.T = T; a.inv_te = T > 0.f ? 1.f / T : 1.f;
     a.q_logits = q_logits; a.q_stride = q_stride;
     a.q_max = q_max; a.q_sumexp = q_sumexp;
@@ -813,13 +846,15 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     a.prow = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * g1 * sizeof(QStat));
     a.qrow = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * gamma * sizeof(QStat));
     a.decision = reinterpret_cast<int32_t *>(w); w += align256(size_t(B) * sizeof(int32_t));
-    a.nrch = int(rchunks(V));
+    a.nrch = (V + kVThreads * (rbig ? kRPerBig : kRPerSmall) - 1) / (kVThreads * (rbig ? kRPerBig : kRPerSmall));
     a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.psum = reinterpret_cast<float *>(w);
 
-    verify_stats_kernel<<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
+    if (vbig) verify_stats_kernel<kVPerBig><<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
+    else verify_stats_kernel<kVPerSmall><<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
     DS_TRY_LAUNCH();
-    verify_residual_kernel<<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
+    if (rbig) verify_residual_kernel<kRPerBig><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
+    else verify_residual_kernel<kRPerSmall><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
     DS_TRY_LAUNCH();
     return DS_OK;
 }
@@ -866,7 +901,8 @@ extern "C" ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd,
     char *w = static_cast<char *>(ws);
     a.state = reinterpret_cast<WalkState *>(w); w += align256(size_t(B) * sizeof(WalkState));
     a.rbuf = reinterpret_cast<float *>(w); w += align256(size_t(B) * 2 * size_t(V) * sizeof(float));
-    a.nrch = int(rchunks(V));
+    const bool rbig = big_chunks(B, V, kVThreads * kRPerBig);
+    a.nrch = (V + kVThreads * (rbig ? kRPerBig : kRPerSmall) - 1) / (kVThreads * (rbig ? kRPerBig : kRPerSmall));
     a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.psum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.cnt = reinterpret_cast<unsigned *>(w);
@@ -890,7 +926,8 @@ extern "C" ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, tree_walk_kernel, a) != cudaSuccess) { (void)cudaGetLastError(); return DS_ERR_CUDA; }
-    tree_residual_kernel<<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
+    if (rbig) tree_residual_kernel<kRPerBig><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
+    else tree_residual_kernel<kRPerSmall><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
     DS_TRY_LAUNCH();
     return DS_OK;
 }

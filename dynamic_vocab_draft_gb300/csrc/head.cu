@@ -65,9 +65,12 @@ __device__ __forceinline__ void write_row(const HeadArgs &a, int r, const Stat &
 // A warp takes whole rows: the 16 16-byte loads per lane that cover 4096 columns of its row
 // are issued together (8 KB of one row in flight per warp, ~128 KB per SM with 16 warps), then
 // multiplied against h, which sits in shared memory as bf16 (one 16-byte load gives the 8
-// values a W vector meets).  The id of the warp's next row is loaded one row ahead and lane 0
-// computes the row's Gumbel noise while the loads are in flight.  Rows longer than 4096
-// columns take several such rounds.
+// values a W vector meets).  Rows longer than 4096 columns take several such rounds.
+//
+// The warp's rows come in batches of 32: lane l loads the id of the batch's row l and computes
+// its Gumbel noise up front (all lanes at once), the rows then stream with their ids already in
+// registers, lane l keeps row l's logit, and after the batch every lane folds its own row into
+// its softmax/draw state -- no lane works alone per row.
 //
 // grid (gx, B): block (x, b) handles rows j = x*16 + warp, step gx*16, of list b.
 constexpr int kGvU = 16;               // loads per lane per round (4096 bf16)
@@ -88,7 +91,6 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
     const int stride = gridDim.x * kGvWarps;
     Stat st = stat_empty();
 
-    // the first row's first round is requested before h is staged, so the two latencies overlap
     auto load_round = [&](uint4 (&w)[kGvU], const uint4 *row, int k0) {
 #pragma unroll
         for (int u = 0; u < kGvU; ++u) {
@@ -96,11 +98,13 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
             w[u] = k < d ? ld_stream(row + (k >> 3)) : make_uint4(0, 0, 0, 0);
         }
     };
-    int j = blockIdx.x * kGvWarps + warp;
-    int v = j < n ? ids[j] : 0;
+    const int j0 = blockIdx.x * kGvWarps + warp;  // the warp's rows: j0 + i * stride
+    // the first batch's ids, and the first row's first round, are requested before h is staged
+    int my_v = j0 + lane * stride < n ? ids[j0 + lane * stride] : -1;
     uint4 w[kGvU];
     bool preloaded = false;
-    if (j < n) {
+    if (j0 < n) {
+        const int v = __shfl_sync(0xFFFFFFFFu, my_v, 0);
         const bool ok = v >= 0 && v < a.V;
         load_round(w, reinterpret_cast<const uint4 *>(a.W + size_t(ok ? v : 0) * d), 0);
         preloaded = true;
@@ -109,53 +113,67 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
     for (int k = threadIdx.x; k < d / 8; k += blockDim.x) hs[k] = h[k];
     __syncthreads();
 
-    while (j < n) {
-        const int jn = j + stride;
-        const int vn = jn < n ? ids[jn] : 0;      // next row's id, one row ahead
-        const bool ok = v >= 0 && v < a.V;
-        const uint4 *row = reinterpret_cast<const uint4 *>(a.W + size_t(ok ? v : 0) * d);
-        float a0 = 0.f, a1 = 0.f;
-        float gum = 0.f;
-        for (int k0 = 0; k0 < d; k0 += kGvRound) {
-            if (!preloaded) load_round(w, row, k0);
-            preloaded = false;
-            if (k0 == 0 && a.T > 0.f && lane == 0 && ok)
-                gum = gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(b));
+    for (int jb = j0; jb < n; jb += 32 * stride) {
+        // this batch: lane l owns row jb + l * stride
+        const int my_j = jb + lane * stride;
+        const bool my_ok = my_j < n && my_v >= 0 && my_v < a.V;
+        float my_gum = 0.f, my_acc = 0.f;
+        if (a.T > 0.f && my_ok) my_gum = gumbel(a.seed, uint32_t(my_v), uint32_t(a.pos), uint32_t(b));
+        const int nrows = min(32, (n - jb + stride - 1) / stride);
+        // ids of the next batch, one batch ahead
+        const int nj = my_j + 32 * stride;
+        const int next_v = nj < n ? ids[nj] : -1;
+        for (int k = 0; k < nrows; ++k) {
+            const int v = __shfl_sync(0xFFFFFFFFu, my_v, k);
+            const bool ok = v >= 0 && v < a.V;
+            const uint4 *row = reinterpret_cast<const uint4 *>(a.W + size_t(ok ? v : 0) * d);
+            float a0 = 0.f, a1 = 0.f;
+            for (int k0 = 0; k0 < d; k0 += kGvRound) {
+                if (!preloaded) load_round(w, row, k0);
+                preloaded = false;
 #pragma unroll
-            for (int u = 0; u < kGvU; ++u) {
-                const int k = k0 + (u * 32 + lane) * 8;
-                if (k < d) {
-                    const uint4 x = hs[k >> 3];
-                    a0 = fmaf(bf16lo(w[u].x), bf16lo(x.x), a0);
-                    a1 = fmaf(bf16hi(w[u].x), bf16hi(x.x), a1);
-                    a0 = fmaf(bf16lo(w[u].y), bf16lo(x.y), a0);
-                    a1 = fmaf(bf16hi(w[u].y), bf16hi(x.y), a1);
-                    a0 = fmaf(bf16lo(w[u].z), bf16lo(x.z), a0);
-                    a1 = fmaf(bf16hi(w[u].z), bf16hi(x.z), a1);
-                    a0 = fmaf(bf16lo(w[u].w), bf16lo(x.w), a0);
-                    a1 = fmaf(bf16hi(w[u].w), bf16hi(x.w), a1);
+                for (int u = 0; u < kGvU; ++u) {
+                    const int kk = k0 + (u * 32 + lane) * 8;
+                    if (kk < d) {
+                        const uint4 x = hs[kk >> 3];
+                        a0 = fmaf(bf16lo(w[u].x), bf16lo(x.x), a0);
+                        a1 = fmaf(bf16hi(w[u].x), bf16hi(x.x), a1);
+                        a0 = fmaf(bf16lo(w[u].y), bf16lo(x.y), a0);
+                        a1 = fmaf(bf16hi(w[u].y), bf16hi(x.y), a1);
+                        a0 = fmaf(bf16lo(w[u].z), bf16lo(x.z), a0);
+                        a1 = fmaf(bf16hi(w[u].z), bf16hi(x.z), a1);
+                        a0 = fmaf(bf16lo(w[u].w), bf16lo(x.w), a0);
+                        a1 = fmaf(bf16hi(w[u].w), bf16hi(x.w), a1);
+                    }
                 }
             }
+            const float acc = warp_sum(a0 + a1);
+            if (lane == k) my_acc = acc;
         }
-        const float acc = warp_sum(a0 + a1);
-        if (lane == 0) {
-            if (!ok) {
+        // every lane folds its own row of the batch
+        if (my_j < n) {
+            if (!my_ok) {
                 set_status(a.status, DS_DEV_BAD_INDEX);
-                lout[j] = 0.f;
+                lout[my_j] = 0.f;
             } else {
-                lout[j] = acc;
-                const float x = acc * a.inv_te;
-                stat_add(st, x, a.T > 0.f ? x + gum : acc, v, j);
+                lout[my_j] = my_acc;
+                const float x = my_acc * a.inv_te;
+                stat_add(st, x, a.T > 0.f ? x + my_gum : my_acc, my_v, my_j);
             }
         }
-        j = jn;
-        v = vn;
+        my_v = next_v;
+    }
+    // the warp's lanes, then the block's warps, then the blocks: fixed orders throughout
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const Stat other = shfl_xor_stat(st, o);
+        st = (lane & o) ? stat_merge(other, st) : stat_merge(st, other);
     }
     if (lane == 0) warp_stat[warp] = st;
     __syncthreads();
     if (threadIdx.x == 0) {
         Stat c = warp_stat[0];
-        for (int w = 1; w < kGvWarps; ++w) c = stat_merge(c, warp_stat[w]);
+        for (int w2 = 1; w2 < kGvWarps; ++w2) c = stat_merge(c, warp_stat[w2]);
         st_stat(&partials[size_t(b) * kGvMaxBlocks + blockIdx.x], c);
     }
     if (!last_block_done(&counters[b], gridDim.x)) return;

@@ -95,8 +95,8 @@ def oracle_sample(inp, budget_s, max_steps, warmup):
     gamma = cfg.gamma
     ref = oracle.chain_step(inp, seqs=[0])       # warm (and needed for the verify sample)
     pos = ref[0]["positions"]
-    for _ in range(max(0, min(warmup, 1))):
-        oracle.chain_step(inp, seqs=[0], positions=[0], verify=False)
+    for i in range(max(0, warmup)):
+        oracle.chain_step(inp, seqs=[0], positions=[i % gamma], verify=False)
     t0 = time.perf_counter()
     n = 0
     while n < max_steps and (time.perf_counter() - t0) < budget_s:
@@ -119,12 +119,16 @@ def run_reference(args):
     cfg = wl.config(args.config)
     if cfg.mode == "chain":
         inp = wl.chain_inputs(cfg, args.seed)
-        value, n, dt = oracle_sample(inp, budget_s=90.0, max_steps=args.steps, warmup=args.warmup)
+        warm = args.warmup
+        value, n, dt = oracle_sample(inp, budget_s=90.0, max_steps=args.steps, warmup=warm)
         sample = (f"{n} oracle draft positions of sequence 0 (router + top-k + shortlist + head + sample; "
                   f"verification of the whole chain after every {cfg.gamma}th), {dt:.1f} s")
         ms_per_step = 1e3 * dt / max(n, 1) * cfg.gamma * cfg.B
     else:
         inp = wl.tree_inputs(cfg, args.seed)
+        warm = min(args.warmup, 2)                 # a whole tree step of the oracle takes seconds
+        for _ in range(warm):
+            oracle.tree_step(inp, seqs=[0])
         t0 = time.perf_counter()
         n = 0
         while n < max(1, min(args.steps, 3)) and time.perf_counter() - t0 < 90.0:
@@ -139,7 +143,7 @@ def run_reference(args):
     cfgd["seed"] = args.seed
     cfgd["l2"] = "n/a (host)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": n, "warmup": min(args.warmup, 1), "ms_per_step": ms_per_step,
+            "steps": n, "warmup": warm, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": cfgd,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},

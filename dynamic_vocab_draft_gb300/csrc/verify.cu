@@ -616,6 +616,8 @@ tree_walk_kernel(TreeArgs a)
     __shared__ ClusterRed s_cr;
     __shared__ int s_kids[64];
     __shared__ int s_nkids, s_accept;
+    __shared__ int s_cj[64];                     // per child: list index of its token (-1: none)
+    __shared__ float s_cu[64], s_cq[64], s_cqm[64], s_cqs[64];   // its uniform, q(x), q's max / sum-exp
     cg::cluster_group cl = cg::this_cluster();
     const int CL = int(cl.num_blocks()), crank = int(cl.block_rank());
     const int b = blockIdx.x / CL;
@@ -684,17 +686,42 @@ tree_walk_kernel(TreeArgs a)
             on += pj;
         }
         __threadfence();                         // r is read across the cluster after the barrier
+        // every child's test inputs at once (one thread per child): the index j of its token
+        // in the list, the uniform, and -- when the head's row statistics are given -- q(x)
+        // and the statistics the rejection pass needs
+        if (tid < nk) {
+            const int n = s_kids[tid];
+            const int i = n - dep * a.Wd, hr = b * a.Wd + i;
+            const int x = a.node_tokens[size_t(dep) * a.B * a.Wd + hr];
+            int j = -1;
+            if (x >= 0 && x < a.V) {
+                const int c = a.cluster_of[x];
+                const int pc = unsigned(c) < unsigned(a.M) ? s_cpos[c] : -1;
+                if (pc >= 0) j = pc + a.rank[x];
+            }
+            if (j >= nb) j = -1;
+            s_cj[tid] = j;
+            s_cu[tid] = a.u_node[size_t(b) * a.N + n];
+            if (a.q_max) {
+                const float qm = a.q_max[size_t(dep) * a.B * a.Wd + hr];
+                const float qs = a.q_sumexp[size_t(dep) * a.B * a.Wd + hr];
+                const float *ql = a.q_logits + size_t(dep) * a.q_stride + int64_t(lo) * a.Wd + int64_t(i) * nb;
+                s_cqm[tid] = qm;
+                s_cqs[tid] = qs;
+                s_cq[tid] = j >= 0 ? __expf(ql[j] * a.inv_te - qm) / qs : 0.f;
+            }
+        }
         const float O = row.o / row.s;
-        float R = O + cluster_sum(on, fscr, s_cr, nred);
+        float R = O + cluster_sum(on, fscr, s_cr, nred);   // (its barriers also publish s_c*)
         int next = -1;
         for (int k = 0; k < nk; ++k) {
             const int n = s_kids[k];
-            const int i = n - dep * a.Wd, hr = b * a.Wd + i;
+            const int i = n - dep * a.Wd;
             const float *ql = a.q_logits + size_t(dep) * a.q_stride + int64_t(lo) * a.Wd + int64_t(i) * nb;
             float qm, qs;
             if (a.q_max) {
-                qm = a.q_max[size_t(dep) * a.B * a.Wd + hr];
-                qs = a.q_sumexp[size_t(dep) * a.B * a.Wd + hr];
+                qm = s_cqm[k];
+                qs = s_cqs[k];
             } else {
                 RowStat q = rowstat_empty();
                 for (int j = gt; j < nb; j += GT) rowstat_add(q, ql[j], ql[j] * a.inv_te, false, j);
@@ -702,16 +729,14 @@ tree_walk_kernel(TreeArgs a)
                 qm = q.m; qs = q.s;
             }
             if (tid == 0) {                      // every CTA takes the same test on the same data
-                const int x = a.node_tokens[size_t(dep) * a.B * a.Wd + hr];
-                int j = -1;
-                if (x >= 0 && x < a.V) {
-                    const int c = a.cluster_of[x];
-                    const int pc = unsigned(c) < unsigned(a.M) ? s_cpos[c] : -1;
-                    if (pc >= 0) j = pc + a.rank[x];
-                }
+                const int j = s_cj[k];
                 int acc = 0;
-                if (j < 0 || j >= nb) set_status(a.status, DS_DEV_BAD_INDEX);
-                else acc = a.u_node[size_t(b) * a.N + n] * (__expf(ql[j] * a.inv_te - qm) / qs) < __ldcg(&r[j]) / R;
+                if (j < 0) {
+                    set_status(a.status, DS_DEV_BAD_INDEX);
+                } else {
+                    const float q = a.q_max ? s_cq[k] : __expf(ql[j] * a.inv_te - qm) / qs;
+                    acc = s_cu[k] * q < __ldcg(&r[j]) / R;
+                }
                 s_accept = acc;
             }
             __syncthreads();

@@ -281,6 +281,64 @@ def test_head_union_path(ds, name, B, G, T):
         _check_head(inp, Hrows, G, ids, T, pos, out)
 
 
+@pytest.mark.parametrize("union", [False, True])
+def test_head_empty_lists(ds, union):
+    # An empty list gives token = token_idx = -1 and touches no logit; the other lists of the
+    # same call are unaffected.  Batch 1 with an empty list; two lists with the first empty;
+    # and (union path) an empty union.
+    inp = gu.chain_inputs("tiny")
+    cfg = inp["cfg"]
+    V, M, d = cfg.V, cfg.M, cfg.d
+    cof = torch.empty(V, dtype=torch.int32, device=gu.dev())
+    rk = torch.empty(V, dtype=torch.int32, device=gu.dev())
+    ds.vocab_index(gu.i32(inp["csr_off"]), gu.i32(inp["csr_tok"]), cof, rk, gu.status())
+    S1 = oracle.shortlist(inp["csr_off"], inp["csr_tok"], np.array([3, 7], np.int32))
+    sizes = np.diff(inp["csr_off"])
+    cases = [(1, [np.zeros(0, np.int32)], [[]])]
+    if union:
+        cases += [(2, [np.zeros(0, np.int32), S1], [[], [3, 7]]), (2, [np.zeros(0, np.int32)] * 2, [[], []])]
+    else:
+        cases += [(2, [np.zeros(0, np.int32), S1], [[], [3, 7]])]
+    rng = np.random.default_rng(11)
+    for B, lists, clus in cases:
+        offs = np.concatenate([[0], np.cumsum([len(x) for x in lists])]).astype(np.int32)
+        ids = np.concatenate(lists + [np.zeros(1, np.int32)]).astype(np.int32)
+        cpos = np.full((B, M), -1, np.int32)
+        for b, cl in enumerate(clus):
+            run = 0
+            for c in cl:
+                cpos[b, c] = run
+                run += sizes[c]
+        H = wl.to_bf16_bits(rng.standard_normal((B, d)).astype(np.float32))
+        cap = max(int(offs[-1]), 1)
+        logits = torch.full((cap,), float("nan"), dtype=torch.float32, device=gu.dev())
+        tok = torch.full((B,), 7, dtype=torch.int32, device=gu.dev())
+        tix = torch.full((B,), 7, dtype=torch.int32, device=gu.dev())
+        st = gu.status()
+        ws = ds.workspace(ds.head_workspace_bytes(B), gu.dev())
+        un = None
+        if union:
+            uids = np.concatenate([S1] if any(len(x) for x in lists) else [np.zeros(0, np.int32)]).astype(np.int32)
+            ucl = np.concatenate([[c] * sizes[c] for c in (3, 7)]).astype(np.int32) if len(uids) else np.zeros(0, np.int32)
+            un = (gu.i32(np.concatenate([uids, [0]])), gu.i32(np.concatenate([ucl, [0]])),
+                  gu.i32(np.array([len(uids)], np.int32)))
+        ds.gathered_head(gu.bf16(H), 1, gu.device_head(inp), gu.i32(offs), gu.i32(ids), 1.0, inp["gumbel_seed"], 1,
+                         logits, tok, tix, ws, st, cpos=gu.i32(cpos.ravel()), rank_in_cluster=rk, union=un)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        t, j = tok.cpu().numpy(), tix.cpu().numpy()
+        for b in range(B):
+            if len(lists[b]) == 0:
+                assert t[b] == -1 and j[b] == -1, (B, b, t, j)
+            else:
+                l_ref = oracle.head(H[b:b + 1], inp["W"], lists[b])[0]
+                lg = logits.cpu().numpy()[offs[b]:offs[b + 1]]
+                assert_close(lg, l_ref, "head logits next to an empty list")
+                rtok, ridx, _, _ = oracle.draft_sample(l_ref, lists[b], 1.0, inp["gumbel_seed"], 1, b)
+                if token_same_or_excused(int(j[b]), ridx, l_ref, lists[b], 1.0, inp["gumbel_seed"], 1, b):
+                    assert t[b] == rtok
+
+
 @pytest.mark.parametrize("G", [1, 10])
 def test_head_union_full_size_sampled(ds, G):
     # Llama-3-8B shape, 32 lists (G=1, batched chain) or 8 lists x 10 nodes (tree): every

@@ -70,15 +70,43 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
     return c;
 }
 
-// Gumbel noise g = -log(-log u) of full-vocabulary token v for draft position `pos`, head
-// row `row`: counter (v >> 2, pos, row, 0), word v & 3, u = (2 (w >> 9) + 1) 2^-24 in (0, 1).
+// -log(u) for u in (0, 1) on the hardware base-2 logarithm, kept accurate near u = 1, where the
+// result is small: there t = 1 - u is exact and -log(1 - t) = t + t^2/2 + t^3/3 + ... is summed
+// to t^7/7 (t < 1/16: truncation below 1e-9 relative).  Elsewhere the base-2 logarithm's
+// relative error (about 2^-22) carries over to the result.
+__device__ __forceinline__ float neg_log_unit(float u)
+{
+    const float t = 1.f - u;
+    if (t < 0.0625f) {
+        float p = 1.f / 7.f;
+        p = fmaf(p, t, 1.f / 6.f);
+        p = fmaf(p, t, 1.f / 5.f);
+        p = fmaf(p, t, 1.f / 4.f);
+        p = fmaf(p, t, 1.f / 3.f);
+        p = fmaf(p, t, 1.f / 2.f);
+        p = fmaf(p, t, 1.f);
+        return p * t;
+    }
+    return -0.69314718055994531f * __log2f(u);
+}
+
+// Gumbel noise g = -log(-log u) of a 32-bit word w: u = (2 (w >> 9) + 1) 2^-24 in (0, 1).  The
+// inner logarithm is neg_log_unit; the outer one's argument E = -log u lies in [6e-8, 17.4],
+// where the base-2 logarithm's absolute error (about 2^-22 ln 2) is far below the noise scale.
+__device__ __forceinline__ float gumbel_from_word(uint32_t x)
+{
+    const float u = float(2u * (x >> 9) + 1u) * 5.9604644775390625e-8f;   // * 2^-24, exact
+    return -0.69314718055994531f * __log2f(neg_log_unit(u));
+}
+
+// Gumbel noise of full-vocabulary token v for draft position `pos`, head row `row`: counter
+// (v >> 2, pos, row, 0), word v & 3.
 __device__ __forceinline__ float gumbel(uint64_t seed, uint32_t v, uint32_t pos, uint32_t row)
 {
     const uint4 w = philox4x32_10(make_uint4(v >> 2, pos, row, 0u), uint32_t(seed),
                                   uint32_t(seed >> 32));
     const uint32_t x = (v & 3u) == 0 ? w.x : (v & 3u) == 1 ? w.y : (v & 3u) == 2 ? w.z : w.w;
-    const float u = float(2u * (x >> 9) + 1u) * 5.9604644775390625e-8f;   // * 2^-24, exact
-    return -logf(-logf(u));
+    return gumbel_from_word(x);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -237,72 +237,6 @@ struct UnionEp {
     }
 };
 
-// Batch-1 list path: the same tensor-core GEMM over the one list (the list is its own union),
-// with the softmax statistics and the draft draw fused into the epilogue.  The tag of a row is
-// its index j in the list; the 128 threads that hold accumulator column 0 (head row 0) write
-// l_j and fold (l_j / Te, key_j) into a per-thread state; at the end the CTA folds its threads
-// and the last CTA folds the CTAs, both in a fixed order.
-// Off: at the list sizes of batch-1 drafting (tens of thousands of rows, one or two tiles per
-// SM) the per-row GEMV below is faster; the tensor-core path pays for its start-up and for the
-// tiles split between CTAs.
-constexpr bool kListOnTensorCores = false;
-
-struct ListEp {
-    HeadArgs h;
-    Stat *partials;
-    unsigned *counters;
-    struct State { Stat st{-INFINITY, 0.f, -INFINITY, -1, -1}; };
-
-    __device__ int n_rows() const { return max(h.vs_offsets[1] - h.vs_offsets[0], 0); }
-    __device__ void pick(int u, int &v, int &c) const
-    {
-        v = h.vs_ids[h.vs_offsets[0] + u];
-        if (v < 0 || v >= h.V) { set_status(h.status, DS_DEV_BAD_INDEX); v = -1; }
-        c = u;
-    }
-    __device__ void col_info(int r, int &i, long long &l) const { i = r; l = 0; }
-    __device__ int row_aux(int) const { return 0; }
-    __device__ void emit(State &es, const float (&x)[16], int cb, int v, int j, int,
-                         const int32_t *, const long long *) const
-    {
-        if (cb != 0 || j < 0) return;
-        float *lout = h.logits + h.vs_offsets[0];
-        if (v < 0) { lout[j] = 0.f; return; }
-        lout[j] = x[0];
-        const float xs = x[0] * h.inv_te;
-        const float key = h.T > 0.f ? xs + gumbel(h.seed, uint32_t(v), uint32_t(h.pos), 0u) : x[0];
-        stat_add(es.st, xs, key, v, j);
-    }
-    __device__ void finish(State &es) const
-    {
-        __shared__ Stat ws[tc::kThreads / 32];
-        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        Stat st = es.st;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const Stat other = shfl_xor_stat(st, o);
-            st = (lane & o) ? stat_merge(other, st) : stat_merge(st, other);
-        }
-        if (lane == 0) ws[warp] = st;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            Stat c = ws[0];
-            for (int w = 1; w < tc::kThreads / 32; ++w) c = stat_merge(c, ws[w]);
-            st_stat(&partials[blockIdx.x], c);
-        }
-        if (!last_block_done(&counters[0], gridDim.x)) return;
-        if (warp != 0) return;
-        Stat c = stat_empty();
-        for (int i = lane; i < int(gridDim.x); i += 32) c = stat_merge(c, ld_stat(&partials[i]));
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const Stat other = shfl_xor_stat(c, o);
-            c = (lane & o) ? stat_merge(other, c) : stat_merge(c, other);
-        }
-        if (lane == 0) write_row(h, 0, c);
-    }
-};
-
 // Softmax statistics and the draft draw of every head row from its stored logits.
 // grid (chunks, R): block (x, r) folds elements [x*kRsChunk, ...) of row r; the last block of the
 // row combines the partials in a fixed order.
@@ -430,19 +364,6 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
     a.token = token; a.token_idx = token_idx;
     a.status = dev_status;
 
-    // A tensor-core head CTA fills its SM (shared memory and registers); kHeadSideSms SMs are
-    // left free so the next position's router and shortlist build run beside it.
-    int tc_grid = num_sms() - kHeadSideSms;
-    if (tc_grid > tc::kMaxGrid) tc_grid = tc::kMaxGrid;
-    if (tc_grid < 1) tc_grid = 1;
-    if (kListOnTensorCores && nu == 0 && B == 1 && G == 1 && (V + tc::kRows - 1) / tc::kRows <= kUnionMaxTiles) {
-        // batch 1: the tensor-core GEMM over the list, statistics and draw in its epilogue
-        ListEp ep;
-        ep.h = a; ep.partials = partials; ep.counters = counters;
-        const tc::Operands op{W, H, d, 1, dev_status};
-        return tc::launch<1>(op, ep, reinterpret_cast<float *>(wsb + lay.parts),
-                             reinterpret_cast<unsigned *>(wsb + lay.tile_cnt), tc_grid, stream);
-    }
     if (nu == 0) {
         if (G != 1) return DS_ERR_UNSUPPORTED;
         // One 512-thread block per SM.  At batch 1 a few SMs are left to the side stream, so the
@@ -473,6 +394,11 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
     ep.ids = union_ids; ep.cluster = union_cluster; ep.count = union_count;
     ep.rank = rank_in_cluster; ep.cpos = cpos; ep.vs_offsets = vs_offsets;
     ep.logits = logits; ep.V = V; ep.M = M; ep.G = G; ep.status = dev_status;
+    // A tensor-core head CTA fills its SM (shared memory and registers); kHeadSideSms SMs are
+    // left free so the next position's router and shortlist build run beside it.
+    int tc_grid = num_sms() - kHeadSideSms;
+    if (tc_grid > tc::kMaxGrid) tc_grid = tc::kMaxGrid;
+    if (tc_grid < 1) tc_grid = 1;
     const tc::Operands op{W, H, d, int(rows), dev_status};
     const ds_status st = tc::launch_for(op, ep, parts, tile_cnt, tc_grid, stream);
     if (st != DS_OK) return st;

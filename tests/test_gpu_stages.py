@@ -607,3 +607,73 @@ def test_verify_tree_full_size(ds, T):
             assert acc_ref.sum() >= B
         if mode == "partial":
             assert (acc_ref >= 1).all() and (acc_ref < D).all()
+
+
+# ---------------------------------------------------------------------------------------
+# Device-side errors: an id the kernels cannot use sets DS_DEV_BAD_INDEX (0x10) in the status
+# word; nothing faults and the other rows of the call are still computed.
+# ---------------------------------------------------------------------------------------
+BAD_INDEX = 0x10
+
+
+@pytest.mark.parametrize("union", [False, True])
+def test_head_bad_token_id_sets_status(ds, union):
+    inp = gu.chain_inputs("tiny")
+    cfg = inp["cfg"]
+    V, M, d = cfg.V, cfg.M, cfg.d
+    cof = torch.empty(V, dtype=torch.int32, device=gu.dev())
+    rk = torch.empty(V, dtype=torch.int32, device=gu.dev())
+    ds.vocab_index(gu.i32(inp["csr_off"]), gu.i32(inp["csr_tok"]), cof, rk, gu.status())
+    ids = np.array([[3, 7]], np.int32)
+    S = oracle.shortlist(inp["csr_off"], inp["csr_tok"], ids[0]).copy()
+    S[5] = V + 17                                       # not a token id
+    cpos = _host_cpos(inp, ids)
+    H = wl.to_bf16_bits(np.random.default_rng(2).standard_normal((1, d)).astype(np.float32))
+    logits = torch.full((S.size,), float("nan"), dtype=torch.float32, device=gu.dev())
+    tok = torch.empty(1, dtype=torch.int32, device=gu.dev())
+    tix = torch.empty(1, dtype=torch.int32, device=gu.dev())
+    st = gu.status()
+    ws = ds.workspace(ds.head_workspace_bytes(1), gu.dev())
+    un = None
+    if union:
+        sizes = np.diff(inp["csr_off"])
+        ucl = np.concatenate([[c] * sizes[c] for c in ids[0]]).astype(np.int32)
+        un = (gu.i32(S), gu.i32(ucl), gu.i32(np.array([S.size], np.int32)))
+    ds.gathered_head(gu.bf16(H), 1, gu.device_head(inp), gu.i32(np.array([0, S.size], np.int32)), gu.i32(S),
+                     1.0, inp["gumbel_seed"], 1, logits, tok, tix, ws, st, cpos=gu.i32(cpos.ravel()),
+                     rank_in_cluster=rk, union=un)
+    torch.cuda.synchronize()
+    assert st.item() & BAD_INDEX
+    good = np.delete(np.arange(S.size), 5)
+    l_ref = oracle.head(H, inp["W"], S[good])[0]
+    assert_close(logits.cpu().numpy()[good], l_ref, "head logits beside a bad id")
+
+
+def test_verify_draft_token_outside_its_list_sets_status(ds):
+    inp = gu.chain_inputs("tiny")
+    cfg = inp["cfg"]
+    rows = _chain_oracle(inp, 1, 1.0)
+    V, M, gamma = cfg.V, cfg.M, cfg.gamma
+    q = np.zeros((gamma, V), np.float32)
+    offs = np.zeros((gamma, 2), np.int32)
+    cpos = np.zeros((gamma, M), np.int32)
+    draft = np.zeros((gamma, 1), np.int32)
+    for t in range(gamma):
+        l = rows[0][t]["logits"]
+        q[t, :l.size] = l
+        offs[t] = [0, l.size]
+        cpos[t] = _host_cpos(inp, rows[0][t]["ids"][None]).ravel()
+        draft[t, 0] = rows[0][t]["token"]
+    # a token whose cluster the first position's list does not select
+    outside = np.setdiff1d(np.arange(V), rows[0][0]["S"])[0]
+    draft[0, 0] = outside
+    cof, rk = _vocab_index_dev(ds, inp)
+    acc = torch.empty(1, dtype=torch.int32, device=gu.dev())
+    corr = torch.empty(1, dtype=torch.int32, device=gu.dev())
+    st = gu.status()
+    ws = ds.workspace(ds.verify_workspace_bytes(1, gamma, V), gu.dev())
+    ds.verify(gu.f32(inp["z"][:1]), 1.0, gu.f32(q), gu.i32(offs), gu.i32(cpos), cof, rk, gu.i32(draft),
+              gu.f32(inp["u"][:1]), acc, corr, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() & BAD_INDEX
+    assert acc.item() == 0                              # the bad draft is rejected

@@ -75,6 +75,7 @@ __device__ __forceinline__ void write_row(const HeadArgs &a, int r, const Stat &
 // grid (gx, B): block (x, b) handles rows j = x*16 + warp, step gx*16, of list b.
 constexpr int kGvU = 16;               // loads per lane per round (4096 bf16)
 constexpr int kGvRound = kGvU * 256;
+constexpr int kGvFold = 8;             // block partials a lane of the last block loads at once
 
 __global__ void __launch_bounds__(kGvWarps * 32, 1)
 head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__ counters)
@@ -171,16 +172,30 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
     }
     if (lane == 0) warp_stat[warp] = st;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        Stat c = warp_stat[0];
-        for (int w2 = 1; w2 < kGvWarps; ++w2) c = stat_merge(c, warp_stat[w2]);
-        st_stat(&partials[size_t(b) * kGvMaxBlocks + blockIdx.x], c);
+    if (warp == 0) {
+        // the block's warps: a fixed tree over lanes 0..15
+        Stat c = lane < kGvWarps ? warp_stat[lane] : stat_empty();
+#pragma unroll
+        for (int o = 1; o < kGvWarps; o <<= 1) {
+            const Stat other = shfl_xor_stat(c, o);
+            c = (lane & o) ? stat_merge(other, c) : stat_merge(c, other);
+        }
+        if (lane == 0) st_stat(&partials[size_t(b) * kGvMaxBlocks + blockIdx.x], c);
     }
     if (!last_block_done(&counters[b], gridDim.x)) return;
     if (warp != 0) return;
-    // Final combine in a fixed order: lane l folds partials l, l+32, ...; then a fixed tree.
+    // Final combine in a fixed order: lane l folds partials l, l+32, ... (their loads issued
+    // together, kGvFold at a time), then a fixed tree over the lanes.
+    const Stat *pb = partials + size_t(b) * kGvMaxBlocks;
     Stat c = stat_empty();
-    for (int i = lane; i < int(gridDim.x); i += 32) c = stat_merge(c, ld_stat(&partials[size_t(b) * kGvMaxBlocks + i]));
+    for (int i0 = lane; i0 < int(gridDim.x); i0 += 32 * kGvFold) {
+        Stat q[kGvFold];
+#pragma unroll
+        for (int f = 0; f < kGvFold; ++f)
+            q[f] = i0 + 32 * f < int(gridDim.x) ? ld_stat(pb + i0 + 32 * f) : stat_empty();
+#pragma unroll
+        for (int f = 0; f < kGvFold; ++f) c = stat_merge(c, q[f]);
+    }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const Stat other = shfl_xor_stat(c, o);

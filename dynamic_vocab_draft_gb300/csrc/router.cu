@@ -121,7 +121,7 @@ __device__ void topk_block(const float *__restrict__ s, int M, int k, int32_t *_
     __shared__ unsigned hist[256];
     __shared__ int scan_scratch[33];
     __shared__ uint32_t s_prefix;
-    __shared__ int s_need, s_whole;
+    __shared__ int s_need;
     // thread t owns the contiguous index range [t*E, t*E + E)
     const int E = (M + kTopkThreads - 1) / kTopkThreads;
     const int lo = threadIdx.x * E;
@@ -130,11 +130,9 @@ __device__ void topk_block(const float *__restrict__ s, int M, int k, int32_t *_
     for (int e = 0; e < kTopkPerThread; ++e)
         key[e] = (e < E && lo + e < M) ? order_key(__ldcg(s + lo + e)) : 0u;
 
-    // MSB-first radix select of the k-th largest key, 8 bits per pass.  A pass whose chosen
-    // digit's keys are all needed ends the search: every key at or above the prefix is kept.
-    if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; s_whole = 0; }
+    // MSB-first radix select of the k-th largest key, 8 bits per pass.
+    if (threadIdx.x == 0) { s_prefix = 0u; s_need = k; }
     uint32_t mask = 0u;
-#pragma unroll
     for (int shift = 24; shift >= 0; shift -= 8) {
         if (threadIdx.x < 256) hist[threadIdx.x] = 0u;
         __syncthreads();
@@ -171,7 +169,6 @@ __device__ void topk_block(const float *__restrict__ s, int M, int k, int32_t *_
                     if (before + c[q] >= unsigned(need)) {
                         s_prefix = prefix | (uint32_t(255 - 8 * lane - q) << shift);
                         s_need = need - int(before);
-                        s_whole = before + c[q] == unsigned(need);
                         break;
                     }
                     before += c[q];
@@ -180,17 +177,15 @@ __device__ void topk_block(const float *__restrict__ s, int M, int k, int32_t *_
         }
         mask |= 255u << shift;
         __syncthreads();
-        if (s_whole) break;                 // uniform: read after the barrier
     }
-    const uint32_t theta = s_prefix;      // the k-th largest key's bits under `mask`
+    const uint32_t theta = s_prefix;      // the k-th largest key
     const int need_eq = s_need;           // how many of the keys equal to theta to keep
 
-    // Keep keys above theta, and the first need_eq keys equal to theta in index order (all
-    // of them after an early end), comparing the bits under `mask`.
+    // Keep keys above theta, and the first need_eq keys equal to theta in index order.
     int eq = 0;
 #pragma unroll
     for (int e = 0; e < kTopkPerThread; ++e)
-        if (e < E && lo + e < M && (key[e] & mask) == theta) ++eq;
+        if (e < E && lo + e < M && key[e] == theta) ++eq;
     int tot;
     int eq_before = block_exclusive_scan(eq, scan_scratch, &tot);
     bool sel[kTopkPerThread];
@@ -199,9 +194,8 @@ __device__ void topk_block(const float *__restrict__ s, int M, int k, int32_t *_
     for (int e = 0; e < kTopkPerThread; ++e) {
         const bool valid = e < E && lo + e < M;
         bool keep = false;
-        const uint32_t km = key[e] & mask;
-        if (valid && km > theta) keep = true;
-        if (valid && km == theta) { keep = eq_before < need_eq; ++eq_before; }
+        if (valid && key[e] > theta) keep = true;
+        if (valid && key[e] == theta) { keep = eq_before < need_eq; ++eq_before; }
         sel[e] = keep;
         nsel += keep;
     }

@@ -558,8 +558,9 @@ __device__ RowStat block_rowstat(RowStat st, RowStat *ws)
 }
 
 // Cluster-wide reductions.  Every CTA reduces its own threads, publishes the result in its
-// shared memory, and after a cluster barrier each CTA merges all CTAs' results in rank order,
-// so every thread of the cluster holds the same bits and takes the same decisions.  Two
+// shared memory, and after a cluster barrier each CTA's first warp reads all CTAs' results at
+// once (lane r from rank r) and merges them in a fixed lane tree, so every thread of the
+// cluster holds the same bits and takes the same decisions.  Two
 // publication slots alternate: a CTA rewrites a slot only after the barrier of the next
 // reduction, which every other CTA reaches only once it has finished reading that slot.
 struct ClusterRed {
@@ -575,10 +576,15 @@ __device__ RowStat cluster_rowstat(RowStat st, RowStat *red, ClusterRed &cr, int
     const int slot = k & 1;
     if (threadIdx.x == 0) cr.stat[slot] = mine;
     cl.sync();
-    if (threadIdx.x == 0) {
-        RowStat m = rowstat_empty();
-        for (unsigned r = 0; r < cl.num_blocks(); ++r) m = rowstat_merge(m, cl.map_shared_rank(&cr, r)->stat[slot]);
-        red[32] = m;
+    if (threadIdx.x < 32) {
+        const unsigned lane = threadIdx.x;
+        RowStat m = lane < cl.num_blocks() ? cl.map_shared_rank(&cr, lane)->stat[slot] : rowstat_empty();
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const RowStat q = shfl_xor_rowstat(m, o);
+            m = (lane & o) ? rowstat_merge(q, m) : rowstat_merge(m, q);
+        }
+        if (lane == 0) red[32] = m;
     }
     __syncthreads();
     const RowStat out = red[32];
@@ -593,10 +599,12 @@ __device__ float cluster_sum(float x, float *scratch, ClusterRed &cr, int &k)
     const int slot = k & 1;
     if (threadIdx.x == 0) cr.sum[slot] = mine;
     cl.sync();
-    if (threadIdx.x == 0) {
-        float s = 0.f;
-        for (unsigned r = 0; r < cl.num_blocks(); ++r) s += cl.map_shared_rank(&cr, r)->sum[slot];
-        scratch[32] = s;
+    if (threadIdx.x < 32) {
+        const unsigned lane = threadIdx.x;
+        float s = lane < cl.num_blocks() ? cl.map_shared_rank(&cr, lane)->sum[slot] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+        if (lane == 0) scratch[32] = s;
     }
     __syncthreads();
     const float out = scratch[32];
@@ -685,7 +693,8 @@ tree_walk_kernel(TreeArgs a)
             r[j] = pj;
             on += pj;
         }
-        __threadfence();                         // r is read across the cluster after the barrier
+        // r is read across the cluster only after the next cluster barrier (cluster_sum's), whose
+        // arrive/wait pair has release/acquire semantics at cluster scope: no fence needed here
         // every child's test inputs at once (one thread per child): the index j of its token
         // in the list, the uniform, and -- when the head's row statistics are given -- q(x)
         // and the statistics the rejection pass needs
@@ -749,7 +758,6 @@ tree_walk_kernel(TreeArgs a)
                 rn[j] = w;
                 part += w;
             }
-            __threadfence();
             const float Rn = O + cluster_sum(part, fscr, s_cr, nred);
             if (Rn > 0.f) { cb ^= 1; r = rn; R = Rn; }
         }

@@ -454,6 +454,7 @@ verify_residual_kernel(ChainArgs a)
 constexpr int kWalkThreads = 1024;
 constexpr int kWalkMaxM = 8192;
 constexpr int kWalkMaxCluster = 8;              // CTAs per sequence (portable cluster size)
+constexpr int kWalkU = 4;                       // elements per thread whose loads a pass issues together
 
 struct WalkState {                 // what the walk leaves for the correction draw
     int mode;                      // 0: decided (greedy); 1: draw from p of `row`; 2: residual
@@ -656,13 +657,27 @@ tree_walk_kernel(TreeArgs a)
         }
         __syncthreads();
         const int nk = s_nkids;
-        // one pass over the target row
+        // one pass over the target row (kWalkU elements' loads issued together, then folded in
+        // ascending v)
         RowStat st = rowstat_empty();
-        for (int v = gt; v < a.V; v += GT) {
-            const float zv = z[v];
-            const int c = a.cluster_of[v];
-            const bool off = has_list && (unsigned(c) >= unsigned(a.M) || s_cpos[c] < 0);
-            rowstat_add(st, zv, zv * a.inv_te, off, v);
+        for (int v0 = gt; v0 < a.V; v0 += kWalkU * GT) {
+            float zv[kWalkU];
+            int cv[kWalkU];
+#pragma unroll
+            for (int e = 0; e < kWalkU; ++e) {
+                const int v = v0 + e * GT;
+                zv[e] = v < a.V ? z[v] : 0.f;
+                cv[e] = v < a.V ? a.cluster_of[v] : -1;
+            }
+#pragma unroll
+            for (int e = 0; e < kWalkU; ++e) {
+                const int v = v0 + e * GT;
+                if (v < a.V) {
+                    const int c = cv[e];
+                    const bool off = has_list && (unsigned(c) >= unsigned(a.M) || s_cpos[c] < 0);
+                    rowstat_add(st, zv[e], zv[e] * a.inv_te, off, v);
+                }
+            }
         }
         const RowStat row = cluster_rowstat(st, s_red, s_cr, nred);
         if (a.T == 0.f) {
@@ -687,11 +702,22 @@ tree_walk_kernel(TreeArgs a)
         const int32_t *ids = a.vs_ids + size_t(dep) * a.vs_stride + lo;
         float *r = a.rbuf + (size_t(b) * 2 + cb) * a.V;
         float on = 0.f;
-        for (int j = gt; j < nb; j += GT) {
-            const int v = ids[j];
-            const float pj = (v >= 0 && v < a.V) ? __expf(z[v] * a.inv_te - row.m) / row.s : 0.f;
-            r[j] = pj;
-            on += pj;
+        for (int j0 = gt; j0 < nb; j0 += kWalkU * GT) {
+            int vv[kWalkU];
+            float zv[kWalkU];
+#pragma unroll
+            for (int e = 0; e < kWalkU; ++e) vv[e] = j0 + e * GT < nb ? ids[j0 + e * GT] : -1;
+#pragma unroll
+            for (int e = 0; e < kWalkU; ++e) zv[e] = (vv[e] >= 0 && vv[e] < a.V) ? z[vv[e]] : 0.f;
+#pragma unroll
+            for (int e = 0; e < kWalkU; ++e) {
+                const int j = j0 + e * GT;
+                if (j < nb) {
+                    const float pj = (vv[e] >= 0 && vv[e] < a.V) ? __expf(zv[e] * a.inv_te - row.m) / row.s : 0.f;
+                    r[j] = pj;
+                    on += pj;
+                }
+            }
         }
         // r is read across the cluster only after the next cluster barrier (cluster_sum's), whose
         // arrive/wait pair has release/acquire semantics at cluster scope: no fence needed here
@@ -753,10 +779,23 @@ tree_walk_kernel(TreeArgs a)
             // rejected: r <- max(r - R q, 0) into the other buffer, kept if it has mass
             float *rn = a.rbuf + (size_t(b) * 2 + (cb ^ 1)) * a.V;
             float part = 0.f;
-            for (int j = gt; j < nb; j += GT) {
-                const float w = fmaxf(r[j] - R * (__expf(ql[j] * a.inv_te - qm) / qs), 0.f);
-                rn[j] = w;
-                part += w;
+            for (int j0 = gt; j0 < nb; j0 += kWalkU * GT) {
+                float rv[kWalkU], lv[kWalkU];
+#pragma unroll
+                for (int e = 0; e < kWalkU; ++e) {
+                    const int j = j0 + e * GT;
+                    rv[e] = j < nb ? r[j] : 0.f;
+                    lv[e] = j < nb ? ql[j] : 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < kWalkU; ++e) {
+                    const int j = j0 + e * GT;
+                    if (j < nb) {
+                        const float w = fmaxf(rv[e] - R * (__expf(lv[e] * a.inv_te - qm) / qs), 0.f);
+                        rn[j] = w;
+                        part += w;
+                    }
+                }
             }
             const float Rn = O + cluster_sum(part, fscr, s_cr, nred);
             if (Rn > 0.f) { cb ^= 1; r = rn; R = Rn; }

@@ -363,26 +363,27 @@ def run_ours(args):
     d.check_status()
     value = whole_job_rate(world, tokens_per_step, K, total_ms)
 
-    # e2e through the public API: pinned host inputs -> device, step, results -> host
+    # e2e through the public API: every step copies its inputs from pinned host memory (the
+    # ones only verification reads on a copy stream beside the drafting stages) and its
+    # results (accepted lengths, corrections, draft tokens) back to pinned host memory
     Ke = min(K, args.e2e_steps)
-    outs = [d.accepted, d.correction, d.tokens] + ([d.path] if cfg.mode == "tree" else [])
-    outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    out_h = torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
+    late_names = ("z", "u", "u_node", "u_res")
+    d.capture_io([v for k, v in host.items() if k not in late_names],
+                 [v for k, v in host.items() if k in late_names], out_h)
     e2e_ms = 0.0
     for i in range(Ke):
         l2_flush(i)
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
         s.record(main)
-        for h, dv in host.values():
-            dv.copy_(h, non_blocking=True)
-        d.replay()
-        for oh, o in zip(outs_h, outs):
-            oh.copy_(o, non_blocking=True)
+        d.replay_io()
         e.record(main)
         e.synchronize()
         e2e_ms += s.elapsed_time(e)
+    d.check_status()
     h2d = sum(h.numel() * h.element_size() for h, _ in host.values())
-    d2h = sum(o.numel() * o.element_size() for o in outs_h)
+    d2h = out_h.numel() * out_h.element_size()
     e2e_ms = max_over_ranks(e2e_ms, dev)
     e2e_value = whole_job_rate(world, tokens_per_step, Ke, e2e_ms)
 

@@ -10,6 +10,10 @@ heads of earlier positions stream W.
 
 Buffers are allocated once per drafter; a step launches kernels only.  ``capture()`` records
 one whole step (both streams) into a CUDA graph that ``replay()`` launches in one call.
+``capture_io()`` records a step together with the copies of its inputs from pinned host
+memory and of its results back to the host: the inputs the drafting stages read are copied
+first, the ones only verification reads (target logits, uniforms) on a copy stream while the
+heads run, and the results (one contiguous block per drafter, ``self.out``) in one copy.
 """
 from __future__ import annotations
 
@@ -62,6 +66,37 @@ class _Common:
         """Launch the captured step; timed=True launches the graph that also records the
         per-head timing events."""
         (self.graph_timed if timed else self.graph).replay()
+
+    def capture_io(self, early, late, out_host):
+        """Record a step with its host transfers into a CUDA graph (see the module docstring).
+        early, late: [(pinned host tensor, device buffer)] copied before the step and on the copy
+        stream beside the drafting stages, respectively; out_host: a pinned host tensor shaped
+        like ``self.out`` that receives the results."""
+        assert out_host.shape == self.out.shape and out_host.dtype == self.out.dtype
+        events, self.head_events = self.head_events, None
+        self.step()                              # warm up outside the capture
+        torch.cuda.synchronize()
+        copy = torch.cuda.Stream(device=self.dev)
+        late_ready = torch.cuda.Event()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            main = torch.cuda.current_stream(self.dev)
+            for h, dv in early:
+                dv.copy_(h, non_blocking=True)
+            copy.wait_stream(main)
+            with torch.cuda.stream(copy):
+                for h, dv in late:
+                    dv.copy_(h, non_blocking=True)
+                late_ready.record(copy)
+            self.step(before_verify=late_ready)
+            out_host.copy_(self.out, non_blocking=True)
+        self.head_events = events
+        self.graph_io, self._io_keep = g, (copy, late_ready)
+        return g
+
+    def replay_io(self):
+        """Launch the step recorded by capture_io() (inputs in, step, results out)."""
+        self.graph_io.replay()
 
     def enable_head_timing(self):
         """Time every position's head launch with CUDA events (also inside a captured graph).
@@ -118,10 +153,12 @@ class ChainDrafter(_Common):
         self.logits = torch.zeros(gamma, cap, **f32)
         self.row_max = torch.empty(gamma, B, **f32)
         self.row_sumexp = torch.empty(gamma, B, **f32)
-        self.tokens = torch.empty(gamma, B, **i32)
+        # results in one block: accepted [B], correction [B], draft tokens [gamma, B]
+        self.out = torch.empty((2 + gamma) * B, **i32)
+        self.accepted = self.out[:B]
+        self.correction = self.out[B:2 * B]
+        self.tokens = self.out[2 * B:].view(gamma, B)
         self.token_idx = torch.empty(gamma, B, **i32)
-        self.accepted = torch.empty(B, **i32)
-        self.correction = torch.empty(B, **i32)
         self.ws_router = [api.workspace(api.router_workspace_bytes(B, self.Hr), dev) for _ in range(gamma)]
         self.ws_short = [api.workspace(api.shortlist_workspace_bytes(B, M), dev) for _ in range(gamma)]
         self.ws_head = api.workspace(api.head_workspace_bytes(B), dev)
@@ -154,7 +191,9 @@ class ChainDrafter(_Common):
                    self.tokens, self.u, self.accepted, self.correction, self.ws_verify, self.status,
                    q_max=self.row_max, q_sumexp=self.row_sumexp, stream=stream)
 
-    def step(self):
+    def step(self, before_verify=None):
+        """One speculation step; verification first waits for the event `before_verify`, if
+        given (inputs that only verification reads may still be arriving)."""
         main = torch.cuda.current_stream(self.dev)
         self.side.wait_stream(main)
         for t in range(self.gamma):
@@ -168,6 +207,8 @@ class ChainDrafter(_Common):
             self.head(t)
             if self.head_events:
                 api.event_record(self.head_events[t][1])
+        if before_verify is not None:
+            main.wait_event(before_verify)
         self.verify()
 
     def n_heads(self) -> int:
@@ -221,11 +262,13 @@ class TreeDrafter(_Common):
         self.logits = torch.zeros(D, cap * Wd, **f32)
         self.row_max = torch.empty(D, B * Wd, **f32)
         self.row_sumexp = torch.empty(D, B * Wd, **f32)
-        self.tokens = torch.empty(D, B * Wd, **i32)
+        # results in one block: accepted [B], correction [B], path [B, D], node tokens [D, B*Wd]
+        self.out = torch.empty(2 * B + B * D + D * B * Wd, **i32)
+        self.accepted = self.out[:B]
+        self.correction = self.out[B:2 * B]
+        self.path = self.out[2 * B:2 * B + B * D].view(B, D)
+        self.tokens = self.out[2 * B + B * D:].view(D, B * Wd)
         self.token_idx = torch.empty(D, B * Wd, **i32)
-        self.accepted = torch.empty(B, **i32)
-        self.correction = torch.empty(B, **i32)
-        self.path = torch.empty(B, D, **i32)
         self.ws_router = [api.workspace(api.router_workspace_bytes(B, self.Hr), dev) for _ in range(D)]
         self.ws_short = [api.workspace(api.shortlist_workspace_bytes(B, M), dev) for _ in range(D)]
         self.ws_head = api.workspace(api.head_workspace_bytes(B * Wd), dev)
@@ -255,7 +298,9 @@ class TreeDrafter(_Common):
                         self.u_res, self.accepted, self.correction, self.path, self.ws_verify,
                         self.status, q_max=self.row_max, q_sumexp=self.row_sumexp, stream=stream)
 
-    def step(self):
+    def step(self, before_verify=None):
+        """One speculation step; verification first waits for the event `before_verify`, if
+        given."""
         main = torch.cuda.current_stream(self.dev)
         self.side.wait_stream(main)
         for t in range(self.D):
@@ -269,6 +314,8 @@ class TreeDrafter(_Common):
             self.head(t)
             if self.head_events:
                 api.event_record(self.head_events[t][1])
+        if before_verify is not None:
+            main.wait_event(before_verify)
         self.verify()
 
     def n_heads(self) -> int:

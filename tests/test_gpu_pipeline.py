@@ -118,6 +118,24 @@ def test_chain_step_matches_oracle(pkg, name, T, seqs):
     torch.cuda.synchronize()
     for a, b in zip(snap, (d.logits, d.tokens, d.accepted, d.correction)):
         assert torch.equal(a, b)
+    # the step with its host transfers (inputs from pinned host memory, the target logits and
+    # uniforms on the copy stream, results back in one block): the same results, bit for bit,
+    # with the device inputs and outputs wiped before the replay
+    out_h = _replay_io(d, early=(d.H,), late=(d.z, d.u))
+    assert torch.equal(out_h, torch.cat([snap[2], snap[3], snap[1].flatten()]).cpu())
+
+
+def _replay_io(d, early, late):
+    pin = lambda x: (x.cpu().pin_memory(), x)
+    out_h = torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
+    d.capture_io([pin(x) for x in early], [pin(x) for x in late], out_h)
+    for x in tuple(early) + tuple(late) + (d.out,):
+        x.zero_()
+    out_h.fill_(-7)
+    d.replay_io()
+    torch.cuda.synchronize()
+    d.check_status()
+    return out_h
 
 
 def test_tree_step_matches_oracle(pkg):
@@ -163,3 +181,7 @@ def test_tree_step_matches_oracle(pkg):
                 assert d.accepted[b].item() == ref[b]["accepted"]
                 assert d.path[b].tolist() == ref[b]["path"]
                 assert d.correction[b].item() == ref[b]["correction"]
+        # the step with its host transfers gives the same results block
+        snap = d.out.clone()
+        out_h = _replay_io(d, early=(d.Hr_h, d.Hn), late=(d.z, d.u_node, d.u_res))
+        assert torch.equal(out_h, snap.cpu())

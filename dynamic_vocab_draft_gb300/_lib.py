@@ -39,6 +39,7 @@ SIGNATURES = {
                             P, P, P, P, SZ, P, P]),
     "ds_philox4x32_10": (ST, [P, U64, P, I, P]),
     "ds_event_record": (ST, [P, P]),
+    "ds_copy": (ST, [P, P, SZ, P]),
 }
 
 _lib = None

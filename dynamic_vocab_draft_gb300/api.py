@@ -178,6 +178,20 @@ def philox4x32_10(ctr, seed, out, stream=None):
         _ptr(out, (torch.int32, torch.uint32), "out"), n, _stream(stream)), "ds_philox4x32_10")
 
 
+def copy(dst, src, stream=None):
+    """dst <- src (same byte size, both contiguous) by a kernel on `stream`; each side is a CUDA
+    tensor or a pinned CPU tensor (see ds_copy)."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+            raise ValueError(f"copy: {name} must be a contiguous tensor")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError(f"copy: {name} must be a CUDA tensor or pinned host memory")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("copy: dst and src differ in size")
+    _lib.check(_lib.load().ds_copy(dst.data_ptr(), src.data_ptr(), nbytes, _stream(stream)), "ds_copy")
+
+
 def event_record(event, stream=None):
     """Record a torch.cuda.Event so that it is timeable inside a captured CUDA graph.  The
     event must already exist (torch creates it on its first ordinary record())."""

@@ -10,6 +10,22 @@ __global__ void philox_kernel(const uint4 *__restrict__ ctr, uint64_t seed, uint
     if (i < n) out[i] = ds::philox4x32_10(ctr[i], uint32_t(seed), uint32_t(seed >> 32));
 }
 
+// SM-driven copy: 16-byte vectors when both ends allow them, bytes otherwise.
+__global__ void copy16_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src, size_t n)
+{
+    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x)
+        dst[i] = src[i];
+}
+
+__global__ void copy1_kernel(unsigned char *__restrict__ dst, const unsigned char *__restrict__ src, size_t n)
+{
+    for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n; i += size_t(gridDim.x) * blockDim.x)
+        dst[i] = src[i];
+}
+
+constexpr int kCopyThreads = 256;
+constexpr size_t kCopyMaxBlocks = 1024;
+
 }  // namespace
 
 extern "C" const char *ds_status_string(ds_status s)
@@ -51,4 +67,24 @@ extern "C" ds_status ds_event_record(cudaEvent_t event, cudaStream_t stream)
                               ? cudaEventRecordWithFlags(event, stream, cudaEventRecordExternal)
                               : cudaEventRecord(event, stream);
     return e == cudaSuccess ? DS_OK : DS_ERR_CUDA;
+}
+
+extern "C" ds_status ds_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream)
+{
+    if (bytes == 0) return DS_OK;
+    if (!dst || !src) return DS_ERR_INVALID_ARG;
+    const char *d0 = static_cast<const char *>(dst), *s0 = static_cast<const char *>(src);
+    if (d0 < s0 + bytes && s0 < d0 + bytes) return DS_ERR_INVALID_ARG;     // overlapping ranges
+    if (ds::aligned16(dst) && ds::aligned16(src) && bytes % 16 == 0) {
+        const size_t n = bytes / 16;
+        const size_t blocks = (n + kCopyThreads - 1) / kCopyThreads;
+        copy16_kernel<<<unsigned(blocks < kCopyMaxBlocks ? blocks : kCopyMaxBlocks), kCopyThreads, 0, stream>>>(
+            static_cast<uint4 *>(dst), static_cast<const uint4 *>(src), n);
+    } else {
+        const size_t blocks = (bytes + kCopyThreads - 1) / kCopyThreads;
+        copy1_kernel<<<unsigned(blocks < kCopyMaxBlocks ? blocks : kCopyMaxBlocks), kCopyThreads, 0, stream>>>(
+            static_cast<unsigned char *>(dst), static_cast<const unsigned char *>(src), bytes);
+    }
+    DS_TRY_LAUNCH();
+    return DS_OK;
 }

@@ -12,8 +12,12 @@ Buffers are allocated once per drafter; a step launches kernels only.  ``capture
 one whole step (both streams) into a CUDA graph that ``replay()`` launches in one call.
 ``capture_io()`` records a step together with the copies of its inputs from pinned host
 memory and of its results back to the host: the inputs the drafting stages read are copied
-first, the ones only verification reads (target logits, uniforms) on a copy stream while the
-heads run, and the results (one contiguous block per drafter, ``self.out``) in one copy.
+first (up to 2 MB each by a kernel, ds_copy, which skips the copy engine's start-up; larger
+ones by the copy engine), then the ones only verification reads (target logits, uniforms) by
+the copy engine on a copy stream while the drafting stages run, and the
+results (one contiguous block per drafter, ``self.out``) by one ds_copy.  Host-to-device copies
+on several streams were measured to take turns on one copy engine, so one copy stream is the
+default.
 """
 from __future__ import annotations
 
@@ -67,31 +71,42 @@ class _Common:
         per-head timing events."""
         (self.graph_timed if timed else self.graph).replay()
 
-    def capture_io(self, early, late, out_host):
+    def capture_io(self, early, late, out_host, copy_streams=1, kernel_copy_max=2 << 20):
         """Record a step with its host transfers into a CUDA graph (see the module docstring).
-        early, late: [(pinned host tensor, device buffer)] copied before the step and on the copy
-        stream beside the drafting stages, respectively; out_host: a pinned host tensor shaped
-        like ``self.out`` that receives the results."""
+        early, late: [(pinned host tensor, device buffer)] copied before the step (by ds_copy up
+        to `kernel_copy_max` bytes each, else by the copy engine), and beside the drafting stages
+        (each split into `copy_streams` contiguous parts, one per copy stream), respectively;
+        out_host: a pinned host tensor shaped like ``self.out`` that receives the results."""
         assert out_host.shape == self.out.shape and out_host.dtype == self.out.dtype
         events, self.head_events = self.head_events, None
         self.step()                              # warm up outside the capture
         torch.cuda.synchronize()
-        copy = torch.cuda.Stream(device=self.dev)
-        late_ready = torch.cuda.Event()
+        copies = [torch.cuda.Stream(device=self.dev) for _ in range(max(1, copy_streams))]
+        done = [torch.cuda.Event() for _ in copies]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             main = torch.cuda.current_stream(self.dev)
             for h, dv in early:
-                dv.copy_(h, non_blocking=True)
-            copy.wait_stream(main)
-            with torch.cuda.stream(copy):
-                for h, dv in late:
+                if h.numel() * h.element_size() <= kernel_copy_max:
+                    api.copy(dv, h)
+                else:
                     dv.copy_(h, non_blocking=True)
-                late_ready.record(copy)
-            self.step(before_verify=late_ready)
-            out_host.copy_(self.out, non_blocking=True)
+            # the late copies fork after the early ones: copy-engine transfers queue in the order
+            # they become ready, and the drafting stages must not wait behind the target logits
+            k = len(copies)
+            for i, c in enumerate(copies):
+                c.wait_stream(main)
+                with torch.cuda.stream(c):
+                    for h, dv in late:
+                        hf, df = h.view(-1), dv.view(-1)
+                        lo, hi = hf.numel() * i // k, hf.numel() * (i + 1) // k
+                        if hi > lo:
+                            df[lo:hi].copy_(hf[lo:hi], non_blocking=True)
+                    done[i].record(c)
+            self.step(before_verify=done)
+            api.copy(out_host, self.out)
         self.head_events = events
-        self.graph_io, self._io_keep = g, (copy, late_ready)
+        self.graph_io, self._io_keep = g, (copies, done)
         return g
 
     def replay_io(self):
@@ -192,7 +207,7 @@ class ChainDrafter(_Common):
                    q_max=self.row_max, q_sumexp=self.row_sumexp, stream=stream)
 
     def step(self, before_verify=None):
-        """One speculation step; verification first waits for the event `before_verify`, if
+        """One speculation step; verification first waits for the events in `before_verify`, if
         given (inputs that only verification reads may still be arriving)."""
         main = torch.cuda.current_stream(self.dev)
         self.side.wait_stream(main)
@@ -207,8 +222,8 @@ class ChainDrafter(_Common):
             self.head(t)
             if self.head_events:
                 api.event_record(self.head_events[t][1])
-        if before_verify is not None:
-            main.wait_event(before_verify)
+        for ev in before_verify or ():
+            main.wait_event(ev)
         self.verify()
 
     def n_heads(self) -> int:
@@ -299,7 +314,7 @@ class TreeDrafter(_Common):
                         self.status, q_max=self.row_max, q_sumexp=self.row_sumexp, stream=stream)
 
     def step(self, before_verify=None):
-        """One speculation step; verification first waits for the event `before_verify`, if
+        """One speculation step; verification first waits for the events in `before_verify`, if
         given."""
         main = torch.cuda.current_stream(self.dev)
         self.side.wait_stream(main)
@@ -314,8 +329,8 @@ class TreeDrafter(_Common):
             self.head(t)
             if self.head_events:
                 api.event_record(self.head_events[t][1])
-        if before_verify is not None:
-            main.wait_event(before_verify)
+        for ev in before_verify or ():
+            main.wait_event(ev)
         self.verify()
 
     def n_heads(self) -> int:

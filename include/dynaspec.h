@@ -289,6 +289,21 @@ ds_status ds_philox4x32_10(const uint32_t *ctr, uint64_t seed, uint32_t *out, in
  * ------------------------------------------------------------------------------------- */
 ds_status ds_event_record(cudaEvent_t event, cudaStream_t stream);
 
+/* -------------------------------------------------------------------------------------
+ * ds_copy -- transfer helper (no counterpart in the method): copies `bytes` bytes from src to
+ * dst with a kernel on `stream` instead of a copy engine.  Either end may be pinned host
+ * memory (page-locked, which with unified addressing the GPU reaches by its host address,
+ * over NVLink-C2C on Grace systems) or device memory.  For small transfers between a step
+ * and the host (hidden states in, results out) this avoids the copy engine's start-up time.
+ *   dst, src               device pointers or pinned host pointers; the ranges must not
+ *                          overlap.  16-byte vectors when both are 16-byte aligned and bytes %
+ *                          16 == 0, else byte copies.
+ * Passing pageable host memory is the caller's error: on systems without address translation
+ * services the kernel cannot reach it.  Returns DS_ERR_INVALID_ARG for NULL or overlapping
+ * ranges; bytes == 0 is a no-op.
+ * ------------------------------------------------------------------------------------- */
+ds_status ds_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -106,3 +106,9 @@ def test_host_argument_checks(lib):
     t = list(tree); t[25] = 16
     assert lib.ds_verify_tree(*t) == 4
     assert lib.ds_philox4x32_10(None, 0, FAKE, 4, None) == 1
+    # copy: NULL ends and overlapping ranges are refused before any launch; zero bytes is a no-op
+    assert lib.ds_copy(None, FAKE, 16, None) == 1
+    assert lib.ds_copy(FAKE, None, 16, None) == 1
+    assert lib.ds_copy(FAKE, ctypes.c_void_p(0x10008), 16, None) == 1
+    assert lib.ds_copy(ctypes.c_void_p(0x10008), FAKE, 16, None) == 1
+    assert lib.ds_copy(FAKE, FAKE, 0, None) == 0

@@ -185,3 +185,22 @@ def test_tree_step_matches_oracle(pkg):
         snap = d.out.clone()
         out_h = _replay_io(d, early=(d.Hr_h, d.Hn), late=(d.z, d.u_node, d.u_res))
         assert torch.equal(out_h, snap.cpu())
+
+
+@pytest.mark.parametrize("nbytes", [16, 48, 57344, 1 << 20, 7, 1001])
+def test_copy_between_pinned_host_and_device(pkg, nbytes):
+    # ds_copy in both directions (16-byte vectors when aligned, bytes otherwise), and device to
+    # device, against the source bytes
+    rng = np.random.default_rng(nbytes)
+    src = torch.from_numpy(rng.integers(0, 256, nbytes, dtype=np.uint8)).pin_memory()
+    dev_buf = torch.full((nbytes,), 7, dtype=torch.uint8, device=gu.dev())
+    back = torch.zeros(nbytes, dtype=torch.uint8).pin_memory()
+    dev2 = torch.zeros(nbytes, dtype=torch.uint8, device=gu.dev())
+    pkg.api.copy(dev_buf, src)
+    pkg.api.copy(dev2, dev_buf)
+    pkg.api.copy(back, dev2)
+    torch.cuda.synchronize()
+    assert torch.equal(dev_buf.cpu(), src)
+    assert torch.equal(back, src)
+    with pytest.raises(ValueError):
+        pkg.api.copy(dev_buf, torch.zeros(nbytes, dtype=torch.uint8))     # pageable host memory

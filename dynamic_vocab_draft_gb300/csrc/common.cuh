@@ -167,17 +167,6 @@ __device__ __forceinline__ float warp_sum(float x)
     return x;
 }
 
-__device__ __forceinline__ float warp_max(float x)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
-    return x;
-}
-
-// Read of a value another block of the same grid published before its release fence.
-template <typename T>
-__device__ __forceinline__ T ld_volatile(const T *p) { return *(const volatile T *)p; }
-
 __device__ __forceinline__ Stat ld_stat(const Stat *p)
 {
     const volatile Stat *q = (const volatile Stat *)p;
@@ -244,24 +233,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity)
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(done) : "r"(smem_addr(bar)), "r"(parity) : "memory");
     return done != 0;
-}
-
-// Wait until the phase with the given parity has completed; false after the budget.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity)
-{
-    if (mbar_test(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_test(bar, parity))
-        if (clock64() - t0 > kWaitBudgetCycles) return false;
-    return true;
-}
-
-// Same, but gives up at an absolute clock64() deadline (one budget shared by several waits).
-__device__ __forceinline__ bool mbar_wait_until(uint64_t *bar, unsigned parity, long long deadline)
-{
-    while (!mbar_test(bar, parity))
-        if (clock64() > deadline) return false;
-    return true;
 }
 
 }  // namespace ds

@@ -89,8 +89,10 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int sr
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes));
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
-template <int N> __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N)); }
+// Wait until every cp.async this thread issued has landed.  The producers never commit groups
+// (their copies complete through cp.async.mbarrier.arrive), and wait_all commits the pending
+// ones before waiting, so it covers them; a bare wait_group would not.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr)
 {
@@ -288,7 +290,7 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
             if (++slot == STG) { slot = 0; ++use; }
             if (++ks == nks) { ks = 0; ++t; }
         }
-        cp_async_wait<0>();                                    // nothing in flight when the role ends
+        cp_async_wait_all();                                   // nothing in flight when the role ends
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer: one thread
         if (lane == 0) {

@@ -65,7 +65,8 @@ def test_vocab_index(ds, name):
 # ---------------------------------------------------------------------------------------
 @pytest.mark.parametrize("name,B", [("tiny", 1), ("small_batched", 5), ("llama_b1", 1),
                                     ("batched", 32), ("large_b1_f5", 1), ("large_b8_f10", 8),
-                                    ("large_b64_f100", 64), ("large_b64_f100", 2), ("large_b64_f100", 100)])
+                                    ("large_b64_f100", 64), ("large_b64_f100", 2), ("large_b64_f100", 100),
+                                    ("large_b64_f100", 20), ("large_b64_f100", 40)])
 def test_router_topk(ds, name, B):
     # B = 1: CUDA-core GEMV; 2 <= B <= 64: tensor-core layers; B > 64: CUDA-core batched GEMV.
     # B larger than the configuration's batch stacks the hidden states of several positions.
@@ -267,7 +268,12 @@ def test_head_all_clusters_is_dense_head(ds):
 
 
 @pytest.mark.parametrize("name,B,G,T", [("small_batched", 5, 1, 0.8), ("small_batched", 5, 1, 0.0),
-                                        ("tiny", 1, 3, 1.0), ("small_batched", 3, 7, 1.0)])
+                                        ("tiny", 1, 3, 1.0), ("small_batched", 3, 7, 1.0),
+                                        # 40, 60 and 128 head rows: N = 48, 64 and 128 columns (128
+                                        # is the most the union path takes; its stages hold one
+                                        # 64-column atom instead of two)
+                                        ("small_batched", 5, 8, 1.0), ("small_batched", 5, 12, 0.0),
+                                        ("small_batched", 4, 32, 0.8)])
 def test_head_union_path(ds, name, B, G, T):
     inp = gu.chain_inputs(name)
     cfg = inp["cfg"]

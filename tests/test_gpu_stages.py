@@ -267,6 +267,22 @@ def test_head_all_clusters_is_dense_head(ds):
     assert_close(logits[:cfg.V], dense[0, S], "dense equivalence")
 
 
+@pytest.mark.parametrize("union", [False, True])
+def test_head_rows_longer_than_one_load_round(ds, union):
+    # d = 10248: the batch-1 head takes three rounds of loads per row (4096, 4096 and a ragged
+    # 2056 columns; the first row's first round is issued before h is staged), the union GEMM
+    # 81 k-stages of 128 columns with a ragged last one
+    cfg = wl.config("small_batched").with_(name="small_batched_wide", d=10248)
+    inp = wl.chain_inputs(cfg, 0, with_head=False)
+    inp["W"] = gu._lm_head(cfg.V, cfg.d, inp["seed"])[0]
+    B = 3 if union else 1
+    for pos in (1, cfg.gamma):
+        ids, _ = _oracle_lists(inp, B, pos)
+        Hrows = inp["H"][:B, pos]
+        out = _run_head(ds, inp, Hrows, 1, ids, cfg.T, pos, union=union)
+        _check_head(inp, Hrows, 1, ids, cfg.T, pos, out)
+
+
 @pytest.mark.parametrize("name,B,G,T", [("small_batched", 5, 1, 0.8), ("small_batched", 5, 1, 0.0),
                                         ("tiny", 1, 3, 1.0), ("small_batched", 3, 7, 1.0),
                                         # 40, 60 and 128 head rows: N = 48, 64 and 128 columns (128

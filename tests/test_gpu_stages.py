@@ -495,6 +495,53 @@ def test_verify_chain(ds, name, B, T, mode):
         assert acc_ref.mean() > 0.5 * cfg.gamma           # the accept path is exercised
 
 
+@pytest.mark.parametrize("gamma", [1, 32])
+def test_verify_chain_gamma_limits(ds, gamma):
+    # the fewest and the most draft positions the chain verifier takes; with target rows that
+    # agree with the draft the accept path runs to the end (bonus draw from row gamma + 1)
+    cfg = wl.config("tiny").with_(name=f"tiny_gamma{gamma}", gamma=gamma, budget=tuple([8] * gamma))
+    inp = wl.chain_inputs(cfg, 0, with_head=False)
+    inp["W"] = gu._lm_head(cfg.V, cfg.d, inp["seed"])[0]
+    rows = _chain_oracle(inp, 1, cfg.T)
+    aligned = inp["z"][:1].copy()
+    for t in range(gamma):
+        aligned[0, t] = -60.0
+        aligned[0, t, rows[0][t]["S"]] = rows[0][t]["logits"].astype(np.float32)
+    rng = np.random.default_rng(gamma)
+    longest = 0
+    for z in (inp["z"][:1].copy(), aligned):
+        u = inp["u"][:1].copy()
+        for trial in range(4):
+            acc, acc_ref, _ = _check_chain_verify(ds, inp, rows, z, u, cfg.T)
+            longest = max(longest, int(acc_ref.max()))
+            u = wl.open_uniforms(rng, u.shape)
+    assert longest >= min(gamma, 8)
+
+
+def test_verify_tree_size_limits(ds):
+    # the widest and deepest tree the walk takes: 32 depths of 64 nodes (64 children at the root)
+    cfg = wl.config("tiny_tree")
+    B, D, Wd, V, M = 1, 32, 64, cfg.V, cfg.M
+    N = D * Wd
+    csr_off, csr_tok = wl.cluster_partition(cfg, 0)
+    parent = wl.tree_parents(D, Wd)
+    rng = np.random.default_rng(13)
+    ids = [np.sort(np.stack([rng.choice(M, 6, replace=False) for _ in range(B)]), axis=1) for k in range(D)]
+    S = [[oracle.shortlist(csr_off, csr_tok, ids[k][b]) for k in range(D)] for b in range(B)]
+    qfp = [[(rng.standard_normal(S[b][n // Wd].size) * 2.0).astype(np.float32) for n in range(N)]
+           for b in range(B)]
+    didx = np.array([[int(np.argmax(qfp[b][n])) for n in range(N)] for b in range(B)])
+    u_node = rng.random((B, N)).astype(np.float32)
+    u_res = rng.random((B, D + 1)).astype(np.float32)
+    z0 = (rng.standard_normal((B, 1 + N, V)) * 2.0).astype(np.float32)
+    for mode in ("independent", "aligned"):
+        z = z0 if mode == "independent" else _align_targets(z0, parent, S, qfp, D, Wd)
+        acc_ref = _run_tree_verify(ds, V, M, csr_off, csr_tok, parent, D, Wd, ids, S, qfp, didx, z,
+                                   u_node, u_res, cfg.T, with_stats=True)
+        if mode == "aligned":
+            assert acc_ref.sum() >= 4
+
+
 def _run_tree_verify(ds, V, M, csr_off, csr_tok, parent, D, Wd, ids, S, qfp, didx, z, u_node, u_res, T,
                      with_stats):
     """GPU tree verification on host-built draft data against the oracle's.  ids[k] [B, k_c]

@@ -254,7 +254,9 @@ struct UnionEp {
 
 // Softmax statistics and the draft draw of every head row from its stored logits.
 // grid (chunks, R): block (x, r) folds elements [x*kRsChunk, ...) of row r; the last block of the
-// row combines the partials in a fixed order.
+// row combines the partials in a fixed order.  The grid is sized for the longest possible list
+// (V); blocks past the end of their row's list leave at once and take no part in the fold
+// (block 0 stays for an empty list).
 constexpr int kRsPer = 16;
 constexpr int kRsChunk = 256 * kRsPer;
 
@@ -265,6 +267,8 @@ head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *_
     const int r = blockIdx.y, b = r / G, gi = r - b * G;
     const int off = a.vs_offsets[b];
     const int n = a.vs_offsets[b + 1] - off;
+    const int nblk = n > 0 ? min((n + kRsChunk - 1) / kRsChunk, int(gridDim.x)) : 1;
+    if (int(blockIdx.x) >= nblk) return;                   // uniform over the block
     const float *l = a.logits + int64_t(off) * G + int64_t(gi) * n;
     const int32_t *ids = a.vs_ids + off;
     Stat st = stat_empty();
@@ -294,10 +298,10 @@ head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *_
         for (int w = 1; w < 8; ++w) c = stat_merge(c, ws[w]);
         st_stat(&partials[size_t(r) * kGvMaxBlocks + blockIdx.x], c);
     }
-    if (!last_block_done(&counters[r], gridDim.x)) return;
+    if (!last_block_done(&counters[r], unsigned(nblk))) return;
     if (warp != 0) return;
     Stat c = stat_empty();
-    for (int i = lane; i < int(gridDim.x); i += 32) c = stat_merge(c, ld_stat(&partials[size_t(r) * kGvMaxBlocks + i]));
+    for (int i = lane; i < nblk; i += 32) c = stat_merge(c, ld_stat(&partials[size_t(r) * kGvMaxBlocks + i]));
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const Stat other = shfl_xor_stat(c, o);

@@ -155,7 +155,8 @@ ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *csr_tok, int
  *                          Philox4x32-10 (key = seed, counter = (v >> 2, pos, r, 0), word v & 3,
  *                          u = (2 (w >> 9) + 1) 2^-24).  Ties go to the lower token id.  An
  *                          empty list gives token = token_idx = -1.
- * Limits: d % 8 == 0, d <= 16384, B*G <= 128 (union path) and G == 1 (per-row path).
+ * Limits: d % 8 == 0, d <= 16384; union path: B*G <= 128 and V <= 2^20; per-row path: G == 1
+ *   and B*G <= 65535.  Larger calls return DS_ERR_UNSUPPORTED and launch nothing.
  * ws: ds_head_workspace_bytes(B*G) bytes; holds completion counters (zero it once).
  * ------------------------------------------------------------------------------------- */
 size_t ds_head_workspace_bytes(int rows);

@@ -89,6 +89,13 @@ def test_host_argument_checks(lib):
     assert lib.ds_gathered_head(*a) == 2
     a = list(args); a[23] = 16
     assert lib.ds_gathered_head(*a) == 4
+    # union path: more than 128 head rows, or a vocabulary above 2^20, is unsupported
+    union = list(args); union[8] = FAKE; union[9] = 32; union[10] = FAKE
+    union[11] = FAKE; union[12] = FAKE; union[13] = FAKE; union[23] = 1 << 30
+    a = list(union); a[1] = 8; a[2] = 17
+    assert lib.ds_gathered_head(*a) == 2
+    a = list(union); a[4] = (1 << 20) + 1
+    assert lib.ds_gathered_head(*a) == 2
     # verify: gamma beyond the limit; NULL uniforms
     assert lib.ds_verify(FAKE, 1, 40, 4096, 1.0, FAKE, 4096, None, None, FAKE, FAKE, 32, FAKE, FAKE, FAKE, FAKE,
                          FAKE, FAKE, FAKE, 1 << 24, None, None) == 1

@@ -273,7 +273,7 @@ verify_stats_kernel(ChainArgs a)
     }
 }
 
-// Residual weight of token v at target row tr: max(0, p - q) at a rejection (tr < gamma),
+// What the residual weights of target row tr need: max(0, p - q) at a rejection (tr < gamma),
 // p itself for the bonus draw (tr == gamma).
 struct ResidualRow {
     const float *z;            // target logits of row tr
@@ -282,18 +282,6 @@ struct ResidualRow {
     const int32_t *cposb;      // cpos of list (tr, b)
     float qm, qs;
 };
-
-__device__ __forceinline__ void residual_weight(const ChainArgs &a, const ResidualRow &rr, int v,
-                                                float &r, float &p)
-{
-    p = __expf(rr.z[v] * a.inv_te - rr.pm) / rr.ps;
-    float q = 0.f;
-    if (rr.ql) {
-        const int pc = rr.cposb[a.cluster_of[v]];
-        if (pc >= 0) q = __expf(rr.ql[pc + a.rank[v]] * a.inv_te - rr.qm) / rr.qs;
-    }
-    r = fmaxf(p - q, 0.f);
-}
 
 __device__ ResidualRow residual_row(const ChainArgs &a, int b, int tr)
 {
@@ -320,10 +308,15 @@ __device__ ResidualRow residual_row(const ChainArgs &a, int b, int tr)
 // scanned in thread order and the thread whose run crosses walks it -- then scan that chunk
 // the same way.  Weights without mass fall back to p.  The draw is the smallest v whose
 // cumulative weight exceeds the target; if rounding leaves none, the last v with weight.
-// wf(v, r, p) gives both weights of token v.
-template <int kRPer, class WF>
-__device__ void icdf_draw(WF wf, int V, int nrch, float u, float *__restrict__ rsum, float *__restrict__ psum,
-                          unsigned *counter, int32_t *out)
+// The policy P gives both weights of token v in two steps: load(v) issues the loads that need
+// nothing else (target logit, cluster, rank), weights(raw, r, p) finishes them.  With
+// P::kStaged, stage() fills the list's cluster positions into shared memory while the first
+// loads are in flight and weights() looks them up there instead of in a third round of global
+// loads (fewer dependent round trips, at the price of holding the first loads across a
+// barrier: it pays when the grid is small, not on wide batched grids).
+template <int kRPer, class P>
+__device__ void icdf_draw(const P &pol, int V, int nrch, float u, float *__restrict__ rsum,
+                          float *__restrict__ psum, unsigned *counter, int32_t *out)
 {
     __shared__ float scratch[kVThreads / 32];
     __shared__ float sbuf[kVThreads + 1];
@@ -334,10 +327,26 @@ __device__ void icdf_draw(WF wf, int V, int nrch, float u, float *__restrict__ r
     constexpr int kRChunk = kVThreads * kRPer;
     const int base = c * kRChunk + threadIdx.x * kRPer;
     float rs = 0.f, ps = 0.f;
+    if constexpr (P::kStaged) {
+        typename P::Raw raw[kRPer];
 #pragma unroll
-    for (int i = 0; i < kRPer; ++i) {
-        const int v = base + i;
-        if (v < V) { float r, p; wf(v, r, p); rs += r; ps += p; }
+        for (int i = 0; i < kRPer; ++i) {
+            const int v = base + i;
+            if (v < V) raw[i] = pol.load(v);
+        }
+        pol.stage();
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kRPer; ++i) {
+            const int v = base + i;
+            if (v < V) { float r, p; pol.weights(raw[i], r, p); rs += r; ps += p; }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kRPer; ++i) {
+            const int v = base + i;
+            if (v < V) { float r, p; pol.weights(pol.load(v), r, p); rs += r; ps += p; }
+        }
     }
     rs = block_sum(rs, scratch);
     ps = block_sum(ps, scratch);
@@ -395,7 +404,7 @@ __device__ void icdf_draw(WF wf, int V, int nrch, float u, float *__restrict__ r
     for (int i = 0; i < kRPer; ++i) {
         const int v = lo + i;
         float r = 0.f, p = 0.f;
-        if (v < V) wf(v, r, p);
+        if (v < V) pol.weights(pol.load(v), r, p);     // a staged table is still in place
         wv[i] = s_use_p ? p : r;
         seg += wv[i];
     }
@@ -423,16 +432,50 @@ __device__ void icdf_draw(WF wf, int V, int nrch, float u, float *__restrict__ r
     if (threadIdx.x == 0 && s_hit == 0x7FFFFFFF) *out = s_last;   // target beyond the chunk
 }
 
-template <int kRPer>
+// The residual weights of row tr of a chain (max(0, p - q), or p for the bonus row); with
+// kStage the list's cluster positions are staged in shared memory (dynamic, M ints).
+template <bool kStage>
+struct ChainResidual {
+    static constexpr bool kStaged = kStage;
+    const ChainArgs *a;
+    ResidualRow rr;
+    int *s_cp;
+    struct Raw { float z; int c, rk; };
+    __device__ Raw load(int v) const
+    {
+        Raw x;
+        x.z = rr.z[v];
+        x.c = rr.ql ? a->cluster_of[v] : -1;
+        x.rk = rr.ql ? a->rank[v] : 0;
+        return x;
+    }
+    __device__ void stage() const
+    {
+        if (rr.ql)
+            for (int c = threadIdx.x; c < a->M; c += blockDim.x) s_cp[c] = rr.cposb[c];
+    }
+    __device__ void weights(const Raw &x, float &r, float &p) const
+    {
+        p = __expf(x.z * a->inv_te - rr.pm) / rr.ps;
+        float q = 0.f;
+        if (rr.ql && unsigned(x.c) < unsigned(a->M)) {
+            const int pc = kStage ? s_cp[x.c] : rr.cposb[x.c];
+            if (pc >= 0) q = __expf(rr.ql[pc + x.rk] * a->inv_te - rr.qm) / rr.qs;
+        }
+        r = fmaxf(p - q, 0.f);
+    }
+};
+
+template <int kRPer, bool kStage>
 __global__ void __launch_bounds__(kVThreads)
 verify_residual_kernel(ChainArgs a)
 {
+    extern __shared__ int s_cp[];                    // M entries when staged
     const int b = blockIdx.y;
     const int tr = __ldcg(&a.decision[b]);
     if (tr < 0) return;                              // greedy: decided already (whole group returns)
-    const ResidualRow rr = residual_row(a, b, tr);
-    auto wf = [&](int v, float &r, float &p) { residual_weight(a, rr, v, r, p); };
-    icdf_draw<kRPer>(wf, a.V, a.nrch, a.u[size_t(b) * (a.gamma + 1) + a.gamma], a.rsum + size_t(b) * a.nrch,
+    const ChainResidual<kStage> pol{&a, residual_row(a, b, tr), s_cp};
+    icdf_draw<kRPer>(pol, a.V, a.nrch, a.u[size_t(b) * (a.gamma + 1) + a.gamma], a.rsum + size_t(b) * a.nrch,
               a.psum + size_t(b) * a.nrch, &a.cnt2[b], &a.correction[b]);
 }
 
@@ -816,6 +859,41 @@ tree_walk_kernel(TreeArgs a)
     cl.sync();                                   // no CTA leaves while others may read its slots
 }
 
+// The weights of the tree's correction draw: the walk's residual r (on the list; p off it), or
+// p of the final row; the list's cluster positions staged in shared memory (dynamic, M ints).
+struct TreeResidual {
+    static constexpr bool kStaged = true;
+    const TreeArgs *a;
+    const float *z, *r;
+    const int32_t *cp;
+    float m, s;
+    bool resid;
+    int *s_cp;
+    struct Raw { float z; int c, rk; };
+    __device__ Raw load(int v) const
+    {
+        Raw x;
+        x.z = z[v];
+        x.c = resid ? a->cluster_of[v] : -1;
+        x.rk = resid ? a->rank[v] : 0;
+        return x;
+    }
+    __device__ void stage() const
+    {
+        if (resid)
+            for (int c = threadIdx.x; c < a->M; c += blockDim.x) s_cp[c] = cp[c];
+    }
+    __device__ void weights(const Raw &x, float &w, float &p) const
+    {
+        p = __expf(x.z * a->inv_te - m) / s;
+        w = p;
+        if (resid) {
+            const int pc = unsigned(x.c) < unsigned(a->M) ? s_cp[x.c] : -1;
+            if (pc >= 0) { const int j = pc + x.rk; w = unsigned(j) < unsigned(a->V) ? r[j] : 0.f; }
+        }
+    }
+};
+
 template <int kRPer>
 __global__ void __launch_bounds__(kVThreads)
 tree_residual_kernel(TreeArgs a)
@@ -823,20 +901,17 @@ tree_residual_kernel(TreeArgs a)
     const int b = blockIdx.y;
     const WalkState ws = a.state[b];              // written by the previous launch
     if (ws.mode == 0) return;                     // whole group returns
-    const float *z = a.p_logits + (size_t(b) * (1 + a.N) + ws.row) * a.V;
-    const float *r = a.rbuf + (size_t(b) * 2 + ws.buf) * a.V;
-    const int32_t *cp = a.cpos + (size_t(ws.dep) * a.B + b) * a.M;
-    const bool resid = ws.mode == 2;
-    auto wf = [&](int v, float &w, float &p) {
-        p = __expf(z[v] * a.inv_te - ws.m) / ws.s;
-        w = p;
-        if (resid) {
-            const int c = a.cluster_of[v];
-            const int pc = unsigned(c) < unsigned(a.M) ? cp[c] : -1;
-            if (pc >= 0) { const int j = pc + a.rank[v]; w = unsigned(j) < unsigned(a.V) ? r[j] : 0.f; }
-        }
-    };
-    icdf_draw<kRPer>(wf, a.V, a.nrch, a.u_res[size_t(b) * (a.D + 1) + ws.dep], a.rsum + size_t(b) * a.nrch,
+    extern __shared__ int s_cp[];                 // M entries
+    TreeResidual pol;
+    pol.a = &a;
+    pol.z = a.p_logits + (size_t(b) * (1 + a.N) + ws.row) * a.V;
+    pol.r = a.rbuf + (size_t(b) * 2 + ws.buf) * a.V;
+    pol.cp = a.cpos + (size_t(ws.dep) * a.B + b) * a.M;
+    pol.m = ws.m;
+    pol.s = ws.s;
+    pol.resid = ws.mode == 2;
+    pol.s_cp = s_cp;
+    icdf_draw<kRPer>(pol, a.V, a.nrch, a.u_res[size_t(b) * (a.D + 1) + ws.dep], a.rsum + size_t(b) * a.nrch,
               a.psum + size_t(b) * a.nrch, &a.cnt[b], &a.correction[b]);
 }
 
@@ -925,8 +1000,10 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     if (vbig) verify_stats_kernel<kVPerBig><<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
     else verify_stats_kernel<kVPerSmall><<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
     DS_TRY_LAUNCH();
-    if (rbig) verify_residual_kernel<kRPerBig><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
-    else verify_residual_kernel<kRPerSmall><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
+    // the small-chunk grid (few sequences) stages the list's cluster positions in shared memory
+    const size_t cp_smem = size_t(M) * sizeof(int);   // M <= 8192
+    if (rbig) verify_residual_kernel<kRPerBig, false><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
+    else verify_residual_kernel<kRPerSmall, true><<<dim3(a.nrch, B), kVThreads, cp_smem, stream>>>(a);
     DS_TRY_LAUNCH();
     return DS_OK;
 }
@@ -998,8 +1075,9 @@ extern "C" ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, tree_walk_kernel, a) != cudaSuccess) { (void)cudaGetLastError(); return DS_ERR_CUDA; }
-    if (rbig) tree_residual_kernel<kRPerBig><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
-    else tree_residual_kernel<kRPerSmall><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
+    const size_t cp_smem = size_t(M) * sizeof(int);   // the list's cluster positions (M <= 8192)
+    if (rbig) tree_residual_kernel<kRPerBig><<<dim3(a.nrch, B), kVThreads, cp_smem, stream>>>(a);
+    else tree_residual_kernel<kRPerSmall><<<dim3(a.nrch, B), kVThreads, cp_smem, stream>>>(a);
     DS_TRY_LAUNCH();
     return DS_OK;
 }

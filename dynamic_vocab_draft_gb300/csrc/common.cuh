@@ -3,6 +3,7 @@
 // algebra every head and verify reduction uses.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cfloat>
 #include <cuda_runtime.h>
@@ -251,4 +252,21 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity)
 namespace ds {
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per device
+// (the attribute belongs to the device, so a process driving several GPUs sets it on each).
+// `done` holds one bit per device already set; concurrent first calls may both set it, which is
+// harmless.  False if the device cannot be named or the call fails.
+template <class K>
+inline bool smem_limit_once(K kernel, size_t bytes, std::atomic<unsigned long long> &done)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    const unsigned long long bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)) != cudaSuccess)
+        return false;
+    done.fetch_or(bit, std::memory_order_release);
+    return true;
+}
 }  // namespace ds

@@ -391,13 +391,8 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
         if (gx < 1) gx = 1;
         if (gx > kGvMaxBlocks) gx = kGvMaxBlocks;
         const size_t smem = size_t(d) * sizeof(uint16_t);
-        static bool attr_set = false;
-        if (!attr_set) {
-            if (cudaFuncSetAttribute(head_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     int(kGvMaxD * sizeof(float))) != cudaSuccess)
-                return DS_ERR_CUDA;
-            attr_set = true;
-        }
+        static std::atomic<unsigned long long> smem_set{0};
+        if (!smem_limit_once(head_gemv_kernel, kGvMaxD * sizeof(float), smem_set)) return DS_ERR_CUDA;
         head_gemv_kernel<<<dim3(gx, B), kGvWarps * 32, smem, stream>>>(a, partials, counters);
         DS_TRY_LAUNCH();
         return DS_OK;

@@ -390,13 +390,9 @@ ds_status launch_gemv(const uint16_t *A, int N, int K, const XT *x, int B, const
                       float *y, int topk_k, int32_t *topk_ids, unsigned *counters, cudaStream_t stream)
 {
     const size_t smem = size_t(BT) * K * sizeof(float);
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(gemv_rows_kernel<XT, BT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(size_t(BT) * kRouterMaxK * sizeof(float))) != cudaSuccess)
-            return DS_ERR_CUDA;
-        attr = true;
-    }
+    static std::atomic<unsigned long long> smem_set{0};
+    if (!smem_limit_once(gemv_rows_kernel<XT, BT>, size_t(BT) * kRouterMaxK * sizeof(float), smem_set))
+        return DS_ERR_CUDA;
     dim3 grid((N + kGemvWarps - 1) / kGemvWarps, (B + BT - 1) / BT);
     gemv_rows_kernel<XT, BT><<<grid, kGemvWarps * 32, smem, stream>>>(A, N, K, x, B, bias, act, y,
                                                                        topk_k, topk_ids, counters);

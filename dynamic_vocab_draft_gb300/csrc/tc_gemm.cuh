@@ -420,19 +420,14 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
     ep.finish(est);
 }
 
-// Host: launch gemm_kernel<MT, Ep> on `grid` CTAs (sets the shared-memory attribute once per
-// instantiation).  `parts` holds parts_bytes(R, grid) bytes; `tile_cnt` one zeroed counter per
+// Host: launch gemm_kernel<MT, Ep> on `grid` CTAs (sets the shared-memory limit once per
+// instantiation and device).  `parts` holds parts_bytes(R, grid) bytes; `tile_cnt` one zeroed counter per
 // tile (left zero).
 template <int MT, class Ep>
 ds_status launch(const Operands &op, const Ep &ep, float *parts, unsigned *tile_cnt, int grid, cudaStream_t stream)
 {
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(gemm_kernel<MT, Ep>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(Cfg<MT>::kSmem)) != cudaSuccess)
-            return DS_ERR_CUDA;
-        attr = true;
-    }
+    static std::atomic<unsigned long long> smem_set{0};
+    if (!smem_limit_once(gemm_kernel<MT, Ep>, Cfg<MT>::kSmem, smem_set)) return DS_ERR_CUDA;
     gemm_kernel<MT, Ep><<<grid, kThreads, Cfg<MT>::kSmem, stream>>>(op, ep, parts, tile_cnt);
     DS_TRY_LAUNCH();
     return DS_OK;

@@ -119,3 +119,14 @@ def test_host_argument_checks(lib):
     assert lib.ds_copy(FAKE, ctypes.c_void_p(0x10008), 16, None) == 1
     assert lib.ds_copy(ctypes.c_void_p(0x10008), FAKE, 16, None) == 1
     assert lib.ds_copy(FAKE, FAKE, 0, None) == 0
+
+
+def test_copy_binding_refuses_pageable_host_memory():
+    # ds_copy reaches host memory from a kernel, so the binding takes CUDA tensors or pinned
+    # host tensors only; a pageable tensor is refused before the library is called
+    torch = pytest.importorskip("torch")
+    from dynamic_vocab_draft_gb300 import api
+    with pytest.raises(ValueError):
+        api.copy(torch.zeros(16, dtype=torch.uint8), torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        api.copy(torch.zeros(16, dtype=torch.uint8)[::2], torch.zeros(8, dtype=torch.uint8))

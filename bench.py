@@ -47,6 +47,9 @@ def parse_args():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only the --config workload (by default the llama_b1 run also "
+                         "measures the batched, tree and large workloads, key per_config)")
     return ap.parse_args()
 
 
@@ -139,9 +142,10 @@ def run_reference(args):
         sample = f"{n} whole tree steps of sequence 0 ({cfg.gamma * cfg.width} nodes each + verification), {dt:.1f} s"
         ms_per_step = 1e3 * dt / n * cfg.B
     cores = oracle.get_threads()
+    # the same workload description as the GPU arm's line (the L2 flush it names is the GPU
+    # arm's timing rule; the oracle runs on the host cores)
     cfgd = workload_config(cfg)
     cfgd["seed"] = args.seed
-    cfgd["l2"] = "n/a (host)"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": n, "warmup": warm, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -240,7 +244,21 @@ def committed_traffic():
         return None
 
 
-def build_drafter(cfg, inp, dev, pkg, torch):
+_HEAD_CACHE = {}
+
+
+def device_head(cfg, seed, dev, torch):
+    """The LM head W [V, d] on the device; workloads with the same (V, d, seed) share one copy."""
+    import workloads as wl
+    key = (cfg.V, cfg.d, seed)
+    if key not in _HEAD_CACHE:
+        _HEAD_CACHE.clear()                      # keep one head resident at a time
+        W = wl.lm_head(cfg, seed)
+        _HEAD_CACHE[key] = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
+    return _HEAD_CACHE[key]
+
+
+def build_drafter(cfg, inp, dev, pkg, torch, W):
     """Drafter + pinned host copies of the per-step inputs (name -> (host, device buffer))."""
     def bf(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
@@ -248,7 +266,7 @@ def build_drafter(cfg, inp, dev, pkg, torch):
     def pinned_bf(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
 
-    common = (bf(inp["W"]), bf(inp["W1"]), bf(inp["b1"]), bf(inp["W2"]), bf(inp["b2"]),
+    common = (W, bf(inp["W1"]), bf(inp["b1"]), bf(inp["W2"]), bf(inp["b2"]),
               torch.as_tensor(inp["csr_off"]), torch.as_tensor(inp["csr_tok"]))
     if cfg.mode == "chain":
         d = pkg.pipeline.ChainDrafter(*common, B=cfg.B, gamma=cfg.gamma, budget=cfg.budget, act=cfg.act,
@@ -293,6 +311,139 @@ def algorithmic_bytes(cfg, d):
     return heads, float(sum(heads) + n_pos * router + verify), (union.tolist() if union is not None else None), sizes
 
 
+class Flusher:
+    """Evicts the previous step's inputs from the 129 MB L2 before every timed step: a 512 MB
+    write, then a 256 MB read so the written lines leave L2 too (no dirty line left for the
+    step to write back)."""
+
+    def __init__(self, dev, torch):
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.clean = torch.zeros(L2_CLEAN_BYTES // 4, dtype=torch.int32, device=dev)
+        self.sink = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def __call__(self, i):
+        self.flush.fill_(i & 0xFF)
+        self.sink.copy_(self.clean.sum())
+
+
+def measure(cfg, seed, dev, pkg, torch, world, local_rank, steps, warmup, e2e_steps, head_steps, flush):
+    """Time `steps` whole steps of workload cfg (device-resident inputs), then the per-head times
+    from the instrumented graph, then `e2e_steps` steps with their host transfers.  Returns the
+    measured figures and the inputs (for the oracle baseline)."""
+    import workloads as wl
+    inp = (wl.chain_inputs(cfg, seed, with_head=False) if cfg.mode == "chain"
+           else wl.tree_inputs(cfg, seed, with_head=False))
+    W = device_head(cfg, seed, dev, torch)
+    d, host, tokens_per_step = build_drafter(cfg, inp, dev, pkg, torch, W)
+    d.enable_head_timing()
+    d.capture()
+    main = torch.cuda.current_stream(dev)
+    for _ in range(max(3, warmup)):
+        flush(1)
+        d.replay()
+    torch.cuda.synchronize()
+    d.check_status()
+
+    K = steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush(i)
+        starts[i].record(main)
+        d.replay()
+        ends[i].record(main)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(step_ms), dev)
+    d.check_status()
+    value = whole_job_rate(world, tokens_per_step, K, total_ms)
+    # per-head launch times and the step's breakdown, from the instrumented graph (same step
+    # plus event records around every head), replayed after the timed region
+    head_ms, breakdown = [], []
+    for i in range(max(1, min(K, head_steps))):
+        flush(i)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(main)
+        d.replay(timed=True)
+        s1.record(main)
+        torch.cuda.synchronize()
+        head_ms.append(d.head_times_ms())
+        h0, hl = d.head_events[0][0], d.head_events[-1][1]
+        breakdown.append((s0.elapsed_time(h0), h0.elapsed_time(hl), hl.elapsed_time(s1)))
+
+    # e2e through the public API: every step copies its inputs from pinned host memory (the
+    # ones only verification reads on a copy stream beside the drafting stages) and its
+    # results (accepted lengths, corrections, draft tokens) back to pinned host memory
+    Ke = max(1, min(K, e2e_steps))
+    out_h = torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
+    late_names = ("z", "u", "u_node", "u_res")
+    d.capture_io([v for k, v in host.items() if k not in late_names],
+                 [v for k, v in host.items() if k in late_names], out_h)
+    for _ in range(max(3, warmup)):             # untimed, like the device leg's warm-up
+        flush(1)
+        d.replay_io()
+    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    for i in range(Ke):
+        flush(i)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(main)
+        d.replay_io()
+        e.record(main)
+        e.synchronize()
+        e2e_ms += s.elapsed_time(e)
+    d.check_status()
+    h2d = sum(h.numel() * h.element_size() for h, _ in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_value = whole_job_rate(world, tokens_per_step, Ke, e2e_ms)
+
+    peak, peak_src = load_peak()
+    hm = np.array(head_ms)                               # [samples, positions] ms
+    head_bytes, step_bytes, union, sizes = algorithmic_bytes(cfg, d)
+    per_row = cfg.mode == "chain" and cfg.B == 1
+    achieved = float(sum(head_bytes) / (hm.mean(axis=0).sum() * 1e-3) / 1e9)
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": committed_traffic() if per_row and cfg.name == "llama_b1" else None,
+            "kernel": ("head_gemv_kernel (gathered head, per-row path: one warp per W row, 8 KB in flight)"
+                       if per_row else "tc::gemm_kernel<MT, UnionEp> + head_rowstats_kernel (gathered head "
+                       "over the union of the lists on tcgen05, then the row statistics and draws)"),
+            "algorithmic_bytes_per_launch": float(np.mean(head_bytes)),
+            "avg_launch_us": float(hm.mean() * 1e3), "peak_source": peak_src,
+            "shortlist_sizes": sizes.sum(axis=1).tolist(), "union_rows": union}
+    step_us = total_ms / K * 1e3
+    res = dict(
+        cfg=cfg, inp=inp, value=value, total_ms=total_ms, K=K, tokens_per_step=tokens_per_step, roofline=roof,
+        step_roofline={"algorithmic_bytes": step_bytes, "achieved_gbs": step_bytes / (step_us * 1e-6) / 1e9,
+                       "frac": step_bytes / (step_us * 1e-6) / 1e9 / peak},
+        e2e={"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+             "steps": Ke, "ms_per_step": e2e_ms / Ke},
+        breakdown_us={
+            "before_first_head": 1e3 * float(np.median([x[0] for x in breakdown])),
+            "heads_span": 1e3 * float(np.median([x[1] for x in breakdown])),
+            "heads_busy": 1e3 * float(np.median(hm.sum(axis=1))),
+            "after_last_head (verify)": 1e3 * float(np.median([x[2] for x in breakdown])),
+            "per_position_head": [1e3 * float(x) for x in np.median(hm, axis=0)]},
+        gpu_launches=d.launches_per_step() * K, clocks=clk, wall_s=t_wall,
+        step_ms_p50=float(np.median(step_ms)), step_ms_min=float(np.min(step_ms)))
+    del d, host
+    return res
+
+
+# Workloads measured after the headline, in the same process (same flush and timing).
+PER_CONFIG = ["batched", "tree", "large_b1_f5", "large_b64_f100"]
+
+
 def run_ours(args):
     import torch
     import workloads as wl
@@ -307,112 +458,62 @@ def run_ours(args):
     pkg.load_library()
     cfg = wl.config(args.config)
     seed = args.seed + rank                      # each replica drafts its own sequences
-    inp = wl.chain_inputs(cfg, seed) if cfg.mode == "chain" else wl.tree_inputs(cfg, seed)
-    d, host, tokens_per_step = build_drafter(cfg, inp, dev, pkg, torch)
-    d.enable_head_timing()
-    d.capture()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    clean = torch.zeros(L2_CLEAN_BYTES // 4, dtype=torch.int32, device=dev)
-    sink = torch.zeros((), dtype=torch.int64, device=dev)
-    main = torch.cuda.current_stream(dev)
+    flush = Flusher(dev, torch)
+    r = measure(cfg, seed, dev, pkg, torch, world, local_rank, args.steps, args.warmup, args.e2e_steps,
+                TIMED_HEAD_STEPS, flush)
+    inp = r.pop("inp")
 
-    def l2_flush(i):
-        flush.fill_(i & 0xFF)                    # evicts every input of the previous step
-        sink.copy_(clean.sum())                  # evicts the dirty lines the write left behind
-
-    for _ in range(max(3, args.warmup)):
-        l2_flush(1)
-        d.replay()
-    torch.cuda.synchronize()
-    d.check_status()
-
-    K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    head_ms = []
-    breakdown = []                           # (router before the first head, heads span, verify) ms
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    t_wall = time.perf_counter()
-    for i in range(K):
-        l2_flush(i)
-        starts[i].record(main)
-        d.replay()
-        ends[i].record(main)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
-    # per-head launch times and the step's breakdown, from the instrumented graph (same step
-    # plus event records around every head), replayed after the timed region
-    for i in range(min(K, TIMED_HEAD_STEPS)):
-        l2_flush(i)
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(main)
-        d.replay(timed=True)
-        s1.record(main)
-        torch.cuda.synchronize()
-        head_ms.append(d.head_times_ms())
-        h0, hl = d.head_events[0][0], d.head_events[-1][1]
-        breakdown.append((s0.elapsed_time(h0), h0.elapsed_time(hl), hl.elapsed_time(s1)))
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = max_over_ranks(sum(step_ms), dev)
-    d.check_status()
-    value = whole_job_rate(world, tokens_per_step, K, total_ms)
-
-    # e2e through the public API: every step copies its inputs from pinned host memory (the
-    # ones only verification reads on a copy stream beside the drafting stages) and its
-    # results (accepted lengths, corrections, draft tokens) back to pinned host memory
-    Ke = min(K, args.e2e_steps)
-    out_h = torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
-    late_names = ("z", "u", "u_node", "u_res")
-    d.capture_io([v for k, v in host.items() if k not in late_names],
-                 [v for k, v in host.items() if k in late_names], out_h)
-    for _ in range(max(3, args.warmup)):         # untimed, like the device leg's warm-up
-        l2_flush(1)
-        d.replay_io()
-    torch.cuda.synchronize()
-    e2e_ms = 0.0
-    for i in range(Ke):
-        l2_flush(i)
-        s = torch.cuda.Event(enable_timing=True)
-        e = torch.cuda.Event(enable_timing=True)
-        s.record(main)
-        d.replay_io()
-        e.record(main)
-        e.synchronize()
-        e2e_ms += s.elapsed_time(e)
-    d.check_status()
-    h2d = sum(h.numel() * h.element_size() for h, _ in host.values())
-    d2h = out_h.numel() * out_h.element_size()
-    e2e_ms = max_over_ranks(e2e_ms, dev)
-    e2e_value = whole_job_rate(world, tokens_per_step, Ke, e2e_ms)
-
-    # roofline of the dominant kernel: the gathered head (algorithmic bytes per launch)
-    peak, peak_src = load_peak()
-    hm = np.array(head_ms)                               # [samples, positions] ms
-    head_bytes, step_bytes, union, sizes = algorithmic_bytes(cfg, d)
-    per_row = cfg.mode == "chain" and cfg.B == 1
-    achieved = float(sum(head_bytes) / (hm.mean(axis=0).sum() * 1e-3) / 1e9)
-    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": committed_traffic() if per_row and cfg.name == "llama_b1" else None,
-            "kernel": ("head_gemv_kernel (gathered head, per-row path: one warp per W row, 8 KB in flight)"
-                       if per_row else "tc::gemm_kernel<MT, UnionEp> + head_rowstats_kernel (gathered head "
-                       "over the union of the lists on tcgen05, then the row statistics and draws)"),
-            "algorithmic_bytes_per_launch": float(np.mean(head_bytes)),
-            "avg_launch_us": float(hm.mean() * 1e3), "peak_source": peak_src,
-            "shortlist_sizes": sizes.sum(axis=1).tolist(), "union_rows": union}
+    per_config = None
+    if args.config == "llama_b1" and not args.no_per_config:
+        per_config = {}
+        for name in PER_CONFIG:
+            torch.cuda.empty_cache()
+            c = wl.config(name)
+            q = measure(c, seed, dev, pkg, torch, world, local_rank, args.steps, args.warmup,
+                        args.e2e_steps, min(args.steps, 16), flush)
+            q.pop("inp")
+            unit = "nodes/s" if c.mode == "tree" else "tokens/s"
+            per_config[name] = {
+                "workload": workload_config(c)["workload"], "value": q["value"], "unit": unit,
+                "us_per_step": q["total_ms"] / q["K"] * 1e3, "steps": q["K"],
+                "head_frac": q["roofline"]["frac"], "head_us": q["roofline"]["avg_launch_us"],
+                "head_kernel": q["roofline"]["kernel"],
+                "step_frac": q["step_roofline"]["frac"], "step_algorithmic_bytes": q["step_roofline"]["algorithmic_bytes"],
+                "e2e": {"value": q["e2e"]["value"], "unit": unit, "ms_per_step": q["e2e"]["ms_per_step"],
+                        "h2d_bytes_per_step": q["e2e"]["h2d_bytes_per_step"],
+                        "d2h_bytes_per_step": q["e2e"]["d2h_bytes_per_step"]},
+                "breakdown_us": q["breakdown_us"], "clocks": q["clocks"], "gpu_launches": q["gpu_launches"]}
+        _HEAD_CACHE.clear()
 
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline:
-        import oracle
+        cpu = cpu_baseline(cfg, inp)
+    cfgd = workload_config(cfg)
+    cfgd["seed"] = args.seed
+    line = {"metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": r["K"],
+            "warmup": max(3, args.warmup), "ms_per_step": r["total_ms"] / r["K"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": cfgd, "roofline": r["roofline"], "step_roofline": r["step_roofline"],
+            "cpu_baseline": cpu, "e2e": r["e2e"], "breakdown_us": r["breakdown_us"],
+            "gpu_launches": r["gpu_launches"], "clocks": r["clocks"], "wall_s_timed_region": r["wall_s"],
+            "step_ms_p50": r["step_ms_p50"], "step_ms_min": r["step_ms_min"]}
+    if per_config is not None:
+        line["per_config"] = per_config
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(cfg, inp):
+    """The oracle on the host cores, on a bounded sample of the same workload: all cores (the
+    line's value) and one thread."""
+    import oracle
+    all_cores = oracle.get_threads()
+    out = {}
+    for threads, budget_s in ((all_cores, 12.0), (1, 8.0)):
+        oracle.set_threads(threads)
         if cfg.mode == "chain":
-            v, n, dt = oracle_sample(inp, budget_s=20.0, max_steps=10 ** 9, warmup=1)
+            v, n, dt = oracle_sample(inp, budget_s=budget_s, max_steps=10 ** 9, warmup=1)
             sample = (f"{n} oracle draft positions of sequence 0 of this workload "
                       f"(+ chain verification every {cfg.gamma}th), {dt:.1f} s")
         else:
@@ -421,30 +522,11 @@ def run_ours(args):
             dt = time.perf_counter() - t0
             v = cfg.gamma * cfg.width / dt
             sample = f"one whole tree step of sequence 0 ({cfg.gamma * cfg.width} nodes + tree verification), {dt:.1f} s"
-        cpu = {"value": v, "unit": UNIT, "cores": oracle.get_threads(), "kind": "oracle", "sample": sample}
-    cfgd = workload_config(cfg)
-    cfgd["seed"] = args.seed
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": max(3, args.warmup), "ms_per_step": total_ms / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": cfgd, "roofline": roof,
-            "step_roofline": {
-                "algorithmic_bytes": step_bytes, "achieved_gbs": step_bytes / (total_ms / K * 1e-3) / 1e9,
-                "frac": step_bytes / (total_ms / K * 1e-3) / 1e9 / peak},
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": Ke, "ms_per_step": e2e_ms / Ke},
-            "breakdown_us": {
-                "before_first_head": 1e3 * float(np.median([x[0] for x in breakdown])),
-                "heads_span": 1e3 * float(np.median([x[1] for x in breakdown])),
-                "heads_busy": 1e3 * float(np.median(hm.sum(axis=1))),
-                "after_last_head (verify)": 1e3 * float(np.median([x[2] for x in breakdown])),
-                "per_position_head": [1e3 * float(x) for x in np.median(hm, axis=0)]},
-            "gpu_launches": d.launches_per_step() * K,
-            "clocks": clk,
-            "wall_s_timed_region": t_wall,
-            "step_ms_p50": float(np.median(step_ms)), "step_ms_min": float(np.min(step_ms))}
-    print(json.dumps(line), flush=True)
+        out[threads] = (v, sample)
+    oracle.set_threads(all_cores)
+    v, sample = out[all_cores]
+    return {"value": v, "unit": UNIT, "cores": all_cores, "kind": "oracle", "sample": sample,
+            "single_thread": {"value": out[1][0], "unit": UNIT, "cores": 1, "sample": out[1][1]}}
 
 
 def main():

@@ -25,6 +25,10 @@ SIGNATURES = {
     "ds_vocab_index": (ST, [P, P, I, I, P, P, P, P]),
     "ds_router_workspace_bytes": (SZ, [I, I]),
     "ds_router_topk": (ST, [P, I, I, P, P, I, P, P, I, I, P, I, I, P, P, P, SZ, P, P]),
+    "ds_router_create": (ST, [P, P, P, P, P, I, I, I, I, P, I]),
+    "ds_router_destroy": (ST, [P]),
+    "ds_router_workspace_bytes_h": (SZ, [P, I]),
+    "ds_router_topk_h": (ST, [P, P, I, I, P, P, P, SZ, P, P]),
     "ds_shortlist_workspace_bytes": (SZ, [I, I]),
     "ds_build_shortlist": (ST, [P, P, I, I, P, I, I, P, P, I64, P, P, P, P, P, SZ, P, P]),
     "ds_head_workspace_bytes": (SZ, [I]),
@@ -37,6 +41,8 @@ SIGNATURES = {
     "ds_verify_tree_workspace_bytes": (SZ, [I, I, I, I]),
     "ds_verify_tree": (ST, [P, I, I, I, I, F, P, P, I64, P, P, P, P, I64, P, I, P, P, P, P, P,
                             P, P, P, P, SZ, P, P]),
+    "ds_workspace_bytes": (SZ, [I, I, I, I, I, I, I]),
+    "ds_set_wait_budget": (ST, [I64]),
     "ds_philox4x32_10": (ST, [P, U64, P, I, P]),
     "ds_event_record": (ST, [P, P]),
     "ds_copy": (ST, [P, P, SZ, P]),

@@ -63,6 +63,59 @@ def verify_tree_workspace_bytes(B, D, Wd, V):
     return int(_lib.load().ds_verify_tree_workspace_bytes(B, D, Wd, V))
 
 
+OP = {"router": 1, "shortlist": 2, "head": 3, "verify": 4, "verify_tree": 5}
+
+
+def workspace_bytes(op, B, V=0, M=0, gamma=0, hidden=0, width=0):
+    """ds_workspace_bytes: the workspace of call `op` (a name of OP) for the given sizes."""
+    return int(_lib.load().ds_workspace_bytes(OP[op], B, V, M, gamma, hidden, width))
+
+
+def set_wait_budget(cycles: int) -> None:
+    """ds_set_wait_budget: cycles a kernel's bounded pipeline wait may take (0 = default)."""
+    _lib.check(_lib.load().ds_set_wait_budget(int(cycles)), "ds_set_wait_budget")
+
+
+class Router:
+    """A router handle (ds_router_create): W1 [Hr, d], b1 [Hr], W2 [M, Hr], b2 [M] (CUDA
+    tensors that must outlive the handle), the activation and the per-position budget table."""
+
+    def __init__(self, W1, b1, W2, b2, act, budget):
+        import ctypes
+        self.Hr, self.d = W1.shape
+        self.M = W2.shape[0]
+        self._keep = (W1, b1, W2, b2)
+        bud = torch.as_tensor(list(budget), dtype=torch.int32).contiguous()
+        h = ctypes.c_void_p()
+        _lib.check(_lib.load().ds_router_create(
+            ctypes.byref(h), _ptr(W1, BF16, "W1"), _ptr(b1, BF16, "b1"), _ptr(W2, BF16, "W2"),
+            _ptr(b2, BF16, "b2"), self.d, self.Hr, self.M, ACT.get(act, act), bud.data_ptr(),
+            bud.numel()), "ds_router_create")
+        self.handle = h
+
+    def workspace_bytes(self, B):
+        return int(_lib.load().ds_router_workspace_bytes_h(self.handle, B))
+
+    def topk(self, H, pos, scores, cluster_ids, ws, status, stream=None):
+        """ds_router_topk_h for draft position `pos` (1-based); scores may be None."""
+        B = H.shape[0]
+        _lib.check(_lib.load().ds_router_topk_h(
+            self.handle, _ptr(H, BF16, "H"), B, int(pos), _ptr(scores, F32, "scores", True),
+            _ptr(cluster_ids, I32, "cluster_ids"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+            _ptr(status, I32, "status"), _stream(stream)), "ds_router_topk_h")
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _lib.load().ds_router_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 def vocab_index(csr_off, csr_tok, cluster_of, rank_in_cluster, status, stream=None):
     M = csr_off.numel() - 1
     V = csr_tok.numel()

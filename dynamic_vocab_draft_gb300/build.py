@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libdynaspec.so")
 SOURCES = ["api.cu", "router.cu", "shortlist.cu", "head.cu", "verify.cu"]
-HEADERS = ["common.cuh", "block_scan.cuh"]
+HEADERS = ["common.cuh", "block_scan.cuh", "tc_gemm.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

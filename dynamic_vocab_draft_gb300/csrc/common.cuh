@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cfloat>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/dynaspec.h"
 
@@ -250,8 +251,42 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity)
     } while (0)
 
 namespace ds {
+// A named NVTX range around a library call's host side: a profiler that collects NVTX shows
+// each stage's launches under the call's name.  Without such a tool attached it costs a check.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Budget (SM clock cycles) of the kernels' bounded pipeline waits, process-wide; set by
+// ds_set_wait_budget (tests make it tiny to see a wait give up), kWaitBudgetCycles otherwise.
+inline std::atomic<long long> &wait_budget_cell()
+{
+    static std::atomic<long long> cell{kWaitBudgetCycles};
+    return cell;
+}
+inline long long wait_budget() { return wait_budget_cell().load(std::memory_order_relaxed); }
+
+// Multiprocessors of the current device, looked up once per device: grids are sized from it, so a
+// process driving GPUs of different sizes (or two host threads on different devices) gets each
+// device's own count.  A racing first lookup stores the same value twice, which is harmless.
+// 0 if the device cannot be named or queried.
+inline int sm_count()
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 0;
+    cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 // Raise `kernel`'s dynamic shared-memory limit to `bytes` on the current device, once per device
 // (the attribute belongs to the device, so a process driving several GPUs sets it on each).

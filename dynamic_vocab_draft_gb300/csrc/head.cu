@@ -2,8 +2,8 @@
 // the greedy / Gumbel-max draft draw.
 //
 // DynaSpec summary, Technical Details > System Modules "Gathered LM Head" (a fused index-
-// select + GEMM) and Novel Architectural Elements ("Dynamic Vocabulary Head"; "gathering and
-// matrix multiplication without intermediate memory overhead"); Limitations: the gathered
+// select + GEMM) and Novel Architectural Elements ("Dynamic Vocabulary Head": the selected rows
+// are gathered and multiplied with no intermediate copy in memory); Limitations: the gathered
 // multiplication costs more per row than a dense one.  W[V_S] is never materialised: every
 // kernel streams the selected rows of W straight from HBM.
 //
@@ -21,17 +21,6 @@
 
 namespace ds {
 namespace {
-
-int num_sms()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    }
-    return n;
-}
 
 // ---------------------------------------------------------------------------------------
 // Per-row gathered GEMV
@@ -359,6 +348,7 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
                                       void *ws, size_t ws_bytes, int32_t *dev_status,
                                       cudaStream_t stream)
 {
+    ds::NvtxRange range("ds_gathered_head");
     if (!H || !W || !vs_offsets || !vs_ids || !logits || !token || !token_idx) return DS_ERR_INVALID_ARG;
     if (B < 1 || G < 1 || V < 1 || d < 8 || d % 8 || !(T >= 0.f) || pos < 0) return DS_ERR_INVALID_ARG;
     if (!aligned16(H) || !aligned16(W)) return DS_ERR_INVALID_ARG;
@@ -385,9 +375,11 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
 
     if (nu == 0) {
         if (G != 1) return DS_ERR_UNSUPPORTED;
+        const int sms = sm_count();
+        if (sms <= 0) return DS_ERR_CUDA;
         // One 512-thread block per SM.  At batch 1 a few SMs are left to the side stream, so the
         // next position's router and shortlist build run while this head streams W.
-        int gx = B == 1 ? num_sms() - kHeadSideSms : (num_sms() + B - 1) / B;
+        int gx = B == 1 ? sms - kHeadSideSms : (sms + B - 1) / B;
         if (gx < 1) gx = 1;
         if (gx > kGvMaxBlocks) gx = kGvMaxBlocks;
         const size_t smem = size_t(d) * sizeof(uint16_t);
@@ -402,6 +394,8 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
     if (rows > kUnMaxRows) return DS_ERR_UNSUPPORTED;
     if ((V + kRsChunk - 1) / kRsChunk > kGvMaxBlocks) return DS_ERR_UNSUPPORTED;
     if ((V + tc::kRows - 1) / tc::kRows > kUnionMaxTiles) return DS_ERR_UNSUPPORTED;
+    const int sms = sm_count();
+    if (sms <= 0) return DS_ERR_CUDA;
     float *parts = reinterpret_cast<float *>(wsb + lay.parts);
     unsigned *tile_cnt = reinterpret_cast<unsigned *>(wsb + lay.tile_cnt);
     UnionEp ep;
@@ -410,10 +404,10 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
     ep.logits = logits; ep.V = V; ep.M = M; ep.G = G; ep.status = dev_status;
     // A tensor-core head CTA fills its SM (shared memory and registers); kHeadSideSms SMs are
     // left free so the next position's router and shortlist build run beside it.
-    int tc_grid = num_sms() - kHeadSideSms;
+    int tc_grid = sms - kHeadSideSms;
     if (tc_grid > tc::kMaxGrid) tc_grid = tc::kMaxGrid;
     if (tc_grid < 1) tc_grid = 1;
-    const tc::Operands op{W, H, d, int(rows), dev_status};
+    const tc::Operands op{W, H, d, int(rows), dev_status, wait_budget()};
     const ds_status st = tc::launch_for(op, ep, parts, tile_cnt, tc_grid, stream);
     if (st != DS_OK) return st;
     const int chunks = (V + kRsChunk - 1) / kRsChunk;
@@ -428,6 +422,10 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
 // device array of fixed size instead of a caller workspace.
 // ---------------------------------------------------------------------------------------
 #include <mutex>
+
+#include <cuda.h>      // CUcontext / CUresult types only: the two driver calls below are reached
+                       // through the runtime's entry-point query, so the library does not link
+                       // the driver library
 
 namespace {
 
@@ -446,19 +444,53 @@ static __device__ __align__(256) unsigned char g_head_noalloc_scratch[kNoAllocBy
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void *g_noalloc_addr[kNoAllocMaxDevices];
+unsigned long long g_noalloc_ctx[kNoAllocMaxDevices];   // context the address belongs to
 
-// Device address of the scratch array on the current device, looked up once per device.
-// (In host code the array's name is only a host-side stand-in, not a device address.)
+// Unique id of the calling thread's current context (the driver never reuses one within a
+// process), or 0 when none is current or the driver calls cannot be reached.
+unsigned long long current_context_id()
+{
+    typedef CUresult (*GetCurrent)(CUcontext *);
+    typedef CUresult (*GetId)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static bool resolved = false;
+    if (!resolved) {                                   // under g_noalloc_mutex
+        cudaDriverEntryPointQueryResult q1, q2;
+        void *f1 = nullptr, *f2 = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+            q1 == cudaDriverEntryPointSuccess && q2 == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<GetCurrent>(f1);
+            get_id = reinterpret_cast<GetId>(f2);
+        }
+        (void)cudaGetLastError();
+        resolved = true;
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of the scratch array on the current device.  It is looked up once per device
+// and context: a reset of the device (cudaDeviceReset) destroys the context and the array with
+// it, and the next call looks the address up again in the new context instead of using a stale
+// one.  (In host code the array's name is only a host-side stand-in, not a device address.)
 ds_status noalloc_scratch(void **out)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return DS_ERR_CUDA;
     if (dev < 0 || dev >= kNoAllocMaxDevices) return DS_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_addr[dev]) {
+    const unsigned long long ctx = current_context_id();
+    if (!g_noalloc_addr[dev] || ctx == 0 || ctx != g_noalloc_ctx[dev]) {
         void *p = nullptr;
+        // the lookup also makes the device's primary context current if no context was yet
         if (cudaGetSymbolAddress(&p, g_head_noalloc_scratch) != cudaSuccess || !p) return DS_ERR_CUDA;
         g_noalloc_addr[dev] = p;
+        g_noalloc_ctx[dev] = current_context_id();
     }
     *out = g_noalloc_addr[dev];
     return DS_OK;

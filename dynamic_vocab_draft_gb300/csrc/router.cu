@@ -4,7 +4,7 @@
 // Vocabulary Language Models"), Technical Details > System Modules "Router (Meta-
 // Classifier)": a 2-layer MLP scoring vocabulary clusters from the drafter hidden state
 // H_{t-1}; Key Hyperparameters: ReLU, and a budget k_c(t) that decays with draft position t;
-// abstract: the shortlist is the union of the top-selected clusters.
+// abstract: the shortlist is made of the tokens of the best-scoring clusters.
 //
 // Both layers are GEMV-shaped and HBM-bound at the batch sizes of drafting (one weight row
 // feeds at most a few dozen hidden states), so they run on CUDA cores: one warp per weight
@@ -358,17 +358,6 @@ RouterTcWs router_tc_layout(int B, int Hr)
     return w;
 }
 
-int router_num_sms()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    }
-    return n;
-}
-
 // CTAs of a router GEMM: the first draft position's router runs before any head and may use
 // the whole GPU, but a router layer is only a few hundred (tile, k-stage) units, and a tile
 // split between many CTAs pays for storing and adding its parts, so each CTA takes at least
@@ -376,10 +365,10 @@ int router_num_sms()
 // SMs free for it, and must fit there.
 constexpr int kRouterSideSms = 8;
 constexpr int kRouterMinUnits = 8;
-int router_grid(int pos, int units)
+int router_grid(int pos, int units, int sms)
 {
     int g = pos == 1 ? (units + kRouterMinUnits - 1) / kRouterMinUnits : kRouterSideSms;
-    if (g > router_num_sms()) g = router_num_sms();
+    if (g > sms) g = sms;
     if (g > tc::kMaxGrid) g = tc::kMaxGrid;
     if (g > units) g = units;
     return g < 1 ? 1 : g;
@@ -421,6 +410,7 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
                                     void *ws, size_t ws_bytes, int32_t *dev_status,
                                     cudaStream_t stream)
 {
+    ds::NvtxRange range("ds_router_topk");
     if (!H || !W1 || !b1 || !W2 || !b2 || !budget || !scores || !cluster_ids)
         return DS_ERR_INVALID_ARG;
     if (B < 1 || B > 4096 || d < 8 || d % 8 || Hr < 8 || Hr % 8 || M < 1 || M > kRouterMaxK)
@@ -433,6 +423,8 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
     if (!aligned16(H) || !aligned16(W1) || !aligned16(W2)) return DS_ERR_INVALID_ARG;
     if (!ws || ws_bytes < ds_router_workspace_bytes(B, Hr)) return DS_ERR_WORKSPACE;
 
+    const int sms = sm_count();
+    if (sms <= 0) return DS_ERR_CUDA;
     float *u = static_cast<float *>(ws);
     unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) +
                                                       align256(size_t(B) * size_t(Hr) * sizeof(float)));
@@ -441,7 +433,7 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
         auto grid1 = [&](int rows) {
             if (pos != 1) return kGemv1Blocks;
             const int g = (rows + kGemvWarps - 1) / kGemvWarps;
-            return g < router_num_sms() ? g : router_num_sms();
+            return g < sms ? g : sms;
         };
         gemv1_kernel<uint16_t><<<grid1(Hr), kGemvWarps * 32, 0, stream>>>(W1, Hr, d, H, b1, act, u, 0,
                                                                          nullptr, nullptr);
@@ -459,15 +451,15 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
         float *parts = reinterpret_cast<float *>(w + lay.parts);
         Layer1Ep e1;
         e1.n = Hr; e1.bias = b1; e1.hid2 = hid2; e1.Hr = Hr; e1.act = act;
-        const tc::Operands op1{W1, H, d, B, dev_status};
+        const tc::Operands op1{W1, H, d, B, dev_status, wait_budget()};
         const int u1 = ((Hr + tc::kRows - 1) / tc::kRows) * ((d + 127) / 128);
-        ds_status st = tc::launch_for(op1, e1, parts, tile_cnt, router_grid(pos, u1), stream);
+        ds_status st = tc::launch_for(op1, e1, parts, tile_cnt, router_grid(pos, u1, sms), stream);
         if (st != DS_OK) return st;
         Layer2Ep e2;
         e2.n = M; e2.bias = b2; e2.scores = scores; e2.M = M; e2.B = B;
-        const tc::Operands op2{W2, hid2, Hr, 2 * B, dev_status};
+        const tc::Operands op2{W2, hid2, Hr, 2 * B, dev_status, wait_budget()};
         const int u2 = ((M + tc::kRows - 1) / tc::kRows) * ((Hr + 127) / 128);
-        st = tc::launch_for(op2, e2, parts, tile_cnt, router_grid(pos, u2), stream);
+        st = tc::launch_for(op2, e2, parts, tile_cnt, router_grid(pos, u2, sms), stream);
         if (st != DS_OK) return st;
         topk_rows_kernel<<<B, kTopkThreads, 0, stream>>>(scores, M, k, cluster_ids);
         DS_TRY_LAUNCH();
@@ -478,4 +470,67 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
     const ds_status s2 = launch_gemv<float, kGemvBT>(W2, M, Hr, u, B, b2, -1, scores, k, cluster_ids, counters, stream);
     if (s2 != DS_OK) return s2;
     return DS_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+// Router handle: the weights, sizes, activation and budget table of one router, so that a
+// draft position's call names only its hidden states and position.  Host memory only; the
+// weights stay the caller's.
+// ---------------------------------------------------------------------------------------
+#include <new>
+#include <vector>
+
+struct ds_router {
+    const uint16_t *W1, *b1, *W2, *b2;
+    int d, Hr, M, act;
+    std::vector<int32_t> budget;
+};
+
+extern "C" ds_status ds_router_create(ds_router_t *out, const uint16_t *W1, const uint16_t *b1,
+                                      const uint16_t *W2, const uint16_t *b2, int d, int Hr, int M,
+                                      int act, const int32_t *budget, int gamma)
+{
+    if (!out) return DS_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!W1 || !b1 || !W2 || !b2 || !budget) return DS_ERR_INVALID_ARG;
+    if (d < 8 || d % 8 || Hr < 8 || Hr % 8 || M < 1 || M > kRouterMaxK || gamma < 1) return DS_ERR_INVALID_ARG;
+    if (d > kRouterMaxK || Hr > kRouterMaxK) return DS_ERR_UNSUPPORTED;
+    if (act != DS_ACT_RELU && act != DS_ACT_GELU) return DS_ERR_INVALID_ARG;
+    if (!aligned16(W1) || !aligned16(W2)) return DS_ERR_INVALID_ARG;
+    for (int t = 0; t < gamma; ++t)
+        if (budget[t] < 1 || budget[t] > M) return DS_ERR_INVALID_ARG;
+    ds_router *h = new (std::nothrow) ds_router;
+    if (!h) return DS_ERR_UNSUPPORTED;
+    h->W1 = W1; h->b1 = b1; h->W2 = W2; h->b2 = b2;
+    h->d = d; h->Hr = Hr; h->M = M; h->act = act;
+    h->budget.assign(budget, budget + gamma);
+    *out = h;
+    return DS_OK;
+}
+
+extern "C" ds_status ds_router_destroy(ds_router_t r)
+{
+    delete r;
+    return DS_OK;
+}
+
+// [the router call's workspace | B x M scores when the caller passes none]
+extern "C" size_t ds_router_workspace_bytes_h(ds_router_t r, int B)
+{
+    if (!r || B <= 0) return 0;
+    return align256(ds_router_workspace_bytes(B, r->Hr)) + align256(size_t(B) * size_t(r->M) * sizeof(float));
+}
+
+extern "C" ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, int pos,
+                                      float *scores, int32_t *cluster_ids,
+                                      void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream)
+{
+    if (!r) return DS_ERR_INVALID_ARG;
+    if (B < 1 || B > 4096) return DS_ERR_INVALID_ARG;
+    if (!ws || ws_bytes < ds_router_workspace_bytes_h(r, B)) return DS_ERR_WORKSPACE;
+    const size_t base = align256(ds_router_workspace_bytes(B, r->Hr));
+    if (!scores) scores = reinterpret_cast<float *>(static_cast<char *>(ws) + base);
+    return ds_router_topk(H, B, r->d, r->W1, r->b1, r->Hr, r->W2, r->b2, r->M, r->act,
+                          r->budget.data(), int(r->budget.size()), pos, scores, cluster_ids,
+                          ws, base, dev_status, stream);
 }

@@ -1,8 +1,8 @@
 // Shortlist construction: V_S = the union of the selected clusters' tokens.
 //
-// DynaSpec abstract ("the union of the top-selected clusters defines the drafter's
-// shortlist"); summary, Technical Details > Problem Definition ("Outputs: shortlisted subset
-// V_S").  The clusters partition the vocabulary, so the union is a concatenation: an
+// DynaSpec abstract (the drafter's shortlist is the set of tokens of the best-scoring
+// clusters taken together); summary, Technical Details > Problem Definition (the output of
+// the step is the shortlist V_S).  The clusters partition the vocabulary, so the union is a concatenation: an
 // exclusive scan of the selected clusters' sizes in ascending cluster id gives every
 // cluster's place in the list (cpos), and a copy of the CSR slices fills it.  The same
 // scan over "selected by any list" gives the batch union the batched / tree heads read W
@@ -253,6 +253,7 @@ extern "C" ds_status ds_vocab_index(const int32_t *csr_off, const int32_t *csr_t
                                     int32_t *cluster_of, int32_t *rank_in_cluster,
                                     int32_t *dev_status, cudaStream_t stream)
 {
+    ds::NvtxRange range("ds_vocab_index");
     if (!csr_off || !csr_tok || !cluster_of || !rank_in_cluster) return DS_ERR_INVALID_ARG;
     if (M < 1 || V < 1 || M > V) return DS_ERR_INVALID_ARG;
     vocab_index_kernel<<<(M + 7) / 8, 256, 0, stream>>>(csr_off, csr_tok, M, V, cluster_of,
@@ -275,6 +276,7 @@ extern "C" ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *c
                                         void *ws, size_t ws_bytes, int32_t *dev_status,
                                         cudaStream_t stream)
 {
+    ds::NvtxRange range("ds_build_shortlist");
     if (!csr_off || !csr_tok || !cluster_ids || !vs_offsets || !vs_ids || !cpos)
         return DS_ERR_INVALID_ARG;
     const int nu = (union_ids != nullptr) + (union_cluster != nullptr) + (union_count != nullptr);

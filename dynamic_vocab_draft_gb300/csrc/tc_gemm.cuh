@@ -30,9 +30,11 @@
 // K-major layout the MMA descriptors describe (8-row x 128-byte atoms, 16-byte chunk c of row
 // r at c ^ (r & 7)).
 //
-// Every wait on an mbarrier is bounded and also gives up when another role has failed; a wait
-// that gives up sets DS_DEV_TIMEOUT.  Producers leave no copy in flight, the MMA thread waits
-// (bounded) for its MMAs to finish, and the tensor memory is freed after a final barrier.
+// Every pipeline wait on an mbarrier is bounded (the budget comes from the host) and also gives
+// up when another role has failed; a wait that gives up sets DS_DEV_TIMEOUT.  Producers leave
+// no copy in flight, the MMA thread waits for its own MMAs to finish whatever happened to the
+// pipeline (bounded by the full default budget), and the tensor memory is freed after a final
+// barrier.
 #pragma once
 #include "common.cuh"
 
@@ -78,6 +80,7 @@ struct Operands {
     const uint16_t *B;       // [R, d] bf16
     int d, R;
     int32_t *status;
+    long long wait_budget;   // cycles a pipeline wait may take before it gives up
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -158,15 +161,26 @@ constexpr int kProducers = 256;
 constexpr int kMmaWarp = 16;
 static_assert(kThreads == kProdBase + kProducers + 32, "warp roles");
 
-// Wait for a phase of an mbarrier, giving up after the budget or when another role failed.
-__device__ __forceinline__ bool wait_phase(uint64_t *bar, unsigned parity, volatile int *fail)
+// Wait for a phase of an mbarrier, giving up after `budget` cycles or when another role failed.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, unsigned parity, volatile int *fail, long long budget)
 {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_test(bar, parity)) {
         if (*fail) return false;
-        if (clock64() - t0 > kWaitBudgetCycles) return false;
+        if (clock64() - t0 > budget) return false;
     }
+    return true;
+}
+
+// Wait for this thread's own asynchronous work to finish before its resources are released: a
+// failure elsewhere does not end this wait, and its budget is the full default one whatever the
+// pipeline budget is.
+__device__ __forceinline__ bool wait_drain(uint64_t *bar, unsigned parity)
+{
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity))
+        if (clock64() - t0 > kWaitBudgetCycles) return false;
     return true;
 }
 
@@ -255,7 +269,7 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
         const uint16_t *asrc[APASS];
         int t = g0 / nks, ks = g0 - t * nks, slot = 0, use = 0, cur_t = -1;
         for (int i = g0; i < g1; ++i) {
-            if (use > 0 && !wait_phase(&empty[slot], unsigned(use - 1) & 1u, fail)) {
+            if (use > 0 && !wait_phase(&empty[slot], unsigned(use - 1) & 1u, fail, op.wait_budget)) {
                 s_fail = 1;
                 set_status(op.status, DS_DEV_TIMEOUT);
                 break;
@@ -299,8 +313,8 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
             for (int i = g0; i < g1 && ok; ++i) {
                 const bool first = ks == 0 || i == g0;
                 const int buf = lt & 1;
-                if (first && lt >= 2 && !wait_phase(&acc_empty[buf], unsigned(lt / 2 - 1) & 1u, fail)) { ok = false; break; }
-                if (!wait_phase(&full[slot], unsigned(use) & 1u, fail)) { ok = false; break; }
+                if (first && lt >= 2 && !wait_phase(&acc_empty[buf], unsigned(lt / 2 - 1) & 1u, fail, op.wait_budget)) { ok = false; break; }
+                if (!wait_phase(&full[slot], unsigned(use) & 1u, fail, op.wait_budget)) { ok = false; break; }
                 proxy_fence_async();                           // the producers' copies -> tensor core
                 fence_after();
                 const uint32_t As = smem0 + uint32_t(slot * C::kStageBytes);
@@ -322,7 +336,9 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
             }
             if (!ok) { s_fail = 1; set_status(op.status, DS_DEV_TIMEOUT); }
             commit(&mma_idle);                                 // completes once every MMA issued has
-            if (!wait_phase(&mma_idle, 0u, fail) && !ok) { /* already failing */ }
+            // the tensor memory is freed below, so this waits for the MMAs in flight even when
+            // the pipeline has failed
+            if (!wait_drain(&mma_idle, 0u)) { s_fail = 1; set_status(op.status, DS_DEV_TIMEOUT); }
         }
         __syncwarp();
     } else if (warp < kEpiWarps) {
@@ -341,7 +357,7 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
             const int u = t * kRows + row;
             if (u < nU) ep.pick(u, v, c);
             const int aux = ep.row_aux(v);
-            if (!wait_phase(&acc_full[buf], unsigned(lt / 2) & 1u, fail)) {
+            if (!wait_phase(&acc_full[buf], unsigned(lt / 2) & 1u, fail, op.wait_budget)) {
                 s_fail = 1;
                 set_status(op.status, DS_DEV_TIMEOUT);
             }

@@ -1,7 +1,7 @@
 // Speculative-sampling verification over the full vocabulary.
 //
-// DynaSpec abstract ("the target model still verifies over the full vocabulary, preserving
-// exactness"); summary, Technical Details > Pipeline Flow ("Rejection Sampling
+// DynaSpec abstract (verification by the target model stays over the whole vocabulary, so
+// the output distribution is unchanged); summary, Technical Details > Pipeline Flow ("Rejection Sampling
 // Verification") and System Modules "Target Model".  The pages cite Leviathan et al. 2023
 // and Chen et al. 2023 for the algorithm without printing it; the kernels follow its
 // standard statement (accept x_t iff u_t q_t(x_t) < p_t(x_t); at the first rejection draw
@@ -923,21 +923,10 @@ using namespace ds;
 static int vchunks(int V) { return (V + kVChunkMin - 1) / kVChunkMin; }     // the most chunks
 static size_t rchunks(int V) { return size_t((V + kRChunkMin - 1) / kRChunkMin); }
 
-static int verify_sms()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
-    }
-    return n;
-}
-
 // The larger chunks when rows * chunks still covers every SM twice.
-static bool big_chunks(long long rows, int V, int chunk)
+static bool big_chunks(long long rows, int V, int chunk, int sms)
 {
-    return rows * ((V + chunk - 1) / chunk) >= 2LL * verify_sms();
+    return rows * ((V + chunk - 1) / chunk) >= 2LL * sms;
 }
 
 extern "C" size_t ds_verify_workspace_bytes(int B, int gamma, int V)
@@ -963,6 +952,7 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
                                int32_t *accepted_len, int32_t *correction,
                                void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream)
 {
+    ds::NvtxRange range("ds_verify");
     if (!p_logits || !q_logits || !vs_offsets || !cpos || !cluster_of || !rank_in_cluster ||
         !draft_ids || !uniforms || !accepted_len || !correction)
         return DS_ERR_INVALID_ARG;
@@ -972,9 +962,11 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     if ((q_max == nullptr) != (q_sumexp == nullptr)) return DS_ERR_INVALID_ARG;
     if (B > 65535 / (gamma + 1)) return DS_ERR_UNSUPPORTED;
     if (!ws || ws_bytes < ds_verify_workspace_bytes(B, gamma, V)) return DS_ERR_WORKSPACE;
+    const int sms = sm_count();
+    if (sms <= 0) return DS_ERR_CUDA;
     ChainArgs a;
-    const bool vbig = big_chunks(1LL * B * (gamma + 1), V, kVThreads * kVPerBig);
-    const bool rbig = big_chunks(B, V, kVThreads * kRPerBig);
+    const bool vbig = big_chunks(1LL * B * (gamma + 1), V, kVThreads * kVPerBig, sms);
+    const bool rbig = big_chunks(B, V, kVThreads * kRPerBig, sms);
     a.p_logits = p_logits; a.B = B; a.gamma = gamma; a.V = V;
     a.nch = (V + kVThreads * (vbig ? kVPerBig : kVPerSmall) - 1) / (kVThreads * (vbig ? kVPerBig : kVPerSmall));
     a.T = T; a.inv_te = T > 0.f ? 1.f / T : 1.f;
@@ -1028,6 +1020,7 @@ extern "C" ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd,
                                     int32_t *accepted_len, int32_t *correction, int32_t *path,
                                     void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream)
 {
+    ds::NvtxRange range("ds_verify_tree");
     if (!p_logits || !parent || !q_logits || !vs_offsets || !vs_ids || !cpos || !cluster_of ||
         !rank_in_cluster || !node_tokens || !u_node || !u_res || !accepted_len || !correction || !path)
         return DS_ERR_INVALID_ARG;
@@ -1050,16 +1043,14 @@ extern "C" ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd,
     char *w = static_cast<char *>(ws);
     a.state = reinterpret_cast<WalkState *>(w); w += align256(size_t(B) * sizeof(WalkState));
     a.rbuf = reinterpret_cast<float *>(w); w += align256(size_t(B) * 2 * size_t(V) * sizeof(float));
-    const bool rbig = big_chunks(B, V, kVThreads * kRPerBig);
+    const int sms = sm_count();
+    if (sms <= 0) return DS_ERR_CUDA;
+    const bool rbig = big_chunks(B, V, kVThreads * kRPerBig, sms);
     a.nrch = (V + kVThreads * (rbig ? kRPerBig : kRPerSmall) - 1) / (kVThreads * (rbig ? kRPerBig : kRPerSmall));
     a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.psum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.cnt = reinterpret_cast<unsigned *>(w);
     // one cluster of CL CTAs per sequence, CL = 8, 4, 2 or 1 so that the clusters fit the GPU
-    int sms = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return DS_ERR_CUDA;
     int CL = kWalkMaxCluster;
     while (CL > 1 && long(B) * CL > sms) CL >>= 1;
     cudaLaunchConfig_t cfg = {};

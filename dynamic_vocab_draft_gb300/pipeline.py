@@ -3,10 +3,15 @@
 Pipeline order (DynaSpec summary, Technical Details > Pipeline Flow): router on a parallel
 stream, draft computation on the main stream, a synchronisation, the gathered projection,
 then rejection-sampling verification.  Per draft position t the router and shortlist build
-run on a side stream (Novel Architectural Elements: "Parallel execution of the Router on a
-separate CUDA stream"), an event marks the shortlist ready, and the main stream waits on that
-event before the gathered head.  The routers of later positions therefore run while the
-heads of earlier positions stream W.
+run on a side stream (Novel Architectural Elements: the router runs concurrently, on a CUDA
+stream of its own), an event marks the shortlist ready, and the main stream waits on that
+event before the gathered head.
+
+Dependencies are the method's.  The router of position t reads H_{t-1}, which the drafter
+computes from the token drawn at position t-2, so router t waits for head t-2 (routers 1 and 2
+read hidden states that exist when the step starts); it then runs beside head t-1 (and, in a
+full drafter, beside the drafter computation of H_t).  The head of position t waits for its
+shortlist.
 
 Buffers are allocated once per drafter; a step launches kernels only.  ``capture()`` records
 one whole step (both streams) into a CUDA graph that ``replay()`` launches in one call.
@@ -126,6 +131,36 @@ class _Common:
     def head_times_ms(self):
         return [a.elapsed_time(b) for a, b in self.head_events]
 
+    def _run(self, n, before_verify):
+        """Enqueue one step of n positions (see the module docstring for the dependencies).
+        Events are recorded before anything waits on them, in host order, so the same code
+        serves eager execution and graph capture."""
+        main = torch.cuda.current_stream(self.dev)
+        self.side.wait_stream(main)                # the step's inputs are in place
+
+        def route(t):
+            with torch.cuda.stream(self.side):
+                if t >= 2:
+                    self.side.wait_event(self.head_done[t - 2])
+                self.route(t)
+                self.ready[t].record(self.side)
+
+        for t in range(min(2, n)):
+            route(t)
+        for t in range(n):
+            main.wait_event(self.ready[t])
+            if self.head_events:
+                api.event_record(self.head_events[t][0])
+            self.head(t)
+            if self.head_events:
+                api.event_record(self.head_events[t][1])
+            self.head_done[t].record(main)
+            if t + 2 < n:
+                route(t + 2)
+        for ev in before_verify or ():
+            main.wait_event(ev)
+        self.verify()
+
 
 
 class ChainDrafter(_Common):
@@ -174,20 +209,22 @@ class ChainDrafter(_Common):
         self.correction = self.out[B:2 * B]
         self.tokens = self.out[2 * B:].view(gamma, B)
         self.token_idx = torch.empty(gamma, B, **i32)
-        self.ws_router = [api.workspace(api.router_workspace_bytes(B, self.Hr), dev) for _ in range(gamma)]
+        self.router = api.Router(W1, b1, W2, b2, act, budget)
+        self.ws_router = [api.workspace(self.router.workspace_bytes(B), dev) for _ in range(gamma)]
         self.ws_short = [api.workspace(api.shortlist_workspace_bytes(B, M), dev) for _ in range(gamma)]
         self.ws_head = api.workspace(api.head_workspace_bytes(B), dev)
         self.ws_verify = api.workspace(api.verify_workspace_bytes(B, gamma, V), dev)
         self.side = torch.cuda.Stream(device=dev)
         self.ready = [torch.cuda.Event() for _ in range(gamma)]
+        self.head_done = [torch.cuda.Event() for _ in range(gamma)]
         self.graph = None
         # optional [(start, end)] timing events around each position's head launch
         self.head_events = None
 
     def route(self, t, stream=None):
         """Router + top-k + shortlist of draft position t (0-based) for all sequences."""
-        api.router_topk(self.H[t], self.W1, self.b1, self.W2, self.b2, self.act, self.budget, t + 1,
-                        self.scores[t], self.cluster_ids[t], self.ws_router[t], self.status, stream)
+        self.router.topk(self.H[t], t + 1, self.scores[t], self.cluster_ids[t], self.ws_router[t], self.status,
+                         stream)
         un = (self.union_ids[t], self.union_cluster[t], self.union_count[t]) if self.union else (None,) * 3
         api.build_shortlist(self.csr_off, self.csr_tok, self.cluster_ids[t], self.vs_offsets[t],
                             self.vs_ids[t], self.cpos[t], self.ws_short[t], self.status,
@@ -209,22 +246,7 @@ class ChainDrafter(_Common):
     def step(self, before_verify=None):
         """One speculation step; verification first waits for the events in `before_verify`, if
         given (inputs that only verification reads may still be arriving)."""
-        main = torch.cuda.current_stream(self.dev)
-        self.side.wait_stream(main)
-        for t in range(self.gamma):
-            with torch.cuda.stream(self.side):
-                self.route(t)
-                self.ready[t].record(self.side)
-        for t in range(self.gamma):
-            main.wait_event(self.ready[t])
-            if self.head_events:
-                api.event_record(self.head_events[t][0])
-            self.head(t)
-            if self.head_events:
-                api.event_record(self.head_events[t][1])
-        for ev in before_verify or ():
-            main.wait_event(ev)
-        self.verify()
+        self._run(self.gamma, before_verify)
 
     def n_heads(self) -> int:
         return self.gamma
@@ -284,18 +306,20 @@ class TreeDrafter(_Common):
         self.path = self.out[2 * B:2 * B + B * D].view(B, D)
         self.tokens = self.out[2 * B + B * D:].view(D, B * Wd)
         self.token_idx = torch.empty(D, B * Wd, **i32)
-        self.ws_router = [api.workspace(api.router_workspace_bytes(B, self.Hr), dev) for _ in range(D)]
+        self.router = api.Router(W1, b1, W2, b2, act, budget)
+        self.ws_router = [api.workspace(self.router.workspace_bytes(B), dev) for _ in range(D)]
         self.ws_short = [api.workspace(api.shortlist_workspace_bytes(B, M), dev) for _ in range(D)]
         self.ws_head = api.workspace(api.head_workspace_bytes(B * Wd), dev)
         self.ws_verify = api.workspace(api.verify_tree_workspace_bytes(B, D, Wd, V), dev)
         self.side = torch.cuda.Stream(device=dev)
         self.ready = [torch.cuda.Event() for _ in range(D)]
+        self.head_done = [torch.cuda.Event() for _ in range(D)]
         self.graph = None
         self.head_events = None
 
     def route(self, t, stream=None):
-        api.router_topk(self.Hr_h[t], self.W1, self.b1, self.W2, self.b2, self.act, self.budget, t + 1,
-                        self.scores[t], self.cluster_ids[t], self.ws_router[t], self.status, stream)
+        self.router.topk(self.Hr_h[t], t + 1, self.scores[t], self.cluster_ids[t], self.ws_router[t],
+                         self.status, stream)
         api.build_shortlist(self.csr_off, self.csr_tok, self.cluster_ids[t], self.vs_offsets[t],
                             self.vs_ids[t], self.cpos[t], self.ws_short[t], self.status,
                             self.union_ids[t], self.union_cluster[t], self.union_count[t], stream)
@@ -316,22 +340,7 @@ class TreeDrafter(_Common):
     def step(self, before_verify=None):
         """One speculation step; verification first waits for the events in `before_verify`, if
         given."""
-        main = torch.cuda.current_stream(self.dev)
-        self.side.wait_stream(main)
-        for t in range(self.D):
-            with torch.cuda.stream(self.side):
-                self.route(t)
-                self.ready[t].record(self.side)
-        for t in range(self.D):
-            main.wait_event(self.ready[t])
-            if self.head_events:
-                api.event_record(self.head_events[t][0])
-            self.head(t)
-            if self.head_events:
-                api.event_record(self.head_events[t][1])
-        for ev in before_verify or ():
-            main.wait_event(ev)
-        self.verify()
+        self._run(self.D, before_verify)
 
     def n_heads(self) -> int:
         return self.D

@@ -14,7 +14,9 @@
  *
  * Conventions shared by every call
  *   - Pointers are DEVICE pointers owned by the caller unless marked "host".  The library
- *     never allocates, frees or retains memory and keeps no state between calls.
+ *     never allocates, frees or retains device memory.  It keeps no state between calls
+ *     except in a router handle (ds_router_create: host memory the caller releases with
+ *     ds_router_destroy) and the process-wide wait budget (ds_set_wait_budget).
  *   - bf16 tensors are passed as their raw 16-bit patterns (uint16_t).  Row-major layouts.
  *   - Every call is asynchronous on `stream` and returns a ds_status at once.  Errors the
  *     host can see (NULL pointers, bad sizes, a workspace that is too small, d % 8 != 0)
@@ -53,8 +55,8 @@ typedef int32_t ds_status;
 #define DS_DEV_CAPACITY     0x20  /* a shortlist larger than the capacity the caller gave   */
 #define DS_DEV_TIMEOUT      0x40  /* a bounded wait inside a kernel gave up (about 1 s)     */
 
-/* Router activations (summary, Key Hyperparameters: "2-layer MLP with ReLU"; the Tiny
- * workload names GELU, taken in its exact erf form). */
+/* Router activations (summary, Key Hyperparameters: a two-layer MLP with ReLU activation; the
+ * Tiny workload names GELU, taken in its exact erf form). */
 #define DS_ACT_RELU 0
 #define DS_ACT_GELU 1
 
@@ -81,7 +83,7 @@ ds_status ds_vocab_index(const int32_t *csr_off, const int32_t *csr_tok, int M, 
  * ds_router_topk -- router MLP + position-aware top-k (summary, System Modules "Router
  * (Meta-Classifier)": a 2-layer MLP predicting relevant clusters from H_{t-1}; Key
  * Novelty and Key Hyperparameters: the budget k_c(t) shrinks with draft position t;
- * abstract: "the union of the top-selected clusters").
+ * abstract: the shortlist is formed from the tokens of the best-scoring clusters).
  *   H [B, d] bf16          hidden states the router reads (H_{t-1} of each sequence)
  *   W1 [Hr, d], b1 [Hr]    first layer (out x in), bf16
  *   W2 [M, Hr], b2 [M]     second layer, bf16
@@ -104,8 +106,34 @@ ds_status ds_router_topk(const uint16_t *H, int B, int d,
                          void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
+ * Router handle -- the same router call with its weights, sizes, activation and budget table
+ * bound once (summary, Problem Definition: per draft position the router's input is only the
+ * hidden state H_{t-1}; the rest is fixed for the drafter).
+ *   ds_router_create       checks the arguments as ds_router_topk does (plus every budget
+ *                          entry in [1, M]) and returns a handle in *out.  The handle holds
+ *                          non-owning views of W1, b1, W2, b2 (device memory that must outlive
+ *                          it) and a host copy of budget[0..gamma).  Host memory only;
+ *                          DS_ERR_UNSUPPORTED if it cannot be allocated.  *out is NULL on error.
+ *   ds_router_destroy      releases the handle (NULL: no-op).  Not while a call using it is
+ *                          being made on another host thread.
+ *   ds_router_topk_h       ds_router_topk for draft position `pos` (1-based).  scores may be
+ *                          NULL: the workspace then holds them.
+ *   ds_router_workspace_bytes_h  bytes of `ws` for B hidden states (the router call's
+ *                          workspace followed by room for the scores); zero it once.
+ * ------------------------------------------------------------------------------------- */
+typedef struct ds_router *ds_router_t;
+ds_status ds_router_create(ds_router_t *out, const uint16_t *W1, const uint16_t *b1,
+                           const uint16_t *W2, const uint16_t *b2, int d, int Hr, int M,
+                           int act, const int32_t *budget, int gamma);
+ds_status ds_router_destroy(ds_router_t r);
+size_t ds_router_workspace_bytes_h(ds_router_t r, int B);
+ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, int pos,
+                           float *scores, int32_t *cluster_ids,
+                           void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
  * ds_build_shortlist -- V_S as the union of the selected clusters (abstract; summary,
- * Problem Definition "Outputs: shortlisted subset V_S").  Clusters partition V, so the union
+ * Problem Definition, whose output is the shortlist V_S).  Clusters partition V, so the union
  * needs no de-duplication.  Order (the pages fix only the set): selected clusters in
  * ascending id, each cluster's tokens in CSR order.
  *   cluster_ids [B, k]     ascending per row (as ds_router_topk writes them)
@@ -133,8 +161,8 @@ ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *csr_tok, int
 /* -------------------------------------------------------------------------------------
  * ds_gathered_head -- logits over the shortlist only, plus the draft draw (summary, System
  * Modules "Gathered LM Head": a fused index-select + GEMM; Novel Architectural Elements
- * "Dynamic Vocabulary Head"; Key Novelty: "restricting the drafter's computation to this
- * dynamic subset").  W[V_S] is never materialised: rows are streamed straight from W.
+ * "Dynamic Vocabulary Head"; Key Novelty: the drafter computes logits for the dynamic
+ * subset only).  W[V_S] is never materialised: rows are streamed straight from W.
  *   H [B*G, d] bf16        head rows; rows b*G .. b*G+G-1 share list b (G = 1 for chain
  *                          drafting, G = nodes per depth for tree drafting)
  *   W [V, d] bf16          the LM head
@@ -182,7 +210,9 @@ ds_status ds_gathered_head(const uint16_t *H, int B, int G,
  *   - At most 32 head rows (B*G <= 32); larger calls return DS_ERR_UNSUPPORTED and launch
  *     nothing.
  *   - The first call on a device looks the array's device address up for that device
- *     (with that device current); make that first call before any stream capture.
+ *     (with that device current); make that first call before any stream capture.  The
+ *     address is kept per device and context: after a reset of the device
+ *     (cudaDeviceReset) the next call looks it up again, so that call too is a first call.
  *   - Every call shares the one array, which keeps the last call's contents; each call clears
  *     the counters it needs on `stream` before launching.  Calls that overlap on the GPU (on
  *     different streams, or from several host threads) race on the array: serialise them.
@@ -199,9 +229,9 @@ ds_status ds_gathered_head_noalloc(const uint16_t *H, int B, int G,
                                    int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
- * ds_verify -- rejection-sampling verification over the full vocabulary (abstract: "the
- * target model still verifies over the full vocabulary, preserving exactness"; summary,
- * Pipeline Flow "Rejection Sampling Verification").  The pages cite Leviathan et al. and
+ * ds_verify -- rejection-sampling verification over the full vocabulary (abstract: the target
+ * model's check stays over the whole vocabulary, which keeps the output distribution exact;
+ * summary, Pipeline Flow "Rejection Sampling Verification").  The pages cite Leviathan et al. and
  * Chen et al. without printing the algorithm; this is its standard statement:
  *   p_t = softmax(z_t / T) over all V, q_t = softmax(l_t / T) over the shortlist S_t (0
  *   elsewhere).  For t = 1..gamma in order accept x_t iff u_t q_t(x_t) < p_t(x_t).  At the
@@ -275,6 +305,34 @@ ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd, int V, flo
                          void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
+ * ds_workspace_bytes -- one query for every call's workspace (the per-call queries above give
+ * the same numbers).  op and the sizes it reads:
+ *   DS_OP_ROUTER       B, hidden (= Hr)                 ds_router_workspace_bytes(B, hidden)
+ *   DS_OP_SHORTLIST    B, M                             ds_shortlist_workspace_bytes(B, M)
+ *   DS_OP_HEAD         B, width (= G, head rows per list) ds_head_workspace_bytes(B * width)
+ *   DS_OP_VERIFY       B, gamma, V                      ds_verify_workspace_bytes(B, gamma, V)
+ *   DS_OP_VERIFY_TREE  B, gamma (= D), width (= Wd), V  ds_verify_tree_workspace_bytes(...)
+ * Arguments an op does not read are ignored.  0 for an unknown op or sizes out of range.
+ * ------------------------------------------------------------------------------------- */
+#define DS_OP_ROUTER      1
+#define DS_OP_SHORTLIST   2
+#define DS_OP_HEAD        3
+#define DS_OP_VERIFY      4
+#define DS_OP_VERIFY_TREE 5
+size_t ds_workspace_bytes(int op, int B, int V, int M, int gamma, int hidden, int width);
+
+/* -------------------------------------------------------------------------------------
+ * ds_set_wait_budget -- how many SM clock cycles a kernel's bounded pipeline wait (the
+ * tensor-core GEMM's mbarrier waits, used by the batched router and the union head) may take
+ * before it gives up and sets DS_DEV_TIMEOUT; process-wide, read when a call is made.
+ * cycles = 0 restores the default (about one second at 2 GHz); cycles < 0 is refused.  Meant
+ * for tests that make a wait run out on purpose (no counterpart in the method).  After a
+ * call that timed out its outputs are undefined and its workspace must be zero-filled again
+ * before reuse (completion counters may be left set).
+ * ------------------------------------------------------------------------------------- */
+ds_status ds_set_wait_budget(int64_t cycles);
+
+/* -------------------------------------------------------------------------------------
  * ds_philox4x32_10 -- the device Philox4x32-10 the head draws its Gumbel noise from
  * (Salmon, Moraes, Dror, Shaw, SC'11), exposed so that it can be checked on its own.
  *   ctr [n, 4] counters, out [n, 4] words; key = the two 32-bit halves of `seed`.
@@ -299,9 +357,11 @@ ds_status ds_event_record(cudaEvent_t event, cudaStream_t stream);
  *   dst, src               device pointers or pinned host pointers; the ranges must not
  *                          overlap.  16-byte vectors when both are 16-byte aligned and bytes %
  *                          16 == 0, else byte copies.
- * Passing pageable host memory is the caller's error: on systems without address translation
- * services the kernel cannot reach it.  Returns DS_ERR_INVALID_ARG for NULL or overlapping
- * ranges; bytes == 0 is a no-op.
+ * Each end is looked up with cudaPointerGetAttributes before anything is launched: device,
+ * managed and page-locked host memory are accepted (page-locked memory through the device
+ * alias the runtime reports); pageable or foreign host memory, which a kernel cannot reach on
+ * systems without address translation services, returns DS_ERR_INVALID_ARG and launches
+ * nothing.  Also DS_ERR_INVALID_ARG for NULL or overlapping ranges; bytes == 0 is a no-op.
  * ------------------------------------------------------------------------------------- */
 ds_status ds_copy(void *dst, const void *src, size_t bytes, cudaStream_t stream);
 

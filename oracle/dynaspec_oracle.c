@@ -11,12 +11,12 @@
  * mlsanity.com/paper/2510.13847 and the summary "DynaSpec: Context-aware Dynamic
  * Speculative Sampling for Large-Vocabulary Language Models" on papers.lunadong.com):
  *   - router: a 2-layer MLP scoring vocabulary clusters from the drafter hidden state
- *     (summary, Technical Details > System Modules "Router"; Key Hyperparameters
- *     "router_architecture: 2-layer MLP with ReLU");
+ *     (summary, Technical Details > System Modules "Router"; Key Hyperparameters: two
+ *     layers with a ReLU between them);
  *   - position-aware budget: k_c(t) clusters kept at draft position t (summary, Key Novelty;
  *     Key Hyperparameters "shortlist_budget_decay");
- *   - shortlist: the union of the top-selected clusters (abstract; summary, Problem
- *     Definition "Outputs: shortlisted subset V_S");
+ *   - shortlist: the tokens of the best-scoring clusters taken together (abstract; summary,
+ *     Problem Definition, whose output is the shortlist V_S);
  *   - gathered head: logits only for the shortlisted LM-head rows (summary, System Modules
  *     "Gathered LM Head"; Novel Architectural Elements "Dynamic Vocabulary Head");
  *   - verification over the full vocabulary by rejection sampling (abstract; summary,
@@ -159,7 +159,7 @@ int orc_router(const uint16_t *H, int B, int d, const uint16_t *W1, const uint16
 }
 
 /* ------------------------------------------------------------------------------------ */
-/* Position-aware budget + top-k (abstract: "the union of the top-selected clusters";     */
+/* Position-aware budget + top-k (abstract: the shortlist comes from the best clusters;   */
 /* summary, Key Hyperparameters: k_c(t) decays with draft position t).  The decay law has */
 /* no stated form; the caller passes k = the budget table's entry for the position.       */
 /* Keeps the k clusters with the largest score, ties to the lower cluster id, and lists   */
@@ -218,7 +218,7 @@ int64_t orc_shortlist(const int32_t *csr_off, const int32_t *csr_tok, int M,
 
 /* ------------------------------------------------------------------------------------ */
 /* Gathered head: l_j = h . W[S_j] for every shortlisted token (summary, System Modules   */
-/* "Gathered LM Head": logits only for the selected vocabulary subset).  rows of H [R, d] */
+/* "Gathered LM Head": logits for the selected part of the vocabulary).  rows of H [R, d] */
 /* share the list S [n]; l [R, n] fp64.                                                    */
 /* ------------------------------------------------------------------------------------ */
 void orc_head(const uint16_t *H, int R, int d, const uint16_t *W, const int32_t *S,

@@ -38,7 +38,7 @@ def test_status_strings(lib):
     for code in (0, 1, 2, 3, 4, 0x10, 0x20, 0x40, 0x30, 12345):
         s = lib.ds_status_string(code)
         assert isinstance(s, bytes) and s
-    assert lib.ds_version() == 1
+    assert lib.ds_version() == 2
 
 
 def test_workspace_queries(lib):
@@ -121,6 +121,15 @@ def test_host_argument_checks(lib):
     assert lib.ds_copy(FAKE, FAKE, 0, None) == 0
 
 
+def test_copy_refuses_memory_the_device_cannot_reach(lib):
+    # two ordinary (pageable) host buffers, as a C caller would pass them: the library looks
+    # both ends up before launching and refuses them (here, without a GPU, the lookup itself
+    # fails, which is refused the same way)
+    a = ctypes.create_string_buffer(64)
+    b = ctypes.create_string_buffer(64)
+    assert lib.ds_copy(ctypes.cast(a, ctypes.c_void_p), ctypes.cast(b, ctypes.c_void_p), 64, None) == 1
+
+
 def test_copy_binding_refuses_pageable_host_memory():
     # ds_copy reaches host memory from a kernel, so the binding takes CUDA tensors or pinned
     # host tensors only; a pageable tensor is refused before the library is called
@@ -130,3 +139,47 @@ def test_copy_binding_refuses_pageable_host_memory():
         api.copy(torch.zeros(16, dtype=torch.uint8), torch.zeros(16, dtype=torch.uint8))
     with pytest.raises(ValueError):
         api.copy(torch.zeros(16, dtype=torch.uint8)[::2], torch.zeros(8, dtype=torch.uint8))
+
+
+def test_unified_workspace_query_matches_the_per_call_queries(lib):
+    # ds_workspace_bytes(op, B, V, M, gamma, hidden, width) dispatches to the per-call queries
+    for B in (1, 5, 32):
+        assert lib.ds_workspace_bytes(1, B, 0, 0, 0, 1024, 0) == lib.ds_router_workspace_bytes(B, 1024)
+        assert lib.ds_workspace_bytes(2, B, 0, 1024, 0, 0, 0) == lib.ds_shortlist_workspace_bytes(B, 1024)
+        assert lib.ds_workspace_bytes(3, B, 0, 0, 0, 0, 10) == lib.ds_head_workspace_bytes(B * 10)
+        assert lib.ds_workspace_bytes(4, B, 128256, 0, 6, 0, 0) == lib.ds_verify_workspace_bytes(B, 6, 128256)
+        assert lib.ds_workspace_bytes(5, B, 128256, 0, 6, 0, 10) == lib.ds_verify_tree_workspace_bytes(B, 6, 10, 128256)
+    assert lib.ds_workspace_bytes(9, 1, 1, 1, 1, 1, 1) == 0
+    assert lib.ds_workspace_bytes(3, 0, 0, 0, 0, 0, 1) == 0
+
+
+def test_router_handle_host_side(lib):
+    # the handle is host memory: create / query / destroy need no device
+    budget = (ctypes.c_int32 * 3)(8, 6, 4)
+    bptr = ctypes.cast(budget, ctypes.c_void_p)
+    h = ctypes.c_void_p()
+    # bad arguments: NULL out, NULL weight, d % 8, act, a budget entry beyond M
+    assert lib.ds_router_create(None, FAKE, FAKE, FAKE, FAKE, 256, 512, 32, 1, bptr, 3) == 1
+    assert lib.ds_router_create(ctypes.byref(h), None, FAKE, FAKE, FAKE, 256, 512, 32, 1, bptr, 3) == 1
+    assert h.value is None
+    assert lib.ds_router_create(ctypes.byref(h), FAKE, FAKE, FAKE, FAKE, 250, 512, 32, 1, bptr, 3) == 1
+    assert lib.ds_router_create(ctypes.byref(h), FAKE, FAKE, FAKE, FAKE, 256, 512, 32, 5, bptr, 3) == 1
+    assert lib.ds_router_create(ctypes.byref(h), FAKE, FAKE, FAKE, FAKE, 256, 512, 5, 1, bptr, 3) == 1
+    assert lib.ds_router_create(ctypes.byref(h), FAKE, FAKE, FAKE, FAKE, 256, 512, 32, 1, bptr, 3) == 0
+    assert h.value
+    # workspace: the router call's plus the scores (B x M fp32), 256-byte aligned parts
+    for B in (1, 5):
+        base = lib.ds_router_workspace_bytes(B, 512)
+        assert lib.ds_router_workspace_bytes_h(h, B) == ((base + 255) // 256) * 256 + ((B * 32 * 4 + 255) // 256) * 256
+    # NULL handle, too small a workspace, position outside the table: refused before any launch
+    assert lib.ds_router_topk_h(None, FAKE, 1, 1, None, FAKE, FAKE, 1 << 20, None, None) == 1
+    assert lib.ds_router_topk_h(h, FAKE, 1, 1, None, FAKE, FAKE, 16, None, None) == 4
+    assert lib.ds_router_topk_h(h, FAKE, 1, 4, None, FAKE, FAKE, 1 << 20, None, None) == 1
+    assert lib.ds_router_destroy(h) == 0
+    assert lib.ds_router_destroy(None) == 0
+
+
+def test_wait_budget_arguments(lib):
+    assert lib.ds_set_wait_budget(-1) == 1
+    assert lib.ds_set_wait_budget(1000) == 0
+    assert lib.ds_set_wait_budget(0) == 0          # back to the default

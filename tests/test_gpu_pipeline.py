@@ -3,13 +3,15 @@ side-stream router and CUDA-graph replay) against the oracle's whole step on the
 inputs.  Per sequence, positions are compared in order; an excused near-tie ends the
 comparison of that sequence (everything after it depends on the tie's outcome).
 """
+import functools
+
 import numpy as np
 import pytest
 
 torch = pytest.importorskip("torch")
 
 import oracle                          # noqa: E402
-from parity import (assert_close, topk_same_or_excused, token_same_or_excused, TIE,  # noqa: E402
+from parity import (assert_close, topk_same_or_excused, token_same_or_excused, TIE, ICDF_TOL,  # noqa: E402
                     softmax_full, q_dense, icdf_acceptable, accept_margin)
 import gpu_util as gu                  # noqa: E402
 
@@ -39,9 +41,12 @@ def make_chain(pkg, inp, T):
     return d
 
 
-def compare_chain(inp, d, T, seqs):
+def compare_chain(inp, d, T, seqs, ref=None, z=None):
+    """Compare the drafter's step with the oracle's (`ref`, default: the oracle's whole step on
+    the same inputs); z: the target logits the step verified against (default inp["z"])."""
     cfg = inp["cfg"]
-    ref = oracle.chain_step(inp, T=T, seqs=seqs)
+    z = inp["z"] if z is None else z
+    ref = oracle.chain_step(inp, T=T, seqs=seqs) if ref is None else ref
     scores = d.scores.cpu().numpy()
     offs = d.vs_offsets.cpu().numpy()
     ids_all = d.vs_ids.cpu().numpy()
@@ -74,14 +79,14 @@ def compare_chain(inp, d, T, seqs):
         if acc[b] != r["accepted"]:
             t = min(acc[b], r["accepted"])
             p = r["positions"][t]
-            pz = softmax_full(inp["z"][b, t], T)[p["token"]]
+            pz = softmax_full(z[b, t], T)[p["token"]]
             qx = q_dense(p["logits"], p["S"], T, cfg.V)[p["token"]]
             assert T > 0 and accept_margin(pz, qx, inp["u"][b, t]) < TIE
             continue
         if corr[b] != r["correction"]:
             assert T > 0
             t = acc[b]
-            pz = softmax_full(inp["z"][b, t], T)
+            pz = softmax_full(z[b, t], T)
             if t < cfg.gamma:
                 p = r["positions"][t]
                 w = np.maximum(pz - q_dense(p["logits"], p["S"], T, cfg.V), 0)
@@ -98,6 +103,7 @@ def compare_chain(inp, d, T, seqs):
     ("llama_b1", 1.0, None), ("llama_b1", 0.0, None),
     ("batched", None, [0, 13, 31]),
     ("large_b1_f5", None, None), ("large_b1_f100", None, None), ("large_b8_f10", None, [0, 7]),
+    ("large_b64_f10", None, [0, 21, 42, 63]),
 ])
 def test_chain_step_matches_oracle(pkg, name, T, seqs):
     inp = gu.chain_inputs(name)
@@ -125,6 +131,51 @@ def test_chain_step_matches_oracle(pkg, name, T, seqs):
     assert torch.equal(out_h, torch.cat([snap[2], snap[3], snap[1].flatten()]).cpu())
 
 
+def _aligned_chain_ref(inp, T, seqs, upto):
+    """Target rows that agree with the oracle's draft rows at positions t < upto for the
+    sequences `seqs` (z = draft logits on the list, -60 elsewhere), and the oracle's whole step
+    verified against them: the accept walk runs past t = 1 (to the bonus draw when upto =
+    gamma)."""
+    cfg = inp["cfg"]
+    dr = oracle.chain_step(inp, T=T, seqs=seqs, verify=False)
+    z = inp["z"].copy()
+    for b in seqs:
+        for t in range(upto):
+            p = dr[b]["positions"][t]
+            z[b, t] = -60.0
+            z[b, t, p["S"]] = p["logits"].astype(np.float32)
+    acc, corr = oracle.verify_chain(
+        z[seqs], [[p["logits"] for p in dr[b]["positions"]] for b in seqs],
+        [[p["S"] for p in dr[b]["positions"]] for b in seqs],
+        np.array([[p["idx"] for p in dr[b]["positions"]] for b in seqs]), inp["u"][seqs], T)
+    ref = {b: dict(positions=dr[b]["positions"], accepted=int(acc[i]), correction=int(corr[i]))
+           for i, b in enumerate(seqs)}
+    return z, ref
+
+
+@pytest.mark.parametrize("name,seqs,upto", [
+    ("large_b64_f10", [0, 21, 42, 63], 6), ("large_b64_f10", [5, 50], 3),
+    ("batched", [0, 13, 31], 6), ("batched", [4, 20], 3),
+])
+def test_chain_step_aligned_targets(pkg, name, seqs, upto):
+    # Whole steps on the wide verification grid (B = 32 at V = 128,256; B = 64 at V = 262,144)
+    # where the sampled sequences' target rows agree with their draft rows, so acceptances,
+    # the residual draw after a later rejection and the bonus draw are compared end to end.
+    inp = gu.chain_inputs(name)
+    cfg = inp["cfg"]
+    T = cfg.T
+    z, ref = _aligned_chain_ref(inp, T, seqs, upto)
+    d = make_chain(pkg, inp, T)
+    d.z.copy_(gu.f32(z))
+    d.step()
+    torch.cuda.synchronize()
+    d.check_status()
+    full = compare_chain(inp, d, T, seqs, ref=ref, z=z)
+    assert full >= max(1, len(seqs) // 2)
+    acc = [ref[b]["accepted"] for b in seqs]
+    assert max(acc) >= min(upto, cfg.gamma - 1)
+
+
 def _replay_io(d, early, late):
     pin = lambda x: (x.cpu().pin_memory(), x)
     out_h = torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory()
@@ -138,49 +189,115 @@ def _replay_io(d, early, late):
     return out_h
 
 
-def test_tree_step_matches_oracle(pkg):
-    for name, seqs in (("tiny_tree", None),):
-        inp = gu.tree_inputs(name)
-        cfg = inp["cfg"]
-        d = pkg.pipeline.TreeDrafter(
-            gu.device_head(inp), gu.bf16(inp["W1"]), gu.bf16(inp["b1"]), gu.bf16(inp["W2"]), gu.bf16(inp["b2"]),
-            torch.as_tensor(inp["csr_off"]), torch.as_tensor(inp["csr_tok"]), inp["parent"],
-            B=cfg.B, D=cfg.gamma, Wd=cfg.width, budget=cfg.budget, act=cfg.act, T=cfg.T, seed=inp["gumbel_seed"])
-        d.Hr_h.copy_(gu.bf16(np.ascontiguousarray(inp["Hr_h"].transpose(1, 0, 2))))
-        d.Hn.copy_(gu.bf16(inp["Hn"]))
-        d.z.copy_(gu.f32(inp["z"]))
-        d.u_node.copy_(gu.f32(inp["u_node"]))
-        d.u_res.copy_(gu.f32(inp["u_res"]))
-        d.step()
-        torch.cuda.synchronize()
-        d.check_status()
-        ref = oracle.tree_step(inp)
-        Wd, D = cfg.width, cfg.gamma
-        offs = d.vs_offsets.cpu().numpy()
-        logits = d.logits.cpu().numpy()
-        toks = d.tokens.cpu().numpy()
-        tix = d.token_idx.cpu().numpy()
-        for b in (range(cfg.B) if seqs is None else seqs):
-            ok = True
-            for k in range(D):
-                dp = ref[b]["depths"][k]
-                if not topk_same_or_excused(d.cluster_ids[k][b].cpu().numpy(), dp["scores"], cfg.budget[k]):
+@functools.lru_cache(maxsize=2)
+def _tree_draft(name, seqs):
+    """The oracle's drafting part of a tree step (routers, lists, node logits and tokens)."""
+    return oracle.tree_step(gu.tree_inputs(name), seqs=list(seqs), verify=False)
+
+
+def _tree_targets(inp, dr, seqs, aligned):
+    """Target logits: the workload's, or, for the sampled sequences, rows that agree with the
+    first child's draft row at every node (z = that row on the depth's list, -60 elsewhere), so
+    the walk accepts deep into the tree."""
+    if not aligned:
+        return inp["z"]
+    cfg = inp["cfg"]
+    D, Wd = cfg.gamma, cfg.width
+    parent = np.asarray(inp["parent"])
+    z = inp["z"].copy()
+    for b in seqs:
+        for n in range(-1, D * Wd):
+            dep = n // Wd + 1 if n >= 0 else 0          # 0-based depth of n's children
+            if dep >= D:
+                continue
+            kids = np.nonzero(parent == n)[0]
+            if kids.size == 0:
+                continue
+            dd = dr[b]["depths"][dep]
+            z[b, n + 1] = -60.0
+            z[b, n + 1, dd["S"]] = dd["nodes"][int(kids[0]) % Wd]["logits"].astype(np.float32)
+    return z
+
+
+@pytest.mark.parametrize("name,seqs,aligned", [
+    ("tiny_tree", (0, 1), False), ("tiny_tree", (0, 1), True),
+    ("tree", (0, 5), False), ("tree", (0, 5), True),
+])
+def test_tree_step_matches_oracle(pkg, name, seqs, aligned):
+    # The whole tree step (routers, per-depth lists, node rows on the union head, draws, tree
+    # verification) against the oracle, on the tiny tree and at the tree workload's full size
+    # (B = 8, 6 depths x 10 nodes, V = 128,256) on sampled sequences, with the workload's
+    # target rows and with rows that make the walk accept deep into the tree.
+    inp = gu.tree_inputs(name)
+    cfg = inp["cfg"]
+    D, Wd, T = cfg.gamma, cfg.width, cfg.T
+    seqs = list(seqs)
+    dr = _tree_draft(name, tuple(seqs))
+    z = _tree_targets(inp, dr, seqs, aligned)
+    d = pkg.pipeline.TreeDrafter(
+        gu.device_head(inp), gu.bf16(inp["W1"]), gu.bf16(inp["b1"]), gu.bf16(inp["W2"]), gu.bf16(inp["b2"]),
+        torch.as_tensor(inp["csr_off"]), torch.as_tensor(inp["csr_tok"]), inp["parent"],
+        B=cfg.B, D=D, Wd=Wd, budget=cfg.budget, act=cfg.act, T=T, seed=inp["gumbel_seed"])
+    d.Hr_h.copy_(gu.bf16(np.ascontiguousarray(inp["Hr_h"].transpose(1, 0, 2))))
+    d.Hn.copy_(gu.bf16(inp["Hn"]))
+    d.z.copy_(gu.f32(z))
+    d.u_node.copy_(gu.f32(inp["u_node"]))
+    d.u_res.copy_(gu.f32(inp["u_res"]))
+    d.step()
+    torch.cuda.synchronize()
+    d.check_status()
+    N = D * Wd
+    Sx = [[dr[b]["depths"][k]["S"] for k in range(D)] for b in seqs]
+    Lx = [[dr[b]["depths"][n // Wd]["nodes"][n % Wd]["logits"] for n in range(N)] for b in seqs]
+    Ix = np.array([[dr[b]["depths"][n // Wd]["nodes"][n % Wd]["idx"] for n in range(N)] for b in seqs])
+    acc_ref, corr_ref, path_ref = oracle.verify_tree(z[seqs], inp["parent"], Sx, Lx, Ix, inp["u_node"][seqs],
+                                                     inp["u_res"][seqs], T)
+    offs = d.vs_offsets.cpu().numpy()
+    logits = d.logits.cpu().numpy()
+    toks = d.tokens.cpu().numpy()
+    tix = d.token_idx.cpu().numpy()
+    full = 0
+    for i, b in enumerate(seqs):
+        ok = True
+        for k in range(D):
+            dp = dr[b]["depths"][k]
+            if not topk_same_or_excused(d.cluster_ids[k][b].cpu().numpy(), dp["scores"], cfg.budget[k]):
+                ok = False
+                break
+            n_b = dp["S"].size
+            assert offs[k, b + 1] - offs[k, b] == n_b
+            for j in range(Wd):
+                base = offs[k, b] * Wd + j * n_b
+                nd = dp["nodes"][j]
+                assert_close(logits[k, base:base + n_b], nd["logits"], "tree head logits")
+                if not token_same_or_excused(int(tix[k, b * Wd + j]), nd["idx"], nd["logits"], dp["S"],
+                                             T, inp["gumbel_seed"], k + 1, b * Wd + j):
                     ok = False
-                    break
-                n_b = dp["S"].size
-                for i in range(Wd):
-                    base = offs[k, b] * Wd + i * n_b
-                    nd = dp["nodes"][i]
-                    assert_close(logits[k, base:base + n_b], nd["logits"], "tree head logits")
-                    if not token_same_or_excused(int(tix[k, b * Wd + i]), nd["idx"], nd["logits"], dp["S"],
-                                                 cfg.T, inp["gumbel_seed"], k + 1, b * Wd + i):
-                        ok = False
-                    else:
-                        assert toks[k, b * Wd + i] == nd["token"]
-            if ok:
-                assert d.accepted[b].item() == ref[b]["accepted"]
-                assert d.path[b].tolist() == ref[b]["path"]
-                assert d.correction[b].item() == ref[b]["correction"]
+                else:
+                    assert toks[k, b * Wd + j] == nd["token"]
+            if not ok:
+                break
+        if not ok:
+            continue
+        assert d.accepted[b].item() == acc_ref[i], (b, d.accepted[b].item(), acc_ref[i])
+        assert d.path[b].tolist() == path_ref[i].tolist()
+        cg = d.correction[b].item()
+        if cg != corr_ref[i]:
+            # inverse-CDF near-tie: the GPU's token lies between the oracle's draws at
+            # u_res -/+ ICDF_TOL with the same accepted path
+            assert T > 0
+            ur = inp["u_res"][seqs]
+            lo = oracle.verify_tree(z[seqs], inp["parent"], Sx, Lx, Ix, inp["u_node"][seqs],
+                                    np.clip(ur - ICDF_TOL, 0, 1).astype(np.float32), T)
+            hi = oracle.verify_tree(z[seqs], inp["parent"], Sx, Lx, Ix, inp["u_node"][seqs],
+                                    np.clip(ur + ICDF_TOL, 0, 1).astype(np.float32), T)
+            assert lo[0][i] == acc_ref[i] and hi[0][i] == acc_ref[i]
+            assert lo[1][i] <= cg <= hi[1][i], (b, cg, corr_ref[i], lo[1][i], hi[1][i])
+        full += 1
+    assert full >= 1
+    if aligned:
+        assert max(acc_ref) >= 2                         # the walk went past the first depths
+    if name == "tiny_tree" and not aligned:
         # the step with its host transfers gives the same results block
         snap = d.out.clone()
         out_h = _replay_io(d, early=(d.Hr_h, d.Hn), late=(d.z, d.u_node, d.u_res))

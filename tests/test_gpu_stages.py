@@ -371,7 +371,8 @@ def test_head_union_full_size_sampled(ds, G):
     rng = np.random.default_rng(5)
     Hrows = inp["H"][:B, 1] if G == 1 else wl.to_bf16_bits(rng.standard_normal((B * G, 4096)).astype(np.float32))
     out = _run_head(ds, inp, Hrows, G, ids, 0.7, 1, union=True)
-    _check_head(inp, Hrows, G, ids, 0.7, 1, out, rows_to_check=[0, 5, B * G // 2, B * G - 1])
+    # every row of the first and the last list
+    _check_head(inp, Hrows, G, ids, 0.7, 1, out, rows_to_check=list(range(G)) + list(range((B - 1) * G, B * G)))
 
 
 # ---------------------------------------------------------------------------------------
@@ -493,6 +494,59 @@ def test_verify_chain(ds, name, B, T, mode):
         u = wl.open_uniforms(rng, u.shape)
     if mode == "aligned" and T > 0:
         assert acc_ref.mean() > 0.5 * cfg.gamma           # the accept path is exercised
+
+
+def _synthetic_chain_rows(inp, B, T, rng):
+    """Seeded draft data at a workload's sizes without running the drafter: per (sequence,
+    position) a random set of budget[t] clusters, its shortlist, N(0, 2^2) draft logits and a
+    token drawn from them."""
+    cfg = inp["cfg"]
+    rows = []
+    for b in range(B):
+        r = []
+        for t in range(cfg.gamma):
+            ids = np.sort(rng.choice(cfg.M, cfg.budget[t], replace=False)).astype(np.int32)
+            S = oracle.shortlist(inp["csr_off"], inp["csr_tok"], ids)
+            l = rng.standard_normal(S.size) * 2.0
+            idx = int(np.argmax(l / T + rng.gumbel(size=S.size))) if T > 0 else int(np.argmax(l))
+            r.append(dict(ids=ids, S=S, logits=l, token=int(S[idx]), idx=idx))
+        rows.append(r)
+    return rows
+
+
+@pytest.mark.parametrize("T", [0.7, 0.0])
+@pytest.mark.parametrize("mode", ["independent", "aligned", "half"])
+def test_verify_chain_wide_grid(ds, T, mode):
+    # The batched workload's sizes (B = 32, gamma = 6, V = 128,256): the verifier takes its wide
+    # grid here (8192-element statistics chunks, 2048-element residual chunks without staging),
+    # and with target rows that agree with the draft the accept walk runs past t = 1 and, in
+    # "aligned", to the bonus draw from row gamma + 1.
+    inp = gu.chain_inputs("batched")
+    cfg = inp["cfg"]
+    B = cfg.B
+    rng = np.random.default_rng(23)
+    rows = _synthetic_chain_rows(inp, B, T if T > 0 else 1.0, rng)
+    z = inp["z"][:B].copy()
+    if mode != "independent":
+        upto = cfg.gamma if mode == "aligned" else cfg.gamma // 2
+        for b in range(B):
+            for t in range(upto):
+                S, l = rows[b][t]["S"], rows[b][t]["logits"]
+                z[b, t] = -60.0
+                z[b, t, S] = l.astype(np.float32)
+                if T == 0.0:
+                    z[b, t, rows[b][t]["token"]] += 1.0
+    u = inp["u"][:B].copy()
+    longest = 0
+    for trial in range(2):
+        acc, acc_ref, n_exact = _check_chain_verify(ds, inp, rows, z, u, T)
+        longest = max(longest, int(acc_ref.max()))
+        assert n_exact >= B // 2
+        u = wl.open_uniforms(rng, u.shape)
+    if mode == "aligned":
+        assert longest == cfg.gamma                        # a bonus draw was compared
+    if mode == "half":
+        assert longest >= cfg.gamma // 2
 
 
 @pytest.mark.parametrize("gamma", [1, 32])
@@ -746,3 +800,45 @@ def test_verify_draft_token_outside_its_list_sets_status(ds):
     torch.cuda.synchronize()
     assert st.item() & BAD_INDEX
     assert acc.item() == 0                              # the bad draft is rejected
+
+
+# ---------------------------------------------------------------------------------------
+# Bounded waits: a pipeline wait that runs out of budget gives up, reports DS_DEV_TIMEOUT
+# (0x40) in the status word and lets the call return; nothing hangs or faults, and the
+# context stays usable.
+# ---------------------------------------------------------------------------------------
+TIMEOUT = 0x40
+
+
+def test_bounded_wait_gives_up_and_reports_timeout(ds):
+    # The union head (tensor-core GEMM) with a pipeline-wait budget of one cycle: the MMA
+    # thread's wait for the first stage cannot be met that fast, so it gives up and the other
+    # roles stop after it (the MMA thread still drains its own work before the tensor memory is
+    # freed).  Then, with the default budget back and a fresh workspace, the same call is exact.
+    inp = gu.chain_inputs("small_batched")
+    cfg = inp["cfg"]
+    B = 5
+    ids, _ = _oracle_lists(inp, B, 1)
+    Hrows = inp["H"][:B, 1]
+    vs_off, vs_ids, cpos, un, st = _gpu_shortlist(ds, inp, ids, union=True)
+    assert st.item() == 0
+    cof, rk = _vocab_index_dev(ds, inp)
+    R = B
+    logits = torch.zeros(B * cfg.V, dtype=torch.float32, device=gu.dev())
+    tok = torch.empty(R, dtype=torch.int32, device=gu.dev())
+    tix = torch.empty(R, dtype=torch.int32, device=gu.dev())
+    statuses = []
+    try:
+        ds.set_wait_budget(1)
+        for trial in range(2):
+            st = gu.status()
+            ws = ds.workspace(ds.head_workspace_bytes(R), gu.dev())     # a timed-out call's counters stay behind
+            ds.gathered_head(gu.bf16(Hrows), 1, gu.device_head(inp), vs_off, vs_ids, 0.8, inp["gumbel_seed"], 1,
+                             logits, tok, tix, ws, st, cpos=cpos, rank_in_cluster=rk, union=un)
+            torch.cuda.synchronize()
+            statuses.append(int(st.item()))
+    finally:
+        ds.set_wait_budget(0)
+    assert all(x & TIMEOUT for x in statuses), statuses
+    out = _run_head(ds, inp, Hrows, 1, ids, 0.8, 1, union=True)
+    _check_head(inp, Hrows, 1, ids, 0.8, 1, out)

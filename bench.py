@@ -78,6 +78,8 @@ def whole_job_rate(world, units_per_step, steps, job_ms):
 def workload_config(cfg):
     kind = (f"chain drafting, B={cfg.B}, gamma={cfg.gamma}" if cfg.mode == "chain" else
             f"tree drafting, B={cfg.B}, depth {cfg.gamma} x {cfg.width} nodes")
+    if cfg.static:
+        kind += f", one fixed {cfg.static}-token shortlist (no router)"
     return {"workload": f"{cfg.name}: {kind}, V={cfg.V}, d={cfg.d}, T={cfg.T}",
             "V": cfg.V, "d": cfg.d, "clusters": cfg.M, "router": f"{cfg.d}->{cfg.Hr}->{cfg.M} {cfg.act}",
             "B": cfg.B, "gamma": cfg.gamma, "budget": list(cfg.budget), "T": cfg.T,
@@ -269,8 +271,12 @@ def build_drafter(cfg, inp, dev, pkg, torch, W):
     common = (W, bf(inp["W1"]), bf(inp["b1"]), bf(inp["W2"]), bf(inp["b2"]),
               torch.as_tensor(inp["csr_off"]), torch.as_tensor(inp["csr_tok"]))
     if cfg.mode == "chain":
-        d = pkg.pipeline.ChainDrafter(*common, B=cfg.B, gamma=cfg.gamma, budget=cfg.budget, act=cfg.act,
-                                      T=cfg.T, seed=inp["gumbel_seed"])
+        if cfg.static:
+            d = pkg.pipeline.StaticChainDrafter(W, inp["static_ids"], B=cfg.B, gamma=cfg.gamma, T=cfg.T,
+                                                seed=inp["gumbel_seed"])
+        else:
+            d = pkg.pipeline.ChainDrafter(*common, B=cfg.B, gamma=cfg.gamma, budget=cfg.budget, act=cfg.act,
+                                          T=cfg.T, seed=inp["gumbel_seed"])
         host = {"H": (pinned_bf(inp["H"].transpose(1, 0, 2)), d.H),
                 "z": (torch.from_numpy(inp["z"]).pin_memory(), d.z),
                 "u": (torch.from_numpy(inp["u"]).pin_memory(), d.u)}
@@ -298,14 +304,19 @@ def algorithmic_bytes(cfg, d):
     n_pos = cfg.gamma
     offs = d.vs_offsets.cpu().numpy()
     sizes = np.diff(offs, axis=1)                                       # [pos, B]
-    union = d.union_count.cpu().numpy()[:, 0] if getattr(d, "union", True) and hasattr(d, "union_count") else None
+    if not getattr(d, "union", True):
+        union = None
+    elif cfg.static:
+        union = np.full(n_pos, cfg.static)                              # the one list is the union
+    else:
+        union = d.union_count.cpu().numpy()[:, 0]
     heads = []
     for t in range(n_pos):
         S = float(sizes[t].sum())
         rows = S if union is None else float(union[t])                   # W rows streamed
         ids_bytes = 4 * rows if union is None else 8 * rows              # list ids / union ids + clusters
         heads.append(rows * 2 * dd + ids_bytes + 4 * S * G + cfg.B * G * 2 * dd)
-    router = 2 * (Hr * dd + Hr + M * Hr + M) + cfg.B * (2 * dd + 4 * Hr * 2 + 4 * M)
+    router = 0 if cfg.static else 2 * (Hr * dd + Hr + M * Hr + M) + cfg.B * (2 * dd + 4 * Hr * 2 + 4 * M)
     rows_target = cfg.gamma + 1 if cfg.mode == "chain" else 1 + cfg.gamma * cfg.width
     verify = 4 * cfg.B * rows_target * V
     return heads, float(sum(heads) + n_pos * router + verify), (union.tolist() if union is not None else None), sizes
@@ -440,8 +451,78 @@ def measure(cfg, seed, dev, pkg, torch, world, local_rank, steps, warmup, e2e_st
     return res
 
 
+STANDIN_F = 14336                 # drafter stand-in MLP width (Llama-3-8B's)
+
+
+def measure_overlap(cfg, seed, dev, pkg, torch, steps, warmup, flush):
+    """The router's overlap with the drafter at batch 1 (DynaSpec summary, Pipeline Flow: the
+    router runs on its own stream beside the drafter).  A drafter stand-in with the weight bytes
+    of an EAGLE step runs before every head (ds_drafter_standin, scale 0 so the hidden states stay
+    the workload's); router t+1 waits for the drafter step that computes its input.  The same
+    step with the routers serialised on the main stream gives the router's full cost, so
+    serial - overlapped = the router time the overlap hides."""
+    import workloads as wl
+    inp = wl.chain_inputs(cfg, seed, with_head=False)
+    W = device_head(cfg, seed, dev, torch)
+    d, host, tokens_per_step = build_drafter(cfg, inp, dev, pkg, torch, W)
+    g = torch.Generator(device=dev).manual_seed(seed + 101)
+    mk = lambda *shape: (torch.randn(*shape, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    d.attach_drafter(mk(cfg.d, 2 * cfg.d), mk(cfg.d, cfg.d), mk(2 * STANDIN_F, cfg.d), mk(cfg.d, STANDIN_F),
+                     scale=0.0)
+    d.H_base.copy_(d.H)
+    d.x0.fill_(int(inp["csr_tok"][0]))
+    standin_bytes = 2 * (2 * cfg.d * cfg.d + cfg.d * cfg.d + 3 * STANDIN_F * cfg.d)
+    main = torch.cuda.current_stream(dev)
+    out = {"standin_weight_bytes_per_step": standin_bytes * cfg.gamma, "standin_F": STANDIN_F}
+    for serial in (False, True):
+        d.serial_router = serial
+        d.head_events = None
+        d.route_events = None
+        if not serial:
+            d.enable_head_timing()
+            d.enable_overlap_timing()
+        d.capture()
+        for _ in range(max(3, warmup)):
+            flush(1)
+            d.replay()
+        torch.cuda.synchronize()
+        d.check_status()
+        ms = []
+        for i in range(steps):
+            flush(i)
+            a = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            d.replay()
+            e.record(main)
+            e.synchronize()
+            ms.append(a.elapsed_time(e))
+        out["serial_us" if serial else "overlapped_us"] = 1e3 * float(np.median(ms))
+        if not serial:
+            ov = []
+            for i in range(max(1, min(steps, 16))):
+                flush(i)
+                d.replay(timed=True)
+                torch.cuda.synchronize()
+                ov.append(d.overlap_times_ms())
+            ov = np.median(np.array(ov), axis=0)           # [gamma, 6] ms
+            out["router_us_per_position"] = [1e3 * float(x) for x in ov[:, 1] - ov[:, 0]]
+            out["drafter_us_per_position"] = [1e3 * float(x) for x in ov[:, 3] - ov[:, 2]]
+            out["head_us_per_position"] = [1e3 * float(x) for x in ov[:, 5] - ov[:, 4]]
+            # router t (t >= 1) starts after drafter step t-1; what the head of t waits for beyond
+            # its own drafter step is the exposed part
+            out["router_exposed_us_per_position"] = [1e3 * float(max(0.0, ov[t, 1] - ov[t, 3]))
+                                                     for t in range(cfg.gamma)]
+    d.check_status()
+    out["hidden_router_us_per_step"] = out["serial_us"] - out["overlapped_us"]
+    out["router_total_us_per_step"] = float(sum(out["router_us_per_position"]))
+    out["tokens_per_s_overlapped"] = tokens_per_step / (out["overlapped_us"] * 1e-6)
+    del d, host
+    return out
+
+
 # Workloads measured after the headline, in the same process (same flush and timing).
-PER_CONFIG = ["batched", "tree", "large_b1_f5", "large_b64_f100"]
+PER_CONFIG = ["llama_b1_static32k", "batched", "tree", "large_b1_f5", "large_b64_f100"]
 
 
 def run_ours(args):
@@ -483,6 +564,9 @@ def run_ours(args):
                         "h2d_bytes_per_step": q["e2e"]["h2d_bytes_per_step"],
                         "d2h_bytes_per_step": q["e2e"]["d2h_bytes_per_step"]},
                 "breakdown_us": q["breakdown_us"], "clocks": q["clocks"], "gpu_launches": q["gpu_launches"]}
+        torch.cuda.empty_cache()
+        per_config["llama_b1_drafter_overlap"] = measure_overlap(
+            wl.config("llama_b1"), seed, dev, pkg, torch, max(args.steps, 20), args.warmup, flush)
         _HEAD_CACHE.clear()
 
     if rank != 0:

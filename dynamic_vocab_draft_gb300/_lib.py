@@ -43,6 +43,11 @@ SIGNATURES = {
                             P, P, P, P, SZ, P, P]),
     "ds_workspace_bytes": (SZ, [I, I, I, I, I, I, I]),
     "ds_set_wait_budget": (ST, [I64]),
+    "ds_kmeans_workspace_bytes": (SZ, [I, I, I]),
+    "ds_kmeans_init": (ST, [P, I, I, P, I, P, P, P, P]),
+    "ds_kmeans_step": (ST, [P, I, I, I, P, P, P, P, P, P, SZ, P, P]),
+    "ds_drafter_standin_workspace_bytes": (SZ, [I, I]),
+    "ds_drafter_standin": (ST, [P, P, I, P, P, P, P, P, I, I, P, F, P, P, SZ, P, P]),
     "ds_philox4x32_10": (ST, [P, U64, P, I, P]),
     "ds_event_record": (ST, [P, P]),
     "ds_copy": (ST, [P, P, SZ, P]),

@@ -224,6 +224,47 @@ def verify_tree(p_logits, D, Wd, T, parent, q_logits, vs_offsets, vs_ids, cpos, 
         _stream(stream)), "ds_verify_tree")
 
 
+def kmeans_workspace_bytes(V, d, M):
+    return int(_lib.load().ds_kmeans_workspace_bytes(V, d, M))
+
+
+def kmeans_init(W, init_rows, cent, inv_norm, status, stream=None):
+    """ds_kmeans_init: W [V, d] bf16; init_rows [M] int32; cent [M, d], inv_norm [V] fp32 (out)."""
+    V, d = W.shape
+    M = init_rows.numel()
+    _lib.check(_lib.load().ds_kmeans_init(
+        _ptr(W, BF16, "W"), V, d, _ptr(init_rows, I32, "init_rows"), M, _ptr(cent, F32, "cent"),
+        _ptr(inv_norm, F32, "inv_norm"), _ptr(status, I32, "status"), _stream(stream)), "ds_kmeans_init")
+
+
+def kmeans_step(W, inv_norm, cent, assign, csr_off, csr_tok, ws, status, stream=None):
+    """ds_kmeans_step: one Lloyd iteration; cent [M, d] fp32 in/out."""
+    V, d = W.shape
+    M = cent.shape[0]
+    _lib.check(_lib.load().ds_kmeans_step(
+        _ptr(W, BF16, "W"), V, d, M, _ptr(inv_norm, F32, "inv_norm"), _ptr(cent, F32, "cent"),
+        _ptr(assign, I32, "assign"), _ptr(csr_off, I32, "csr_off"), _ptr(csr_tok, I32, "csr_tok"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
+        _stream(stream)), "ds_kmeans_step")
+
+
+def drafter_standin_workspace_bytes(d, F):
+    return int(_lib.load().ds_drafter_standin_workspace_bytes(d, F))
+
+
+def drafter_standin(h_prev, x_prev, E, Wfc, Wmix, Wug, Wdn, h_base, scale, h_out, ws, status, stream=None):
+    """ds_drafter_standin: h_prev, h_base, h_out [d] bf16; x_prev a one-element int32 CUDA tensor;
+    E [V, d]; Wfc [d, 2d]; Wmix [d, d]; Wug [2F, d]; Wdn [d, F]."""
+    d = h_prev.numel()
+    F = Wdn.shape[1]
+    _lib.check(_lib.load().ds_drafter_standin(
+        _ptr(h_prev, BF16, "h_prev"), _ptr(x_prev, I32, "x_prev"), E.shape[0], _ptr(E, BF16, "E"),
+        _ptr(Wfc, BF16, "Wfc"), _ptr(Wmix, BF16, "Wmix"), _ptr(Wug, BF16, "Wug"), _ptr(Wdn, BF16, "Wdn"),
+        d, F, _ptr(h_base, BF16, "h_base"), float(scale), _ptr(h_out, BF16, "h_out"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
+        _stream(stream)), "ds_drafter_standin")
+
+
 def philox4x32_10(ctr, seed, out, stream=None):
     n = ctr.shape[0]
     _lib.check(_lib.load().ds_philox4x32_10(

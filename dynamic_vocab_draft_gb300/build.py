@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libdynaspec.so")
-SOURCES = ["api.cu", "router.cu", "shortlist.cu", "head.cu", "verify.cu"]
+SOURCES = ["api.cu", "router.cu", "shortlist.cu", "head.cu", "verify.cu", "drafter.cu", "kmeans.cu"]
 HEADERS = ["common.cuh", "block_scan.cuh", "tc_gemm.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -22,6 +22,13 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
 
+// fp32 -> bf16, round to nearest even (finite inputs).
+__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    return uint16_t((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+
 // Dot product of 8 packed bf16 (one 16-byte vector) with 8 fp32 values.
 __device__ __forceinline__ float dot8(uint4 w, const float4 x0, const float4 x1, float acc)
 {

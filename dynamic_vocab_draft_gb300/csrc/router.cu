@@ -287,12 +287,6 @@ topk_rows_kernel(const float *__restrict__ scores, int M, int k, int32_t *__rest
 constexpr int kRouterTcMaxB = 64;                 // 2B vectors fit one 128-column accumulator
 constexpr int kRouterMaxTiles = kRouterMaxK / tc::kRows;
 
-__device__ __forceinline__ uint16_t f32_to_bf16_rne(float f)
-{
-    const uint32_t u = __float_as_uint(f);
-    return uint16_t((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);      // finite inputs
-}
-
 struct DenseRows {
     int n;
     using State = tc::NoState;

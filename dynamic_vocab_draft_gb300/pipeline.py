@@ -134,20 +134,51 @@ class _Common:
     def _run(self, n, before_verify):
         """Enqueue one step of n positions (see the module docstring for the dependencies).
         Events are recorded before anything waits on them, in host order, so the same code
-        serves eager execution and graph capture."""
+        serves eager execution and graph capture.
+
+        With a drafter stand-in attached (ChainDrafter.attach_drafter) position t first runs the
+        drafter step that computes H[t+1] from H[t] and the previous token on the main stream;
+        the router of position t+1 reads H[t+1] and so waits for that step; with
+        ``serial_router`` the routers run on the main stream right before their heads instead
+        (the schedule without overlap, for comparison)."""
         main = torch.cuda.current_stream(self.dev)
         self.side.wait_stream(main)                # the step's inputs are in place
+        drafter = getattr(self, "drafter", None)
+        serial = getattr(self, "serial_router", False)
+        timing = self.head_events is not None and getattr(self, "route_events", None) is not None
 
-        def route(t):
-            with torch.cuda.stream(self.side):
-                if t >= 2:
-                    self.side.wait_event(self.head_done[t - 2])
+        def route(t, after):
+            if serial:
                 self.route(t)
+                self.ready[t].record(main)
+                return
+            with torch.cuda.stream(self.side):
+                if after is not None:
+                    self.side.wait_event(after)
+                if timing:
+                    api.event_record(self.route_events[t][0])
+                self.route(t)
+                if timing:
+                    api.event_record(self.route_events[t][1])
                 self.ready[t].record(self.side)
 
-        for t in range(min(2, n)):
-            route(t)
+        if drafter is None:
+            for t in range(min(2, n)):
+                route(t, None)
+        elif not serial:
+            route(0, None)
         for t in range(n):
+            if drafter is not None:
+                if timing:
+                    api.event_record(self.draft_events[t][0])
+                self.draft(t)
+                if timing:
+                    api.event_record(self.draft_events[t][1])
+                self.drafted[t].record(main)
+                if serial:
+                    route(t, None)
+                elif t + 1 < n:
+                    route(t + 1, self.drafted[t])
             main.wait_event(self.ready[t])
             if self.head_events:
                 api.event_record(self.head_events[t][0])
@@ -155,8 +186,8 @@ class _Common:
             if self.head_events:
                 api.event_record(self.head_events[t][1])
             self.head_done[t].record(main)
-            if t + 2 < n:
-                route(t + 2)
+            if drafter is None and t + 2 < n:
+                route(t + 2, self.head_done[t])
         for ev in before_verify or ():
             main.wait_event(ev)
         self.verify()
@@ -248,6 +279,56 @@ class ChainDrafter(_Common):
         given (inputs that only verification reads may still be arriving)."""
         self._run(self.gamma, before_verify)
 
+    def attach_drafter(self, Wfc, Wmix, Wug, Wdn, scale=0.0, E=None):
+        """Put a drafter stand-in (ds_drafter_standin) before every head, batch 1 only.  The step
+        then reads H[0] (the hidden state before the first position) and ``self.x0`` (the last
+        accepted token) and computes H[t+1] = bf16(H_base[t+1] + scale * f(H[t], x_t)) for
+        t = 0..gamma-1, x_t being the token drawn at position t (x0 for t = 0); ``self.H_base``
+        [gamma+1, 1, d] holds the base hidden states.  With scale = 0, H[t+1] = H_base[t+1]
+        exactly, so results equal those of the plain step on those hidden states.  E: token
+        embeddings (default: the LM head, tied)."""
+        if self.B != 1:
+            raise ValueError("the drafter stand-in runs at batch 1")
+        dev = self.dev
+        self.drafter = dict(E=self.W if E is None else E, Wfc=Wfc, Wmix=Wmix, Wug=Wug, Wdn=Wdn, scale=float(scale))
+        self.H_base = torch.zeros_like(self.H)
+        self.x0 = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ws_draft = api.workspace(api.drafter_standin_workspace_bytes(self.d, Wdn.shape[1]), dev)
+        self.drafted = [torch.cuda.Event() for _ in range(self.gamma)]
+        self.serial_router = False
+
+    def draft(self, t, stream=None):
+        """The drafter stand-in of position t: H[t+1] from H[t] and the previous token."""
+        dr = self.drafter
+        x_prev = self.x0 if t == 0 else self.tokens[t - 1]
+        api.drafter_standin(self.H[t, 0], x_prev, dr["E"], dr["Wfc"], dr["Wmix"], dr["Wug"], dr["Wdn"],
+                            self.H_base[t + 1, 0], dr["scale"], self.H[t + 1, 0], self.ws_draft, self.status,
+                            stream=stream)
+
+    def enable_overlap_timing(self):
+        """With a drafter attached: also time each position's router + shortlist (side stream)
+        and drafter step (main stream) inside the instrumented graph.  Call after
+        enable_head_timing() and before capture()."""
+        mk = lambda: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(self.gamma)]
+        self.route_events, self.draft_events = mk(), mk()
+        for a, b in self.route_events + self.draft_events:
+            a.record()
+            b.record()
+        torch.cuda.synchronize()
+
+    def overlap_times_ms(self):
+        """Per position: (router start, router end, drafter start, drafter end, head start, head
+        end), in ms from the first drafter step's start (from the last instrumented replay)."""
+        t0 = self.draft_events[0][0]
+        out = []
+        for t in range(self.gamma):
+            r0, r1 = self.route_events[t]
+            d0, d1 = self.draft_events[t]
+            h0, h1 = self.head_events[t]
+            out.append(tuple(t0.elapsed_time(e) for e in (r0, r1, d0, d1, h0, h1)))
+        return out
+
     def n_heads(self) -> int:
         return self.gamma
 
@@ -255,7 +336,8 @@ class ChainDrafter(_Common):
         n_router = router_launches(self.B)
         n_short = 4 if self.union else (1 if self.B == 1 else 3)
         n_head = 2 if self.union else 1
-        return self.gamma * (n_router + n_short + n_head) + 2
+        n_draft = 5 if getattr(self, "drafter", None) is not None else 0
+        return self.gamma * (n_router + n_short + n_head + n_draft) + 2
 
 
 class TreeDrafter(_Common):
@@ -347,3 +429,103 @@ class TreeDrafter(_Common):
 
     def launches_per_step(self) -> int:
         return self.D * (router_launches(self.B) + 4 + 2) + 2
+
+
+class StaticChainDrafter(_Common):
+    """The static-shortlist baseline: chain drafting with one fixed token list at every draft
+    position and for every sequence, through the same head and verification kernels, with no
+    router and no per-position shortlist build.  The pages compare DynaSpec's context-dependent
+    lists (about 28K tokens on average) with a fixed 32K-token list (DynaSpec abstract; summary,
+    Key Results and Comparison to Prior Work).
+
+    The list enters the library as a two-cluster partition of the vocabulary: cluster 0 holds
+    the list's tokens in list order, cluster 1 the rest, and every sequence selects cluster 0.
+    The head and the verifier then find a token's list position through the same cluster
+    inverse as for dynamic lists.  Inputs as for ChainDrafter (``self.H``: the heads read
+    H[t+1]; ``self.z``, ``self.u``).
+    """
+
+    def __init__(self, W, static_ids, *, B, gamma, T, seed, union=None):
+        dev = W.device
+        self.dev = dev
+        self.W = W
+        V = W.shape[0]
+        ids = torch.as_tensor(static_ids, dtype=torch.int32).flatten().cpu()
+        n = ids.numel()
+        if n < 1 or n > V:
+            raise ValueError("the static list needs 1..V tokens")
+        member = torch.zeros(V, dtype=torch.bool)
+        member[ids.long()] = True
+        if int(member.sum()) != n:
+            raise ValueError("the static list repeats a token")
+        rest = torch.nonzero(~member).flatten().to(torch.int32)
+        self._setup_vocab(torch.tensor([0, n, V], dtype=torch.int32), torch.cat([ids, rest]), dev)
+        self.d = W.shape[1]
+        self.B, self.gamma, self.n_static = B, gamma, n
+        self.T, self.seed = float(T), int(seed)
+        self.union = (B > 1) if union is None else bool(union)
+        M = self.M                                         # 2
+        i32 = dict(dtype=torch.int32, device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        cap = B * n
+        # the lists, built once: every sequence selects cluster 0
+        offs1 = torch.zeros(B + 1, **i32)
+        vs1 = torch.zeros(cap, **i32)
+        cpos1 = torch.empty(B * M, **i32)
+        un = (torch.empty(V, **i32), torch.empty(V, **i32), torch.zeros(1, **i32)) if self.union else (None,) * 3
+        ws = api.workspace(api.shortlist_workspace_bytes(B, M), dev)
+        api.build_shortlist(self.csr_off, self.csr_tok, torch.zeros(B, 1, **i32), offs1, vs1, cpos1, ws,
+                            self.status, *un)
+        self.vs_offsets = offs1.repeat(gamma, 1).contiguous()
+        self.vs_ids = vs1
+        self.cpos = cpos1.repeat(gamma, 1).contiguous()
+        self.union_ids, self.union_cluster, self.union_count = un
+        self.H = torch.zeros(gamma + 1, B, self.d, dtype=torch.bfloat16, device=dev)
+        self.z = torch.zeros(B, gamma + 1, V, **f32)
+        self.u = torch.full((B, gamma + 1), 0.5, **f32)
+        self.logits = torch.zeros(gamma, cap, **f32)
+        self.row_max = torch.empty(gamma, B, **f32)
+        self.row_sumexp = torch.empty(gamma, B, **f32)
+        self.out = torch.empty((2 + gamma) * B, **i32)
+        self.accepted = self.out[:B]
+        self.correction = self.out[B:2 * B]
+        self.tokens = self.out[2 * B:].view(gamma, B)
+        self.token_idx = torch.empty(gamma, B, **i32)
+        self.ws_head = api.workspace(api.head_workspace_bytes(B), dev)
+        self.ws_verify = api.workspace(api.verify_workspace_bytes(B, gamma, V), dev)
+        self.graph = None
+        self.head_events = None
+        torch.cuda.synchronize()
+        self.check_status()
+
+    def head(self, t, stream=None):
+        api.gathered_head(self.H[t + 1], 1, self.W, self.vs_offsets[t], self.vs_ids, self.T,
+                          self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],
+                          self.ws_head, self.status, cpos=self.cpos[t], rank_in_cluster=self.rank,
+                          union=(self.union_ids, self.union_cluster, self.union_count) if self.union else None,
+                          row_max=self.row_max[t], row_sumexp=self.row_sumexp[t], stream=stream)
+
+    def verify(self, stream=None):
+        api.verify(self.z, self.T, self.logits, self.vs_offsets, self.cpos, self.cluster_of, self.rank,
+                   self.tokens, self.u, self.accepted, self.correction, self.ws_verify, self.status,
+                   q_max=self.row_max, q_sumexp=self.row_sumexp, stream=stream)
+
+    def step(self, before_verify=None):
+        """One speculation step: the gamma heads on the current stream, then verification
+        (which first waits for the events in `before_verify`, if given)."""
+        main = torch.cuda.current_stream(self.dev)
+        for t in range(self.gamma):
+            if self.head_events:
+                api.event_record(self.head_events[t][0])
+            self.head(t)
+            if self.head_events:
+                api.event_record(self.head_events[t][1])
+        for ev in before_verify or ():
+            main.wait_event(ev)
+        self.verify()
+
+    def n_heads(self) -> int:
+        return self.gamma
+
+    def launches_per_step(self) -> int:
+        return self.gamma * (2 if self.union else 1) + 2

@@ -333,6 +333,56 @@ size_t ds_workspace_bytes(int op, int B, int V, int M, int gamma, int hidden, in
 ds_status ds_set_wait_budget(int64_t cycles);
 
 /* -------------------------------------------------------------------------------------
+ * Spherical k-means over the LM-head rows -- the offline step that forms the clusters the
+ * router scores (summary, Key Novelty and Key Hyperparameters: the LM-head rows are clustered
+ * by spherical k-means; the pages give no iteration details).  Lloyd iteration for the cosine
+ * objective, centroids of unit length:
+ *   ds_kmeans_init   inv_norm [V] fp32 (out): 1 / |W_v| (0 for a zero row); cent [M, d] fp32
+ *                    (out): rows init_rows[0..M) of W scaled to unit length (init_rows: device,
+ *                    M distinct row ids, e.g. a seeded random draw the caller makes).
+ *   ds_kmeans_step   one iteration from cent (in/out):
+ *                      assign [V] (out): argmax_c <W_v, bf16(cent_c)>, fp32 accumulation on the
+ *                        tensor cores, ties to the lower c;
+ *                      csr_off [M+1], csr_tok [V] (out): the clusters as CSR, ascending cluster
+ *                        id, each cluster's tokens in ascending token id (the input of
+ *                        ds_vocab_index and ds_build_shortlist);
+ *                      cent (out): normalised sum of W_v * inv_norm[v] over each cluster's
+ *                        tokens, added in that order in fp32; an empty cluster keeps its row.
+ * Device errors: DS_DEV_BAD_INDEX for an init row outside [0, V).
+ * Limits: d % 8 == 0, d <= 8192, M <= min(V, 4096), V <= 2^20.
+ * ws: ds_kmeans_workspace_bytes(V, d, M) bytes (completion counters: zero it once).
+ * ------------------------------------------------------------------------------------- */
+size_t ds_kmeans_workspace_bytes(int V, int d, int M);
+ds_status ds_kmeans_init(const uint16_t *W, int V, int d, const int32_t *init_rows, int M,
+                         float *cent, float *inv_norm, int32_t *dev_status, cudaStream_t stream);
+ds_status ds_kmeans_step(const uint16_t *W, int V, int d, int M, const float *inv_norm, float *cent,
+                         int32_t *assign, int32_t *csr_off, int32_t *csr_tok,
+                         void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
+ * ds_drafter_standin -- measurement helper (the drafter trunk is not part of the DynaSpec path
+ * and has no trained weights here): one drafter step with the shape and weight bytes of an
+ * EAGLE-style step at batch 1, so that the router's overlap with the drafter (summary, Pipeline
+ * Flow; Novel Architectural Elements: the router on its own stream beside the drafter) can be
+ * measured on the method's schedule.  fp32 accumulation:
+ *   u = [h_prev ; E[x_prev]] (2d);  y1 = Wfc u;  y2 = Wmix y1;
+ *   a_j = silu(Wug[j] . y2) * (Wug[F + j] . y2)  (j < F);  h_out = bf16(h_base + scale * (Wdn a))
+ *   h_prev [d], h_base [d] bf16; x_prev (device, one int32): the previous draft token;
+ *   E [V, d] bf16 (token embeddings; the LM head when they are tied);
+ *   Wfc [d, 2d], Wmix [d, d], Wug [2F, d], Wdn [d, F] bf16 row-major;  h_out [d] bf16 (out).
+ * h_out depends on x_prev through the whole chain; with scale = 0 it equals h_base bit for bit.
+ * Device errors: DS_DEV_BAD_INDEX when x_prev is outside [0, V) (row 0 is used).
+ * Limits: d % 8 == 0, F % 8 == 0.  ws: ds_drafter_standin_workspace_bytes(d, F) bytes.
+ * Five launches on `stream`, on all but eight SMs (those are left to a side stream).
+ * ------------------------------------------------------------------------------------- */
+size_t ds_drafter_standin_workspace_bytes(int d, int F);
+ds_status ds_drafter_standin(const uint16_t *h_prev, const int32_t *x_prev, int V,
+                             const uint16_t *E, const uint16_t *Wfc, const uint16_t *Wmix,
+                             const uint16_t *Wug, const uint16_t *Wdn, int d, int F,
+                             const uint16_t *h_base, float scale, uint16_t *h_out,
+                             void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
  * ds_philox4x32_10 -- the device Philox4x32-10 the head draws its Gumbel noise from
  * (Salmon, Moraes, Dror, Shaw, SC'11), exposed so that it can be checked on its own.
  *   ctr [n, 4] counters, out [n, 4] words; key = the two 32-bit halves of `seed`.

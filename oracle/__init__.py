@@ -69,6 +69,10 @@ def lib():
         L.orc_verify_tree.argtypes = [_I, _I, _I, _I, _D, _P, _P, _P, _P, _P, _P, _P,
                                       _P, _P, _P, _P, _P]
         L.orc_verify_tree.restype = _I
+        L.orc_kmeans_init.argtypes = [_P, _I, _I, _P, _I, _P]
+        L.orc_kmeans_init.restype = _I
+        L.orc_kmeans_step.argtypes = [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P]
+        L.orc_kmeans_step.restype = _I
         _lib = L
     return _lib
 
@@ -314,3 +318,62 @@ def tree_step(inp: dict, T: float | None = None, seqs=None, verify=True):
         for i, b in enumerate(seq_list):
             out[b].update(accepted=int(acc[i]), correction=int(corr[i]), path=path[i].tolist())
     return out
+
+
+def static_chain_step(inp: dict, T: float | None = None, seqs=None, verify=True):
+    """The static-shortlist baseline's chain step: the fixed list inp["static_ids"] at every
+    position (no router), then the same head, draft sampling and verification as chain_step
+    (DynaSpec abstract and summary, Comparison to Prior Work: the fixed-shortlist drafters the
+    pages compare against).  Same return layout as chain_step (without scores and ids)."""
+    cfg = inp["cfg"]
+    T = cfg.T if T is None else T
+    seqs = list(range(cfg.B) if seqs is None else seqs)
+    S = np.asarray(inp["static_ids"], dtype=np.int32)
+    out = {}
+    for b in seqs:
+        rows = []
+        for t in range(cfg.gamma):
+            l = head(inp["H"][b, t + 1][None], inp["W"], S)[0]
+            tok, idx, m, ssum = draft_sample(l, S, T, inp["gumbel_seed"], t + 1, b)
+            rows.append(dict(S=S, logits=l, token=tok, idx=idx, m=m, s=ssum))
+        out[b] = dict(positions=rows)
+    if verify:
+        acc, corr = verify_chain(
+            inp["z"][seqs], [[p["logits"] for p in out[b]["positions"]] for b in seqs],
+            [[S] * cfg.gamma for _ in seqs],
+            np.array([[p["idx"] for p in out[b]["positions"]] for b in seqs]), inp["u"][seqs], T)
+        for i, b in enumerate(seqs):
+            out[b].update(accepted=int(acc[i]), correction=int(corr[i]))
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# Spherical k-means over the LM-head rows (the offline clustering step before the path)
+# ---------------------------------------------------------------------------------------
+def kmeans_init(W, init_rows) -> np.ndarray:
+    """Centroids [M, d] (fp64): the rows init_rows of W scaled to unit length."""
+    W = _c(W, np.uint16)
+    V, d = W.shape
+    init = _c(init_rows, np.int32)
+    cent = np.zeros((init.size, d), dtype=np.float64)
+    if lib().orc_kmeans_init(_ptr(W), V, d, _ptr(init), init.size, _ptr(cent)):
+        raise ValueError("kmeans_init: a row index outside W")
+    return cent
+
+
+def kmeans_step(W, cent, round_bf16=True):
+    """One Lloyd step of spherical k-means (see dynaspec_oracle.c).  Returns (new centroids,
+    assignment [V], csr_off [M+1], csr_tok [V], objective of the assignment)."""
+    W = _c(W, np.uint16)
+    V, d = W.shape
+    cent = np.array(cent, dtype=np.float64, order="C", copy=True)
+    M = cent.shape[0]
+    assign = np.zeros(V, dtype=np.int32)
+    off = np.zeros(M + 1, dtype=np.int32)
+    tok = np.zeros(V, dtype=np.int32)
+    obj = np.zeros(1)
+    rc = lib().orc_kmeans_step(_ptr(W), V, d, M, int(bool(round_bf16)), _ptr(cent), _ptr(assign),
+                               _ptr(off), _ptr(tok), _ptr(obj))
+    if rc:
+        raise RuntimeError(f"orc_kmeans_step failed ({rc})")
+    return cent, assign, off, tok, float(obj[0])

@@ -465,3 +465,105 @@ int orc_verify_tree(int B, int D, int Wd, int V, double T, const float *z,
     }
     return err;
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* Spherical k-means over the LM-head rows: the offline step that forms the vocabulary     */
+/* clusters the router scores (summary, Key Novelty and Key Hyperparameters: clusters of the */
+/* LM-head rows by spherical k-means).  The pages give no iteration details; reading: the    */
+/* standard Lloyd iteration for the cosine objective J = sum_v <W_v / |W_v|, mu_c(v)>,        */
+/* centroids of unit length:                                                                */
+/*   assignment  c(v) = argmax_c <W_v, mu_c>  (the row's own norm does not change the argmax), */
+/*               ties to the lower c;                                                       */
+/*   update      mu_c = S_c / |S_c|, S_c = sum of W_v / |W_v| over the tokens of cluster c;  */
+/*               an empty cluster keeps its centroid;                                       */
+/*   the CSR lists clusters in ascending id, each cluster's tokens in ascending token id.    */
+/* With round_bf16 the assignment scores the centroids rounded to bf16 (round to nearest     */
+/* even), the operand precision of the CUDA path's tensor-core contraction; the scores are  */
+/* computed in fp64 and compared rounded to fp32, the precision that path decides in.        */
+/* ------------------------------------------------------------------------------------ */
+static double row_norm(const uint16_t *w, int d)
+{
+    double s = 0.0;
+    for (int k = 0; k < d; ++k) { double x = bf16_to_f64(w[k]); s += x * x; }
+    return sqrt(s);
+}
+
+static double round_bf16(double x)
+{
+    float f = (float)x;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Initial centroids: rows init[0..M) of W scaled to unit length.  cent [M, d]. */
+int orc_kmeans_init(const uint16_t *W, int V, int d, const int32_t *init, int M, double *cent)
+{
+    for (int c = 0; c < M; ++c) {
+        if (init[c] < 0 || init[c] >= V) return 1;
+        const uint16_t *w = W + (size_t)init[c] * d;
+        double n = row_norm(w, d);
+        for (int k = 0; k < d; ++k) cent[(size_t)c * d + k] = n > 0.0 ? bf16_to_f64(w[k]) / n : 0.0;
+    }
+    return 0;
+}
+
+/* One Lloyd step.  cent [M, d] in/out; assign [V], csr_off [M+1], csr_tok [V] out; *obj = J
+ * of the new assignment under the centroids it was made with (exact fp64 centroids). */
+int orc_kmeans_step(const uint16_t *W, int V, int d, int M, int round, double *cent,
+                    int32_t *assign, int32_t *csr_off, int32_t *csr_tok, double *obj)
+{
+    double *mu = (double *)malloc(sizeof(double) * (size_t)M * d);
+    double *inv = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!mu || !inv) { free(mu); free(inv); return 2; }
+    for (size_t i = 0; i < (size_t)M * d; ++i) mu[i] = round ? round_bf16(cent[i]) : cent[i];
+    double J = 0.0;
+    #pragma omp parallel for schedule(static) reduction(+:J)
+    for (int v = 0; v < V; ++v) {
+        const uint16_t *w = W + (size_t)v * d;
+        double n = row_norm(w, d);
+        inv[v] = n > 0.0 ? 1.0 / n : 0.0;
+        int best = 0;
+        float bs = 0.f;
+        for (int c = 0; c < M; ++c) {
+            double s = 0.0;
+            for (int k = 0; k < d; ++k) s += bf16_to_f64(w[k]) * mu[(size_t)c * d + k];
+            if (c == 0 || f32(s) > bs) { bs = f32(s); best = c; }
+        }
+        assign[v] = best;
+        double e = 0.0;
+        for (int k = 0; k < d; ++k) e += bf16_to_f64(w[k]) * cent[(size_t)best * d + k];
+        J += e * inv[v];
+    }
+    *obj = J;
+    /* CSR: counts, exclusive scan, tokens in ascending id within each cluster */
+    for (int c = 0; c <= M; ++c) csr_off[c] = 0;
+    for (int v = 0; v < V; ++v) csr_off[assign[v] + 1]++;
+    for (int c = 0; c < M; ++c) csr_off[c + 1] += csr_off[c];
+    int32_t *fill = (int32_t *)malloc(sizeof(int32_t) * (size_t)M);
+    if (!fill) { free(mu); free(inv); return 2; }
+    for (int c = 0; c < M; ++c) fill[c] = csr_off[c];
+    for (int v = 0; v < V; ++v) csr_tok[fill[assign[v]]++] = v;
+    free(fill);
+    /* update: normalised sum of the unit rows of each cluster, in ascending token order */
+    #pragma omp parallel for schedule(dynamic)
+    for (int c = 0; c < M; ++c) {
+        if (csr_off[c + 1] == csr_off[c]) continue;            /* empty: keep the centroid */
+        double *dst = cent + (size_t)c * d;
+        for (int k = 0; k < d; ++k) dst[k] = 0.0;
+        for (int r = csr_off[c]; r < csr_off[c + 1]; ++r) {
+            int v = csr_tok[r];
+            const uint16_t *w = W + (size_t)v * d;
+            for (int k = 0; k < d; ++k) dst[k] += bf16_to_f64(w[k]) * inv[v];
+        }
+        double n = 0.0;
+        for (int k = 0; k < d; ++k) n += dst[k] * dst[k];
+        n = sqrt(n);
+        if (n > 0.0) for (int k = 0; k < d; ++k) dst[k] /= n;
+    }
+    free(mu);
+    free(inv);
+    return 0;
+}

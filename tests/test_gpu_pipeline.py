@@ -176,6 +176,151 @@ def test_chain_step_aligned_targets(pkg, name, seqs, upto):
     assert max(acc) >= min(upto, cfg.gamma - 1)
 
 
+@pytest.mark.parametrize("name,T", [("tiny_static", None), ("tiny_static", 0.0), ("small_batched_static", None),
+                                    ("llama_b1_static32k", None)])
+def test_static_chain_step_matches_oracle(pkg, name, T):
+    # The static-shortlist baseline: one fixed list at every position (per-row head at batch 1,
+    # the union head at batch 5), the same verification, against the oracle's composition of
+    # its head, draw and verification steps on that list.
+    inp = gu.chain_inputs(name)
+    cfg = inp["cfg"]
+    T = cfg.T if T is None else T
+    d = pkg.pipeline.StaticChainDrafter(gu.device_head(inp), inp["static_ids"], B=cfg.B, gamma=cfg.gamma, T=T,
+                                        seed=inp["gumbel_seed"])
+    d.H.copy_(gu.bf16(np.ascontiguousarray(inp["H"].transpose(1, 0, 2))))
+    d.z.copy_(gu.f32(inp["z"]))
+    d.u.copy_(gu.f32(inp["u"]))
+    d.step()
+    torch.cuda.synchronize()
+    d.check_status()
+    ref = oracle.static_chain_step(inp, T=T)
+    offs = d.vs_offsets.cpu().numpy()
+    ids = d.vs_ids.cpu().numpy()
+    logits = d.logits.cpu().numpy()
+    tix = d.token_idx.cpu().numpy()
+    toks = d.tokens.cpu().numpy()
+    full = 0
+    for b in range(cfg.B):
+        ok = True
+        for t in range(cfg.gamma):
+            p = ref[b]["positions"][t]
+            assert np.array_equal(ids[offs[t, b]:offs[t, b + 1]], p["S"])      # list order kept
+            assert_close(logits[t, offs[t, b]:offs[t, b + 1]], p["logits"], "static head logits")
+            if not token_same_or_excused(int(tix[t, b]), p["idx"], p["logits"], p["S"], T, inp["gumbel_seed"],
+                                         t + 1, b):
+                ok = False
+                break
+            assert toks[t, b] == p["token"]
+        if not ok:
+            continue
+        if d.accepted[b].item() != ref[b]["accepted"]:
+            t = min(d.accepted[b].item(), ref[b]["accepted"])
+            p = ref[b]["positions"][t]
+            pz = softmax_full(inp["z"][b, t], T)[p["token"]]
+            qx = q_dense(p["logits"], p["S"], T, cfg.V)[p["token"]]
+            assert T > 0 and accept_margin(pz, qx, inp["u"][b, t]) < TIE
+            continue
+        if d.correction[b].item() != ref[b]["correction"]:
+            assert T > 0
+            t = ref[b]["accepted"]
+            pz = softmax_full(inp["z"][b, t], T)
+            if t < cfg.gamma:
+                p = ref[b]["positions"][t]
+                w = np.maximum(pz - q_dense(p["logits"], p["S"], T, cfg.V), 0)
+                w = w if w.sum() > 0 else pz
+            else:
+                w = pz
+            assert icdf_acceptable(w, float(inp["u"][b, cfg.gamma]), int(d.correction[b].item()))
+        full += 1
+    assert full >= max(1, cfg.B // 2)
+    # graph replay gives the same results
+    snap = d.out.clone()
+    d.capture()
+    d.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(snap, d.out)
+
+
+def _standin_weights(d, F, seed):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    mk = lambda *shape: (torch.randn(*shape, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    return mk(d, 2 * d), mk(d, d), mk(2 * F, d), mk(d, F)
+
+
+def test_drafter_standin_numerics(pkg):
+    # The drafter stand-in (a measurement helper with the weight volume of an EAGLE step) against
+    # the same chain in numpy fp64: h_out = bf16(h_base + scale * Wdn (silu(Wg y2) * (Wu y2))),
+    # y2 = Wmix Wfc [h_prev; E[x]].  scale = 0 returns h_base bit for bit; a token outside the
+    # vocabulary sets DS_DEV_BAD_INDEX.
+    d, F, V = 264, 520, 777
+    Wfc, Wmix, Wug, Wdn = _standin_weights(d, F, 3)
+    g = torch.Generator(device="cuda").manual_seed(4)
+    E = (torch.randn(V, d, generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+    h_prev = torch.randn(d, generator=g, device="cuda").to(torch.bfloat16)
+    h_base = (torch.randn(d, generator=g, device="cuda") * 0.1).to(torch.bfloat16)
+    ws = pkg.api.workspace(pkg.api.drafter_standin_workspace_bytes(d, F), gu.dev())
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)
+    # scale 1000 makes the chain's term (~0.4) dominate the base (~0.1), so an error in any layer shows
+    for x, scale in ((5, 1000.0), (776, 1000.0), (5, 0.0)):
+        x_prev = torch.tensor([x], dtype=torch.int32, device="cuda")
+        out = torch.empty(d, dtype=torch.bfloat16, device="cuda")
+        st = gu.status()
+        pkg.api.drafter_standin(h_prev, x_prev, E, Wfc, Wmix, Wug, Wdn, h_base, scale, out, ws, st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        if scale == 0.0:
+            assert torch.equal(out, h_base)
+            continue
+        u = np.concatenate([f64(h_prev), f64(E[x])])
+        y2 = f64(Wmix) @ (f64(Wfc) @ u)
+        gg, uu = f64(Wug)[:F] @ y2, f64(Wug)[F:] @ y2
+        ref = f64(h_base) + scale * (f64(Wdn) @ (gg / (1.0 + np.exp(-gg)) * uu))
+        got = f64(out)
+        # one bf16 rounding of the result (8 significant bits) plus fp32 accumulation
+        assert np.all(np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-3), np.abs(got - ref).max()
+    st = gu.status()
+    pkg.api.drafter_standin(h_prev, torch.tensor([V], dtype=torch.int32, device="cuda"), E, Wfc, Wmix, Wug, Wdn,
+                            h_base, 1.0, out, ws, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0x10
+
+
+@pytest.mark.parametrize("serial", [False, True])
+def test_chain_step_with_drafter_standin(pkg, serial):
+    # The step with a drafter stand-in before every head (router t+1 waiting for the drafter
+    # step that computes the hidden state it reads; or, serial, the routers on the main stream)
+    # and scale 0: the hidden states are the workload's, so every result equals the plain
+    # step's, bit for bit, eagerly and from a CUDA graph.
+    inp = gu.chain_inputs("tiny")
+    cfg = inp["cfg"]
+    ref = make_chain(pkg, inp, cfg.T)
+    ref.step()
+    torch.cuda.synchronize()
+    d = make_chain(pkg, inp, cfg.T)
+    d.attach_drafter(*_standin_weights(cfg.d, 512, 9), scale=0.0)
+    d.serial_router = serial
+    d.H_base.copy_(d.H)
+    d.H[1:].zero_()                                     # computed by the drafter step
+    d.x0.fill_(17)
+    d.step()
+    torch.cuda.synchronize()
+    d.check_status()
+    for a, b in ((ref.out, d.out), (ref.logits, d.logits), (ref.vs_ids, d.vs_ids)):
+        assert torch.equal(a, b)
+    d.enable_head_timing()
+    d.enable_overlap_timing()
+    d.capture()
+    d.out.zero_()
+    d.replay(timed=True)
+    torch.cuda.synchronize()
+    assert torch.equal(ref.out, d.out)
+    if not serial:
+        ov = d.overlap_times_ms()
+        for t in range(1, cfg.gamma):
+            # router t starts after the drafter step that produced its input, head t after router t
+            assert ov[t][0] >= ov[t - 1][3] - 1e-3 and ov[t][4] >= ov[t][1] - 1e-3
+
+
 def _replay_io(d, early, late):
     pin = lambda x: (x.cpu().pin_memory(), x)
     out_h = torch.empty(d.out.shape, dtype=d.out.dtype).pin_memory()

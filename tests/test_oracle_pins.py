@@ -574,3 +574,96 @@ def test_verify_tree_output_follows_target_chi_square():
     _, pval = scipy_stats.chisquare(np.bincount(first, minlength=V), p * n)
     assert pval > 1e-4
     assert (node == 1).any() and (node == 2).any() and (acc == 0).any()
+
+
+# ---------------------------------------------------------------------------------------
+# Spherical k-means over the LM-head rows (the offline clustering step)
+# ---------------------------------------------------------------------------------------
+def _bf16_rows(x):
+    return wl.to_bf16_bits(np.asarray(x, np.float32))
+
+
+def test_kmeans_recovers_a_planted_partition():
+    # Six orthonormal directions, 100 rows around each (cosine to their direction > 0.9), rows
+    # of different lengths, ids shuffled: seeded with one row of each group, one step must
+    # return exactly the planted groups, listed in ascending token id.
+    rng = np.random.default_rng(31)
+    M, per, d = 6, 100, 64
+    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    dirs = Q[:M]
+    labels = np.repeat(np.arange(M), per)
+    perm = rng.permutation(M * per)
+    labels = labels[perm]
+    X = dirs[labels] + 0.02 * rng.standard_normal((M * per, d))
+    X *= rng.uniform(0.5, 3.0, size=(M * per, 1))
+    W = _bf16_rows(X)
+    init = np.array([np.nonzero(labels == c)[0][0] for c in range(M)], np.int32)
+    cent = oracle.kmeans_init(W, init)
+    cent, assign, off, tok, _ = oracle.kmeans_step(W, cent)
+    assert np.array_equal(assign, labels)
+    for c in range(M):
+        assert np.array_equal(tok[off[c]:off[c + 1]], np.nonzero(labels == c)[0])
+
+
+def test_kmeans_assignment_is_the_nearest_centroid_by_cosine():
+    # The assignment against scipy's cosine distance (an independent library routine): with
+    # exact centroids it is argmin_c cosdist(W_v, mu_c); with bf16 centroids, against the
+    # centroids rounded to bf16, up to fp32 near-ties.
+    from scipy.spatial.distance import cdist
+    rng = np.random.default_rng(5)
+    V, d, M = 700, 48, 9
+    W = _bf16_rows(rng.standard_normal((V, d)))
+    Wf = wl.bf16_bits_to_f32(W).astype(np.float64)
+    mu = rng.standard_normal((M, d))
+    mu /= np.linalg.norm(mu, axis=1, keepdims=True)
+    _, assign, _, _, _ = oracle.kmeans_step(W, mu, round_bf16=False)
+    assert np.array_equal(assign, np.argmin(cdist(Wf, mu, "cosine"), axis=1))
+    mub = wl.bf16_bits_to_f32(wl.to_bf16_bits(mu.astype(np.float32))).astype(np.float64)
+    _, assign_b, _, _, _ = oracle.kmeans_step(W, mu, round_bf16=True)
+    ref = np.argmin(cdist(Wf, mub, "cosine"), axis=1)
+    s = Wf @ mub.T
+    for v in np.nonzero(assign_b != ref)[0]:
+        assert abs(s[v, assign_b[v]] - s[v, ref[v]]) < 1e-6 * np.linalg.norm(Wf[v])
+
+
+def test_kmeans_update_and_csr():
+    # The update against numpy: each centroid is the normalised sum of its tokens' unit rows; a
+    # cluster no token picks keeps its centroid; the CSR lists every token once, by cluster,
+    # ascending inside a cluster, and agrees with the assignment.
+    rng = np.random.default_rng(6)
+    V, d, M = 500, 40, 8
+    X = rng.standard_normal((V, d))
+    X[:, 0] = np.abs(X[:, 0]) + 0.5                     # every row has a positive first coordinate
+    W = _bf16_rows(X)
+    Wf = wl.bf16_bits_to_f32(W).astype(np.float64)
+    mu = rng.standard_normal((M, d)) * 0.3
+    mu[:, 0] = 3.0                                      # near the rows' common direction ...
+    mu[M - 1] = 0.0
+    mu[M - 1, 0] = -1.0                                 # ... except one, away from every row: stays empty
+    mu /= np.linalg.norm(mu, axis=1, keepdims=True)
+    new, assign, off, tok, _ = oracle.kmeans_step(W, mu, round_bf16=False)
+    assert off[0] == 0 and off[M] == V and np.all(np.diff(off) >= 0)
+    assert np.array_equal(np.sort(tok), np.arange(V))
+    for c in range(M):
+        part = tok[off[c]:off[c + 1]]
+        assert np.all(np.diff(part) > 0) and np.all(assign[part] == c)
+        if part.size == 0:
+            assert np.array_equal(new[c], mu[c])
+        else:
+            s = (Wf[part] / np.linalg.norm(Wf[part], axis=1, keepdims=True)).sum(axis=0)
+            np.testing.assert_allclose(new[c], s / np.linalg.norm(s), rtol=1e-12, atol=1e-14)
+    assert off[M] - off[M - 1] == 0
+
+
+def test_kmeans_objective_never_decreases():
+    # Lloyd's property for the cosine objective with exact centroids: J of the assignment made
+    # from the updated centroids is at least J of the previous one.
+    cfg = wl.config("tiny")
+    W = wl.lm_head(cfg, 0)
+    init = np.random.default_rng(2).permutation(cfg.V)[:cfg.M]
+    cent = oracle.kmeans_init(W, init)
+    prev = -np.inf
+    for _ in range(5):
+        cent, _, _, _, J = oracle.kmeans_step(W, cent, round_bf16=False)
+        assert J >= prev - 1e-9 * abs(J)
+        prev = J

@@ -23,7 +23,7 @@ import numpy as np
 __all__ = [
     "Config", "CONFIGS", "config", "to_bf16_bits", "bf16_bits_to_f32",
     "cluster_partition", "chain_inputs", "tree_inputs", "open_uniforms",
-    "tree_parents",
+    "tree_parents", "static_shortlist",
 ]
 
 
@@ -37,7 +37,9 @@ class Config:
     B: sequences; gamma: draft positions (chain) or tree depth (tree);
     budget: clusters kept per position, length gamma;
     T: temperature (0 = greedy); sigma_p: std of the target logits;
-    width: tree nodes per depth (tree workloads only).
+    width: tree nodes per depth (tree workloads only);
+    static: size of a fixed shortlist used at every position instead of the router's
+    (0: the dynamic shortlist).
     """
     name: str
     V: int
@@ -53,6 +55,7 @@ class Config:
     sigma_p: float
     mode: str = "chain"
     width: int = 0
+    static: int = 0
 
     def with_(self, **kw) -> "Config":
         return dataclasses.replace(self, **kw)
@@ -87,6 +90,11 @@ CONFIGS = {
                    sizes=("lognormal", 0.5), B=8, gamma=6, budget=LLAMA_BUDGET,
                    T=1.0, sigma_p=3.0, mode="tree", width=10),
 }
+# The static-shortlist baseline on the Llama shape: one fixed list of 32,768 tokens at every
+# position (the pages compare DynaSpec's ~28K dynamic lists with 32K static ones), with the
+# same hidden states, target logits and uniforms as llama_b1.
+CONFIGS["llama_b1_static32k"] = CONFIGS["llama_b1"].with_(name="llama_b1_static32k", static=32768)
+CONFIGS["tiny_static"] = CONFIGS["tiny"].with_(name="tiny_static", static=1000)
 # Small parity cases the oracle finishes in seconds: several tiles, ragged tails (V, d and
 # the router width are not multiples of the kernels' tile sizes).
 CONFIGS["small_batched"] = Config("small_batched", V=9001, d=392, M=70, Hr=328, act="relu",
@@ -95,6 +103,7 @@ CONFIGS["small_batched"] = Config("small_batched", V=9001, d=392, M=70, Hr=328, 
 CONFIGS["tiny_tree"] = Config("tiny_tree", V=4096, d=256, M=32, Hr=512, act="gelu",
                               sizes=("uniform", 64, 192), B=2, gamma=3, budget=(8, 6, 4),
                               T=1.0, sigma_p=2.0, mode="tree", width=4)
+CONFIGS["small_batched_static"] = CONFIGS["small_batched"].with_(name="small_batched_static", static=2500)
 for _b in (1, 8, 64):
     for _f in (5, 10, 20, 40, 100):
         CONFIGS[f"large_b{_b}_f{_f}"] = Config(
@@ -177,6 +186,14 @@ def cluster_partition(cfg: Config, seed: int):
     return offsets, tokens
 
 
+def static_shortlist(cfg: Config, seed: int) -> np.ndarray:
+    """A fixed shortlist of cfg.static token ids, in list order: the first cfg.static entries of
+    a seeded permutation of V.  It stands in for a frequency-ranked list (the most frequent
+    tokens of a corpus, highest first), which would need a corpus; like such a list, its ids
+    are in no particular order."""
+    return np.random.default_rng([seed, 8]).permutation(cfg.V)[:cfg.static].astype(np.int32)
+
+
 def _router_weights(cfg: Config, seed: int):
     rng = np.random.default_rng([seed, 2])
     return dict(
@@ -217,6 +234,8 @@ def chain_inputs(cfg: Config, seed: int = 0, with_head: bool = True) -> dict:
     z *= np.float32(cfg.sigma_p)
     out["z"] = z
     out["u"] = open_uniforms(np.random.default_rng([seed, 7]), (cfg.B, cfg.gamma + 1))
+    if cfg.static:
+        out["static_ids"] = static_shortlist(cfg, seed)
     if with_head:
         out["W"] = lm_head(cfg, seed)
     return out

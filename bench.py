@@ -249,15 +249,16 @@ def committed_traffic():
 _HEAD_CACHE = {}
 
 
-def device_head(cfg, seed, dev, torch):
-    """The LM head W [V, d] on the device; workloads with the same (V, d, seed) share one copy."""
+def device_head(cfg, seed, dev, torch, host=False):
+    """The LM head W [V, d] on the device (host=True: its host bits too, for the oracle);
+    workloads with the same (V, d, seed) share one copy."""
     import workloads as wl
     key = (cfg.V, cfg.d, seed)
     if key not in _HEAD_CACHE:
         _HEAD_CACHE.clear()                      # keep one head resident at a time
         W = wl.lm_head(cfg, seed)
-        _HEAD_CACHE[key] = torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16)
-    return _HEAD_CACHE[key]
+        _HEAD_CACHE[key] = (W, torch.from_numpy(W.view(np.int16)).to(dev).view(torch.bfloat16))
+    return _HEAD_CACHE[key] if host else _HEAD_CACHE[key][1]
 
 
 def build_drafter(cfg, inp, dev, pkg, torch, W):
@@ -543,6 +544,7 @@ def run_ours(args):
     r = measure(cfg, seed, dev, pkg, torch, world, local_rank, args.steps, args.warmup, args.e2e_steps,
                 TIMED_HEAD_STEPS, flush)
     inp = r.pop("inp")
+    inp["W"] = device_head(cfg, seed, dev, torch, host=True)[0]      # the oracle baseline reads it
 
     per_config = None
     if args.config == "llama_b1" and not args.no_per_config:

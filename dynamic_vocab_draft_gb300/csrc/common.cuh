@@ -144,18 +144,20 @@ __device__ __forceinline__ void stat_add(Stat &a, float x, float key, int v, int
     }
 }
 
-__device__ __forceinline__ Stat stat_merge(Stat a, const Stat &b)
+// a (earlier in the fixed order) merged with b, without branches: a state without elements has
+// m = -inf and v = -1; the scale of each sum is exp(its max - the new max), one of them exactly 1.
+__device__ __forceinline__ Stat stat_merge(const Stat &a, const Stat &b)
 {
-    if (b.m > a.m) {
-        a.s = (a.m == -INFINITY ? 0.f : a.s * __expf(a.m - b.m)) + b.s;
-        a.m = b.m;
-    } else if (b.m != -INFINITY) {
-        a.s += b.s * __expf(b.m - a.m);
-    }
-    if (b.v >= 0 && (a.v < 0 || b.key > a.key || (b.key == a.key && b.v < a.v))) {
-        a.key = b.key; a.v = b.v; a.j = b.j;
-    }
-    return a;
+    Stat r;
+    r.m = fmaxf(a.m, b.m);
+    const float ea = a.m == -INFINITY ? 0.f : __expf(a.m - r.m);
+    const float eb = b.m == -INFINITY ? 0.f : __expf(b.m - r.m);
+    r.s = fmaf(a.s, ea, b.s * eb);
+    const bool tb = b.v >= 0 && (a.v < 0 || b.key > a.key || (b.key == a.key && b.v < a.v));
+    r.key = tb ? b.key : a.key;
+    r.v = tb ? b.v : a.v;
+    r.j = tb ? b.j : a.j;
+    return r;
 }
 
 __device__ __forceinline__ Stat shfl_xor_stat(const Stat &a, int mask)
@@ -167,6 +169,21 @@ __device__ __forceinline__ Stat shfl_xor_stat(const Stat &a, int mask)
     b.v = __shfl_xor_sync(0xFFFFFFFFu, a.v, mask);
     b.j = __shfl_xor_sync(0xFFFFFFFFu, a.j, mask);
     return b;
+}
+
+// One butterfly level over lanes: both lanes of a pair merge the same two states in lane order
+// (the lower lane's first), so they hold the same result and the whole tree's order is fixed.
+__device__ __forceinline__ Stat stat_butterfly(const Stat &mine, int lane, int o)
+{
+    const Stat other = shfl_xor_stat(mine, o);
+    const bool hi = (lane & o) != 0;
+    Stat lo_s, hi_s;
+    lo_s.m = hi ? other.m : mine.m;   hi_s.m = hi ? mine.m : other.m;
+    lo_s.s = hi ? other.s : mine.s;   hi_s.s = hi ? mine.s : other.s;
+    lo_s.key = hi ? other.key : mine.key; hi_s.key = hi ? mine.key : other.key;
+    lo_s.v = hi ? other.v : mine.v;   hi_s.v = hi ? mine.v : other.v;
+    lo_s.j = hi ? other.j : mine.j;   hi_s.j = hi ? mine.j : other.j;
+    return stat_merge(lo_s, hi_s);
 }
 
 __device__ __forceinline__ float warp_sum(float x)

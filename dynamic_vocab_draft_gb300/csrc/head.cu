@@ -74,6 +74,11 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
     const int b = blockIdx.y;
     const int d = a.d;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // h's first 8 * blockDim columns are requested before anything else: the list's offsets,
+    // then its ids, then the first W rows form a chain of dependent loads, and h's load (which
+    // needs none of them) should not wait behind it
+    const uint4 *h = reinterpret_cast<const uint4 *>(a.H + size_t(b) * d);
+    const uint4 h0 = int(threadIdx.x) < d / 8 ? h[threadIdx.x] : make_uint4(0, 0, 0, 0);
     const int base = a.vs_offsets[b];
     const int n = a.vs_offsets[b + 1] - base;
     const int32_t *ids = a.vs_ids + base;
@@ -99,8 +104,8 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
         load_round(w, reinterpret_cast<const uint4 *>(a.W + size_t(ok ? v : 0) * d), 0);
         preloaded = true;
     }
-    const uint4 *h = reinterpret_cast<const uint4 *>(a.H + size_t(b) * d);
-    for (int k = threadIdx.x; k < d / 8; k += blockDim.x) hs[k] = h[k];
+    if (int(threadIdx.x) < d / 8) hs[threadIdx.x] = h0;
+    for (int k = threadIdx.x + blockDim.x; k < d / 8; k += blockDim.x) hs[k] = h[k];
     __syncthreads();
 
     for (int jb = j0; jb < n; jb += 32 * stride) {
@@ -156,8 +161,7 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
     // the warp's lanes, then the block's warps, then the blocks: fixed orders throughout
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const Stat other = shfl_xor_stat(st, o);
-        st = (lane & o) ? stat_merge(other, st) : stat_merge(st, other);
+        st = stat_butterfly(st, lane, o);
     }
     if (lane == 0) warp_stat[warp] = st;
     __syncthreads();
@@ -166,8 +170,7 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
         Stat c = lane < kGvWarps ? warp_stat[lane] : stat_empty();
 #pragma unroll
         for (int o = 1; o < kGvWarps; o <<= 1) {
-            const Stat other = shfl_xor_stat(c, o);
-            c = (lane & o) ? stat_merge(other, c) : stat_merge(c, other);
+            c = stat_butterfly(c, lane, o);
         }
         if (lane == 0) st_stat(&partials[size_t(b) * kGvMaxBlocks + blockIdx.x], c);
     }
@@ -187,8 +190,7 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
     }
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const Stat other = shfl_xor_stat(c, o);
-        c = (lane & o) ? stat_merge(other, c) : stat_merge(c, other);
+        c = stat_butterfly(c, lane, o);
     }
     if (lane == 0) write_row(a, b, c);
 }
@@ -277,8 +279,7 @@ head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *_
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const Stat other = shfl_xor_stat(st, o);
-        st = (lane & o) ? stat_merge(other, st) : stat_merge(st, other);
+        st = stat_butterfly(st, lane, o);
     }
     if (lane == 0) ws[warp] = st;
     __syncthreads();
@@ -293,8 +294,7 @@ head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *_
     for (int i = lane; i < nblk; i += 32) c = stat_merge(c, ld_stat(&partials[size_t(r) * kGvMaxBlocks + i]));
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const Stat other = shfl_xor_stat(c, o);
-        c = (lane & o) ? stat_merge(other, c) : stat_merge(c, other);
+        c = stat_butterfly(c, lane, o);
     }
     if (lane == 0) write_row(a, r, c);
 }

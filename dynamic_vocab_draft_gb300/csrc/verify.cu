@@ -55,18 +55,35 @@ __device__ __forceinline__ QStat ldcg(const QStat *p)
     return QStat{f.x, f.y};
 }
 
-__device__ __forceinline__ PStat pstat_merge(PStat a, const PStat &b)
+// a (earlier in the fixed order) merged with b, without branches (an empty state has m = -inf
+// and aid = -1; one of the two scales is exactly 1).
+__device__ __forceinline__ PStat pstat_merge(const PStat &a, const PStat &b)
 {
-    if (b.m > a.m) { a.s = (a.m == -INFINITY ? 0.f : a.s * __expf(a.m - b.m)) + b.s; a.m = b.m; }
-    else if (b.m != -INFINITY) a.s += b.s * __expf(b.m - a.m);
-    if (b.aid >= 0 && (a.aid < 0 || b.amax > a.amax || (b.amax == a.amax && b.aid < a.aid))) { a.amax = b.amax; a.aid = b.aid; }
-    return a;
+    PStat r;
+    r.m = fmaxf(a.m, b.m);
+    const float ea = a.m == -INFINITY ? 0.f : __expf(a.m - r.m);
+    const float eb = b.m == -INFINITY ? 0.f : __expf(b.m - r.m);
+    r.s = fmaf(a.s, ea, b.s * eb);
+    const bool tb = b.aid >= 0 && (a.aid < 0 || b.amax > a.amax || (b.amax == a.amax && b.aid < a.aid));
+    r.amax = tb ? b.amax : a.amax;
+    r.aid = tb ? b.aid : a.aid;
+    return r;
 }
 
 __device__ __forceinline__ PStat shfl_xor_pstat(const PStat &a, int o)
 {
     return PStat{__shfl_xor_sync(0xFFFFFFFFu, a.m, o), __shfl_xor_sync(0xFFFFFFFFu, a.s, o),
                  __shfl_xor_sync(0xFFFFFFFFu, a.amax, o), __shfl_xor_sync(0xFFFFFFFFu, a.aid, o)};
+}
+
+// One butterfly level: both lanes of a pair merge the pair in lane order (see stat_butterfly).
+__device__ __forceinline__ PStat pstat_butterfly(const PStat &mine, int lane, int o)
+{
+    const PStat other = shfl_xor_pstat(mine, o);
+    const bool hi = (lane & o) != 0;
+    const PStat lo_s{hi ? other.m : mine.m, hi ? other.s : mine.s, hi ? other.amax : mine.amax, hi ? other.aid : mine.aid};
+    const PStat hi_s{hi ? mine.m : other.m, hi ? mine.s : other.s, hi ? mine.amax : other.amax, hi ? mine.aid : other.aid};
+    return pstat_merge(lo_s, hi_s);
 }
 
 __device__ float block_sum(float x, float *scratch)
@@ -227,8 +244,7 @@ verify_stats_kernel(ChainArgs a)
         }
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const PStat q = shfl_xor_pstat(acc, o);
-            acc = (lane & o) ? pstat_merge(q, acc) : pstat_merge(acc, q);
+            acc = pstat_butterfly(acc, lane, o);
         }
         if (lane == 0) {
             if (r < g1) { rows[r] = acc; a.prow[size_t(b) * g1 + r] = QStat{acc.m, acc.s}; }
@@ -552,20 +568,19 @@ __device__ __forceinline__ void rowstat_add(RowStat &a, float z, float x, bool o
     if (z > a.amax || a.aid < 0) { a.amax = z; a.aid = v; }      // v ascending per thread
 }
 
-__device__ __forceinline__ RowStat rowstat_merge(RowStat a, const RowStat &b)
+// a (earlier in the fixed order) merged with b, without branches.
+__device__ __forceinline__ RowStat rowstat_merge(const RowStat &a, const RowStat &b)
 {
-    if (b.m > a.m) {
-        const float sc = a.m == -INFINITY ? 0.f : __expf(a.m - b.m);
-        a.s = a.s * sc + b.s;
-        a.o = a.o * sc + b.o;
-        a.m = b.m;
-    } else if (b.m != -INFINITY) {
-        const float sc = __expf(b.m - a.m);
-        a.s += b.s * sc;
-        a.o += b.o * sc;
-    }
-    if (b.aid >= 0 && (a.aid < 0 || b.amax > a.amax || (b.amax == a.amax && b.aid < a.aid))) { a.amax = b.amax; a.aid = b.aid; }
-    return a;
+    RowStat r;
+    r.m = fmaxf(a.m, b.m);
+    const float ea = a.m == -INFINITY ? 0.f : __expf(a.m - r.m);
+    const float eb = b.m == -INFINITY ? 0.f : __expf(b.m - r.m);
+    r.s = fmaf(a.s, ea, b.s * eb);
+    r.o = fmaf(a.o, ea, b.o * eb);
+    const bool tb = b.aid >= 0 && (a.aid < 0 || b.amax > a.amax || (b.amax == a.amax && b.aid < a.aid));
+    r.amax = tb ? b.amax : a.amax;
+    r.aid = tb ? b.aid : a.aid;
+    return r;
 }
 
 __device__ __forceinline__ RowStat shfl_xor_rowstat(const RowStat &a, int o)
@@ -575,6 +590,18 @@ __device__ __forceinline__ RowStat shfl_xor_rowstat(const RowStat &a, int o)
                    __shfl_xor_sync(0xFFFFFFFFu, a.aid, o)};
 }
 
+// One butterfly level: both lanes of a pair merge the pair in lane order (see stat_butterfly).
+__device__ __forceinline__ RowStat rowstat_butterfly(const RowStat &mine, int lane, int o)
+{
+    const RowStat other = shfl_xor_rowstat(mine, o);
+    const bool hi = (lane & o) != 0;
+    const RowStat lo_s{hi ? other.m : mine.m, hi ? other.s : mine.s, hi ? other.o : mine.o,
+                       hi ? other.amax : mine.amax, hi ? other.aid : mine.aid};
+    const RowStat hi_s{hi ? mine.m : other.m, hi ? mine.s : other.s, hi ? mine.o : other.o,
+                       hi ? mine.amax : other.amax, hi ? mine.aid : other.aid};
+    return rowstat_merge(lo_s, hi_s);
+}
+
 // Fixed-order block reduction (warp trees, then warp 0 over the warp results); the result is
 // returned to every thread.
 __device__ RowStat block_rowstat(RowStat st, RowStat *ws)
@@ -582,8 +609,7 @@ __device__ RowStat block_rowstat(RowStat st, RowStat *ws)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const RowStat q = shfl_xor_rowstat(st, o);
-        st = (lane & o) ? rowstat_merge(q, st) : rowstat_merge(st, q);
+        st = rowstat_butterfly(st, lane, o);
     }
     __syncthreads();
     if (lane == 0) ws[warp] = st;
@@ -592,8 +618,7 @@ __device__ RowStat block_rowstat(RowStat st, RowStat *ws)
         RowStat c = lane < nw ? ws[lane] : rowstat_empty();
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const RowStat q = shfl_xor_rowstat(c, o);
-            c = (lane & o) ? rowstat_merge(q, c) : rowstat_merge(c, q);
+            c = rowstat_butterfly(c, lane, o);
         }
         if (lane == 0) ws[32] = c;
     }
@@ -625,8 +650,7 @@ __device__ RowStat cluster_rowstat(RowStat st, RowStat *red, ClusterRed &cr, int
         RowStat m = lane < cl.num_blocks() ? cl.map_shared_rank(&cr, lane)->stat[slot] : rowstat_empty();
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const RowStat q = shfl_xor_rowstat(m, o);
-            m = (lane & o) ? rowstat_merge(q, m) : rowstat_merge(m, q);
+            m = rowstat_butterfly(m, lane, o);
         }
         if (lane == 0) red[32] = m;
     }

@@ -525,7 +525,7 @@ def test_verify_chain_wide_grid(ds, T, mode):
     cfg = inp["cfg"]
     B = cfg.B
     rng = np.random.default_rng(23)
-    rows = _synthetic_chain_rows(inp, B, T if T > 0 else 1.0, rng)
+    rows = _synthetic_chain_rows(inp, B, T, rng)           # T = 0: greedy drafts (the argmax)
     z = inp["z"][:B].copy()
     if mode != "independent":
         upto = cfg.gamma if mode == "aligned" else cfg.gamma // 2

@@ -53,6 +53,31 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p)
     return r;
 }
 
+// L2 eviction-priority policies for loads that carry a cache hint: data read once (the LM-head
+// rows of one draft position) is marked to leave L2 first; data every draft position reads
+// again (the router weights) is marked to leave it last.
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ld_stream with an L2 cache policy.
+__device__ __forceinline__ uint4 ld_stream_hint(const uint4 *p, uint64_t policy)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p), "l"(policy));
+    return r;
+}
+
 __device__ __forceinline__ void set_status(int32_t *st, int32_t bit)
 {
     if (st) atomicOr(st, bit);

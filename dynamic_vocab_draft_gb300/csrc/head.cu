@@ -26,7 +26,13 @@ namespace {
 // Per-row gathered GEMV
 // ---------------------------------------------------------------------------------------
 constexpr int kGvWarps = 16;           // one 512-thread block per SM
-constexpr int kHeadSideSms = 8;        // SMs a batch-1 head leaves to the side stream
+constexpr int kHeadSideSms = 8;        // SMs a tensor-core (union) head leaves to the side stream
+// SMs the batch-1 head leaves to the side stream.  The router of position t+2 runs there while
+// head t+1 streams W (it reads H_{t+1}, which exists only once head t has drawn its token); both
+// stream from the same saturated HBM, so the router's share of it follows its share of the SMs,
+// and with 8 SMs its 10.5 MB took longer than the later, shorter heads (measured on one GB300:
+// step 349.5 us with 8, 325.5 with 12, 318.9 with 16, 319.1 with 24 SMs).
+constexpr int kHeadSideSmsB1 = 16;
 constexpr int kGvMaxD = 16384;
 constexpr int kGvMaxBlocks = 1024;     // per list; bounds the partials in the workspace
 
@@ -379,7 +385,7 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
         if (sms <= 0) return DS_ERR_CUDA;
         // One 512-thread block per SM.  At batch 1 a few SMs are left to the side stream, so the
         // next position's router and shortlist build run while this head streams W.
-        int gx = B == 1 ? sms - kHeadSideSms : (sms + B - 1) / B;
+        int gx = B == 1 ? sms - kHeadSideSmsB1 : (sms + B - 1) / B;
         if (gx < 1) gx = 1;
         if (gx > kGvMaxBlocks) gx = kGvMaxBlocks;
         const size_t smem = size_t(d) * sizeof(uint16_t);

@@ -266,7 +266,8 @@ gemv1_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict_
     if (topk_k > 0 && last_block_done(counter, gridDim.x)) topk_block(y, N, topk_k, topk_ids);
 }
 
-constexpr int kGemv1Blocks = 32;       // 256 warps: one wave on 16 SMs (2 blocks each)
+constexpr int kGemv1Blocks = 64;       // a later position's router: four 256-thread blocks on each of
+                                       // the 16 SMs the batch-1 head leaves free
 
 // One block per row: the top-k of scores[b][0..M).
 __global__ void __launch_bounds__(kTopkThreads)

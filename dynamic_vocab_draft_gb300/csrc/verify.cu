@@ -39,6 +39,7 @@ constexpr int kMaxGamma = 32;
 // Residual chunks: 2048 elements (8 per thread) under the same rule, else 1024.
 constexpr int kRPerBig = 8, kRPerSmall = 4;
 constexpr int kRChunkMin = kVThreads * kRPerSmall;
+constexpr int kSmallMaxB = 8;          // up to this many sequences on the small-chunk grid: one launch
 
 struct PStat { float m, s, amax; int aid; };   // target-row chunk: max, sum-exp, argmax
 struct QStat { float m, s; };
@@ -183,6 +184,8 @@ struct ChainArgs {
     int32_t *decision;  // [B]: -1 done, else the target row to draw from (t* or gamma)
     int nrch;           // residual-pass chunks
     float *rsum, *psum; // [B][nrch]
+    unsigned *bar;      // grid barrier of the single-launch path: arrivals, generation
+    long long wait_budget;
 };
 
 // Index of full-vocabulary token v in list (t, b), or -1.
@@ -194,17 +197,12 @@ __device__ __forceinline__ int list_index(const ChainArgs &a, int t, int b, int 
     return p < 0 ? -1 : p + a.rank[v];
 }
 
+// Chunk c of target row t of sequence b: its max / sum-exp / argmax (and, at T > 0 without the
+// head's row statistics, those of the draft row's chunk c).  The whole block calls it.
 template <int kVPer>
-__global__ void __launch_bounds__(kVThreads)
-verify_stats_kernel(ChainArgs a)
+__device__ void stats_unit(const ChainArgs &a, int b, int t, int c, PStat *scratch)
 {
-    __shared__ PStat scratch[kVThreads / 32];
-    __shared__ PStat rows[kMaxGamma + 1];
-    __shared__ QStat qrows[kMaxGamma];
-    __shared__ int rej[kMaxGamma];
     const int g1 = a.gamma + 1;
-    const int b = blockIdx.y / g1, t = blockIdx.y % g1;
-    const int c = blockIdx.x;
     const int lo = c * kVThreads * kVPer;
     {
         const float *row = a.p_logits + (size_t(b) * g1 + t) * a.V;
@@ -221,9 +219,18 @@ verify_stats_kernel(ChainArgs a)
         }
         if (threadIdx.x == 0) a.qstat[(size_t(b) * a.gamma + t) * a.nch + c] = q;
     }
-    if (!last_block_done(&a.cnt1[b], unsigned(g1) * a.nch)) return;
+}
 
-    // Fold the chunk statistics of this sequence's rows: warp w takes rows w, w+8, ...
+// Sequence b, once every chunk's statistics are stored: fold them (fixed order), take all gamma
+// accept tests at once and decide (accepted length; at T = 0 the correction too; else the
+// target row to draw the correction from).  The whole block calls it.
+__device__ void fold_decide(const ChainArgs &a, int b)
+{
+    __shared__ PStat rows[kMaxGamma + 1];
+    __shared__ QStat qrows[kMaxGamma];
+    __shared__ int rej[kMaxGamma];
+    const int g1 = a.gamma + 1;
+    // warp w folds rows w, w+8, ...
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nrows = g1 + (a.T > 0.f && !a.q_max ? a.gamma : 0);
     if (a.T > 0.f && a.q_max && threadIdx.x < a.gamma) {
@@ -287,6 +294,19 @@ verify_stats_kernel(ChainArgs a)
             a.decision[b] = ts;
         }
     }
+    __syncthreads();                                   // the block may call again (shared state)
+}
+
+template <int kVPer>
+__global__ void __launch_bounds__(kVThreads)
+verify_stats_kernel(ChainArgs a)
+{
+    __shared__ PStat scratch[kVThreads / 32];
+    const int g1 = a.gamma + 1;
+    const int b = blockIdx.y / g1, t = blockIdx.y % g1;
+    stats_unit<kVPer>(a, b, t, blockIdx.x, scratch);
+    if (!last_block_done(&a.cnt1[b], unsigned(g1) * a.nch)) return;
+    fold_decide(a, b);
 }
 
 // What the residual weights of target row tr need: max(0, p - q) at a rejection (tr < gamma),
@@ -330,16 +350,11 @@ __device__ ResidualRow residual_row(const ChainArgs &a, int b, int tr)
 // loads are in flight and weights() looks them up there instead of in a third round of global
 // loads (fewer dependent round trips, at the price of holding the first loads across a
 // barrier: it pays when the grid is small, not on wide batched grids).
+// Pass 1 for chunk c: its mass of the primary and the fallback weights, stored at rsum[c], psum[c].
 template <int kRPer, class P>
-__device__ void icdf_draw(const P &pol, int V, int nrch, float u, float *__restrict__ rsum,
-                          float *__restrict__ psum, unsigned *counter, int32_t *out)
+__device__ void icdf_chunk(const P &pol, int V, int c, float *__restrict__ rsum, float *__restrict__ psum)
 {
     __shared__ float scratch[kVThreads / 32];
-    __shared__ float sbuf[kVThreads + 1];
-    __shared__ float fscan[33];
-    __shared__ int s_chunk, s_use_p, s_hit, s_last;
-    __shared__ float s_target;
-    const int c = blockIdx.x;
     constexpr int kRChunk = kVThreads * kRPer;
     const int base = c * kRChunk + threadIdx.x * kRPer;
     float rs = 0.f, ps = 0.f;
@@ -367,8 +382,22 @@ __device__ void icdf_draw(const P &pol, int V, int nrch, float u, float *__restr
     rs = block_sum(rs, scratch);
     ps = block_sum(ps, scratch);
     if (threadIdx.x == 0) { rsum[c] = rs; psum[c] = ps; }
-    if (!last_block_done(counter, unsigned(nrch))) return;
+}
 
+// Pass 2, once every chunk's masses are stored: the draw (see icdf_draw).
+template <int kRPer, class P>
+__device__ void icdf_locate(const P &pol, int V, int nrch, float u, const float *__restrict__ rsum,
+                            const float *__restrict__ psum, int32_t *out)
+{
+    __shared__ float sbuf[kVThreads + 1];
+    __shared__ float fscan[33];
+    __shared__ int s_chunk, s_use_p, s_hit, s_last;
+    __shared__ float s_target;
+    constexpr int kRChunk = kVThreads * kRPer;
+    if constexpr (P::kStaged) {                        // this block's table may hold another list
+        pol.stage();
+        __syncthreads();
+    }
     const int E = (nrch + kVThreads - 1) / kVThreads;
     const int c0 = threadIdx.x * E, c1 = min(nrch, c0 + E);
     float rrun = 0.f, prun = 0.f;
@@ -446,6 +475,18 @@ __device__ void icdf_draw(const P &pol, int V, int nrch, float u, float *__restr
     }
     __syncthreads();
     if (threadIdx.x == 0 && s_hit == 0x7FFFFFFF) *out = s_last;   // target beyond the chunk
+    __syncthreads();                                   // the block may call again (shared state)
+}
+
+// Both passes in one launch over (chunks, ...): every block stores its chunk's masses, the last
+// block of the group draws.
+template <int kRPer, class P>
+__device__ void icdf_draw(const P &pol, int V, int nrch, float u, float *__restrict__ rsum,
+                          float *__restrict__ psum, unsigned *counter, int32_t *out)
+{
+    icdf_chunk<kRPer>(pol, V, blockIdx.x, rsum, psum);
+    if (!last_block_done(counter, unsigned(nrch))) return;
+    icdf_locate<kRPer>(pol, V, nrch, u, rsum, psum, out);
 }
 
 // The residual weights of row tr of a chain (max(0, p - q), or p for the bonus row); with
@@ -493,6 +534,74 @@ verify_residual_kernel(ChainArgs a)
     const ChainResidual<kStage> pol{&a, residual_row(a, b, tr), s_cp};
     icdf_draw<kRPer>(pol, a.V, a.nrch, a.u[size_t(b) * (a.gamma + 1) + a.gamma], a.rsum + size_t(b) * a.nrch,
               a.psum + size_t(b) * a.nrch, &a.cnt2[b], &a.correction[b]);
+}
+
+// ---------------------------------------------------------------------------------------
+// Few sequences: the whole chain verification as one cooperative launch (every block resident
+// at once), its four phases separated by a grid barrier instead of by launches and last-block
+// folds: chunk statistics of every row; the fold and accept tests of each sequence; the
+// residual's chunk masses; the inverse-CDF draw of each sequence.  Same functions, same order of
+// arithmetic as the two-launch path, so the results are the same.
+// ---------------------------------------------------------------------------------------
+
+// All blocks of the launch meet here.  Bounded: a block that waits longer than the budget sets
+// DS_DEV_TIMEOUT and goes on (the outputs are then undefined).  bar[0] counts arrivals (left at
+// zero), bar[1] is the generation; both start at zero in a zeroed workspace.
+__device__ void grid_barrier(unsigned *bar, unsigned nblocks, long long budget, int32_t *status)
+{
+    __threadfence();                                   // every thread's results, before the arrival
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        volatile unsigned *gen = bar + 1;
+        const unsigned g = *gen;                       // read before arriving
+        if (atomicAdd(&bar[0], 1u) == nblocks - 1) {
+            atomicExch(&bar[0], 0u);
+            __threadfence();
+            atomicAdd(&bar[1], 1u);
+        } else {
+            const long long t0 = clock64();
+            while (*gen == g) {
+                if (clock64() - t0 > budget) { set_status(status, DS_DEV_TIMEOUT); break; }
+            }
+        }
+        __threadfence();                               // the others' results, after the barrier
+    }
+    __syncthreads();
+}
+
+template <int kVPer, int kRPer>
+__global__ void __launch_bounds__(kVThreads)
+verify_small_kernel(ChainArgs a)
+{
+    extern __shared__ int s_cp[];                      // M entries (the residual's cluster positions)
+    __shared__ PStat scratch[kVThreads / 32];
+    const int g1 = a.gamma + 1;
+    const unsigned nb = gridDim.x;
+    const long long n1 = 1LL * a.B * g1 * a.nch;
+    for (long long w = blockIdx.x; w < n1; w += nb) {
+        const int row = int(w / a.nch), c = int(w % a.nch);
+        stats_unit<kVPer>(a, row / g1, row % g1, c, scratch);
+    }
+    grid_barrier(a.bar, nb, a.wait_budget, a.status);
+    for (int b = blockIdx.x; b < a.B; b += nb) fold_decide(a, b);
+    if (a.T == 0.f) return;                            // greedy: every sequence is decided (uniform)
+    grid_barrier(a.bar, nb, a.wait_budget, a.status);
+    const long long n3 = 1LL * a.B * a.nrch;
+    for (long long w = blockIdx.x; w < n3; w += nb) {
+        const int b = int(w / a.nrch), c = int(w % a.nrch);
+        const int tr = __ldcg(&a.decision[b]);
+        if (tr < 0) continue;                          // uniform over the block
+        const ChainResidual<true> pol{&a, residual_row(a, b, tr), s_cp};
+        icdf_chunk<kRPer>(pol, a.V, c, a.rsum + size_t(b) * a.nrch, a.psum + size_t(b) * a.nrch);
+    }
+    grid_barrier(a.bar, nb, a.wait_budget, a.status);
+    for (int b = blockIdx.x; b < a.B; b += nb) {
+        const int tr = __ldcg(&a.decision[b]);
+        if (tr < 0) continue;
+        const ChainResidual<true> pol{&a, residual_row(a, b, tr), s_cp};
+        icdf_locate<kRPer>(pol, a.V, a.nrch, a.u[size_t(b) * g1 + a.gamma], a.rsum + size_t(b) * a.nrch,
+                           a.psum + size_t(b) * a.nrch, &a.correction[b]);
+    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -958,7 +1067,7 @@ extern "C" size_t ds_verify_workspace_bytes(int B, int gamma, int V)
     if (B <= 0 || gamma <= 0 || V <= 0) return 0;
     const size_t nch = size_t(vchunks(V));
     const size_t g1 = size_t(gamma) + 1;
-    return align256(2 * size_t(B) * sizeof(unsigned)) +
+    return align256((2 * size_t(B) + 2) * sizeof(unsigned)) +
            align256(size_t(B) * g1 * nch * sizeof(PStat)) +
            align256(size_t(B) * gamma * nch * sizeof(QStat)) +
            align256(size_t(B) * g1 * sizeof(QStat)) +
@@ -1002,8 +1111,9 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     a.accepted = accepted_len; a.correction = correction; a.status = dev_status;
     char *w = static_cast<char *>(ws);
     const size_t nch = size_t(a.nch), g1 = size_t(gamma) + 1;
-    a.cnt1 = reinterpret_cast<unsigned *>(w); a.cnt2 = a.cnt1 + B;
-    w += align256(2 * size_t(B) * sizeof(unsigned));
+    a.cnt1 = reinterpret_cast<unsigned *>(w); a.cnt2 = a.cnt1 + B; a.bar = a.cnt2 + B;
+    w += align256((2 * size_t(B) + 2) * sizeof(unsigned));
+    a.wait_budget = wait_budget();
     a.pstat = reinterpret_cast<PStat *>(w); w += align256(size_t(B) * g1 * nch * sizeof(PStat));
     a.qstat = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * gamma * nch * sizeof(QStat));
     a.prow = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * g1 * sizeof(QStat));
@@ -1013,11 +1123,30 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.psum = reinterpret_cast<float *>(w);
 
+    const size_t cp_smem = size_t(M) * sizeof(int);   // M <= 8192
+    if (!vbig && !rbig && B <= kSmallMaxB) {
+        // few sequences: one cooperative launch of one block per SM (all resident at once)
+        const long long units = 1LL * B * (gamma + 1) * a.nch;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(units < sms ? units : sms));
+        cfg.blockDim = dim3(kVThreads);
+        cfg.dynamicSmemBytes = cp_smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, verify_small_kernel<kVPerSmall, kRPerSmall>, a) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return DS_ERR_CUDA;
+        }
+        return DS_OK;
+    }
     if (vbig) verify_stats_kernel<kVPerBig><<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
     else verify_stats_kernel<kVPerSmall><<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
     DS_TRY_LAUNCH();
     // the small-chunk grid (few sequences) stages the list's cluster positions in shared memory
-    const size_t cp_smem = size_t(M) * sizeof(int);   // M <= 8192
     if (rbig) verify_residual_kernel<kRPerBig, false><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
     else verify_residual_kernel<kRPerSmall, true><<<dim3(a.nrch, B), kVThreads, cp_smem, stream>>>(a);
     DS_TRY_LAUNCH();

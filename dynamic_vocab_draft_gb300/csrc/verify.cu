@@ -39,7 +39,6 @@ constexpr int kMaxGamma = 32;
 // Residual chunks: 2048 elements (8 per thread) under the same rule, else 1024.
 constexpr int kRPerBig = 8, kRPerSmall = 4;
 constexpr int kRChunkMin = kVThreads * kRPerSmall;
-constexpr int kSmallMaxB = 8;          // up to this many sequences on the small-chunk grid: one launch
 
 struct PStat { float m, s, amax; int aid; };   // target-row chunk: max, sum-exp, argmax
 struct QStat { float m, s; };
@@ -184,8 +183,6 @@ struct ChainArgs {
     int32_t *decision;  // [B]: -1 done, else the target row to draw from (t* or gamma)
     int nrch;           // residual-pass chunks
     float *rsum, *psum; // [B][nrch]
-    unsigned *bar;      // grid barrier of the single-launch path: arrivals, generation
-    long long wait_budget;
 };
 
 // Index of full-vocabulary token v in list (t, b), or -1.
@@ -534,74 +531,6 @@ verify_residual_kernel(ChainArgs a)
     const ChainResidual<kStage> pol{&a, residual_row(a, b, tr), s_cp};
     icdf_draw<kRPer>(pol, a.V, a.nrch, a.u[size_t(b) * (a.gamma + 1) + a.gamma], a.rsum + size_t(b) * a.nrch,
               a.psum + size_t(b) * a.nrch, &a.cnt2[b], &a.correction[b]);
-}
-
-// ---------------------------------------------------------------------------------------
-// Few sequences: the whole chain verification as one cooperative launch (every block resident
-// at once), its four phases separated by a grid barrier instead of by launches and last-block
-// folds: chunk statistics of every row; the fold and accept tests of each sequence; the
-// residual's chunk masses; the inverse-CDF draw of each sequence.  Same functions, same order of
-// arithmetic as the two-launch path, so the results are the same.
-// ---------------------------------------------------------------------------------------
-
-// All blocks of the launch meet here.  Bounded: a block that waits longer than the budget sets
-// DS_DEV_TIMEOUT and goes on (the outputs are then undefined).  bar[0] counts arrivals (left at
-// zero), bar[1] is the generation; both start at zero in a zeroed workspace.
-__device__ void grid_barrier(unsigned *bar, unsigned nblocks, long long budget, int32_t *status)
-{
-    __threadfence();                                   // every thread's results, before the arrival
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        volatile unsigned *gen = bar + 1;
-        const unsigned g = *gen;                       // read before arriving
-        if (atomicAdd(&bar[0], 1u) == nblocks - 1) {
-            atomicExch(&bar[0], 0u);
-            __threadfence();
-            atomicAdd(&bar[1], 1u);
-        } else {
-            const long long t0 = clock64();
-            while (*gen == g) {
-                if (clock64() - t0 > budget) { set_status(status, DS_DEV_TIMEOUT); break; }
-            }
-        }
-        __threadfence();                               // the others' results, after the barrier
-    }
-    __syncthreads();
-}
-
-template <int kVPer, int kRPer>
-__global__ void __launch_bounds__(kVThreads)
-verify_small_kernel(ChainArgs a)
-{
-    extern __shared__ int s_cp[];                      // M entries (the residual's cluster positions)
-    __shared__ PStat scratch[kVThreads / 32];
-    const int g1 = a.gamma + 1;
-    const unsigned nb = gridDim.x;
-    const long long n1 = 1LL * a.B * g1 * a.nch;
-    for (long long w = blockIdx.x; w < n1; w += nb) {
-        const int row = int(w / a.nch), c = int(w % a.nch);
-        stats_unit<kVPer>(a, row / g1, row % g1, c, scratch);
-    }
-    grid_barrier(a.bar, nb, a.wait_budget, a.status);
-    for (int b = blockIdx.x; b < a.B; b += nb) fold_decide(a, b);
-    if (a.T == 0.f) return;                            // greedy: every sequence is decided (uniform)
-    grid_barrier(a.bar, nb, a.wait_budget, a.status);
-    const long long n3 = 1LL * a.B * a.nrch;
-    for (long long w = blockIdx.x; w < n3; w += nb) {
-        const int b = int(w / a.nrch), c = int(w % a.nrch);
-        const int tr = __ldcg(&a.decision[b]);
-        if (tr < 0) continue;                          // uniform over the block
-        const ChainResidual<true> pol{&a, residual_row(a, b, tr), s_cp};
-        icdf_chunk<kRPer>(pol, a.V, c, a.rsum + size_t(b) * a.nrch, a.psum + size_t(b) * a.nrch);
-    }
-    grid_barrier(a.bar, nb, a.wait_budget, a.status);
-    for (int b = blockIdx.x; b < a.B; b += nb) {
-        const int tr = __ldcg(&a.decision[b]);
-        if (tr < 0) continue;
-        const ChainResidual<true> pol{&a, residual_row(a, b, tr), s_cp};
-        icdf_locate<kRPer>(pol, a.V, a.nrch, a.u[size_t(b) * g1 + a.gamma], a.rsum + size_t(b) * a.nrch,
-                           a.psum + size_t(b) * a.nrch, &a.correction[b]);
-    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -1067,7 +996,7 @@ extern "C" size_t ds_verify_workspace_bytes(int B, int gamma, int V)
     if (B <= 0 || gamma <= 0 || V <= 0) return 0;
     const size_t nch = size_t(vchunks(V));
     const size_t g1 = size_t(gamma) + 1;
-    return align256((2 * size_t(B) + 2) * sizeof(unsigned)) +
+    return align256(2 * size_t(B) * sizeof(unsigned)) +
            align256(size_t(B) * g1 * nch * sizeof(PStat)) +
            align256(size_t(B) * gamma * nch * sizeof(QStat)) +
            align256(size_t(B) * g1 * sizeof(QStat)) +
@@ -1111,9 +1040,8 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     a.accepted = accepted_len; a.correction = correction; a.status = dev_status;
     char *w = static_cast<char *>(ws);
     const size_t nch = size_t(a.nch), g1 = size_t(gamma) + 1;
-    a.cnt1 = reinterpret_cast<unsigned *>(w); a.cnt2 = a.cnt1 + B; a.bar = a.cnt2 + B;
-    w += align256((2 * size_t(B) + 2) * sizeof(unsigned));
-    a.wait_budget = wait_budget();
+    a.cnt1 = reinterpret_cast<unsigned *>(w); a.cnt2 = a.cnt1 + B;
+    w += align256(2 * size_t(B) * sizeof(unsigned));
     a.pstat = reinterpret_cast<PStat *>(w); w += align256(size_t(B) * g1 * nch * sizeof(PStat));
     a.qstat = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * gamma * nch * sizeof(QStat));
     a.prow = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * g1 * sizeof(QStat));
@@ -1123,30 +1051,11 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.psum = reinterpret_cast<float *>(w);
 
-    const size_t cp_smem = size_t(M) * sizeof(int);   // M <= 8192
-    if (!vbig && !rbig && B <= kSmallMaxB) {
-        // few sequences: one cooperative launch of one block per SM (all resident at once)
-        const long long units = 1LL * B * (gamma + 1) * a.nch;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(unsigned(units < sms ? units : sms));
-        cfg.blockDim = dim3(kVThreads);
-        cfg.dynamicSmemBytes = cp_smem;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeCooperative;
-        attr[0].val.cooperative = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, verify_small_kernel<kVPerSmall, kRPerSmall>, a) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return DS_ERR_CUDA;
-        }
-        return DS_OK;
-    }
     if (vbig) verify_stats_kernel<kVPerBig><<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
     else verify_stats_kernel<kVPerSmall><<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
     DS_TRY_LAUNCH();
     // the small-chunk grid (few sequences) stages the list's cluster positions in shared memory
+    const size_t cp_smem = size_t(M) * sizeof(int);   // M <= 8192
     if (rbig) verify_residual_kernel<kRPerBig, false><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
     else verify_residual_kernel<kRPerSmall, true><<<dim3(a.nrch, B), kVThreads, cp_smem, stream>>>(a);
     DS_TRY_LAUNCH();

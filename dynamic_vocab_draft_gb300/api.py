@@ -104,20 +104,6 @@ class Router:
             _ptr(cluster_ids, I32, "cluster_ids"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
             _ptr(status, I32, "status"), _stream(stream)), "ds_router_topk_h")
 
-    def route_b1_workspace_bytes(self):
-        return int(_lib.load().ds_route_b1_workspace_bytes(self.handle))
-
-    def route_b1(self, H, pos, csr_off, csr_tok, scores, cluster_ids, vs_offsets, vs_ids, cpos, ws, status,
-                 blocks=0, stream=None):
-        """ds_route_b1: router, top-k and shortlist of draft position `pos` for one hidden state H [d]
-        (or [1, d]), in one launch."""
-        _lib.check(_lib.load().ds_route_b1(
-            self.handle, _ptr(H, BF16, "H"), int(pos), _ptr(csr_off, I32, "csr_off"), _ptr(csr_tok, I32, "csr_tok"),
-            csr_tok.numel(), _ptr(scores, F32, "scores"), _ptr(cluster_ids, I32, "cluster_ids"),
-            _ptr(vs_offsets, I32, "vs_offsets"), _ptr(vs_ids, I32, "vs_ids"), vs_ids.numel(),
-            _ptr(cpos, I32, "cpos"), int(blocks), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
-            _ptr(status, I32, "status"), _stream(stream)), "ds_route_b1")
-
     def close(self):
         if getattr(self, "handle", None):
             _lib.load().ds_router_destroy(self.handle)

@@ -269,172 +269,6 @@ gemv1_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict_
 constexpr int kGemv1Blocks = 64;       // a later position's router: four 256-thread blocks on each of
                                        // the 16 SMs the batch-1 head leaves free
 
-// ---------------------------------------------------------------------------------------
-// Batch 1: router, top-k and shortlist of one draft position in one launch.  Layer 1 (every
-// block, a warp per weight row) -> barrier -> layer 2 -> barrier -> each block then takes the
-// top-k of the same scores itself (the same keys and the same code give every block the same
-// clusters), scans the selected clusters' sizes and copies its share of their CSR slices.  The
-// two barriers replace two kernel boundaries on the side stream.
-//
-// The barrier is bounded.  The blocks of this launch are not guaranteed to be resident at once
-// (they may share the GPU with the head that runs beside them), but nothing they wait for
-// depends on them: a block that starts late only delays the others; a wait longer than the
-// budget sets DS_DEV_TIMEOUT.
-// ---------------------------------------------------------------------------------------
-__device__ void route_barrier(unsigned *bar, unsigned nblocks, long long budget, int32_t *status)
-{
-    __threadfence();                                   // every thread's results, before the arrival
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        volatile unsigned *gen = bar + 1;
-        const unsigned g = *gen;                       // read before arriving
-        if (atomicAdd(&bar[0], 1u) == nblocks - 1) {
-            atomicExch(&bar[0], 0u);                   // left at zero for the next barrier and launch
-            __threadfence();
-            atomicAdd(&bar[1], 1u);
-        } else {
-            const long long t0 = clock64();
-            while (*gen == g) {
-                if (clock64() - t0 > budget) { set_status(status, DS_DEV_TIMEOUT); break; }
-            }
-        }
-        __threadfence();                               // the others' results, after the barrier
-    }
-    __syncthreads();
-}
-
-struct RouteB1Args {
-    const uint16_t *h;                 // [d] hidden state the router reads
-    const uint16_t *W1, *b1, *W2, *b2;
-    int d, Hr, M, act, k;
-    const int32_t *csr_off, *csr_tok;
-    int V;
-    float *u, *scores;                 // [Hr] hidden layer (workspace), [M] out
-    int32_t *cluster_ids, *vs_offsets, *vs_ids, *cpos;
-    int64_t capacity;
-    unsigned *bar;
-    long long wait_budget;
-    int32_t *status;
-};
-
-// Warp dot product of a bf16 weight row with x (bf16 or fp32), 16 loads of 16 bytes per lane in
-// flight, x loaded next to the weights (the gemv1_kernel loop).
-template <typename XT>
-__device__ __forceinline__ float warp_row_dot(const uint16_t *__restrict__ A, int K, const XT *__restrict__ x, int lane)
-{
-    const uint4 *row = reinterpret_cast<const uint4 *>(A);
-    float a0 = 0.f, a1 = 0.f;
-    for (int k0 = 0; k0 < K; k0 += kGemvU * 256) {
-        uint4 w[kGemvU];
-        float xv[kGemvU][8];
-#pragma unroll
-        for (int u = 0; u < kGemvU; ++u) {
-            const int k = k0 + u * 256 + lane * 8;
-            w[u] = k < K ? ld_stream(row + (k >> 3)) : make_uint4(0, 0, 0, 0);
-            if (k < K) {
-                if constexpr (sizeof(XT) == 2) {
-                    const uint4 q = *reinterpret_cast<const uint4 *>(x + k);
-                    xv[u][0] = bf16lo(q.x); xv[u][1] = bf16hi(q.x); xv[u][2] = bf16lo(q.y); xv[u][3] = bf16hi(q.y);
-                    xv[u][4] = bf16lo(q.z); xv[u][5] = bf16hi(q.z); xv[u][6] = bf16lo(q.w); xv[u][7] = bf16hi(q.w);
-                } else {
-                    const float4 q0 = __ldcg(reinterpret_cast<const float4 *>(x + k));
-                    const float4 q1 = __ldcg(reinterpret_cast<const float4 *>(x + k + 4));
-                    xv[u][0] = q0.x; xv[u][1] = q0.y; xv[u][2] = q0.z; xv[u][3] = q0.w;
-                    xv[u][4] = q1.x; xv[u][5] = q1.y; xv[u][6] = q1.z; xv[u][7] = q1.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xv[u][e] = 0.f;
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kGemvU; ++u) {
-            a0 = fmaf(bf16lo(w[u].x), xv[u][0], a0);
-            a1 = fmaf(bf16hi(w[u].x), xv[u][1], a1);
-            a0 = fmaf(bf16lo(w[u].y), xv[u][2], a0);
-            a1 = fmaf(bf16hi(w[u].y), xv[u][3], a1);
-            a0 = fmaf(bf16lo(w[u].z), xv[u][4], a0);
-            a1 = fmaf(bf16hi(w[u].z), xv[u][5], a1);
-            a0 = fmaf(bf16lo(w[u].w), xv[u][6], a0);
-            a1 = fmaf(bf16hi(w[u].w), xv[u][7], a1);
-        }
-    }
-    return warp_sum(a0 + a1);
-}
-
-__device__ void topk_block(const float *__restrict__ s, int M, int k, int32_t *__restrict__ dst);
-
-__global__ void __launch_bounds__(kGemvWarps * 32)
-route_b1_kernel(RouteB1Args a)
-{
-    extern __shared__ int sm[];                        // [M] list positions | [k] selected clusters
-    int *spos = sm;
-    int32_t *sel = sm + a.M;
-    __shared__ int scratch[33];
-    const int lane = threadIdx.x & 31;
-    const int nw = gridDim.x * kGemvWarps;
-    const int gw = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
-    for (int i = gw; i < a.Hr; i += nw) {
-        const float s = warp_row_dot<uint16_t>(a.W1 + size_t(i) * a.d, a.d, a.h, lane);
-        if (lane == 0) a.u[i] = act_fn(s + bf16_to_f32(a.b1[i]), a.act);
-    }
-    route_barrier(a.bar, gridDim.x, a.wait_budget, a.status);
-    for (int c = gw; c < a.M; c += nw) {
-        const float s = warp_row_dot<float>(a.W2 + size_t(c) * a.Hr, a.Hr, a.u, lane);
-        if (lane == 0) a.scores[c] = s + bf16_to_f32(a.b2[c]);
-    }
-    route_barrier(a.bar, gridDim.x, a.wait_budget, a.status);
-    topk_block(a.scores, a.M, a.k, sel);               // reads the scores through L2
-    __syncthreads();
-    // cluster c's slice of the CSR, or an empty one (and DS_DEV_BAD_INDEX) if it is out of range
-    auto slice = [&](int c, int &lo) {
-        lo = a.csr_off[c];
-        const int hi = a.csr_off[c + 1];
-        if (lo < 0 || hi < lo || hi > a.V) {
-            if (blockIdx.x == 0) set_status(a.status, DS_DEV_BAD_INDEX);
-            lo = 0;
-            return 0;
-        }
-        return hi - lo;
-    };
-    // the list: clusters in ascending id (topk_block lists them so), each its CSR slice
-    for (int c = threadIdx.x; c < a.M; c += blockDim.x) spos[c] = -1;
-    __syncthreads();
-    const int E = (a.k + blockDim.x - 1) / blockDim.x;   // selected clusters per thread, in order
-    const int j0 = threadIdx.x * E;
-    int sum = 0;
-    for (int j = j0; j < j0 + E && j < a.k; ++j) {
-        int lo;
-        sum += slice(sel[j], lo);
-    }
-    int tot;
-    int run = block_exclusive_scan(sum, scratch, &tot);
-    for (int j = j0; j < j0 + E && j < a.k; ++j) {
-        const int c = sel[j];
-        int lo;
-        spos[c] = run;
-        run += slice(c, lo);
-    }
-    __syncthreads();
-    if (blockIdx.x == 0) {
-        for (int j = threadIdx.x; j < a.k; j += blockDim.x) a.cluster_ids[j] = sel[j];
-        for (int c = threadIdx.x; c < a.M; c += blockDim.x) a.cpos[c] = spos[c];
-        if (threadIdx.x == 0) {
-            a.vs_offsets[0] = 0;
-            a.vs_offsets[1] = tot;
-            if (int64_t(tot) > a.capacity) set_status(a.status, DS_DEV_CAPACITY);
-        }
-    }
-    // this block's share of the selected clusters, a warp per cluster
-    for (int j = gw; j < a.k; j += nw) {
-        const int c = sel[j];
-        int lo;
-        const int n = slice(c, lo), dst = spos[c];
-        for (int r = lane; r < n; r += 32)
-            if (int64_t(dst) + r < a.capacity) a.vs_ids[dst + r] = a.csr_tok[lo + r];
-    }
-}
-
 // One block per row: the top-k of scores[b][0..M).
 __global__ void __launch_bounds__(kTopkThreads)
 topk_rows_kernel(const float *__restrict__ scores, int M, int k, int32_t *__restrict__ ids)
@@ -694,46 +528,4 @@ extern "C" ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, i
     return ds_router_topk(H, B, r->d, r->W1, r->b1, r->Hr, r->W2, r->b2, r->M, r->act,
                           r->budget.data(), int(r->budget.size()), pos, scores, cluster_ids,
                           ws, base, dev_status, stream);
-}
-
-// Router + top-k + shortlist of one draft position at batch 1, in one launch (see route_b1_kernel).
-extern "C" size_t ds_route_b1_workspace_bytes(ds_router_t r)
-{
-    if (!r) return 0;
-    return align256(size_t(r->Hr) * sizeof(float)) + 256;
-}
-
-extern "C" ds_status ds_route_b1(ds_router_t r, const uint16_t *H, int pos,
-                                 const int32_t *csr_off, const int32_t *csr_tok, int V,
-                                 float *scores, int32_t *cluster_ids,
-                                 int32_t *vs_offsets, int32_t *vs_ids, int64_t vs_capacity, int32_t *cpos,
-                                 int blocks, void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream)
-{
-    ds::NvtxRange range("ds_route_b1");
-    if (!r || !H || !csr_off || !csr_tok || !scores || !cluster_ids || !vs_offsets || !vs_ids || !cpos)
-        return DS_ERR_INVALID_ARG;
-    if (V < 1 || vs_capacity < 0 || blocks < 0 || pos < 1 || pos > int(r->budget.size())) return DS_ERR_INVALID_ARG;
-    if (!aligned16(H) || !aligned16(scores)) return DS_ERR_INVALID_ARG;
-    if (!ws || ws_bytes < ds_route_b1_workspace_bytes(r)) return DS_ERR_WORKSPACE;
-    const int sms = sm_count();
-    if (sms <= 0) return DS_ERR_CUDA;
-    RouteB1Args a;
-    a.h = H; a.W1 = r->W1; a.b1 = r->b1; a.W2 = r->W2; a.b2 = r->b2;
-    a.d = r->d; a.Hr = r->Hr; a.M = r->M; a.act = r->act; a.k = r->budget[pos - 1];
-    a.csr_off = csr_off; a.csr_tok = csr_tok; a.V = V;
-    a.u = static_cast<float *>(ws);
-    a.bar = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + align256(size_t(r->Hr) * sizeof(float)));
-    a.scores = scores; a.cluster_ids = cluster_ids; a.vs_offsets = vs_offsets; a.vs_ids = vs_ids; a.cpos = cpos;
-    a.capacity = vs_capacity; a.wait_budget = wait_budget(); a.status = dev_status;
-    // the first position has the GPU to itself (a warp per weight row of layer 1); later ones run
-    // beside a head on the SMs it leaves free
-    int g = blocks > 0 ? blocks : pos == 1 ? (r->Hr + kGemvWarps - 1) / kGemvWarps : kGemv1Blocks;
-    if (g > 4 * sms) g = 4 * sms;
-    if (g < 1) g = 1;
-    const size_t smem = size_t(r->M + a.k) * sizeof(int);
-    static std::atomic<unsigned long long> smem_set{0};
-    if (!smem_limit_once(route_b1_kernel, size_t(2) * kRouterMaxK * sizeof(int), smem_set)) return DS_ERR_CUDA;
-    route_b1_kernel<<<g, kGemvWarps * 32, smem, stream>>>(a);
-    DS_TRY_LAUNCH();
-    return DS_OK;
 }

@@ -241,10 +241,7 @@ class ChainDrafter(_Common):
         self.tokens = self.out[2 * B:].view(gamma, B)
         self.token_idx = torch.empty(gamma, B, **i32)
         self.router = api.Router(W1, b1, W2, b2, act, budget)
-        # batch 1 without a union: router, top-k and shortlist of a position in one launch
-        self.fused_route = B == 1 and not self.union
-        wsb = self.router.route_b1_workspace_bytes() if self.fused_route else self.router.workspace_bytes(B)
-        self.ws_router = [api.workspace(wsb, dev) for _ in range(gamma)]
+        self.ws_router = [api.workspace(self.router.workspace_bytes(B), dev) for _ in range(gamma)]
         self.ws_short = [api.workspace(api.shortlist_workspace_bytes(B, M), dev) for _ in range(gamma)]
         self.ws_head = api.workspace(api.head_workspace_bytes(B), dev)
         self.ws_verify = api.workspace(api.verify_workspace_bytes(B, gamma, V), dev)
@@ -257,11 +254,6 @@ class ChainDrafter(_Common):
 
     def route(self, t, stream=None):
         """Router + top-k + shortlist of draft position t (0-based) for all sequences."""
-        if self.fused_route:
-            self.router.route_b1(self.H[t, 0], t + 1, self.csr_off, self.csr_tok, self.scores[t, 0],
-                                 self.cluster_ids[t], self.vs_offsets[t], self.vs_ids[t], self.cpos[t],
-                                 self.ws_router[t], self.status, stream=stream)
-            return
         self.router.topk(self.H[t], t + 1, self.scores[t], self.cluster_ids[t], self.ws_router[t], self.status,
                          stream)
         un = (self.union_ids[t], self.union_cluster[t], self.union_count[t]) if self.union else (None,) * 3
@@ -341,7 +333,7 @@ class ChainDrafter(_Common):
         return self.gamma
 
     def launches_per_step(self) -> int:
-        n_router = 0 if self.fused_route else router_launches(self.B)
+        n_router = router_launches(self.B)
         n_short = 4 if self.union else (1 if self.B == 1 else 3)
         n_head = 2 if self.union else 1
         n_draft = 5 if getattr(self, "drafter", None) is not None else 0

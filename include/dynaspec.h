@@ -132,24 +132,6 @@ ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, int pos,
                            void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
- * ds_route_b1 -- batch 1: ds_router_topk_h (B = 1, draft position pos) followed by
- * ds_build_shortlist (B = 1, no union) in one launch, with the same outputs: scores [M],
- * cluster_ids [k], vs_offsets [2], vs_ids [vs_capacity], cpos [M].  The launch's blocks meet at
- * two bounded barriers (after each router layer); each block then selects the same top-k
- * clusters itself and copies its share of their CSR slices.  blocks: 0 = the library's choice
- * (the whole GPU at pos = 1, 64 blocks for a router that runs beside a head).
- * Device errors: DS_DEV_BAD_INDEX (a CSR slice out of range), DS_DEV_CAPACITY, DS_DEV_TIMEOUT.
- * ws: ds_route_b1_workspace_bytes(router) bytes (zero it once; calls in flight together need
- * their own).
- * ------------------------------------------------------------------------------------- */
-size_t ds_route_b1_workspace_bytes(ds_router_t router);
-ds_status ds_route_b1(ds_router_t router, const uint16_t *H, int pos,
-                      const int32_t *csr_off, const int32_t *csr_tok, int V,
-                      float *scores, int32_t *cluster_ids,
-                      int32_t *vs_offsets, int32_t *vs_ids, int64_t vs_capacity, int32_t *cpos,
-                      int blocks, void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
-
-/* -------------------------------------------------------------------------------------
  * ds_build_shortlist -- V_S as the union of the selected clusters (abstract; summary,
  * Problem Definition, whose output is the shortlist V_S).  Clusters partition V, so the union
  * needs no de-duplication.  Order (the pages fix only the set): selected clusters in

@@ -36,6 +36,7 @@ SIGNATURES = {
                               P, P, P, P, P, P, SZ, P, P]),
     "ds_gathered_head_noalloc": (ST, [P, I, I, P, I, I, P, P, P, I, P, P, P, P, F, U64, I,
                                       P, P, P, P, P, P, P]),
+    "ds_prefetch_rows": (ST, [P, I, I, P, P, I, I, P]),
     "ds_verify_workspace_bytes": (SZ, [I, I, I]),
     "ds_verify": (ST, [P, I, I, I, F, P, I64, P, P, P, P, I, P, P, P, P, P, P, P, SZ, P, P]),
     "ds_verify_tree_workspace_bytes": (SZ, [I, I, I, I]),

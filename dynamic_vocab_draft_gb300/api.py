@@ -181,6 +181,14 @@ def gathered_head(H, G, W, vs_offsets, vs_ids, T, seed, pos, logits, token, toke
         _stream(stream)), "ds_gathered_head")
 
 
+def prefetch_rows(W, vs_ids, offsets, first_rows, blocks=0, stream=None):
+    """ds_prefetch_rows: L2 prefetch of the W rows of a list's first `first_rows` entries."""
+    V, d = W.shape
+    _lib.check(_lib.load().ds_prefetch_rows(
+        _ptr(W, BF16, "W"), V, d, _ptr(vs_ids, I32, "vs_ids"), _ptr(offsets, I32, "offsets"), int(first_rows),
+        int(blocks), _stream(stream)), "ds_prefetch_rows")
+
+
 def verify(p_logits, T, q_logits, vs_offsets, cpos, cluster_of, rank_in_cluster, draft_ids,
            uniforms, accepted_len, correction, ws, status, q_max=None, q_sumexp=None, stream=None):
     """p_logits [B, gamma+1, V]; q_logits [gamma, q_stride]; vs_offsets [gamma, B+1];

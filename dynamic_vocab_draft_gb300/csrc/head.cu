@@ -527,3 +527,43 @@ extern "C" ds_status ds_gathered_head_noalloc(const uint16_t *H, int B, int G,
                             logits, row_max, row_sumexp, token, token_idx,
                             scratch, kNoAllocBytes, dev_status, stream);
 }
+
+// ---------------------------------------------------------------------------------------
+// ds_prefetch_rows: bring the W rows a list names first into L2 ahead of the head that reads
+// them.  A draft position's list is known before the previous position's head has finished (its
+// router runs beside that head), and its W rows do not depend on the token that head draws, so
+// they can be fetched while that head's last rows stream and HBM has room to spare.  Marked
+// evict-last so the rest of the running head's stream does not push them out first; the head's
+// own loads, which carry no hint, read them back at normal priority.
+// ---------------------------------------------------------------------------------------
+namespace ds {
+namespace {
+__global__ void prefetch_rows_kernel(const uint16_t *__restrict__ W, int V, int d, const int32_t *__restrict__ ids,
+                                     const int32_t *__restrict__ offsets, int first)
+{
+    const int lo = offsets[0];
+    const int n = min(offsets[1] - lo, first);
+    const int lane = threadIdx.x & 31;
+    const int lines = (d * 2 + 127) / 128;                 // 128-byte lines per row
+    for (int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); j < n; j += gridDim.x * (blockDim.x >> 5)) {
+        const int v = ids[lo + j];
+        if (v < 0 || v >= V) continue;
+        const char *row = reinterpret_cast<const char *>(W + size_t(v) * d);
+        for (int l = lane; l < lines; l += 32)
+            asm volatile("prefetch.global.L2::evict_last [%0];" :: "l"(row + size_t(l) * 128));
+    }
+}
+}  // namespace
+}  // namespace ds
+
+extern "C" ds_status ds_prefetch_rows(const uint16_t *W, int V, int d, const int32_t *ids, const int32_t *offsets,
+                                      int first_rows, int blocks, cudaStream_t stream)
+{
+    ds::NvtxRange range("ds_prefetch_rows");
+    if (!W || !ids || !offsets || V < 1 || d < 8 || d % 8 || first_rows < 0 || blocks < 0) return DS_ERR_INVALID_ARG;
+    if (first_rows == 0) return DS_OK;
+    const int g = blocks > 0 ? blocks : 64;
+    prefetch_rows_kernel<<<g, 256, 0, stream>>>(W, V, d, ids, offsets, first_rows);
+    DS_TRY_LAUNCH();
+    return DS_OK;
+}

@@ -204,7 +204,7 @@ class ChainDrafter(_Common):
     """
 
     def __init__(self, W, W1, b1, W2, b2, csr_off, csr_tok, *, B, gamma, budget, act, T, seed,
-                 union=None):
+                 union=None, prefetch_rows=0):
         dev = W.device
         self.dev = dev
         self.W, self.W1, self.b1, self.W2, self.b2 = W, W1, b1, W2, b2
@@ -215,6 +215,8 @@ class ChainDrafter(_Common):
         self.budget = torch.tensor(list(budget), dtype=torch.int32)
         self.act, self.T, self.seed = act, float(T), int(seed)
         self.union = (B > 1) if union is None else bool(union)
+        # batch 1: the side stream fetches this many of the next head's first W rows into L2
+        self.prefetch_rows = int(prefetch_rows) if B == 1 and not self.union else 0
         V, M = self.V, self.M
         cap = B * V
         i32 = dict(dtype=torch.int32, device=dev)
@@ -260,6 +262,8 @@ class ChainDrafter(_Common):
         api.build_shortlist(self.csr_off, self.csr_tok, self.cluster_ids[t], self.vs_offsets[t],
                             self.vs_ids[t], self.cpos[t], self.ws_short[t], self.status,
                             un[0], un[1], un[2], stream)
+        if self.prefetch_rows and t > 0:
+            api.prefetch_rows(self.W, self.vs_ids[t], self.vs_offsets[t], self.prefetch_rows, stream=stream)
 
     def head(self, t, stream=None):
         api.gathered_head(self.H[t + 1], 1, self.W, self.vs_offsets[t], self.vs_ids[t], self.T,
@@ -337,7 +341,8 @@ class ChainDrafter(_Common):
         n_short = 4 if self.union else (1 if self.B == 1 else 3)
         n_head = 2 if self.union else 1
         n_draft = 5 if getattr(self, "drafter", None) is not None else 0
-        return self.gamma * (n_router + n_short + n_head + n_draft) + 2
+        n_pref = self.gamma - 1 if self.prefetch_rows else 0
+        return self.gamma * (n_router + n_short + n_head + n_draft) + n_pref + 2
 
 
 class TreeDrafter(_Common):

@@ -229,6 +229,18 @@ ds_status ds_gathered_head_noalloc(const uint16_t *H, int B, int G,
                                    int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
+ * ds_prefetch_rows -- fetch into L2 (marked evict-last) the W rows of the first `first_rows`
+ * entries of the list vs_ids[offsets[0] .. offsets[1]) (offsets: two device ints, as
+ * ds_build_shortlist writes them for one list).  A draft position's list is known before the
+ * previous position's head has finished and its rows do not depend on that head's token, so
+ * they can be fetched while that head's last rows stream; the entries a batch-1 head reads
+ * first are 0 .. (its warps - 1).  A hint only: results never depend on it.  Ids outside
+ * [0, V) are skipped.  blocks: 0 = 64 (the side stream's share of the GPU).
+ * ------------------------------------------------------------------------------------- */
+ds_status ds_prefetch_rows(const uint16_t *W, int V, int d, const int32_t *vs_ids, const int32_t *offsets,
+                           int first_rows, int blocks, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
  * ds_verify -- rejection-sampling verification over the full vocabulary (abstract: the target
  * model's check stays over the whole vocabulary, which keeps the output distribution exact;
  * summary, Pipeline Flow "Rejection Sampling Verification").  The pages cite Leviathan et al. and

@@ -104,6 +104,17 @@ class Router:
             _ptr(cluster_ids, I32, "cluster_ids"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
             _ptr(status, I32, "status"), _stream(stream)), "ds_router_topk_h")
 
+    def topk_list_b1(self, H, pos, csr_off, V, scores, cluster_ids, cpos, vs_offsets, list_table, capacity,
+                     ws, status, stream=None):
+        """ds_router_topk_list_b1: batch 1, the router and top-k of position `pos` with the list's
+        table (list_table [2 (k+1)] int32), cpos [M] and vs_offsets [2] instead of copied ids."""
+        _lib.check(_lib.load().ds_router_topk_list_b1(
+            self.handle, _ptr(H, BF16, "H"), int(pos), _ptr(csr_off, I32, "csr_off"), int(V),
+            _ptr(scores, F32, "scores"), _ptr(cluster_ids, I32, "cluster_ids"), _ptr(cpos, I32, "cpos"),
+            _ptr(vs_offsets, I32, "vs_offsets"), _ptr(list_table, I32, "list_table"), int(capacity),
+            _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
+            _stream(stream)), "ds_router_topk_list_b1")
+
     def close(self):
         if getattr(self, "handle", None):
             _lib.load().ds_router_destroy(self.handle)
@@ -187,6 +198,19 @@ def prefetch_rows(W, vs_ids, offsets, first_rows, blocks=0, stream=None):
     _lib.check(_lib.load().ds_prefetch_rows(
         _ptr(W, BF16, "W"), V, d, _ptr(vs_ids, I32, "vs_ids"), _ptr(offsets, I32, "offsets"), int(first_rows),
         int(blocks), _stream(stream)), "ds_prefetch_rows")
+
+
+def gathered_head_b1_table(H, W, list_table, k, csr_tok, T, seed, pos, logits, token, token_idx, ws, status,
+                           row_max=None, row_sumexp=None, stream=None):
+    """ds_gathered_head_b1_table: the batch-1 head over the list a table describes (H [d] or [1, d])."""
+    V, d = W.shape
+    _lib.check(_lib.load().ds_gathered_head_b1_table(
+        _ptr(H, BF16, "H"), _ptr(W, BF16, "W"), V, d, _ptr(list_table, I32, "list_table"), int(k),
+        _ptr(csr_tok, I32, "csr_tok"), float(T), int(seed) & 0xFFFFFFFFFFFFFFFF, int(pos),
+        _ptr(logits, F32, "logits"), _ptr(row_max, F32, "row_max", True), _ptr(row_sumexp, F32, "row_sumexp", True),
+        _ptr(token, I32, "token"), _ptr(token_idx, I32, "token_idx"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
+        _stream(stream)), "ds_gathered_head_b1_table")
 
 
 def verify(p_logits, T, q_logits, vs_offsets, cpos, cluster_of, rank_in_cluster, draft_ids,

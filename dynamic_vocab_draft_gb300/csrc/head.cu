@@ -41,6 +41,11 @@ struct HeadArgs {
     const uint16_t *W;
     int V, d;
     const int32_t *vs_offsets, *vs_ids;
+    // batch 1 without copied ids: the list's table (tk selected clusters: {list start, CSR start},
+    // then {list size, 0}) and the CSR tokens; used instead of vs_offsets / vs_ids when set
+    const int2 *table;
+    int tk;
+    const int32_t *csr_tok;
     float T, inv_te;
     uint64_t seed;
     int pos;
@@ -68,6 +73,7 @@ __device__ __forceinline__ void write_row(const HeadArgs &a, int r, const Stat &
 // its softmax/draw state -- no lane works alone per row.
 //
 // grid (gx, B): block (x, b) handles rows j = x*16 + warp, step gx*16, of list b.
+constexpr int kGvMaxTable = 8193;      // list-table entries: up to 8192 selected clusters + the end
 constexpr int kGvU = 16;               // loads per lane per round (4096 bf16)
 constexpr int kGvRound = kGvU * 256;
 constexpr int kGvFold = 8;             // block partials a lane of the last block loads at once
@@ -75,7 +81,7 @@ constexpr int kGvFold = 8;             // block partials a lane of the last bloc
 __global__ void __launch_bounds__(kGvWarps * 32, 1)
 head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__ counters)
 {
-    extern __shared__ uint4 hs[];                 // h as bf16, d / 8 vectors
+    extern __shared__ uint4 hs[];                 // h as bf16, d / 8 vectors; then the list table
     __shared__ Stat warp_stat[kGvWarps];
     const int b = blockIdx.y;
     const int d = a.d;
@@ -85,9 +91,31 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
     // needs none of them) should not wait behind it
     const uint4 *h = reinterpret_cast<const uint4 *>(a.H + size_t(b) * d);
     const uint4 h0 = int(threadIdx.x) < d / 8 ? h[threadIdx.x] : make_uint4(0, 0, 0, 0);
-    const int base = a.vs_offsets[b];
-    const int n = a.vs_offsets[b + 1] - base;
-    const int32_t *ids = a.vs_ids + base;
+    int2 *tab = reinterpret_cast<int2 *>(hs + d / 8);
+    int base, n;
+    if (a.table) {
+        // the table takes the place of the offsets in the chain: staged once, then searched
+        for (int s = threadIdx.x; s <= a.tk; s += blockDim.x) tab[s] = a.table[s];
+        __syncthreads();
+        base = 0;
+        n = tab[a.tk].x;
+    } else {
+        base = a.vs_offsets[b];
+        n = a.vs_offsets[b + 1] - base;
+    }
+    const int32_t *ids = a.vs_ids ? a.vs_ids + base : nullptr;
+    // token id of list entry j: the copied list, or the CSR slice of the selected cluster whose
+    // list start is the last one <= j (binary search over the table)
+    auto row_id = [&](int j) -> int {
+        if (!a.table) return ids[j];
+        int lo = 0, hi = a.tk;                        // tab[lo].x <= j < tab[hi].x
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (tab[mid].x <= j) lo = mid; else hi = mid;
+        }
+        const int q = tab[lo].y + (j - tab[lo].x);
+        return unsigned(q) < unsigned(a.V) ? a.csr_tok[q] : -1;    // -1: reported as a bad id
+    };
     float *lout = a.logits + base;
     const int stride = gridDim.x * kGvWarps;
     Stat st = stat_empty();
@@ -101,7 +129,7 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
     };
     const int j0 = blockIdx.x * kGvWarps + warp;  // the warp's rows: j0 + i * stride
     // the first batch's ids, and the first row's first round, are requested before h is staged
-    int my_v = j0 + lane * stride < n ? ids[j0 + lane * stride] : -1;
+    int my_v = j0 + lane * stride < n ? row_id(j0 + lane * stride) : -1;
     uint4 w[kGvU];
     bool preloaded = false;
     if (j0 < n) {
@@ -123,7 +151,7 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
         const int nrows = min(32, (n - jb + stride - 1) / stride);
         // ids of the next batch, one batch ahead
         const int nj = my_j + 32 * stride;
-        const int next_v = nj < n ? ids[nj] : -1;
+        const int next_v = nj < n ? row_id(nj) : -1;
         for (int k = 0; k < nrows; ++k) {
             const int v = __shfl_sync(0xFFFFFFFFu, my_v, k);
             const bool ok = v >= 0 && v < a.V;
@@ -305,6 +333,14 @@ head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *_
     if (lane == 0) write_row(a, r, c);
 }
 
+// The per-row head's dynamic shared memory: h (d bf16) and, with a list table, the table.
+bool head_smem_limit()
+{
+    static std::atomic<unsigned long long> smem_set{0};
+    return smem_limit_once(head_gemv_kernel, size_t(kGvMaxD) * sizeof(uint16_t) + size_t(kGvMaxTable) * sizeof(int2),
+                           smem_set);
+}
+
 }  // namespace
 }  // namespace ds
 
@@ -373,6 +409,7 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
     HeadArgs a;
     a.H = H; a.W = W; a.V = V; a.d = d;
     a.vs_offsets = vs_offsets; a.vs_ids = vs_ids;
+    a.table = nullptr; a.tk = 0; a.csr_tok = nullptr;
     a.T = T; a.inv_te = T > 0.f ? 1.f / T : 1.f;
     a.seed = seed; a.pos = pos;
     a.logits = logits; a.row_max = row_max; a.row_sumexp = row_sumexp;
@@ -389,8 +426,7 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
         if (gx < 1) gx = 1;
         if (gx > kGvMaxBlocks) gx = kGvMaxBlocks;
         const size_t smem = size_t(d) * sizeof(uint16_t);
-        static std::atomic<unsigned long long> smem_set{0};
-        if (!smem_limit_once(head_gemv_kernel, kGvMaxD * sizeof(float), smem_set)) return DS_ERR_CUDA;
+        if (!head_smem_limit()) return DS_ERR_CUDA;
         head_gemv_kernel<<<dim3(gx, B), kGvWarps * 32, smem, stream>>>(a, partials, counters);
         DS_TRY_LAUNCH();
         return DS_OK;
@@ -564,6 +600,45 @@ extern "C" ds_status ds_prefetch_rows(const uint16_t *W, int V, int d, const int
     if (first_rows == 0) return DS_OK;
     const int g = blocks > 0 ? blocks : 64;
     prefetch_rows_kernel<<<g, 256, 0, stream>>>(W, V, d, ids, offsets, first_rows);
+    DS_TRY_LAUNCH();
+    return DS_OK;
+}
+
+// Batch 1 with the list's table (ds_router_topk_list_b1) instead of copied ids: the same head,
+// each listed token found through the table and the CSR.
+extern "C" ds_status ds_gathered_head_b1_table(const uint16_t *H, const uint16_t *W, int V, int d,
+                                               const int32_t *list_table, int k, const int32_t *csr_tok,
+                                               float T, uint64_t seed, int pos,
+                                               float *logits, float *row_max, float *row_sumexp,
+                                               int32_t *token, int32_t *token_idx,
+                                               void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream)
+{
+    ds::NvtxRange range("ds_gathered_head_b1_table");
+    if (!H || !W || !list_table || !csr_tok || !logits || !token || !token_idx) return DS_ERR_INVALID_ARG;
+    if (V < 1 || d < 8 || d % 8 || k < 1 || !(T >= 0.f) || pos < 0) return DS_ERR_INVALID_ARG;
+    if (!aligned16(H) || !aligned16(W) || (reinterpret_cast<uintptr_t>(list_table) & 7u)) return DS_ERR_INVALID_ARG;
+    if (d > kGvMaxD || k + 1 > kGvMaxTable) return DS_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < ds_head_workspace_bytes(1)) return DS_ERR_WORKSPACE;
+    const int sms = sm_count();
+    if (sms <= 0) return DS_ERR_CUDA;
+    const HeadWs lay = head_ws_layout(1);
+    char *wsb = static_cast<char *>(ws);
+    HeadArgs a;
+    a.H = H; a.W = W; a.V = V; a.d = d;
+    a.vs_offsets = nullptr; a.vs_ids = nullptr;
+    a.table = reinterpret_cast<const int2 *>(list_table); a.tk = k; a.csr_tok = csr_tok;
+    a.T = T; a.inv_te = T > 0.f ? 1.f / T : 1.f;
+    a.seed = seed; a.pos = pos;
+    a.logits = logits; a.row_max = row_max; a.row_sumexp = row_sumexp;
+    a.token = token; a.token_idx = token_idx;
+    a.status = dev_status;
+    int gx = sms - kHeadSideSmsB1;
+    if (gx < 1) gx = 1;
+    if (gx > kGvMaxBlocks) gx = kGvMaxBlocks;
+    if (!head_smem_limit()) return DS_ERR_CUDA;
+    const size_t smem = size_t(d) * sizeof(uint16_t) + size_t(k + 1) * sizeof(int2);
+    head_gemv_kernel<<<dim3(gx, 1), kGvWarps * 32, smem, stream>>>(
+        a, reinterpret_cast<Stat *>(wsb + lay.partials), reinterpret_cast<unsigned *>(wsb + lay.row_cnt));
     DS_TRY_LAUNCH();
     return DS_OK;
 }

@@ -207,6 +207,58 @@ __device__ void topk_block(const float *__restrict__ s, int M, int k, int32_t *_
 
 static_assert(kGemvWarps * 32 == kTopkThreads, "the GEMV block runs the top-k epilogue");
 
+// The list of one batch-1 draft position without copying its token ids: after the top-k, the
+// selected clusters' list starts and CSR starts (list_table[s] = {list start, CSR start} for the
+// s-th selected cluster in ascending id, list_table[k] = {list size, 0}), cpos and the list's
+// offsets.  The head finds a listed token through the table and the CSR.
+struct ListOut {
+    const int32_t *csr_off;
+    int V;
+    int2 *table;
+    int32_t *cpos, *vs_offsets;
+    int64_t capacity;
+    int32_t *status;
+};
+
+// Called by the whole block that just wrote ids[0..k) (ascending cluster ids).
+__device__ void list_table_block(const ListOut &o, const int32_t *ids, int k, int M)
+{
+    __shared__ int scratch[33];
+    __syncthreads();                                   // this block's ids, to every thread
+    for (int c = threadIdx.x; c < M; c += blockDim.x) o.cpos[c] = -1;
+    // thread t owns the selected clusters j0 .. j0+E-1, in order
+    const int E = (k + blockDim.x - 1) / blockDim.x;
+    const int j0 = threadIdx.x * E, j1 = min(k, j0 + E);
+    auto slice = [&](int c, int &lo) {
+        lo = 0;
+        if (c < 0 || c >= M) { set_status(o.status, DS_DEV_BAD_INDEX); return 0; }
+        const int l0 = o.csr_off[c], hi = o.csr_off[c + 1];
+        if (l0 < 0 || hi < l0 || hi > o.V) { set_status(o.status, DS_DEV_BAD_INDEX); return 0; }
+        lo = l0;
+        return hi - l0;
+    };
+    int sum = 0;
+    for (int j = j0; j < j1; ++j) { int lo; sum += slice(ids[j], lo); }
+    int tot;
+    int run = block_exclusive_scan(sum, scratch, &tot);     // its barriers order the -1 pass first
+    for (int j = j0; j < j1; ++j) {
+        const int c = ids[j];
+        int lo;
+        const int n = slice(c, lo);
+        o.table[j] = make_int2(run, lo);
+        if (c >= 0 && c < M) o.cpos[c] = run;
+        run += n;
+    }
+    if (threadIdx.x == 0) {
+        // a list longer than the caller's logits is reported and read as empty
+        const bool fits = int64_t(tot) <= o.capacity;
+        if (!fits) set_status(o.status, DS_DEV_CAPACITY);
+        o.table[k] = make_int2(fits ? tot : 0, 0);
+        o.vs_offsets[0] = 0;
+        o.vs_offsets[1] = fits ? tot : 0;
+    }
+}
+
 // Batch 1: y[i] = act(A[i] . x + bias[i]).  No staging: every lane loads the slice of x its
 // weight vectors meet, next to those weights.  Warps stride over rows, so a small grid covers
 // the matrix in one wave -- the router of a later draft position runs on the few SMs the head
@@ -215,7 +267,7 @@ template <typename XT>
 __global__ void __launch_bounds__(kGemvWarps * 32)
 gemv1_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict__ x,
              const uint16_t *__restrict__ bias, int act, float *__restrict__ y,
-             int topk_k, int32_t *__restrict__ topk_ids, unsigned *__restrict__ counter)
+             int topk_k, int32_t *__restrict__ topk_ids, unsigned *__restrict__ counter, ListOut lout)
 {
     const int lane = threadIdx.x & 31;
     const int nw = gridDim.x * kGemvWarps;
@@ -263,7 +315,10 @@ gemv1_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict_
             if (topk_k > 0) __threadfence();
         }
     }
-    if (topk_k > 0 && last_block_done(counter, gridDim.x)) topk_block(y, N, topk_k, topk_ids);
+    if (topk_k > 0 && last_block_done(counter, gridDim.x)) {
+        topk_block(y, N, topk_k, topk_ids);
+        if (lout.table) list_table_block(lout, topk_ids, topk_k, N);
+    }
 }
 
 constexpr int kGemv1Blocks = 64;       // a later position's router: four 256-thread blocks on each of
@@ -397,13 +452,12 @@ extern "C" size_t ds_router_workspace_bytes(int B, int Hr)
     return align256(size_t(B) * size_t(Hr) * sizeof(float)) + align256(size_t(B) * sizeof(unsigned));
 }
 
-extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
-                                    const uint16_t *W1, const uint16_t *b1, int Hr,
-                                    const uint16_t *W2, const uint16_t *b2, int M, int act,
-                                    const int32_t *budget, int n_budget, int pos,
-                                    float *scores, int32_t *cluster_ids,
-                                    void *ws, size_t ws_bytes, int32_t *dev_status,
-                                    cudaStream_t stream)
+namespace {
+// ds_router_topk, and at B = 1 optionally the list's table (list_out.table non-null).
+ds_status router_topk(const uint16_t *H, int B, int d, const uint16_t *W1, const uint16_t *b1, int Hr,
+                      const uint16_t *W2, const uint16_t *b2, int M, int act, const int32_t *budget, int n_budget,
+                      int pos, float *scores, int32_t *cluster_ids, void *ws, size_t ws_bytes, int32_t *dev_status,
+                      cudaStream_t stream, ListOut list_out)
 {
     ds::NvtxRange range("ds_router_topk");
     if (!H || !W1 || !b1 || !W2 || !b2 || !budget || !scores || !cluster_ids)
@@ -431,10 +485,10 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
             return g < sms ? g : sms;
         };
         gemv1_kernel<uint16_t><<<grid1(Hr), kGemvWarps * 32, 0, stream>>>(W1, Hr, d, H, b1, act, u, 0,
-                                                                         nullptr, nullptr);
+                                                                         nullptr, nullptr, ListOut{});
         DS_TRY_LAUNCH();
         gemv1_kernel<float><<<grid1(M), kGemvWarps * 32, 0, stream>>>(W2, M, Hr, u, b2, -1, scores, k,
-                                                                      cluster_ids, counters);
+                                                                      cluster_ids, counters, list_out);
         DS_TRY_LAUNCH();
         return DS_OK;
     }
@@ -465,6 +519,20 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
     const ds_status s2 = launch_gemv<float, kGemvBT>(W2, M, Hr, u, B, b2, -1, scores, k, cluster_ids, counters, stream);
     if (s2 != DS_OK) return s2;
     return DS_OK;
+}
+}  // namespace
+
+extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
+                                    const uint16_t *W1, const uint16_t *b1, int Hr,
+                                    const uint16_t *W2, const uint16_t *b2, int M, int act,
+                                    const int32_t *budget, int n_budget, int pos,
+                                    float *scores, int32_t *cluster_ids,
+                                    void *ws, size_t ws_bytes, int32_t *dev_status,
+                                    cudaStream_t stream)
+{
+    ListOut none{};
+    return router_topk(H, B, d, W1, b1, Hr, W2, b2, M, act, budget, n_budget, pos, scores, cluster_ids,
+                       ws, ws_bytes, dev_status, stream, none);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -528,4 +596,23 @@ extern "C" ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, i
     return ds_router_topk(H, B, r->d, r->W1, r->b1, r->Hr, r->W2, r->b2, r->M, r->act,
                           r->budget.data(), int(r->budget.size()), pos, scores, cluster_ids,
                           ws, base, dev_status, stream);
+}
+
+// Batch 1: the router and top-k of a draft position with the list's table instead of its copied
+// ids (see ListOut); one launch fewer than ds_router_topk_h + ds_build_shortlist.
+extern "C" ds_status ds_router_topk_list_b1(ds_router_t r, const uint16_t *H, int pos,
+                                            const int32_t *csr_off, int V,
+                                            float *scores, int32_t *cluster_ids,
+                                            int32_t *cpos, int32_t *vs_offsets, int32_t *list_table,
+                                            int64_t capacity,
+                                            void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream)
+{
+    if (!r || !csr_off || !cpos || !vs_offsets || !list_table || V < 1 || capacity < 0) return DS_ERR_INVALID_ARG;
+    if (!scores) return DS_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(list_table) & 7u) != 0) return DS_ERR_INVALID_ARG;
+    ListOut lo;
+    lo.csr_off = csr_off; lo.V = V; lo.table = reinterpret_cast<int2 *>(list_table);
+    lo.cpos = cpos; lo.vs_offsets = vs_offsets; lo.capacity = capacity; lo.status = dev_status;
+    return router_topk(H, 1, r->d, r->W1, r->b1, r->Hr, r->W2, r->b2, r->M, r->act, r->budget.data(),
+                       int(r->budget.size()), pos, scores, cluster_ids, ws, ws_bytes, dev_status, stream, lo);
 }

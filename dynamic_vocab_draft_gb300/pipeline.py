@@ -3,7 +3,7 @@
 Pipeline order (DynaSpec summary, Technical Details > Pipeline Flow): router on a parallel
 stream, draft computation on the main stream, a synchronisation, the gathered projection,
 then rejection-sampling verification.  Per draft position t the router and shortlist build
-run on a side stream (Novel Architectural Elements: the router runs concurrently, on a CUDA
+(at batch 1 with small budgets: the router and the list's cluster table) run on a side stream (Novel Architectural Elements: the router runs concurrently, on a CUDA
 stream of its own), an event marks the shortlist ready, and the main stream waits on that
 event before the gathered head.
 
@@ -26,6 +26,7 @@ default.
 """
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 from . import api
@@ -201,10 +202,18 @@ class ChainDrafter(_Common):
     Per-step inputs are written into ``self.H`` [gamma+1, B, d] (hidden states; the router at
     position t reads H[t-1], the head H[t]), ``self.z`` [B, gamma+1, V] (target logits) and
     ``self.u`` [B, gamma+1] (verification uniforms).
+
+    At batch 1 a list can be named by a table of its selected clusters instead of a copy of its
+    token ids (``list_table``): the router's top-k block writes the table and the head reads
+    each token through it and the CSR, one launch fewer per position on the side stream.  The
+    head stages the table in shared memory and searches it once per row, so the default (None)
+    takes the table only for budgets up to ``TABLE_MAX_K`` clusters.
     """
 
+    TABLE_MAX_K = 512
+
     def __init__(self, W, W1, b1, W2, b2, csr_off, csr_tok, *, B, gamma, budget, act, T, seed,
-                 union=None, prefetch_rows=0):
+                 union=None, prefetch_rows=0, list_table=None):
         dev = W.device
         self.dev = dev
         self.W, self.W1, self.b1, self.W2, self.b2 = W, W1, b1, W2, b2
@@ -217,6 +226,10 @@ class ChainDrafter(_Common):
         self.union = (B > 1) if union is None else bool(union)
         # batch 1: the side stream fetches this many of the next head's first W rows into L2
         self.prefetch_rows = int(prefetch_rows) if B == 1 and not self.union else 0
+        # batch 1: the list as a table of its selected clusters (no copy of its ids)
+        if list_table is None:
+            list_table = max(int(x) for x in budget) <= self.TABLE_MAX_K
+        self.table_mode = bool(list_table) and B == 1 and not self.union and not self.prefetch_rows
         V, M = self.V, self.M
         cap = B * V
         i32 = dict(dtype=torch.int32, device=dev)
@@ -229,6 +242,8 @@ class ChainDrafter(_Common):
         self.vs_offsets = torch.zeros(gamma, B + 1, **i32)
         self.vs_ids = torch.zeros(gamma, cap, **i32)
         self.cpos = torch.empty(gamma, B * M, **i32)
+        if self.table_mode:
+            self.list_table = torch.zeros(gamma, 2 * (max(int(x) for x in budget) + 1), **i32)
         if self.union:
             self.union_ids = torch.empty(gamma, V, **i32)
             self.union_cluster = torch.empty(gamma, V, **i32)
@@ -256,6 +271,11 @@ class ChainDrafter(_Common):
 
     def route(self, t, stream=None):
         """Router + top-k + shortlist of draft position t (0-based) for all sequences."""
+        if self.table_mode:
+            self.router.topk_list_b1(self.H[t], t + 1, self.csr_off, self.V, self.scores[t], self.cluster_ids[t],
+                                     self.cpos[t], self.vs_offsets[t], self.list_table[t], self.logits.shape[1],
+                                     self.ws_router[t], self.status, stream)
+            return
         self.router.topk(self.H[t], t + 1, self.scores[t], self.cluster_ids[t], self.ws_router[t], self.status,
                          stream)
         un = (self.union_ids[t], self.union_cluster[t], self.union_count[t]) if self.union else (None,) * 3
@@ -266,6 +286,12 @@ class ChainDrafter(_Common):
             api.prefetch_rows(self.W, self.vs_ids[t], self.vs_offsets[t], self.prefetch_rows, stream=stream)
 
     def head(self, t, stream=None):
+        if self.table_mode:
+            api.gathered_head_b1_table(self.H[t + 1], self.W, self.list_table[t], int(self.budget[t]), self.csr_tok,
+                                       self.T, self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],
+                                       self.ws_head, self.status, row_max=self.row_max[t],
+                                       row_sumexp=self.row_sumexp[t], stream=stream)
+            return
         api.gathered_head(self.H[t + 1], 1, self.W, self.vs_offsets[t], self.vs_ids[t], self.T,
                           self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],
                           self.ws_head, self.status, cpos=self.cpos[t], rank_in_cluster=self.rank,
@@ -282,6 +308,18 @@ class ChainDrafter(_Common):
         """One speculation step; verification first waits for the events in `before_verify`, if
         given (inputs that only verification reads may still be arriving)."""
         self._run(self.gamma, before_verify)
+
+    def list_ids(self, t, b=0):
+        """The token ids of list (t, b) as a host array: copied ids, or (batch 1 with a table) the
+        CSR slices of the selected clusters the table names."""
+        if not self.table_mode:
+            o = self.vs_offsets[t].cpu().numpy()
+            return self.vs_ids[t, o[b]:o[b + 1]].cpu().numpy()
+        k = int(self.budget[t])
+        tab = self.list_table[t, :2 * (k + 1)].cpu().numpy().reshape(k + 1, 2)
+        tok = self.csr_tok.cpu().numpy()
+        parts = [tok[tab[s, 1]:tab[s, 1] + (tab[s + 1, 0] - tab[s, 0])] for s in range(k)]
+        return np.concatenate(parts) if parts else np.zeros(0, np.int32)
 
     def attach_drafter(self, Wfc, Wmix, Wug, Wdn, scale=0.0, E=None):
         """Put a drafter stand-in (ds_drafter_standin) before every head, batch 1 only.  The step
@@ -338,7 +376,7 @@ class ChainDrafter(_Common):
 
     def launches_per_step(self) -> int:
         n_router = router_launches(self.B)
-        n_short = 4 if self.union else (1 if self.B == 1 else 3)
+        n_short = 4 if self.union else (0 if self.table_mode else 1 if self.B == 1 else 3)
         n_head = 2 if self.union else 1
         n_draft = 5 if getattr(self, "drafter", None) is not None else 0
         n_pref = self.gamma - 1 if self.prefetch_rows else 0

@@ -132,6 +132,38 @@ ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, int pos,
                            void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
+ * Batch 1 without copying the list's ids.  The list of one sequence is a pure function of its
+ * selected clusters and the CSR, so instead of copying the tokens (ds_build_shortlist) the
+ * router's top-k block writes a table of the selected clusters, and the head reads each listed
+ * token from the CSR through it: one launch fewer per draft position, same results.
+ *   ds_router_topk_list_b1  ds_router_topk_h at B = 1 for draft position pos, plus:
+ *       list_table [2 (k+1)] int32 (out; 8-byte aligned): pairs {list start, CSR start} of the
+ *                  k selected clusters in ascending id, then {list size, 0};
+ *       cpos [M], vs_offsets [2] (out): as ds_build_shortlist writes them for one list;
+ *       csr_off [M+1], V: the clusters; capacity: list entries the caller's logits hold.
+ *       Device errors: DS_DEV_BAD_INDEX (a CSR slice out of range, read as empty),
+ *       DS_DEV_CAPACITY (the list is longer than capacity; the table then ends the list at 0
+ *       entries, so the head writes nothing).
+ *       ws: ds_router_workspace_bytes_h(router, 1) bytes.
+ *   ds_gathered_head_b1_table  ds_gathered_head at B = G = 1 on that list: entry j's token is
+ *       csr_tok[CSR start + (j - list start)] of the last selected cluster whose list start is
+ *       <= j.  k: the number of selected clusters (the table's pairs before the end pair).
+ *       Outputs and limits as ds_gathered_head's per-row path (k <= 8192);
+ *       ws: ds_head_workspace_bytes(1) bytes.
+ * ------------------------------------------------------------------------------------- */
+ds_status ds_router_topk_list_b1(ds_router_t router, const uint16_t *H, int pos,
+                                 const int32_t *csr_off, int V,
+                                 float *scores, int32_t *cluster_ids,
+                                 int32_t *cpos, int32_t *vs_offsets, int32_t *list_table, int64_t capacity,
+                                 void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+ds_status ds_gathered_head_b1_table(const uint16_t *H, const uint16_t *W, int V, int d,
+                                    const int32_t *list_table, int k, const int32_t *csr_tok,
+                                    float T, uint64_t seed, int pos,
+                                    float *logits, float *row_max, float *row_sumexp,
+                                    int32_t *token, int32_t *token_idx,
+                                    void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+
+/* -------------------------------------------------------------------------------------
  * ds_build_shortlist -- V_S as the union of the selected clusters (abstract; summary,
  * Problem Definition, whose output is the shortlist V_S).  Clusters partition V, so the union
  * needs no de-duplication.  Order (the pages fix only the set): selected clusters in

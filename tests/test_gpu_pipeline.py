@@ -29,12 +29,12 @@ def pkg():
     return p
 
 
-def make_chain(pkg, inp, T):
+def make_chain(pkg, inp, T, **kw):
     cfg = inp["cfg"]
     d = pkg.pipeline.ChainDrafter(
         gu.device_head(inp), gu.bf16(inp["W1"]), gu.bf16(inp["b1"]), gu.bf16(inp["W2"]), gu.bf16(inp["b2"]),
         torch.as_tensor(inp["csr_off"]), torch.as_tensor(inp["csr_tok"]),
-        B=cfg.B, gamma=cfg.gamma, budget=cfg.budget, act=cfg.act, T=T, seed=inp["gumbel_seed"])
+        B=cfg.B, gamma=cfg.gamma, budget=cfg.budget, act=cfg.act, T=T, seed=inp["gumbel_seed"], **kw)
     d.H.copy_(gu.bf16(np.ascontiguousarray(inp["H"].transpose(1, 0, 2))))
     d.z.copy_(gu.f32(inp["z"]))
     d.u.copy_(gu.f32(inp["u"]))
@@ -49,7 +49,6 @@ def compare_chain(inp, d, T, seqs, ref=None, z=None):
     ref = oracle.chain_step(inp, T=T, seqs=seqs) if ref is None else ref
     scores = d.scores.cpu().numpy()
     offs = d.vs_offsets.cpu().numpy()
-    ids_all = d.vs_ids.cpu().numpy()
     logits = d.logits.cpu().numpy()
     toks = d.tokens.cpu().numpy()
     tix = d.token_idx.cpu().numpy()
@@ -66,8 +65,7 @@ def compare_chain(inp, d, T, seqs, ref=None, z=None):
             if not topk_same_or_excused(cids, p["scores"], cfg.budget[t]):
                 ok = False
                 break
-            S = ids_all[t, offs[t, b]:offs[t, b + 1]]
-            assert np.array_equal(S, p["S"])
+            assert np.array_equal(d.list_ids(t, b), p["S"])
             assert_close(logits[t, offs[t, b]:offs[t, b + 1]], p["logits"], "head logits")
             if not token_same_or_excused(int(tix[t, b]), p["idx"], p["logits"], p["S"], T,
                                          inp["gumbel_seed"], t + 1, b):
@@ -129,6 +127,25 @@ def test_chain_step_matches_oracle(pkg, name, T, seqs):
     # with the device inputs and outputs wiped before the replay
     out_h = _replay_io(d, early=(d.H,), late=(d.z, d.u))
     assert torch.equal(out_h, torch.cat([snap[2], snap[3], snap[1].flatten()]).cpu())
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 1.0), ("llama_b1", 1.0), ("llama_b1", 0.0), ("large_b1_f100", 1.0)])
+def test_chain_b1_list_table_and_copied_list_agree(pkg, name, T):
+    # Batch 1 runs through the list table by default; the copied-list path (a shortlist launch
+    # per position) gives the same step, bit for bit, and both match the oracle.
+    inp = gu.chain_inputs(name)
+    outs = []
+    for table in (True, False):
+        d = make_chain(pkg, inp, T, list_table=table)
+        assert d.table_mode == table
+        d.step()
+        torch.cuda.synchronize()
+        d.check_status()
+        compare_chain(inp, d, T, [0])
+        outs.append((d.out.clone(), d.logits.clone(), d.vs_offsets.clone(), d.cpos.clone(), d.token_idx.clone()))
+        del d
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
 
 
 def _aligned_chain_ref(inp, T, seqs, upto):
@@ -305,7 +322,9 @@ def test_chain_step_with_drafter_standin(pkg, serial):
     d.step()
     torch.cuda.synchronize()
     d.check_status()
-    for a, b in ((ref.out, d.out), (ref.logits, d.logits), (ref.vs_ids, d.vs_ids)):
+    assert ref.table_mode == d.table_mode
+    for a, b in ((ref.out, d.out), (ref.logits, d.logits),
+                 (ref.list_table, d.list_table) if d.table_mode else (ref.vs_ids, d.vs_ids)):
         assert torch.equal(a, b)
     d.enable_head_timing()
     d.enable_overlap_timing()
@@ -319,6 +338,29 @@ def test_chain_step_with_drafter_standin(pkg, serial):
         for t in range(1, cfg.gamma):
             # router t starts after the drafter step that produced its input, head t after router t
             assert ov[t][0] >= ov[t - 1][3] - 1e-3 and ov[t][4] >= ov[t][1] - 1e-3
+
+
+def test_prefetch_rows_changes_no_result(pkg):
+    # The side stream's L2 prefetch of the next head's first rows (ds_prefetch_rows) is a hint:
+    # the step's outputs are bit for bit those of the step without it, eagerly and from a graph.
+    inp = gu.chain_inputs("llama_b1")
+    cfg = inp["cfg"]
+    outs = []
+    for rows in (0, 2176):
+        d = pkg.pipeline.ChainDrafter(
+            gu.device_head(inp), gu.bf16(inp["W1"]), gu.bf16(inp["b1"]), gu.bf16(inp["W2"]), gu.bf16(inp["b2"]),
+            torch.as_tensor(inp["csr_off"]), torch.as_tensor(inp["csr_tok"]),
+            B=1, gamma=cfg.gamma, budget=cfg.budget, act=cfg.act, T=cfg.T, seed=inp["gumbel_seed"], prefetch_rows=rows)
+        d.H.copy_(gu.bf16(np.ascontiguousarray(inp["H"].transpose(1, 0, 2))))
+        d.z.copy_(gu.f32(inp["z"]))
+        d.u.copy_(gu.f32(inp["u"]))
+        d.capture()
+        d.replay()
+        torch.cuda.synchronize()
+        d.check_status()
+        outs.append((d.out.clone(), d.logits.clone()))
+        del d
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
 
 
 def _replay_io(d, early, late):

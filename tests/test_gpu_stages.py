@@ -200,6 +200,127 @@ def test_shortlist_device_errors(ds):
 
 
 # ---------------------------------------------------------------------------------------
+# Batch 1 through a table of the selected clusters (no copied ids)
+# ---------------------------------------------------------------------------------------
+def _merged_empty_csr(csr_off):
+    """The same token order with every odd cluster emptied into the even one before it."""
+    off = csr_off.copy()
+    M = off.size - 1
+    for i in range(1, M, 2):
+        off[i] = csr_off[i + 1]
+    return off
+
+
+def _table_step(ds, inp, pos, csr_off, cap=None, T=1.0, copy=True):
+    """Router with the list table for position pos, then the table head; also the copy-path
+    head on the same cluster ids.  Returns host arrays."""
+    cfg = inp["cfg"]
+    dev = gu.dev()
+    k = cfg.budget[pos - 1]
+    V, M = cfg.V, cfg.M
+    cap = V if cap is None else cap
+    r = ds.Router(gu.bf16(inp["W1"]), gu.bf16(inp["b1"]), gu.bf16(inp["W2"]), gu.bf16(inp["b2"]), cfg.act,
+                  cfg.budget)
+    H = gu.bf16(inp["H"][:1, pos - 1])
+    scores = torch.empty(1, M, dtype=torch.float32, device=dev)
+    ids = torch.empty(1, k, dtype=torch.int32, device=dev)
+    cpos = torch.full((M,), -9, dtype=torch.int32, device=dev)
+    vs_off = torch.full((2,), -9, dtype=torch.int32, device=dev)
+    table = torch.full((2 * (k + 1),), -9, dtype=torch.int32, device=dev)
+    st = gu.status()
+    ws = ds.workspace(r.workspace_bytes(1), dev)
+    off_d, tok_d = gu.i32(csr_off), gu.i32(inp["csr_tok"])
+    r.topk_list_b1(H, pos, off_d, V, scores, ids, cpos, vs_off, table, cap, ws, st)
+    Hh = gu.bf16(inp["H"][:1, pos])
+    W = gu.device_head(inp)
+    outs = []
+    for mode in ("table", "copy") if copy else ("table",):
+        logits = torch.full((cap + 64,), float("nan"), dtype=torch.float32, device=dev)
+        tok, tix = (torch.full((1,), -5, dtype=torch.int32, device=dev) for _ in range(2))
+        rmax, rsum = (torch.empty(1, dtype=torch.float32, device=dev) for _ in range(2))
+        wsh = ds.workspace(ds.head_workspace_bytes(1), dev)
+        if mode == "table":
+            ds.gathered_head_b1_table(Hh, W, table, k, tok_d, T, inp["gumbel_seed"], pos, logits[:cap], tok, tix,
+                                      wsh, st, row_max=rmax, row_sumexp=rsum)
+        else:
+            ids_h = ids.cpu().numpy()
+            S = oracle.shortlist(csr_off, inp["csr_tok"], ids_h[0])
+            if S.size > cap:
+                break
+            so = torch.tensor([0, S.size], dtype=torch.int32, device=dev)
+            ds.gathered_head(Hh, 1, W, so, gu.i32(S) if S.size else torch.zeros(1, dtype=torch.int32, device=dev),
+                             T, inp["gumbel_seed"], pos, logits[:cap], tok, tix, wsh, st, row_max=rmax,
+                             row_sumexp=rsum)
+        torch.cuda.synchronize()
+        outs.append(tuple(x.cpu().numpy() for x in (logits, tok, tix, rmax, rsum)))
+    r.close()
+    return dict(scores=scores.cpu().numpy()[0], ids=ids.cpu().numpy()[0], cpos=cpos.cpu().numpy(),
+                vs_off=vs_off.cpu().numpy(), table=table.cpu().numpy().reshape(k + 1, 2), st=st.item(), outs=outs)
+
+
+@pytest.mark.parametrize("name,T,empty", [("tiny", 1.0, False), ("tiny", 0.0, True), ("llama_b1", 1.0, False),
+                                          ("llama_b1", 0.0, True), ("large_b1_f5", 1.0, False),
+                                          ("large_b1_f100", 1.0, False)])
+def test_list_table_path_matches_oracle(ds, name, T, empty):
+    # The router writes {list start, CSR start} per selected cluster (ascending id) and the list
+    # size; the head reads each entry's token through it.  Against the oracle's shortlist of the
+    # same clusters, and bit for bit against the head on the copied list.  `empty`: a CSR in
+    # which every odd cluster is empty (selected empty clusters must not shift the lookup).
+    inp = gu.chain_inputs(name)
+    cfg = inp["cfg"]
+    csr_off = _merged_empty_csr(inp["csr_off"]) if empty else inp["csr_off"]
+    sizes = np.diff(csr_off)
+    for pos in sorted({1, 2, cfg.gamma}):
+        k = cfg.budget[pos - 1]
+        o = _table_step(ds, inp, pos, csr_off, T=T)
+        assert o["st"] == 0
+        s_ref, _ = oracle.router(inp["H"][:1, pos - 1], inp["W1"], inp["b1"], inp["W2"], inp["b2"], cfg.act)
+        assert_close(o["scores"], s_ref[0], "router scores")
+        ids = o["ids"]
+        assert np.all(np.diff(ids) > 0)
+        topk_same_or_excused(ids, s_ref[0], k)
+        starts = np.concatenate([[0], np.cumsum(sizes[ids])])
+        assert np.array_equal(o["table"][:k, 0], starts[:k])
+        assert np.array_equal(o["table"][:k, 1], csr_off[ids])
+        assert tuple(o["table"][k]) == (starts[k], 0)
+        assert tuple(o["vs_off"]) == (0, starts[k])
+        cp = np.full(cfg.M, -1)
+        cp[ids] = starts[:k]
+        assert np.array_equal(o["cpos"], cp)
+        S = oracle.shortlist(csr_off, inp["csr_tok"], ids)
+        n = S.size
+        logits, tok, tix, rmax, rsum = o["outs"][0]
+        l_ref = oracle.head(inp["H"][:1, pos], inp["W"], S)[0]
+        assert_close(logits[:n], l_ref, "table head logits")
+        assert np.isnan(logits[n:]).all()
+        rtok, ridx, m, s = oracle.draft_sample(l_ref, S, T, inp["gumbel_seed"], pos, 0)
+        assert_close([rmax[0]], [m], "row max")
+        np.testing.assert_allclose(rsum[0], s, rtol=2e-3)
+        if token_same_or_excused(int(tix[0]), ridx, l_ref, S, T, inp["gumbel_seed"], pos, 0):
+            assert tok[0] == rtok
+        assert S[tix[0]] == tok[0]
+        for a, b in zip(o["outs"][0], o["outs"][1]):       # same rows, same grid: same bits
+            assert np.array_equal(a, b, equal_nan=True)
+
+
+def test_list_table_capacity_and_bad_csr(ds):
+    inp = gu.chain_inputs("tiny")
+    cfg = inp["cfg"]
+    # a list longer than the caller's logits: reported, and read as empty (nothing written)
+    o = _table_step(ds, inp, 1, inp["csr_off"], cap=5)
+    assert o["st"] & 0x20
+    k = cfg.budget[0]
+    assert tuple(o["table"][k]) == (0, 0) and tuple(o["vs_off"]) == (0, 0)
+    assert np.isnan(o["outs"][0][0]).all()
+    # a CSR slice past V: reported, read as empty
+    bad = inp["csr_off"].copy()
+    bad[1:] = np.minimum(bad[1:] + cfg.V, 2 * cfg.V)
+    bad[-1] = 2 * cfg.V
+    o = _table_step(ds, inp, 1, bad, copy=False)
+    assert o["st"] & 0x10
+
+
+# ---------------------------------------------------------------------------------------
 # Gathered head
 # ---------------------------------------------------------------------------------------
 def _run_head(ds, inp, Hrows, G, ids, T, pos, union):

@@ -205,12 +205,17 @@ class ChainDrafter(_Common):
 
     At batch 1 a list can be named by a table of its selected clusters instead of a copy of its
     token ids (``list_table``): the router's top-k block writes the table and the head reads
-    each token through it and the CSR, one launch fewer per position on the side stream.  The
-    head stages the table in shared memory and searches it once per row, so the default (None)
-    takes the table only for budgets up to ``TABLE_MAX_K`` clusters.
+    each token through it and the CSR, one launch fewer on the side stream.  The head stages the
+    table in shared memory and searches it once per row, which costs it a little, so the default
+    (None) takes the table where the launch it saves is on the critical path: at the first
+    position (nothing runs before it) and where the previous position's head is too short to
+    hide the side stream (it moves less than ``TABLE_PREV_BYTES`` of W on average), and only
+    for budgets up to ``TABLE_MAX_K`` clusters.  ``list_table`` may also be a bool (every
+    position) or a sequence of gamma bools.
     """
 
     TABLE_MAX_K = 512
+    TABLE_PREV_BYTES = 100e6
 
     def __init__(self, W, W1, b1, W2, b2, csr_off, csr_tok, *, B, gamma, budget, act, T, seed,
                  union=None, prefetch_rows=0, list_table=None):
@@ -228,8 +233,15 @@ class ChainDrafter(_Common):
         self.prefetch_rows = int(prefetch_rows) if B == 1 and not self.union else 0
         # batch 1: the list as a table of its selected clusters (no copy of its ids)
         if list_table is None:
-            list_table = max(int(x) for x in budget) <= self.TABLE_MAX_K
-        self.table_mode = bool(list_table) and B == 1 and not self.union and not self.prefetch_rows
+            row_bytes = 2.0 * W.shape[1] * W.shape[0] / max(1, int(csr_off.numel()) - 1)   # per cluster
+            list_table = [int(budget[t]) <= self.TABLE_MAX_K
+                          and (t == 0 or int(budget[t - 1]) * row_bytes < self.TABLE_PREV_BYTES)
+                          for t in range(gamma)]
+        per_pos = list(list_table) if isinstance(list_table, (list, tuple)) else [bool(list_table)] * gamma
+        assert len(per_pos) == gamma
+        ok = B == 1 and not self.union and not self.prefetch_rows
+        self.table_pos = [bool(x) and ok for x in per_pos]
+        self.table_mode = any(self.table_pos)
         V, M = self.V, self.M
         cap = B * V
         i32 = dict(dtype=torch.int32, device=dev)
@@ -271,7 +283,7 @@ class ChainDrafter(_Common):
 
     def route(self, t, stream=None):
         """Router + top-k + shortlist of draft position t (0-based) for all sequences."""
-        if self.table_mode:
+        if self.table_pos[t]:
             self.router.topk_list_b1(self.H[t], t + 1, self.csr_off, self.V, self.scores[t], self.cluster_ids[t],
                                      self.cpos[t], self.vs_offsets[t], self.list_table[t], self.logits.shape[1],
                                      self.ws_router[t], self.status, stream)
@@ -286,7 +298,7 @@ class ChainDrafter(_Common):
             api.prefetch_rows(self.W, self.vs_ids[t], self.vs_offsets[t], self.prefetch_rows, stream=stream)
 
     def head(self, t, stream=None):
-        if self.table_mode:
+        if self.table_pos[t]:
             api.gathered_head_b1_table(self.H[t + 1], self.W, self.list_table[t], int(self.budget[t]), self.csr_tok,
                                        self.T, self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],
                                        self.ws_head, self.status, row_max=self.row_max[t],
@@ -312,7 +324,7 @@ class ChainDrafter(_Common):
     def list_ids(self, t, b=0):
         """The token ids of list (t, b) as a host array: copied ids, or (batch 1 with a table) the
         CSR slices of the selected clusters the table names."""
-        if not self.table_mode:
+        if not self.table_pos[t]:
             o = self.vs_offsets[t].cpu().numpy()
             return self.vs_ids[t, o[b]:o[b + 1]].cpu().numpy()
         k = int(self.budget[t])
@@ -376,11 +388,11 @@ class ChainDrafter(_Common):
 
     def launches_per_step(self) -> int:
         n_router = router_launches(self.B)
-        n_short = 4 if self.union else (0 if self.table_mode else 1 if self.B == 1 else 3)
+        n_short = 4 if self.union else (1 if self.B == 1 else 3)
         n_head = 2 if self.union else 1
         n_draft = 5 if getattr(self, "drafter", None) is not None else 0
         n_pref = self.gamma - 1 if self.prefetch_rows else 0
-        return self.gamma * (n_router + n_short + n_head + n_draft) + n_pref + 2
+        return self.gamma * (n_router + n_short + n_head + n_draft) - n_short * sum(self.table_pos) + n_pref + 2
 
 
 class TreeDrafter(_Common):

@@ -131,13 +131,15 @@ def test_chain_step_matches_oracle(pkg, name, T, seqs):
 
 @pytest.mark.parametrize("name,T", [("tiny", 1.0), ("llama_b1", 1.0), ("llama_b1", 0.0), ("large_b1_f100", 1.0)])
 def test_chain_b1_list_table_and_copied_list_agree(pkg, name, T):
-    # Batch 1 runs through the list table by default; the copied-list path (a shortlist launch
-    # per position) gives the same step, bit for bit, and both match the oracle.
+    # Batch 1 through the list table, through copied lists (a shortlist launch per position),
+    # and with the table at the first position only: the same step, bit for bit, and each
+    # matches the oracle.
     inp = gu.chain_inputs(name)
+    gamma = inp["cfg"].gamma
     outs = []
-    for table in (True, False):
+    for table in (True, False, [True] + [False] * (gamma - 1)):
         d = make_chain(pkg, inp, T, list_table=table)
-        assert d.table_mode == table
+        assert d.table_pos == (table if isinstance(table, list) else [table] * gamma)
         d.step()
         torch.cuda.synchronize()
         d.check_status()
@@ -322,10 +324,11 @@ def test_chain_step_with_drafter_standin(pkg, serial):
     d.step()
     torch.cuda.synchronize()
     d.check_status()
-    assert ref.table_mode == d.table_mode
-    for a, b in ((ref.out, d.out), (ref.logits, d.logits),
-                 (ref.list_table, d.list_table) if d.table_mode else (ref.vs_ids, d.vs_ids)):
+    assert ref.table_pos == d.table_pos
+    for a, b in ((ref.out, d.out), (ref.logits, d.logits), (ref.vs_offsets, d.vs_offsets), (ref.cpos, d.cpos)):
         assert torch.equal(a, b)
+    for t in range(cfg.gamma):
+        assert np.array_equal(ref.list_ids(t), d.list_ids(t))
     d.enable_head_timing()
     d.enable_overlap_timing()
     d.capture()

@@ -169,47 +169,55 @@ __device__ __forceinline__ void stat_add(Stat &a, float x, float key, int v, int
     }
 }
 
-// a (earlier in the fixed order) merged with b, without branches: a state without elements has
-// m = -inf and v = -1; the scale of each sum is exp(its max - the new max), one of them exactly 1.
-__device__ __forceinline__ Stat stat_merge(const Stat &a, const Stat &b)
+// The states of each group of kWidth lanes (a power of two <= 32) reduced to one, which every
+// lane of the group ends with.  Two passes of exchanges whose steps are all commutative, so both
+// lanes of a pair compute the same value and the result does not depend on timing: the maximum
+// and the best key first, then the sums, each scaled once to the common maximum (one
+// exponential per lane instead of two per merge level).
+template <int kWidth = 32>
+__device__ __forceinline__ Stat stat_reduce_lanes(const Stat &mine)
 {
-    Stat r;
-    r.m = fmaxf(a.m, b.m);
-    const float ea = a.m == -INFINITY ? 0.f : __expf(a.m - r.m);
-    const float eb = b.m == -INFINITY ? 0.f : __expf(b.m - r.m);
-    r.s = fmaf(a.s, ea, b.s * eb);
-    const bool tb = b.v >= 0 && (a.v < 0 || b.key > a.key || (b.key == a.key && b.v < a.v));
-    r.key = tb ? b.key : a.key;
-    r.v = tb ? b.v : a.v;
-    r.j = tb ? b.j : a.j;
+    float m = mine.m, key = mine.key;
+    int v = mine.v, j = mine.j;
+#pragma unroll
+    for (int o = 1; o < kWidth; o <<= 1) {
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+        const float k2 = __shfl_xor_sync(0xFFFFFFFFu, key, o);
+        const int v2 = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        const int j2 = __shfl_xor_sync(0xFFFFFFFFu, j, o);
+        m = fmaxf(m, m2);
+        const bool take = v2 >= 0 && (v < 0 || k2 > key || (k2 == key && v2 < v));
+        key = take ? k2 : key;
+        v = take ? v2 : v;
+        j = take ? j2 : j;
+    }
+    float s = mine.m == -INFINITY ? 0.f : mine.s * __expf(mine.m - m);
+#pragma unroll
+    for (int o = 1; o < kWidth; o <<= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    return Stat{m, s, key, v, j};
+}
+
+// n states (in registers) merged in index order into one: the maximum and the best key, then
+// the sums scaled to the maximum (independent exponentials), added in index order.
+template <int n>
+__device__ __forceinline__ Stat stat_merge_n(const Stat (&q)[n])
+{
+    Stat r = q[0];
+#pragma unroll
+    for (int f = 1; f < n; ++f) {
+        r.m = fmaxf(r.m, q[f].m);
+        const bool take = q[f].v >= 0 && (r.v < 0 || q[f].key > r.key || (q[f].key == r.key && q[f].v < r.v));
+        r.key = take ? q[f].key : r.key;
+        r.v = take ? q[f].v : r.v;
+        r.j = take ? q[f].j : r.j;
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int f = 0; f < n; ++f) s += q[f].m == -INFINITY ? 0.f : q[f].s * __expf(q[f].m - r.m);
+    r.s = s;
     return r;
 }
 
-__device__ __forceinline__ Stat shfl_xor_stat(const Stat &a, int mask)
-{
-    Stat b;
-    b.m = __shfl_xor_sync(0xFFFFFFFFu, a.m, mask);
-    b.s = __shfl_xor_sync(0xFFFFFFFFu, a.s, mask);
-    b.key = __shfl_xor_sync(0xFFFFFFFFu, a.key, mask);
-    b.v = __shfl_xor_sync(0xFFFFFFFFu, a.v, mask);
-    b.j = __shfl_xor_sync(0xFFFFFFFFu, a.j, mask);
-    return b;
-}
-
-// One butterfly level over lanes: both lanes of a pair merge the same two states in lane order
-// (the lower lane's first), so they hold the same result and the whole tree's order is fixed.
-__device__ __forceinline__ Stat stat_butterfly(const Stat &mine, int lane, int o)
-{
-    const Stat other = shfl_xor_stat(mine, o);
-    const bool hi = (lane & o) != 0;
-    Stat lo_s, hi_s;
-    lo_s.m = hi ? other.m : mine.m;   hi_s.m = hi ? mine.m : other.m;
-    lo_s.s = hi ? other.s : mine.s;   hi_s.s = hi ? mine.s : other.s;
-    lo_s.key = hi ? other.key : mine.key; hi_s.key = hi ? mine.key : other.key;
-    lo_s.v = hi ? other.v : mine.v;   hi_s.v = hi ? mine.v : other.v;
-    lo_s.j = hi ? other.j : mine.j;   hi_s.j = hi ? mine.j : other.j;
-    return stat_merge(lo_s, hi_s);
-}
 
 __device__ __forceinline__ float warp_sum(float x)
 {

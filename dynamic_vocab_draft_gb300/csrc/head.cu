@@ -192,40 +192,30 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
         }
         my_v = next_v;
     }
-    // the warp's lanes, then the block's warps, then the blocks: fixed orders throughout
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        st = stat_butterfly(st, lane, o);
-    }
+    // the warp's lanes, then the block's warps, then the blocks (every step's result independent
+    // of timing)
+    st = stat_reduce_lanes(st);
     if (lane == 0) warp_stat[warp] = st;
     __syncthreads();
     if (warp == 0) {
-        // the block's warps: a fixed tree over lanes 0..15
-        Stat c = lane < kGvWarps ? warp_stat[lane] : stat_empty();
-#pragma unroll
-        for (int o = 1; o < kGvWarps; o <<= 1) {
-            c = stat_butterfly(c, lane, o);
-        }
+        const Stat c = stat_reduce_lanes<kGvWarps>(lane < kGvWarps ? warp_stat[lane] : stat_empty());
         if (lane == 0) st_stat(&partials[size_t(b) * kGvMaxBlocks + blockIdx.x], c);
     }
     if (!last_block_done(&counters[b], gridDim.x)) return;
     if (warp != 0) return;
-    // Final combine in a fixed order: lane l folds partials l, l+32, ... (their loads issued
-    // together, kGvFold at a time), then a fixed tree over the lanes.
+    // Final combine: lane l merges partials l, l+32, ... (their loads issued together, kGvFold
+    // at a time), then the lanes.
     const Stat *pb = partials + size_t(b) * kGvMaxBlocks;
     Stat c = stat_empty();
     for (int i0 = lane; i0 < int(gridDim.x); i0 += 32 * kGvFold) {
-        Stat q[kGvFold];
+        Stat q[kGvFold + 1];
+        q[0] = c;
 #pragma unroll
         for (int f = 0; f < kGvFold; ++f)
-            q[f] = i0 + 32 * f < int(gridDim.x) ? ld_stat(pb + i0 + 32 * f) : stat_empty();
-#pragma unroll
-        for (int f = 0; f < kGvFold; ++f) c = stat_merge(c, q[f]);
+            q[f + 1] = i0 + 32 * f < int(gridDim.x) ? ld_stat(pb + i0 + 32 * f) : stat_empty();
+        c = stat_merge_n(q);
     }
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        c = stat_butterfly(c, lane, o);
-    }
+    c = stat_reduce_lanes(c);
     if (lane == 0) write_row(a, b, c);
 }
 
@@ -311,25 +301,26 @@ head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *_
         }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        st = stat_butterfly(st, lane, o);
-    }
+    st = stat_reduce_lanes(st);
     if (lane == 0) ws[warp] = st;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        Stat c = ws[0];
-        for (int w = 1; w < 8; ++w) c = stat_merge(c, ws[w]);
-        st_stat(&partials[size_t(r) * kGvMaxBlocks + blockIdx.x], c);
+    if (warp == 0) {
+        const Stat c = stat_reduce_lanes<8>(lane < 8 ? ws[lane] : stat_empty());
+        if (lane == 0) st_stat(&partials[size_t(r) * kGvMaxBlocks + blockIdx.x], c);
     }
     if (!last_block_done(&counters[r], unsigned(nblk))) return;
     if (warp != 0) return;
+    // lane l merges partials l, l+32, ... (their loads issued together, kGvFold at a time)
+    const Stat *pr = partials + size_t(r) * kGvMaxBlocks;
     Stat c = stat_empty();
-    for (int i = lane; i < nblk; i += 32) c = stat_merge(c, ld_stat(&partials[size_t(r) * kGvMaxBlocks + i]));
+    for (int i0 = lane; i0 < nblk; i0 += 32 * kGvFold) {
+        Stat q[kGvFold + 1];
+        q[0] = c;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        c = stat_butterfly(c, lane, o);
+        for (int f = 0; f < kGvFold; ++f) q[f + 1] = i0 + 32 * f < nblk ? ld_stat(pr + i0 + 32 * f) : stat_empty();
+        c = stat_merge_n(q);
     }
+    c = stat_reduce_lanes(c);
     if (lane == 0) write_row(a, r, c);
 }
 

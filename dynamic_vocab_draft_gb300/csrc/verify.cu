@@ -70,20 +70,27 @@ __device__ __forceinline__ PStat pstat_merge(const PStat &a, const PStat &b)
     return r;
 }
 
-__device__ __forceinline__ PStat shfl_xor_pstat(const PStat &a, int o)
+// The warp's states reduced to one, held by every lane: the maximum and the argmax first, then
+// the sums scaled once to the common maximum; every step is commutative, so the result does not
+// depend on timing (see stat_reduce_lanes).
+__device__ __forceinline__ PStat pstat_reduce_lanes(const PStat &mine)
 {
-    return PStat{__shfl_xor_sync(0xFFFFFFFFu, a.m, o), __shfl_xor_sync(0xFFFFFFFFu, a.s, o),
-                 __shfl_xor_sync(0xFFFFFFFFu, a.amax, o), __shfl_xor_sync(0xFFFFFFFFu, a.aid, o)};
-}
-
-// One butterfly level: both lanes of a pair merge the pair in lane order (see stat_butterfly).
-__device__ __forceinline__ PStat pstat_butterfly(const PStat &mine, int lane, int o)
-{
-    const PStat other = shfl_xor_pstat(mine, o);
-    const bool hi = (lane & o) != 0;
-    const PStat lo_s{hi ? other.m : mine.m, hi ? other.s : mine.s, hi ? other.amax : mine.amax, hi ? other.aid : mine.aid};
-    const PStat hi_s{hi ? mine.m : other.m, hi ? mine.s : other.s, hi ? mine.amax : other.amax, hi ? mine.aid : other.aid};
-    return pstat_merge(lo_s, hi_s);
+    float m = mine.m, amax = mine.amax;
+    int aid = mine.aid;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+        const float a2 = __shfl_xor_sync(0xFFFFFFFFu, amax, o);
+        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, aid, o);
+        m = fmaxf(m, m2);
+        const bool take = i2 >= 0 && (aid < 0 || a2 > amax || (a2 == amax && i2 < aid));
+        amax = take ? a2 : amax;
+        aid = take ? i2 : aid;
+    }
+    float s = mine.m == -INFINITY ? 0.f : mine.s * __expf(mine.m - m);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    return PStat{m, s, amax, aid};
 }
 
 __device__ float block_sum(float x, float *scratch)
@@ -246,10 +253,7 @@ __device__ void fold_decide(const ChainArgs &a, int b)
                 acc = pstat_merge(acc, PStat{q.m, q.s, -INFINITY, -1});
             }
         }
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            acc = pstat_butterfly(acc, lane, o);
-        }
+        acc = pstat_reduce_lanes(acc);
         if (lane == 0) {
             if (r < g1) { rows[r] = acc; a.prow[size_t(b) * g1 + r] = QStat{acc.m, acc.s}; }
             else { qrows[r - g1] = QStat{acc.m, acc.s}; a.qrow[size_t(b) * a.gamma + (r - g1)] = QStat{acc.m, acc.s}; }
@@ -628,7 +632,8 @@ __device__ __forceinline__ RowStat shfl_xor_rowstat(const RowStat &a, int o)
                    __shfl_xor_sync(0xFFFFFFFFu, a.aid, o)};
 }
 
-// One butterfly level: both lanes of a pair merge the pair in lane order (see stat_butterfly).
+// One butterfly level: both lanes of a pair merge the pair in lane order (the lower lane's
+// first), so they hold the same result and the whole tree's order is fixed.
 __device__ __forceinline__ RowStat rowstat_butterfly(const RowStat &mine, int lane, int o)
 {
     const RowStat other = shfl_xor_rowstat(mine, o);

@@ -2,6 +2,7 @@
 // the Philox4x32-10 generator, warp reductions and the softmax/argmax partial-state
 // algebra every head and verify reduction uses.
 #pragma once
+#include <utility>
 
 #include <atomic>
 #include <cstdint>
@@ -282,6 +283,32 @@ __device__ __forceinline__ void mbar_fence_init()
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
+}
+
+// Programmatic dependent launch.  A kernel launched with the programmatic-serialization
+// attribute (launch_pdl) may begin while the kernel before it in the stream still runs, once
+// every block of that kernel has called pdl_allow (or exited); its blocks then call pdl_wait,
+// which returns when the earlier kernel has completed and its writes are visible (at once for
+// a kernel launched without the attribute).  Only launch latency is hidden: nothing is read
+// before pdl_wait.
+__device__ __forceinline__ void pdl_allow() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity)

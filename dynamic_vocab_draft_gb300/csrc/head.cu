@@ -83,6 +83,7 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
 {
     extern __shared__ uint4 hs[];                 // h as bf16, d / 8 vectors; then the list table
     __shared__ Stat warp_stat[kGvWarps];
+    pdl_allow();                                  // a verification launched next may get ready
     const int b = blockIdx.y;
     const int d = a.d;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -268,36 +269,42 @@ struct UnionEp {
 };
 
 // Softmax statistics and the draft draw of every head row from its stored logits.
-// grid (chunks, R): block (x, r) folds elements [x*kRsChunk, ...) of row r; the last block of the
-// row combines the partials in a fixed order.  The grid is sized for the longest possible list
-// (V); blocks past the end of their row's list leave at once and take no part in the fold
-// (block 0 stays for an empty list).
-constexpr int kRsPer = 16;
+// grid (X, R): block (x, r) folds chunks x, x + X, ... of kRsChunk elements of row r; the last
+// block of the row combines the partials in a fixed order.  X is chosen on the host so that the
+// grid fills the GPU about once (kRsBlocksPerSm blocks per SM) whatever the number of rows;
+// blocks past the end of their row's list leave at once and take no part in the fold (block 0
+// stays for an empty list).
+constexpr int kRsPer = 4;
 constexpr int kRsChunk = 256 * kRsPer;
+constexpr int kRsBlocksPerSm = 8;
 
 __global__ void __launch_bounds__(256)
 head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *__restrict__ counters)
 {
     __shared__ Stat ws[8];
+    pdl_allow();                                  // a verification launched next may get ready
     const int r = blockIdx.y, b = r / G, gi = r - b * G;
     const int off = a.vs_offsets[b];
     const int n = a.vs_offsets[b + 1] - off;
-    const int nblk = n > 0 ? min((n + kRsChunk - 1) / kRsChunk, int(gridDim.x)) : 1;
+    const int nch = n > 0 ? (n + kRsChunk - 1) / kRsChunk : 1;
+    const int nblk = min(nch, int(gridDim.x));
     if (int(blockIdx.x) >= nblk) return;                   // uniform over the block
     const float *l = a.logits + int64_t(off) * G + int64_t(gi) * n;
     const int32_t *ids = a.vs_ids + off;
     Stat st = stat_empty();
-    const int j0 = blockIdx.x * kRsChunk + threadIdx.x * kRsPer;
-    // unrolled by four so the independent noise computations of neighbouring elements overlap
-#pragma unroll 4
-    for (int e = 0; e < kRsPer; ++e) {
-        const int j = j0 + e;
-        if (j < n) {
-            const float lj = l[j];
-            const int v = ids[j];
-            const float x = lj * a.inv_te;
-            const float key = a.T > 0.f ? x + gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(r)) : lj;
-            stat_add(st, x, key, v, j);
+    for (int ch = blockIdx.x; ch < nch; ch += gridDim.x) {
+        const int j0 = ch * kRsChunk + threadIdx.x * kRsPer;
+        // the independent noise computations of a thread's elements overlap
+#pragma unroll
+        for (int e = 0; e < kRsPer; ++e) {
+            const int j = j0 + e;
+            if (j < n) {
+                const float lj = l[j];
+                const int v = ids[j];
+                const float x = lj * a.inv_te;
+                const float key = a.T > 0.f ? x + gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(r)) : lj;
+                stat_add(st, x, key, v, j);
+            }
         }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -443,8 +450,12 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
     const tc::Operands op{W, H, d, int(rows), dev_status, wait_budget()};
     const ds_status st = tc::launch_for(op, ep, parts, tile_cnt, tc_grid, stream);
     if (st != DS_OK) return st;
+    // about kRsBlocksPerSm blocks per SM in all, spread over the rows (at most one per chunk of
+    // the longest possible list)
     const int chunks = (V + kRsChunk - 1) / kRsChunk;
-    head_rowstats_kernel<<<dim3(chunks, unsigned(rows)), 256, 0, stream>>>(a, G, partials, counters);
+    int gx = int((long long)sms * kRsBlocksPerSm / rows);
+    gx = gx < 1 ? 1 : gx > chunks ? chunks : gx;
+    head_rowstats_kernel<<<dim3(gx, unsigned(rows)), 256, 0, stream>>>(a, G, partials, counters);
     DS_TRY_LAUNCH();
     return DS_OK;
 }

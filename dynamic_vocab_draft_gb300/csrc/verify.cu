@@ -303,6 +303,8 @@ __global__ void __launch_bounds__(kVThreads)
 verify_stats_kernel(ChainArgs a)
 {
     __shared__ PStat scratch[kVThreads / 32];
+    pdl_wait();
+    pdl_allow();
     const int g1 = a.gamma + 1;
     const int b = blockIdx.y / g1, t = blockIdx.y % g1;
     stats_unit<kVPer>(a, b, t, blockIdx.x, scratch);
@@ -529,6 +531,7 @@ __global__ void __launch_bounds__(kVThreads)
 verify_residual_kernel(ChainArgs a)
 {
     extern __shared__ int s_cp[];                    // M entries when staged
+    pdl_wait();
     const int b = blockIdx.y;
     const int tr = __ldcg(&a.decision[b]);
     if (tr < 0) return;                              // greedy: decided already (whole group returns)
@@ -1056,14 +1059,17 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.psum = reinterpret_cast<float *>(w);
 
-    if (vbig) verify_stats_kernel<kVPerBig><<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
-    else verify_stats_kernel<kVPerSmall><<<dim3(a.nch, B * (gamma + 1)), kVThreads, 0, stream>>>(a);
-    DS_TRY_LAUNCH();
+    // both launches may start before the kernel ahead of them ends (their blocks wait for it)
+    const dim3 sgrid(a.nch, B * (gamma + 1));
+    cudaError_t e = vbig ? launch_pdl(verify_stats_kernel<kVPerBig>, sgrid, dim3(kVThreads), 0, stream, a)
+                         : launch_pdl(verify_stats_kernel<kVPerSmall>, sgrid, dim3(kVThreads), 0, stream, a);
+    if (e != cudaSuccess) { (void)cudaGetLastError(); return DS_ERR_CUDA; }
     // the small-chunk grid (few sequences) stages the list's cluster positions in shared memory
     const size_t cp_smem = size_t(M) * sizeof(int);   // M <= 8192
-    if (rbig) verify_residual_kernel<kRPerBig, false><<<dim3(a.nrch, B), kVThreads, 0, stream>>>(a);
-    else verify_residual_kernel<kRPerSmall, true><<<dim3(a.nrch, B), kVThreads, cp_smem, stream>>>(a);
-    DS_TRY_LAUNCH();
+    const dim3 rgrid(a.nrch, B);
+    e = rbig ? launch_pdl(verify_residual_kernel<kRPerBig, false>, rgrid, dim3(kVThreads), 0, stream, a)
+             : launch_pdl(verify_residual_kernel<kRPerSmall, true>, rgrid, dim3(kVThreads), cp_smem, stream, a);
+    if (e != cudaSuccess) { (void)cudaGetLastError(); return DS_ERR_CUDA; }
     return DS_OK;
 }
 

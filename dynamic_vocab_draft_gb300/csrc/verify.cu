@@ -107,13 +107,14 @@ __device__ float block_sum(float x, float *scratch)
 }
 
 // Statistics of one chunk of a row of length n: max and sum-exp of x = value * inv_te, and the
-// argmax of the raw values (ties to the lower index).  Two plain block reductions (the max,
-// then the sum of exp(x - max)); the result is valid in thread 0.
+// argmax of the raw values (ties to the lower index).  Each thread reduces its own values (its
+// maximum, then its sum of exp(x - that maximum)), then one reduction over the block (the lanes
+// in two commutative passes, then the warps); the result is valid in warp 0.
 template <int kVPer>
 __device__ PStat chunk_stats(const float *__restrict__ row, int lo, int n, float inv_te, PStat *scratch)
 {
-    // thread t holds the 4-element groups lo + 1024 k + 4 t, k = 0..7: every round of loads is
-    // one contiguous 4 KB of the row, and all eight rounds are in flight together
+    // thread t holds the 4-element groups lo + 1024 k + 4 t: every round of loads is one
+    // contiguous 4 KB of the row, and all rounds are in flight together
     float vals[kVPer];
     constexpr int kStride = kVThreads * 4;
 #pragma unroll
@@ -134,36 +135,20 @@ __device__ PStat chunk_stats(const float *__restrict__ row, int lo, int n, float
         const int idx = lo + (i >> 2) * kStride + threadIdx.x * 4 + (i & 3);
         if (vals[i] > amax) { amax = vals[i]; aid = idx; }
     }
-    // block max / argmax of the raw values (x = value * inv_te is monotone in the value)
+    // x = value * inv_te is monotone in the value: the thread's maximum of x is amax * inv_te
+    const float tm = aid >= 0 ? amax * inv_te : -INFINITY;
+    float ts = 0.f;
+    if (aid >= 0) {
+#pragma unroll
+        for (int i = 0; i < kVPer; ++i) ts += __expf(vals[i] * inv_te - tm);
+    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xFFFFFFFFu, amax, o);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, aid, o);
-        if (oi >= 0 && (aid < 0 || ov > amax || (ov == amax && oi < aid))) { amax = ov; aid = oi; }
-    }
-    if (lane == 0) { scratch[warp].amax = amax; scratch[warp].aid = aid; }
+    const PStat w = pstat_reduce_lanes(PStat{tm, ts, amax, aid});
+    if (lane == 0) scratch[warp] = w;
     __syncthreads();
-    float bmax = -INFINITY;
-    int bid = -1;
-    for (int w = 0; w < nw; ++w) {
-        const float ov = scratch[w].amax;
-        const int oi = scratch[w].aid;
-        if (oi >= 0 && (bid < 0 || ov > bmax || (ov == bmax && oi < bid))) { bmax = ov; bid = oi; }
-    }
-    const float m = bid >= 0 ? bmax * inv_te : -INFINITY;
-    float sl = 0.f;
-    if (bid >= 0) {
-#pragma unroll
-        for (int i = 0; i < kVPer; ++i) sl += __expf(vals[i] * inv_te - m);
-    }
-    sl = warp_sum(sl);
-    __syncthreads();                                   // everyone has read scratch
-    if (lane == 0) scratch[warp].s = sl;
-    __syncthreads();
-    PStat r{m, 0.f, bmax, bid};
-    if (threadIdx.x == 0) for (int w = 0; w < nw; ++w) r.s += scratch[w].s;
-    __syncthreads();
+    PStat r{-INFINITY, 0.f, -INFINITY, -1};
+    if (warp == 0) r = pstat_reduce_lanes(lane < nw ? scratch[lane] : r);
+    __syncthreads();                                   // the caller may reuse scratch
     return r;
 }
 
@@ -299,7 +284,7 @@ __device__ void fold_decide(const ChainArgs &a, int b)
 }
 
 template <int kVPer>
-__global__ void __launch_bounds__(kVThreads)
+__global__ void __launch_bounds__(kVThreads, 4)
 verify_stats_kernel(ChainArgs a)
 {
     __shared__ PStat scratch[kVThreads / 32];

@@ -30,14 +30,14 @@ SIGNATURES = {
     "ds_router_workspace_bytes_h": (SZ, [P, I]),
     "ds_router_topk_h": (ST, [P, P, I, I, P, P, P, SZ, P, P]),
     "ds_router_topk_list_b1": (ST, [P, P, I, P, I, P, P, P, P, P, I64, P, SZ, P, P]),
-    "ds_gathered_head_b1_table": (ST, [P, P, I, I, P, I, P, F, U64, I, P, P, P, P, P, P, SZ, P, P]),
+    "ds_gathered_head_b1_table": (ST, [P, P, I, I, P, I, P, F, U64, I, P, P, P, P, P, I, P, SZ, P, P]),
     "ds_shortlist_workspace_bytes": (SZ, [I, I]),
     "ds_build_shortlist": (ST, [P, P, I, I, P, I, I, P, P, I64, P, P, P, P, P, SZ, P, P]),
     "ds_head_workspace_bytes": (SZ, [I]),
     "ds_gathered_head": (ST, [P, I, I, P, I, I, P, P, P, I, P, P, P, P, F, U64, I,
-                              P, P, P, P, P, P, SZ, P, P]),
+                              P, P, P, P, P, I, P, SZ, P, P]),
     "ds_gathered_head_noalloc": (ST, [P, I, I, P, I, I, P, P, P, I, P, P, P, P, F, U64, I,
-                                      P, P, P, P, P, P, P]),
+                                      P, P, P, P, P, I, P, P]),
     "ds_prefetch_rows": (ST, [P, I, I, P, P, I, I, P]),
     "ds_verify_workspace_bytes": (SZ, [I, I, I]),
     "ds_verify": (ST, [P, I, I, I, F, P, I64, P, P, P, P, I, P, P, P, P, P, P, P, SZ, P, P]),

@@ -169,8 +169,9 @@ def build_shortlist(csr_off, csr_tok, cluster_ids, vs_offsets, vs_ids, cpos, ws,
 
 def gathered_head(H, G, W, vs_offsets, vs_ids, T, seed, pos, logits, token, token_idx, ws, status,
                   cpos=None, rank_in_cluster=None, union=None, row_max=None, row_sumexp=None,
-                  stream=None):
-    """H [B*G, d]; union = (union_ids, union_cluster, union_count) or None (per-row path)."""
+                  stream=None, free_sms=-1):
+    """H [B*G, d]; union = (union_ids, union_cluster, union_count) or None (per-row path);
+    free_sms: SMs left free for other streams (-1: the library's default, 0: none)."""
     R, d = H.shape
     B = vs_offsets.numel() - 1
     if R != B * G:
@@ -187,7 +188,7 @@ def gathered_head(H, G, W, vs_offsets, vs_ids, T, seed, pos, logits, token, toke
         float(T), int(seed) & 0xFFFFFFFFFFFFFFFF, int(pos),
         _ptr(logits, F32, "logits"), _ptr(row_max, F32, "row_max", True),
         _ptr(row_sumexp, F32, "row_sumexp", True),
-        _ptr(token, I32, "token"), _ptr(token_idx, I32, "token_idx"),
+        _ptr(token, I32, "token"), _ptr(token_idx, I32, "token_idx"), int(free_sms),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
         _stream(stream)), "ds_gathered_head")
 
@@ -201,14 +202,14 @@ def prefetch_rows(W, vs_ids, offsets, first_rows, blocks=0, stream=None):
 
 
 def gathered_head_b1_table(H, W, list_table, k, csr_tok, T, seed, pos, logits, token, token_idx, ws, status,
-                           row_max=None, row_sumexp=None, stream=None):
+                           row_max=None, row_sumexp=None, stream=None, free_sms=-1):
     """ds_gathered_head_b1_table: the batch-1 head over the list a table describes (H [d] or [1, d])."""
     V, d = W.shape
     _lib.check(_lib.load().ds_gathered_head_b1_table(
         _ptr(H, BF16, "H"), _ptr(W, BF16, "W"), V, d, _ptr(list_table, I32, "list_table"), int(k),
         _ptr(csr_tok, I32, "csr_tok"), float(T), int(seed) & 0xFFFFFFFFFFFFFFFF, int(pos),
         _ptr(logits, F32, "logits"), _ptr(row_max, F32, "row_max", True), _ptr(row_sumexp, F32, "row_sumexp", True),
-        _ptr(token, I32, "token"), _ptr(token_idx, I32, "token_idx"),
+        _ptr(token, I32, "token"), _ptr(token_idx, I32, "token_idx"), int(free_sms),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
         _stream(stream)), "ds_gathered_head_b1_table")
 

@@ -36,6 +36,14 @@ constexpr int kHeadSideSmsB1 = 16;
 constexpr int kGvMaxD = 16384;
 constexpr int kGvMaxBlocks = 1024;     // per list; bounds the partials in the workspace
 
+// SMs a head launch uses: all but `free_sms` (the caller's choice) or, for free_sms < 0, all but
+// the path's default reserve.  At least one.
+int head_sms(int sms, int free_sms, int default_free)
+{
+    const int f = free_sms < 0 ? default_free : free_sms;
+    return sms - f < 1 ? 1 : sms - f;
+}
+
 struct HeadArgs {
     const uint16_t *H;
     const uint16_t *W;
@@ -384,7 +392,7 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
                                       const int32_t *union_count,
                                       float T, uint64_t seed, int pos,
                                       float *logits, float *row_max, float *row_sumexp,
-                                      int32_t *token, int32_t *token_idx,
+                                      int32_t *token, int32_t *token_idx, int free_sms,
                                       void *ws, size_t ws_bytes, int32_t *dev_status,
                                       cudaStream_t stream)
 {
@@ -420,7 +428,8 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
         if (sms <= 0) return DS_ERR_CUDA;
         // One 512-thread block per SM.  At batch 1 a few SMs are left to the side stream, so the
         // next position's router and shortlist build run while this head streams W.
-        int gx = B == 1 ? sms - kHeadSideSmsB1 : (sms + B - 1) / B;
+        const int use = head_sms(sms, free_sms, B == 1 ? kHeadSideSmsB1 : 0);
+        int gx = B == 1 ? use : (use + B - 1) / B;
         if (gx < 1) gx = 1;
         if (gx > kGvMaxBlocks) gx = kGvMaxBlocks;
         const size_t smem = size_t(d) * sizeof(uint16_t);
@@ -444,7 +453,7 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
     ep.logits = logits; ep.V = V; ep.M = M; ep.G = G; ep.status = dev_status;
     // A tensor-core head CTA fills its SM (shared memory and registers); kHeadSideSms SMs are
     // left free so the next position's router and shortlist build run beside it.
-    int tc_grid = sms - kHeadSideSms;
+    int tc_grid = head_sms(sms, free_sms, kHeadSideSms);
     if (tc_grid > tc::kMaxGrid) tc_grid = tc::kMaxGrid;
     if (tc_grid < 1) tc_grid = 1;
     const tc::Operands op{W, H, d, int(rows), dev_status, wait_budget()};
@@ -550,7 +559,7 @@ extern "C" ds_status ds_gathered_head_noalloc(const uint16_t *H, int B, int G,
                                               const int32_t *union_count,
                                               float T, uint64_t seed, int pos,
                                               float *logits, float *row_max, float *row_sumexp,
-                                              int32_t *token, int32_t *token_idx,
+                                              int32_t *token, int32_t *token_idx, int free_sms,
                                               int32_t *dev_status, cudaStream_t stream)
 {
     if (B < 1 || G < 1) return DS_ERR_INVALID_ARG;
@@ -562,7 +571,7 @@ extern "C" ds_status ds_gathered_head_noalloc(const uint16_t *H, int B, int G,
     if (cudaMemsetAsync(scratch, 0, kNoAllocCounters, stream) != cudaSuccess) return DS_ERR_CUDA;
     return ds_gathered_head(H, B, G, W, V, d, vs_offsets, vs_ids, cpos, M, rank_in_cluster,
                             union_ids, union_cluster, union_count, T, seed, pos,
-                            logits, row_max, row_sumexp, token, token_idx,
+                            logits, row_max, row_sumexp, token, token_idx, free_sms,
                             scratch, kNoAllocBytes, dev_status, stream);
 }
 
@@ -612,7 +621,7 @@ extern "C" ds_status ds_gathered_head_b1_table(const uint16_t *H, const uint16_t
                                                const int32_t *list_table, int k, const int32_t *csr_tok,
                                                float T, uint64_t seed, int pos,
                                                float *logits, float *row_max, float *row_sumexp,
-                                               int32_t *token, int32_t *token_idx,
+                                               int32_t *token, int32_t *token_idx, int free_sms,
                                                void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream)
 {
     ds::NvtxRange range("ds_gathered_head_b1_table");
@@ -634,8 +643,7 @@ extern "C" ds_status ds_gathered_head_b1_table(const uint16_t *H, const uint16_t
     a.logits = logits; a.row_max = row_max; a.row_sumexp = row_sumexp;
     a.token = token; a.token_idx = token_idx;
     a.status = dev_status;
-    int gx = sms - kHeadSideSmsB1;
-    if (gx < 1) gx = 1;
+    int gx = head_sms(sms, free_sms, kHeadSideSmsB1);
     if (gx > kGvMaxBlocks) gx = kGvMaxBlocks;
     if (!head_smem_limit()) return DS_ERR_CUDA;
     const size_t smem = size_t(d) * sizeof(uint16_t) + size_t(k + 1) * sizeof(int2);

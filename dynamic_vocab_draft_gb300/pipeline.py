@@ -298,18 +298,20 @@ class ChainDrafter(_Common):
             api.prefetch_rows(self.W, self.vs_ids[t], self.vs_offsets[t], self.prefetch_rows, stream=stream)
 
     def head(self, t, stream=None):
+        # the last position's head has the GPU to itself (no router runs beside it)
+        free = 0 if t == self.gamma - 1 else -1
         if self.table_pos[t]:
             api.gathered_head_b1_table(self.H[t + 1], self.W, self.list_table[t], int(self.budget[t]), self.csr_tok,
                                        self.T, self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],
                                        self.ws_head, self.status, row_max=self.row_max[t],
-                                       row_sumexp=self.row_sumexp[t], stream=stream)
+                                       row_sumexp=self.row_sumexp[t], stream=stream, free_sms=free)
             return
         api.gathered_head(self.H[t + 1], 1, self.W, self.vs_offsets[t], self.vs_ids[t], self.T,
                           self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],
                           self.ws_head, self.status, cpos=self.cpos[t], rank_in_cluster=self.rank,
                           union=(self.union_ids[t], self.union_cluster[t], self.union_count[t])
                           if self.union else None,
-                          row_max=self.row_max[t], row_sumexp=self.row_sumexp[t], stream=stream)
+                          row_max=self.row_max[t], row_sumexp=self.row_sumexp[t], stream=stream, free_sms=free)
 
     def verify(self, stream=None):
         api.verify(self.z, self.T, self.logits, self.vs_offsets, self.cpos, self.cluster_of, self.rank,
@@ -462,11 +464,13 @@ class TreeDrafter(_Common):
                             self.union_ids[t], self.union_cluster[t], self.union_count[t], stream)
 
     def head(self, t, stream=None):
+        # the last depth's head has the GPU to itself (no router runs beside it)
         api.gathered_head(self.Hn[t], self.Wd, self.W, self.vs_offsets[t], self.vs_ids[t], self.T,
                           self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],
                           self.ws_head, self.status, cpos=self.cpos[t], rank_in_cluster=self.rank,
                           union=(self.union_ids[t], self.union_cluster[t], self.union_count[t]),
-                          row_max=self.row_max[t], row_sumexp=self.row_sumexp[t], stream=stream)
+                          row_max=self.row_max[t], row_sumexp=self.row_sumexp[t], stream=stream,
+                          free_sms=0 if t == self.D - 1 else -1)
 
     def verify(self, stream=None):
         api.verify_tree(self.z, self.D, self.Wd, self.T, self.parent, self.logits, self.vs_offsets,
@@ -554,11 +558,12 @@ class StaticChainDrafter(_Common):
         self.check_status()
 
     def head(self, t, stream=None):
+        # nothing runs beside the static list's heads: every SM
         api.gathered_head(self.H[t + 1], 1, self.W, self.vs_offsets[t], self.vs_ids, self.T,
                           self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],
                           self.ws_head, self.status, cpos=self.cpos[t], rank_in_cluster=self.rank,
                           union=(self.union_ids, self.union_cluster, self.union_count) if self.union else None,
-                          row_max=self.row_max[t], row_sumexp=self.row_sumexp[t], stream=stream)
+                          row_max=self.row_max[t], row_sumexp=self.row_sumexp[t], stream=stream, free_sms=0)
 
     def verify(self, stream=None):
         api.verify(self.z, self.T, self.logits, self.vs_offsets, self.cpos, self.cluster_of, self.rank,

@@ -148,7 +148,7 @@ ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, int pos,
  *   ds_gathered_head_b1_table  ds_gathered_head at B = G = 1 on that list: entry j's token is
  *       csr_tok[CSR start + (j - list start)] of the last selected cluster whose list start is
  *       <= j.  k: the number of selected clusters (the table's pairs before the end pair).
- *       Outputs and limits as ds_gathered_head's per-row path (k <= 8192);
+ *       Outputs, free_sms and limits as ds_gathered_head's per-row path (k <= 8192);
  *       ws: ds_head_workspace_bytes(1) bytes.
  * ------------------------------------------------------------------------------------- */
 ds_status ds_router_topk_list_b1(ds_router_t router, const uint16_t *H, int pos,
@@ -160,7 +160,7 @@ ds_status ds_gathered_head_b1_table(const uint16_t *H, const uint16_t *W, int V,
                                     const int32_t *list_table, int k, const int32_t *csr_tok,
                                     float T, uint64_t seed, int pos,
                                     float *logits, float *row_max, float *row_sumexp,
-                                    int32_t *token, int32_t *token_idx,
+                                    int32_t *token, int32_t *token_idx, int free_sms,
                                     void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
@@ -215,6 +215,10 @@ ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *csr_tok, int
  *                          Philox4x32-10 (key = seed, counter = (v >> 2, pos, r, 0), word v & 3,
  *                          u = (2 (w >> 9) + 1) 2^-24).  Ties go to the lower token id.  An
  *                          empty list gives token = token_idx = -1.
+ *   free_sms               SMs the launch leaves free for work on other streams (the next
+ *                          position's router beside the head): -1 = the default (16 on the
+ *                          batch-1 per-row path, 8 on the union path, 0 otherwise); 0 = every SM
+ *                          (nothing runs beside it); at least one SM is always used.
  * Limits: d % 8 == 0, d <= 16384; union path: B*G <= 128 and V <= 2^20; per-row path: G == 1
  *   and B*G <= 65535.  Larger calls return DS_ERR_UNSUPPORTED and launch nothing.
  * ws: ds_head_workspace_bytes(B*G) bytes; holds completion counters (zero it once).
@@ -228,7 +232,7 @@ ds_status ds_gathered_head(const uint16_t *H, int B, int G,
                            const int32_t *union_count,
                            float T, uint64_t seed, int pos,
                            float *logits, float *row_max, float *row_sumexp,
-                           int32_t *token, int32_t *token_idx,
+                           int32_t *token, int32_t *token_idx, int free_sms,
                            void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
@@ -257,7 +261,7 @@ ds_status ds_gathered_head_noalloc(const uint16_t *H, int B, int G,
                                    const int32_t *union_count,
                                    float T, uint64_t seed, int pos,
                                    float *logits, float *row_max, float *row_sumexp,
-                                   int32_t *token, int32_t *token_idx,
+                                   int32_t *token, int32_t *token_idx, int free_sms,
                                    int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------

@@ -38,7 +38,7 @@ def test_status_strings(lib):
     for code in (0, 1, 2, 3, 4, 0x10, 0x20, 0x40, 0x30, 12345):
         s = lib.ds_status_string(code)
         assert isinstance(s, bytes) and s
-    assert lib.ds_version() == 2
+    assert lib.ds_version() == 3
 
 
 def test_workspace_queries(lib):
@@ -78,7 +78,7 @@ def test_host_argument_checks(lib):
                                   None, None, None, FAKE, 1 << 20, None, None) == 1
     # head: negative temperature; d % 8; union path needs cpos; per-row path needs G == 1
     args = [FAKE, 1, 1, FAKE, 4096, 256, FAKE, FAKE, None, 0, None, None, None, None,
-            1.0, 0, 1, FAKE, None, None, FAKE, FAKE, FAKE, 1 << 24, None, None]
+            1.0, 0, 1, FAKE, None, None, FAKE, FAKE, -1, FAKE, 1 << 24, None, None]
     a = list(args); a[14] = -1.0
     assert lib.ds_gathered_head(*a) == 1
     a = list(args); a[5] = 250
@@ -87,11 +87,11 @@ def test_host_argument_checks(lib):
     assert lib.ds_gathered_head(*a) == 1
     a = list(args); a[2] = 4
     assert lib.ds_gathered_head(*a) == 2
-    a = list(args); a[23] = 16
+    a = list(args); a[24] = 16
     assert lib.ds_gathered_head(*a) == 4
     # union path: more than 128 head rows, or a vocabulary above 2^20, is unsupported
     union = list(args); union[8] = FAKE; union[9] = 32; union[10] = FAKE
-    union[11] = FAKE; union[12] = FAKE; union[13] = FAKE; union[23] = 1 << 30
+    union[11] = FAKE; union[12] = FAKE; union[13] = FAKE; union[24] = 1 << 30
     a = list(union); a[1] = 8; a[2] = 17
     assert lib.ds_gathered_head(*a) == 2
     a = list(union); a[4] = (1 << 20) + 1

@@ -72,7 +72,7 @@ def _call_noalloc(pkg, H, B, G, W, cfg, vs_off, vs_ids, cpos, rk, un, T, seed, p
     return lib.ds_gathered_head_noalloc(
         P(H), B, G, P(W), cfg.V, cfg.d, P(vs_off), P(vs_ids), P(cpos), cfg.M, P(rk),
         P(u[0]), P(u[1]), P(u[2]), float(T), seed, pos,
-        P(out["logits"]), P(out["rmax"]), P(out["rsum"]), P(out["tok"]), P(out["tix"]),
+        P(out["logits"]), P(out["rmax"]), P(out["rsum"]), P(out["tok"]), P(out["tix"]), -1,
         P(st), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 

@@ -225,25 +225,34 @@ def head_source_hash():
     return h.hexdigest()[:16]
 
 
-def committed_traffic():
-    """DRAM bytes per head launch from the committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
+def committed_head_profile():
+    """The committed ncu summary's per-launch figures for the batch-1 head (DRAM bytes, mean
+    duration in µs), if it was taken on the current kernel source (else {})."""
     path = os.path.join(ROOT, "profiles", "head_gemv_llama_b1.md")
     try:
         text = open(path).read()
     except OSError:
-        return None
+        return {}
     vals = {}
     for line in text.splitlines():
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
             vals[k.strip()] = v.strip().strip("`")
     if vals.get("source_sha") != head_source_hash():
-        return None
-    try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+        return {}
+    out = {}
+    for key, name in (("traffic", "dram_bytes_per_launch"), ("launch_us", "ncu_launch_us_mean")):
+        try:
+            out[key] = float(vals[name])
+        except (KeyError, ValueError):
+            pass
+    return out
+
+
+def committed_traffic():
+    """DRAM bytes per head launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    return committed_head_profile().get("traffic")
 
 
 _HEAD_CACHE = {}
@@ -433,6 +442,13 @@ def measure(cfg, seed, dev, pkg, torch, world, local_rank, steps, warmup, e2e_st
             "algorithmic_bytes_per_launch": float(np.mean(head_bytes)),
             "avg_launch_us": float(hm.mean() * 1e3), "peak_source": peak_src,
             "shortlist_sizes": sizes.sum(axis=1).tolist(), "union_rows": union}
+    if per_row and cfg.name == "llama_b1":
+        # the same launches' mean duration in the committed ncu launch list (cold, serialised;
+        # without the latency of the events that bracket each head inside the graph)
+        prof = committed_head_profile()
+        if "launch_us" in prof:
+            roof["ncu_avg_launch_us"] = prof["launch_us"]
+            roof["ncu_frac"] = float(np.mean(head_bytes)) / (prof["launch_us"] * 1e-6) / 1e9 / peak
     step_us = total_ms / K * 1e3
     res = dict(
         cfg=cfg, inp=inp, value=value, total_ms=total_ms, K=K, tokens_per_step=tokens_per_step, roofline=roof,

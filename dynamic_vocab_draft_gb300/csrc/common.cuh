@@ -311,6 +311,12 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Fetch the 128-byte line holding p into L2 (a hint: nothing waits for it).
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
+}
+
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity)
 {
     uint32_t done;

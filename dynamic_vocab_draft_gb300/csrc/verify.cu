@@ -222,6 +222,26 @@ __device__ void fold_decide(const ChainArgs &a, int b)
     // warp w folds rows w, w+8, ...
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nrows = g1 + (a.T > 0.f && !a.q_max ? a.gamma : 0);
+    // The accept tests' inputs (each draft token, its place in its list, its draft logit, its
+    // target logit, the uniform) need none of the row statistics: the last warp, which has the
+    // fewest rows to fold, requests them first, so their chain of dependent loads runs while the
+    // other warps fold.
+    constexpr int kTestWarp = kVThreads / 32 - 1;
+    const bool tester = warp == kTestWarp && lane < a.gamma;
+    int x = -1, j = -1;
+    float l = 0.f, z = 0.f, uu = 0.f;
+    if (tester) {
+        x = a.draft_ids[size_t(lane) * a.B + b];
+        if (a.T > 0.f) {
+            j = list_index(a, lane, b, x);
+            if (j >= 0) {
+                const int *off = a.vs_offsets + size_t(lane) * (a.B + 1);
+                l = a.q_logits[size_t(lane) * a.q_stride + off[b] + j];
+                z = a.p_logits[(size_t(b) * g1 + lane) * a.V + x];
+            }
+            uu = a.u[size_t(b) * g1 + lane];
+        }
+    }
     if (a.T > 0.f && a.q_max && threadIdx.x < a.gamma) {
         const int tt = threadIdx.x;
         const QStat q{a.q_max[size_t(tt) * a.B + b], a.q_sumexp[size_t(tt) * a.B + b]};
@@ -246,25 +266,18 @@ __device__ void fold_decide(const ChainArgs &a, int b)
     }
     __syncthreads();
     // All gamma accept tests at once; the first rejection decides.
-    if (threadIdx.x < a.gamma) {
-        const int tt = threadIdx.x;
-        const int x = a.draft_ids[size_t(tt) * a.B + b];
+    if (tester) {
+        const int tt = lane;
         int reject;
         if (a.T == 0.f) {
             reject = (x != rows[tt].aid);
+        } else if (j < 0) {
+            set_status(a.status, DS_DEV_BAD_INDEX);
+            reject = 1;
         } else {
-            const int j = list_index(a, tt, b, x);
-            if (j < 0) {
-                set_status(a.status, DS_DEV_BAD_INDEX);
-                reject = 1;
-            } else {
-                const int *off = a.vs_offsets + size_t(tt) * (a.B + 1);
-                const float l = a.q_logits[size_t(tt) * a.q_stride + off[b] + j];
-                const float q = __expf(l * a.inv_te - qrows[tt].m) / qrows[tt].s;
-                const float z = a.p_logits[(size_t(b) * g1 + tt) * a.V + x];
-                const float p = __expf(z * a.inv_te - rows[tt].m) / rows[tt].s;
-                reject = !(a.u[size_t(b) * g1 + tt] * q < p);
-            }
+            const float q = __expf(l * a.inv_te - qrows[tt].m) / qrows[tt].s;
+            const float p = __expf(z * a.inv_te - rows[tt].m) / rows[tt].s;
+            reject = !(uu * q < p);
         }
         rej[tt] = reject;
     }
@@ -516,6 +529,15 @@ __global__ void __launch_bounds__(kVThreads)
 verify_residual_kernel(ChainArgs a)
 {
     extern __shared__ int s_cp[];                    // M entries when staged
+    {
+        // the chunk's cluster ids and ranks are fixed inputs: fetch them into L2 while the
+        // statistics kernel still runs
+        const int v = blockIdx.x * (kVThreads * kRPer) + threadIdx.x * kRPer;
+        if (v < a.V && threadIdx.x % (32 / kRPer) == 0) { // one thread per 128-byte line
+            prefetch_l2(a.cluster_of + v);
+            prefetch_l2(a.rank + v);
+        }
+    }
     pdl_wait();
     const int b = blockIdx.y;
     const int tr = __ldcg(&a.decision[b]);

@@ -152,6 +152,15 @@ __device__ PStat chunk_stats(const float *__restrict__ row, int lo, int n, float
     return r;
 }
 
+// What the residual draw of one sequence needs from the decision, in one 32-byte record: the
+// target row to draw from (-1: decided already), its softmax statistics, and for a rejection
+// the list's offset and the draft row's statistics.
+struct Decision {
+    int tr, off;
+    float pm, ps, qm, qs, pad0, pad1;
+};
+static_assert(sizeof(Decision) == 32, "two 16-byte loads");
+
 struct ChainArgs {
     const float *p_logits;
     int B, gamma, V, nch;
@@ -172,7 +181,7 @@ struct ChainArgs {
     QStat *qstat;       // [B][gamma][nch]
     QStat *prow;        // [B][gamma+1] folded target stats
     QStat *qrow;        // [B][gamma]   folded draft stats
-    int32_t *decision;  // [B]: -1 done, else the target row to draw from (t* or gamma)
+    Decision *decision; // [B]
     int nrch;           // residual-pass chunks
     float *rsum, *psum; // [B][nrch]
 };
@@ -228,15 +237,17 @@ __device__ void fold_decide(const ChainArgs &a, int b)
     // other warps fold.
     constexpr int kTestWarp = kVThreads / 32 - 1;
     const bool tester = warp == kTestWarp && lane < a.gamma;
+    __shared__ int s_off[kMaxGamma];
     int x = -1, j = -1;
     float l = 0.f, z = 0.f, uu = 0.f;
     if (tester) {
         x = a.draft_ids[size_t(lane) * a.B + b];
         if (a.T > 0.f) {
+            const int off = a.vs_offsets[size_t(lane) * (a.B + 1) + b];
+            s_off[lane] = off;
             j = list_index(a, lane, b, x);
             if (j >= 0) {
-                const int *off = a.vs_offsets + size_t(lane) * (a.B + 1);
-                l = a.q_logits[size_t(lane) * a.q_stride + off[b] + j];
+                l = a.q_logits[size_t(lane) * a.q_stride + off + j];
                 z = a.p_logits[(size_t(b) * g1 + lane) * a.V + x];
             }
             uu = a.u[size_t(b) * g1 + lane];
@@ -286,12 +297,15 @@ __device__ void fold_decide(const ChainArgs &a, int b)
         int ts = a.gamma;
         for (int tt = 0; tt < a.gamma; ++tt) if (rej[tt]) { ts = tt; break; }
         a.accepted[b] = ts;
+        Decision dsn{-1, 0, 0.f, 1.f, 0.f, 1.f, 0.f, 0.f};
         if (a.T == 0.f) {
             a.correction[b] = rows[ts].aid;
-            a.decision[b] = -1;
         } else {
-            a.decision[b] = ts;
+            dsn.tr = ts;
+            dsn.pm = rows[ts].m; dsn.ps = rows[ts].s;
+            if (ts < a.gamma) { dsn.off = s_off[ts]; dsn.qm = qrows[ts].m; dsn.qs = qrows[ts].s; }
         }
+        a.decision[b] = dsn;
     }
     __syncthreads();                                   // the block may call again (shared state)
 }
@@ -320,22 +334,26 @@ struct ResidualRow {
     float qm, qs;
 };
 
-__device__ ResidualRow residual_row(const ChainArgs &a, int b, int tr)
+__device__ ResidualRow residual_row(const ChainArgs &a, int b, const Decision &dsn)
 {
-    const int g1 = a.gamma + 1;
+    const int g1 = a.gamma + 1, tr = dsn.tr;
     ResidualRow rr;
     rr.z = a.p_logits + (size_t(b) * g1 + tr) * a.V;
-    const QStat pr = ldcg(&a.prow[size_t(b) * g1 + tr]);
-    rr.pm = pr.m; rr.ps = pr.s;
+    rr.pm = dsn.pm; rr.ps = dsn.ps;
     rr.ql = nullptr; rr.cposb = nullptr; rr.qm = 0.f; rr.qs = 1.f;
     if (tr < a.gamma) {
-        const int *off = a.vs_offsets + size_t(tr) * (a.B + 1);
-        rr.ql = a.q_logits + size_t(tr) * a.q_stride + off[b];
+        rr.ql = a.q_logits + size_t(tr) * a.q_stride + dsn.off;
         rr.cposb = a.cpos + (size_t(tr) * a.B + b) * a.M;
-        const QStat qr = ldcg(&a.qrow[size_t(b) * a.gamma + tr]);
-        rr.qm = qr.m; rr.qs = qr.s;
+        rr.qm = dsn.qm; rr.qs = dsn.qs;
     }
     return rr;
+}
+
+__device__ __forceinline__ Decision ldcg(const Decision *p)
+{
+    const float4 f0 = __ldcg(reinterpret_cast<const float4 *>(p));
+    const float4 f1 = __ldcg(reinterpret_cast<const float4 *>(p) + 1);
+    return Decision{__float_as_int(f0.x), __float_as_int(f0.y), f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
 }
 
 // Inverse-CDF draw of one sequence over V weights, run by a grid (chunks of kRChunk, B).
@@ -385,7 +403,8 @@ __device__ void icdf_chunk(const P &pol, int V, int c, float *__restrict__ rsum,
     if (threadIdx.x == 0) { rsum[c] = rs; psum[c] = ps; }
 }
 
-// Pass 2, once every chunk's masses are stored: the draw (see icdf_draw).
+// Pass 2, once every chunk's masses are stored, by the block that ran pass 1 for its own chunk
+// (a staged table is still in place): the draw (see icdf_draw).
 template <int kRPer, class P>
 __device__ void icdf_locate(const P &pol, int V, int nrch, float u, const float *__restrict__ rsum,
                             const float *__restrict__ psum, int32_t *out)
@@ -395,10 +414,7 @@ __device__ void icdf_locate(const P &pol, int V, int nrch, float u, const float 
     __shared__ int s_chunk, s_use_p, s_hit, s_last;
     __shared__ float s_target;
     constexpr int kRChunk = kVThreads * kRPer;
-    if constexpr (P::kStaged) {                        // this block's table may hold another list
-        pol.stage();
-        __syncthreads();
-    }
+    // a staged table is still in place: this block staged it for its own chunk (icdf_draw)
     const int E = (nrch + kVThreads - 1) / kVThreads;
     const int c0 = threadIdx.x * E, c1 = min(nrch, c0 + E);
     float rrun = 0.f, prun = 0.f;
@@ -540,9 +556,9 @@ verify_residual_kernel(ChainArgs a)
     }
     pdl_wait();
     const int b = blockIdx.y;
-    const int tr = __ldcg(&a.decision[b]);
-    if (tr < 0) return;                              // greedy: decided already (whole group returns)
-    const ChainResidual<kStage> pol{&a, residual_row(a, b, tr), s_cp};
+    const Decision dsn = ldcg(&a.decision[b]);
+    if (dsn.tr < 0) return;                          // greedy: decided already (whole group returns)
+    const ChainResidual<kStage> pol{&a, residual_row(a, b, dsn), s_cp};
     icdf_draw<kRPer>(pol, a.V, a.nrch, a.u[size_t(b) * (a.gamma + 1) + a.gamma], a.rsum + size_t(b) * a.nrch,
               a.psum + size_t(b) * a.nrch, &a.cnt2[b], &a.correction[b]);
 }
@@ -1016,7 +1032,7 @@ extern "C" size_t ds_verify_workspace_bytes(int B, int gamma, int V)
            align256(size_t(B) * gamma * nch * sizeof(QStat)) +
            align256(size_t(B) * g1 * sizeof(QStat)) +
            align256(size_t(B) * gamma * sizeof(QStat)) +
-           align256(size_t(B) * sizeof(int32_t)) +
+           align256(size_t(B) * sizeof(Decision)) +
            2 * align256(size_t(B) * rchunks(V) * sizeof(float));
 }
 
@@ -1061,7 +1077,7 @@ extern "C" ds_status ds_verify(const float *p_logits, int B, int gamma, int V, f
     a.qstat = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * gamma * nch * sizeof(QStat));
     a.prow = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * g1 * sizeof(QStat));
     a.qrow = reinterpret_cast<QStat *>(w); w += align256(size_t(B) * gamma * sizeof(QStat));
-    a.decision = reinterpret_cast<int32_t *>(w); w += align256(size_t(B) * sizeof(int32_t));
+    a.decision = reinterpret_cast<Decision *>(w); w += align256(size_t(B) * sizeof(Decision));
     a.nrch = (V + kVThreads * (rbig ? kRPerBig : kRPerSmall) - 1) / (kVThreads * (rbig ? kRPerBig : kRPerSmall));
     a.rsum = reinterpret_cast<float *>(w); w += align256(size_t(B) * rchunks(V) * sizeof(float));
     a.psum = reinterpret_cast<float *>(w);

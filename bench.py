@@ -32,7 +32,8 @@ METRIC = "draft-head tokens/s (router+gather-GEMM+sample+verify)"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 512 << 20        # > 129 MB L2: written between timed steps ...
 L2_CLEAN_BYTES = 256 << 20        # ... then this much is read, so the written lines leave L2 too
-TIMED_HEAD_STEPS = 64             # replays of the instrumented graph for per-head times
+TIMED_HEAD_STEPS = 256                 # instrumented replays for the per-head times (the event clock
+                                      # ticks in ~2 us steps: many samples average the ticks out)
 FALLBACK_HBM_GBS = 6800.0
 HEAD_KERNEL_SOURCES = ["dynamic_vocab_draft_gb300/csrc/head.cu", "dynamic_vocab_draft_gb300/csrc/common.cuh"]
 
@@ -569,7 +570,7 @@ def run_ours(args):
             torch.cuda.empty_cache()
             c = wl.config(name)
             q = measure(c, seed, dev, pkg, torch, world, local_rank, args.steps, args.warmup,
-                        args.e2e_steps, min(args.steps, 16), flush)
+                        args.e2e_steps, min(args.steps, 64), flush)
             q.pop("inp")
             unit = "nodes/s" if c.mode == "tree" else "tokens/s"
             per_config[name] = {

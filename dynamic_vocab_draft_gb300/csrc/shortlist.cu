@@ -34,11 +34,71 @@ __global__ void vocab_index_kernel(const int32_t *__restrict__ off, const int32_
     }
 }
 
+// Single block, once every list's scan is stored: vs_offsets = exclusive scan of the list
+// sizes; and, if asked, the batch union (clusters selected by any list) with each cluster's
+// start in it (ustart, -1 if out).  Reads what other blocks stored, through L2.
+__device__ void offsets_block(const int32_t *__restrict__ off, int M, int B,
+                              const int32_t *__restrict__ sizes, const int32_t *__restrict__ cpos,
+                              int32_t *__restrict__ vs_offsets, int64_t capacity,
+                              int32_t *__restrict__ ustart, int32_t *__restrict__ union_count, int32_t *st)
+{
+    __shared__ int scratch[33];
+    {
+        const int E = (B + kSlThreads - 1) / kSlThreads;
+        const int lo = threadIdx.x * E;
+        int sum = 0;
+        for (int e = 0; e < E; ++e) if (lo + e < B) sum += __ldcg(&sizes[lo + e]);
+        int tot;
+        int run = block_exclusive_scan(sum, scratch, &tot);
+        for (int e = 0; e < E; ++e) if (lo + e < B) { vs_offsets[lo + e] = run; run += __ldcg(&sizes[lo + e]); }
+        if (threadIdx.x == 0) {
+            vs_offsets[B] = tot;
+            if (int64_t(tot) > capacity) set_status(st, DS_DEV_CAPACITY);
+        }
+    }
+    if (!ustart) return;
+    const int E = (M + kSlThreads - 1) / kSlThreads;
+    const int lo = threadIdx.x * E;
+    int sz[kSlMaxPer];
+    int sum = 0;
+#pragma unroll
+    for (int e = 0; e < kSlMaxPer; ++e) {
+        const int c = lo + e;
+        bool any = false;
+        if (e < E && c < M) {
+            // eight independent loads per round instead of a dependent chain over b
+            int b = 0;
+            for (; b + 8 <= B && !any; b += 8) {
+                int q[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) q[j] = __ldcg(&cpos[size_t(b + j) * M + c]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) any |= q[j] >= 0;
+            }
+            for (; b < B && !any; ++b) any = __ldcg(&cpos[size_t(b) * M + c]) >= 0;
+        }
+        sz[e] = any ? off[c + 1] - off[c] : 0;
+        sum += sz[e];
+    }
+    int tot;
+    int run = block_exclusive_scan(sum, scratch, &tot);
+#pragma unroll
+    for (int e = 0; e < kSlMaxPer; ++e) {
+        const int c = lo + e;
+        if (e < E && c < M) { ustart[c] = sz[e] ? run : -1; run += sz[e]; }
+    }
+    if (threadIdx.x == 0) *union_count = tot;
+}
+
 // One block per list b: cpos[b][c] = exclusive prefix (over ascending c) of the sizes of the
-// clusters b selected, or -1; sizes[b] = |S_b|.
+// clusters b selected, or -1; sizes[b] = |S_b|.  The last block to finish (a completion
+// counter) then computes the offsets and the union's starts (offsets_block).
 __global__ void __launch_bounds__(kSlThreads)
 shortlist_scan_kernel(const int32_t *__restrict__ off, int M, const int32_t *__restrict__ ids, int k,
-                      int32_t *__restrict__ cpos, int32_t *__restrict__ sizes, int32_t *st)
+                      int32_t *__restrict__ cpos, int32_t *__restrict__ sizes,
+                      int32_t *__restrict__ vs_offsets, int64_t capacity,
+                      int32_t *__restrict__ ustart, int32_t *__restrict__ union_count,
+                      unsigned *__restrict__ counter, int32_t *st)
 {
     __shared__ unsigned char flag[kSlMaxM];
     __shared__ int scratch[33];
@@ -71,97 +131,44 @@ shortlist_scan_kernel(const int32_t *__restrict__ off, int M, const int32_t *__r
         if (e < E && c < M) { dst[c] = flag[c] ? run : -1; run += sz[e]; }
     }
     if (threadIdx.x == 0) sizes[b] = tot;
+    if (!last_block_done(counter, gridDim.x)) return;
+    offsets_block(off, M, int(gridDim.x), sizes, cpos, vs_offsets, capacity, ustart, union_count, st);
 }
 
-// Single block: vs_offsets = exclusive scan of the list sizes; and, if asked, the batch
-// union (clusters selected by any list) with each cluster's start in it (ustart, -1 if out).
-__global__ void __launch_bounds__(kSlThreads)
-shortlist_offsets_kernel(const int32_t *__restrict__ off, int M, int B,
-                         const int32_t *__restrict__ sizes, const int32_t *__restrict__ cpos,
-                         int32_t *__restrict__ vs_offsets, int64_t capacity,
-                         int32_t *__restrict__ ustart, int32_t *__restrict__ union_count, int32_t *st)
+// The copies, one launch: blocks [0, xb * B) take one warp per selected cluster of list
+// b = block / xb and copy its CSR slice into the list; the blocks after them (union != null)
+// take one warp per cluster of the batch union and copy its slice and cluster id there.
+__global__ void shortlist_copy_kernel(const int32_t *__restrict__ off, const int32_t *__restrict__ tok,
+                                      int M, int V, const int32_t *__restrict__ ids, int k, int B, int xb,
+                                      const int32_t *__restrict__ cpos,
+                                      const int32_t *__restrict__ vs_offsets, int32_t *__restrict__ vs_ids,
+                                      int64_t capacity, const int32_t *__restrict__ ustart,
+                                      int32_t *__restrict__ union_ids, int32_t *__restrict__ union_cluster)
 {
-    __shared__ int scratch[33];
-    {
-        const int E = (B + kSlThreads - 1) / kSlThreads;
-        const int lo = threadIdx.x * E;
-        int sum = 0;
-        for (int e = 0; e < E; ++e) if (lo + e < B) sum += sizes[lo + e];
-        int tot;
-        int run = block_exclusive_scan(sum, scratch, &tot);
-        for (int e = 0; e < E; ++e) if (lo + e < B) { vs_offsets[lo + e] = run; run += sizes[lo + e]; }
-        if (threadIdx.x == 0) {
-            vs_offsets[B] = tot;
-            if (int64_t(tot) > capacity) set_status(st, DS_DEV_CAPACITY);
-        }
+    const int wpb = blockDim.x >> 5, lane = threadIdx.x & 31;
+    const int nlist = xb * B;
+    if (int(blockIdx.x) < nlist) {
+        const int b = blockIdx.x / xb;
+        const int j = (blockIdx.x - b * xb) * wpb + (threadIdx.x >> 5);
+        if (j >= k) return;
+        const int c = ids[size_t(b) * k + j];
+        if (c < 0 || c >= M) return;                      // flagged by the scan kernel
+        const int p = cpos[size_t(b) * M + c];
+        if (p < 0) return;                                // duplicate / unsorted ids, flagged
+        const int lo = off[c], n = off[c + 1] - lo;
+        if (lo < 0 || n < 0 || lo + n > V) return;
+        const int64_t base = int64_t(vs_offsets[b]) + p;
+        for (int r = lane; r < n; r += 32)
+            if (base + r < capacity) vs_ids[base + r] = tok[lo + r];
+        return;
     }
-    if (!ustart) return;
-    const int E = (M + kSlThreads - 1) / kSlThreads;
-    const int lo = threadIdx.x * E;
-    int sz[kSlMaxPer];
-    int sum = 0;
-#pragma unroll
-    for (int e = 0; e < kSlMaxPer; ++e) {
-        const int c = lo + e;
-        bool any = false;
-        if (e < E && c < M) {
-            // eight independent loads per round instead of a dependent chain over b
-            int b = 0;
-            for (; b + 8 <= B && !any; b += 8) {
-                int q[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) q[j] = cpos[size_t(b + j) * M + c];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) any |= q[j] >= 0;
-            }
-            for (; b < B && !any; ++b) any = cpos[size_t(b) * M + c] >= 0;
-        }
-        sz[e] = any ? off[c + 1] - off[c] : 0;
-        sum += sz[e];
-    }
-    int tot;
-    int run = block_exclusive_scan(sum, scratch, &tot);
-#pragma unroll
-    for (int e = 0; e < kSlMaxPer; ++e) {
-        const int c = lo + e;
-        if (e < E && c < M) { ustart[c] = sz[e] ? run : -1; run += sz[e]; }
-    }
-    if (threadIdx.x == 0) *union_count = tot;
-}
-
-// One warp per selected cluster of list b: copy its CSR slice into the list.
-__global__ void shortlist_expand_kernel(const int32_t *__restrict__ off, const int32_t *__restrict__ tok,
-                                        int M, int V, const int32_t *__restrict__ ids, int k,
-                                        const int32_t *__restrict__ cpos,
-                                        const int32_t *__restrict__ vs_offsets, int32_t *__restrict__ vs_ids,
-                                        int64_t capacity)
-{
-    const int b = blockIdx.y;
-    const int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (j >= k) return;
-    const int c = ids[size_t(b) * k + j];
-    if (c < 0 || c >= M) return;                          // flagged by the scan kernel
-    const int p = cpos[size_t(b) * M + c];
-    if (p < 0) return;                                    // duplicate / unsorted ids, flagged
-    const int lo = off[c], n = off[c + 1] - lo;
-    if (lo < 0 || n < 0 || lo + n > V) return;
-    const int64_t base = int64_t(vs_offsets[b]) + p;
-    for (int r = threadIdx.x & 31; r < n; r += 32)
-        if (base + r < capacity) vs_ids[base + r] = tok[lo + r];
-}
-
-// One warp per cluster of the batch union.
-__global__ void union_expand_kernel(const int32_t *__restrict__ off, const int32_t *__restrict__ tok,
-                                    int M, int V, const int32_t *__restrict__ ustart,
-                                    int32_t *__restrict__ union_ids, int32_t *__restrict__ union_cluster)
-{
-    const int c = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int c = (int(blockIdx.x) - nlist) * wpb + (threadIdx.x >> 5);
     if (c >= M) return;
     const int u = ustart[c];
     if (u < 0) return;
     const int lo = off[c], n = off[c + 1] - lo;
     if (lo < 0 || n < 0 || lo + n > V || u + n > V) return;
-    for (int r = threadIdx.x & 31; r < n; r += 32) {
+    for (int r = lane; r < n; r += 32) {
         union_ids[u + r] = tok[lo + r];
         union_cluster[u + r] = c;
     }
@@ -265,7 +272,7 @@ extern "C" ds_status ds_vocab_index(const int32_t *csr_off, const int32_t *csr_t
 extern "C" size_t ds_shortlist_workspace_bytes(int B, int M)
 {
     if (B <= 0 || M <= 0) return 0;
-    return align256(size_t(B) * sizeof(int32_t)) + align256(size_t(M) * sizeof(int32_t));
+    return align256(size_t(B) * sizeof(int32_t)) + align256(size_t(M) * sizeof(int32_t)) + align256(sizeof(unsigned));
 }
 
 extern "C" ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *csr_tok, int M, int V,
@@ -286,6 +293,8 @@ extern "C" ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *c
     if (!ws || ws_bytes < ds_shortlist_workspace_bytes(B, M)) return DS_ERR_WORKSPACE;
     int32_t *sizes = static_cast<int32_t *>(ws);
     int32_t *ustart = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + align256(size_t(B) * 4));
+    unsigned *counter = reinterpret_cast<unsigned *>(static_cast<char *>(ws) + align256(size_t(B) * 4) +
+                                                     align256(size_t(M) * 4));
 
     if (B == 1 && nu == 0) {
         const int blocks = (k + kSlCopyWarps * (kSlThreads / 32) - 1) / (kSlCopyWarps * (kSlThreads / 32));
@@ -294,17 +303,16 @@ extern "C" ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *c
         DS_TRY_LAUNCH();
         return DS_OK;
     }
-    shortlist_scan_kernel<<<B, kSlThreads, 0, stream>>>(csr_off, M, cluster_ids, k, cpos, sizes, dev_status);
+    // the scan (its last block also computes the offsets and the union's starts), then the copies
+    shortlist_scan_kernel<<<B, kSlThreads, 0, stream>>>(csr_off, M, cluster_ids, k, cpos, sizes, vs_offsets,
+                                                        vs_capacity, nu ? ustart : nullptr, union_count, counter,
+                                                        dev_status);
     DS_TRY_LAUNCH();
-    shortlist_offsets_kernel<<<1, kSlThreads, 0, stream>>>(csr_off, M, B, sizes, cpos, vs_offsets, vs_capacity,
-                                                          nu ? ustart : nullptr, union_count, dev_status);
+    const int xb = (k + 7) / 8;                   // blocks of 8 warps per list
+    const int ub = nu ? (M + 7) / 8 : 0;          // blocks of 8 warps over the union's clusters
+    shortlist_copy_kernel<<<xb * B + ub, 256, 0, stream>>>(csr_off, csr_tok, M, V, cluster_ids, k, B, xb, cpos,
+                                                          vs_offsets, vs_ids, vs_capacity, ustart, union_ids,
+                                                          union_cluster);
     DS_TRY_LAUNCH();
-    shortlist_expand_kernel<<<dim3((k + 7) / 8, B), 256, 0, stream>>>(csr_off, csr_tok, M, V, cluster_ids, k, cpos,
-                                                                     vs_offsets, vs_ids, vs_capacity);
-    DS_TRY_LAUNCH();
-    if (nu) {
-        union_expand_kernel<<<(M + 7) / 8, 256, 0, stream>>>(csr_off, csr_tok, M, V, ustart, union_ids, union_cluster);
-        DS_TRY_LAUNCH();
-    }
     return DS_OK;
 }

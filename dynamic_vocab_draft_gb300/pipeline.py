@@ -390,7 +390,7 @@ class ChainDrafter(_Common):
 
     def launches_per_step(self) -> int:
         n_router = router_launches(self.B)
-        n_short = 4 if self.union else (1 if self.B == 1 else 3)
+        n_short = 1 if self.B == 1 and not self.union else 2
         n_head = 2 if self.union else 1
         n_draft = 5 if getattr(self, "drafter", None) is not None else 0
         n_pref = self.gamma - 1 if self.prefetch_rows else 0
@@ -487,7 +487,7 @@ class TreeDrafter(_Common):
         return self.D
 
     def launches_per_step(self) -> int:
-        return self.D * (router_launches(self.B) + 4 + 2) + 2
+        return self.D * (router_launches(self.B) + 2 + 2) + 2
 
 
 class StaticChainDrafter(_Common):

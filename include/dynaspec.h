@@ -180,7 +180,8 @@ ds_status ds_gathered_head_b1_table(const uint16_t *H, const uint16_t *W, int V,
  * Device errors: DS_DEV_BAD_INDEX (cluster id outside [0, M) or not ascending),
  * DS_DEV_CAPACITY (sum of list sizes > vs_capacity; nothing past the capacity is written).
  * Limits: 1 <= B <= 4096, 1 <= k <= M <= 8192.
- * ws: ds_shortlist_workspace_bytes(B, M) bytes.
+ * ws: ds_shortlist_workspace_bytes(B, M) bytes; holds a completion counter (zero it once;
+ * every call leaves it zero).
  * ------------------------------------------------------------------------------------- */
 size_t ds_shortlist_workspace_bytes(int B, int M);
 ds_status ds_build_shortlist(const int32_t *csr_off, const int32_t *csr_tok, int M, int V,

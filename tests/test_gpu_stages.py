@@ -323,7 +323,7 @@ def test_list_table_capacity_and_bad_csr(ds):
 # ---------------------------------------------------------------------------------------
 # Gathered head
 # ---------------------------------------------------------------------------------------
-def _run_head(ds, inp, Hrows, G, ids, T, pos, union):
+def _run_head(ds, inp, Hrows, G, ids, T, pos, union, free_sms=-1):
     """Head on the GPU for lists built from the oracle's cluster ids; returns host arrays."""
     cfg = inp["cfg"]
     B = ids.shape[0]
@@ -340,7 +340,7 @@ def _run_head(ds, inp, Hrows, G, ids, T, pos, union):
     ws = ds.workspace(ds.head_workspace_bytes(R), gu.dev())
     ds.gathered_head(gu.bf16(Hrows), G, gu.device_head(inp), vs_off, vs_ids, T, inp["gumbel_seed"], pos,
                      logits, tok, tix, ws, st, cpos=cpos, rank_in_cluster=rk,
-                     union=un if union else None, row_max=rmax, row_sumexp=rsum)
+                     union=un if union else None, row_max=rmax, row_sumexp=rsum, free_sms=free_sms)
     torch.cuda.synchronize()
     assert st.item() == 0
     return (vs_off.cpu().numpy(), logits.cpu().numpy(), tok.cpu().numpy(), tix.cpu().numpy(),
@@ -375,6 +375,31 @@ def test_head_per_row_path(ds, name, T):
         Hrows = inp["H"][:1, pos]
         out = _run_head(ds, inp, Hrows, 1, ids, T, pos, union=False)
         _check_head(inp, Hrows, 1, ids, T, pos, out)
+
+
+@pytest.mark.parametrize("union", [False, True])
+def test_head_free_sms(ds, union):
+    # The SMs a head leaves free change only its grid: every SM (0), the default (-1), and more
+    # than the GPU has (one SM is still used) each match the oracle.  The per-row path computes
+    # every logit in one warp whatever the grid, so its logits, draws and maxima are the same
+    # bits; the union GEMM splits its work by the grid (the fp32 parts of a tile add in another
+    # grouping), so there the logits agree to rounding.
+    inp = gu.chain_inputs("small_batched")
+    cfg = inp["cfg"]
+    B = 1 if not union else 3
+    ids, _ = _oracle_lists(inp, B, 1)
+    Hrows = inp["H"][:B, 1]
+    outs = [_run_head(ds, inp, Hrows, 1, ids, cfg.T, 1, union, free_sms=f) for f in (-1, 0, 1 << 20)]
+    for o in outs:
+        _check_head(inp, Hrows, 1, ids, cfg.T, 1, o)
+    for o in outs[1:]:
+        assert np.array_equal(outs[0][0], o[0])     # list offsets
+        if union:
+            np.testing.assert_allclose(o[1], outs[0][1], rtol=1e-5, atol=1e-5)
+        else:
+            for i in (1, 2, 3, 4):                  # logits, tokens, indices, maxima
+                assert np.array_equal(outs[0][i], o[i], equal_nan=True)
+            np.testing.assert_allclose(o[5], outs[0][5], rtol=1e-5)
 
 
 def test_head_all_clusters_is_dense_head(ds):

@@ -476,9 +476,9 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
 // ---------------------------------------------------------------------------------------
 #include <mutex>
 
-#include <cuda.h>      // CUcontext / CUresult types only: the two driver calls below are reached
-                       // through the runtime's entry-point query, so the library does not link
-                       // the driver library
+#include <cuda.h>      // CUcontext / CUresult types only: the two CUDA driver API calls below are
+                       // reached through the runtime's entry-point query, so the library does not
+                       // link the CUDA driver library
 
 namespace {
 
@@ -499,8 +499,8 @@ std::mutex g_noalloc_mutex;
 void *g_noalloc_addr[kNoAllocMaxDevices];
 unsigned long long g_noalloc_ctx[kNoAllocMaxDevices];   // context the address belongs to
 
-// Unique id of the calling thread's current context (the driver never reuses one within a
-// process), or 0 when none is current or the driver calls cannot be reached.
+// Unique id of the calling thread's current context (the CUDA driver never reuses one within a
+// process), or 0 when none is current or the CUDA driver calls cannot be reached.
 unsigned long long current_context_id()
 {
     typedef CUresult (*GetCurrent)(CUcontext *);

@@ -549,9 +549,11 @@ def _chain_oracle(inp, B, T):
     return [ref[b]["positions"] for b in range(B)]
 
 
-def _check_chain_verify(ds, inp, pos_rows, z, u, T):
+def _check_chain_verify(ds, inp, pos_rows, z, u, T, with_stats=False):
     """pos_rows[b][t]: oracle per-position dicts. Runs GPU verify on the oracle's draft data
-    and compares with the oracle's verification of the same data."""
+    and compares with the oracle's verification of the same data.  with_stats: hand the
+    verifier the draft rows' softmax statistics (as the head gives them) instead of letting it
+    reduce the draft rows itself."""
     cfg = inp["cfg"]
     B, gamma, V, M = len(pos_rows), cfg.gamma, cfg.V, cfg.M
     cap = B * V
@@ -580,8 +582,19 @@ def _check_chain_verify(ds, inp, pos_rows, z, u, T):
     corr = torch.empty(B, dtype=torch.int32, device=gu.dev())
     st = gu.status()
     ws = ds.workspace(ds.verify_workspace_bytes(B, gamma, V), gu.dev())
+    stats = {}
+    if with_stats:
+        te = T if T > 0 else 1.0
+        qm = np.zeros((gamma, B), np.float32)
+        qs = np.zeros((gamma, B), np.float32)
+        for t in range(gamma):
+            for b in range(B):
+                x = q[t, offs[t, b]:offs[t, b + 1]].astype(np.float64) / te
+                qm[t, b] = x.max()
+                qs[t, b] = np.exp(x - x.max()).sum()
+        stats = dict(q_max=gu.f32(qm), q_sumexp=gu.f32(qs))
     ds.verify(gu.f32(z), T, gu.f32(q), gu.i32(offs), gu.i32(cpos), cof, rk, gu.i32(draft), gu.f32(u),
-              acc, corr, ws, st)
+              acc, corr, ws, st, **stats)
     torch.cuda.synchronize()
     assert st.item() == 0
     acc, corr = acc.cpu().numpy(), corr.cpu().numpy()
@@ -662,11 +675,13 @@ def _synthetic_chain_rows(inp, B, T, rng):
 
 @pytest.mark.parametrize("T", [0.7, 0.0])
 @pytest.mark.parametrize("mode", ["independent", "aligned", "half"])
-def test_verify_chain_wide_grid(ds, T, mode):
+@pytest.mark.parametrize("with_stats", [False, True])
+def test_verify_chain_wide_grid(ds, T, mode, with_stats):
     # The batched workload's sizes (B = 32, gamma = 6, V = 128,256): the verifier takes its wide
-    # grid here (8192-element statistics chunks, 2048-element residual chunks without staging),
-    # and with target rows that agree with the draft the accept walk runs past t = 1 and, in
-    # "aligned", to the bonus draw from row gamma + 1.
+    # grid here (8192-element statistics chunks, or with the draft rows' statistics given the
+    # pipelined statistics kernel; 2048-element residual chunks without staging), and with
+    # target rows that agree with the draft the accept walk runs past t = 1 and, in "aligned",
+    # to the bonus draw from row gamma + 1.
     inp = gu.chain_inputs("batched")
     cfg = inp["cfg"]
     B = cfg.B
@@ -685,7 +700,7 @@ def test_verify_chain_wide_grid(ds, T, mode):
     u = inp["u"][:B].copy()
     longest = 0
     for trial in range(2):
-        acc, acc_ref, n_exact = _check_chain_verify(ds, inp, rows, z, u, T)
+        acc, acc_ref, n_exact = _check_chain_verify(ds, inp, rows, z, u, T, with_stats)
         longest = max(longest, int(acc_ref.max()))
         assert n_exact >= B // 2
         u = wl.open_uniforms(rng, u.shape)

@@ -24,12 +24,12 @@ SIGNATURES = {
     "ds_version": (I, []),
     "ds_vocab_index": (ST, [P, P, I, I, P, P, P, P]),
     "ds_router_workspace_bytes": (SZ, [I, I]),
-    "ds_router_topk": (ST, [P, I, I, P, P, I, P, P, I, I, P, I, I, P, P, P, SZ, P, P]),
+    "ds_router_topk": (ST, [P, I, I, P, P, I, P, P, I, I, P, I, I, P, P, I, P, SZ, P, P]),
     "ds_router_create": (ST, [P, P, P, P, P, I, I, I, I, P, I]),
     "ds_router_destroy": (ST, [P]),
     "ds_router_workspace_bytes_h": (SZ, [P, I]),
-    "ds_router_topk_h": (ST, [P, P, I, I, P, P, P, SZ, P, P]),
-    "ds_router_topk_list_b1": (ST, [P, P, I, P, I, P, P, P, P, P, I64, P, SZ, P, P]),
+    "ds_router_topk_h": (ST, [P, P, I, I, P, P, I, P, SZ, P, P]),
+    "ds_router_topk_list_b1": (ST, [P, P, I, P, I, P, P, P, P, P, I64, I, P, SZ, P, P]),
     "ds_gathered_head_b1_table": (ST, [P, P, I, I, P, I, P, F, U64, I, P, P, P, P, P, I, P, SZ, P, P]),
     "ds_shortlist_workspace_bytes": (SZ, [I, I]),
     "ds_build_shortlist": (ST, [P, P, I, I, P, I, I, P, P, I64, P, P, P, P, P, SZ, P, P]),

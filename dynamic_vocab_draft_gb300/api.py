@@ -96,23 +96,24 @@ class Router:
     def workspace_bytes(self, B):
         return int(_lib.load().ds_router_workspace_bytes_h(self.handle, B))
 
-    def topk(self, H, pos, scores, cluster_ids, ws, status, stream=None):
-        """ds_router_topk_h for draft position `pos` (1-based); scores may be None."""
+    def topk(self, H, pos, scores, cluster_ids, ws, status, stream=None, sms=-1):
+        """ds_router_topk_h for draft position `pos` (1-based); scores may be None; sms: SMs to
+        size the launches for (-1: the library's default)."""
         B = H.shape[0]
         _lib.check(_lib.load().ds_router_topk_h(
             self.handle, _ptr(H, BF16, "H"), B, int(pos), _ptr(scores, F32, "scores", True),
-            _ptr(cluster_ids, I32, "cluster_ids"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+            _ptr(cluster_ids, I32, "cluster_ids"), int(sms), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
             _ptr(status, I32, "status"), _stream(stream)), "ds_router_topk_h")
 
     def topk_list_b1(self, H, pos, csr_off, V, scores, cluster_ids, cpos, vs_offsets, list_table, capacity,
-                     ws, status, stream=None):
+                     ws, status, stream=None, sms=-1):
         """ds_router_topk_list_b1: batch 1, the router and top-k of position `pos` with the list's
         table (list_table [2 (k+1)] int32), cpos [M] and vs_offsets [2] instead of copied ids."""
         _lib.check(_lib.load().ds_router_topk_list_b1(
             self.handle, _ptr(H, BF16, "H"), int(pos), _ptr(csr_off, I32, "csr_off"), int(V),
             _ptr(scores, F32, "scores"), _ptr(cluster_ids, I32, "cluster_ids"), _ptr(cpos, I32, "cpos"),
             _ptr(vs_offsets, I32, "vs_offsets"), _ptr(list_table, I32, "list_table"), int(capacity),
-            _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
+            int(sms), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
             _stream(stream)), "ds_router_topk_list_b1")
 
     def close(self):
@@ -136,8 +137,9 @@ def vocab_index(csr_off, csr_tok, cluster_of, rank_in_cluster, status, stream=No
         _ptr(status, I32, "status"), _stream(stream)), "ds_vocab_index")
 
 
-def router_topk(H, W1, b1, W2, b2, act, budget, pos, scores, cluster_ids, ws, status, stream=None):
-    """budget: host int32 tensor / sequence of clusters kept per draft position."""
+def router_topk(H, W1, b1, W2, b2, act, budget, pos, scores, cluster_ids, ws, status, stream=None, sms=-1):
+    """budget: host int32 tensor / sequence of clusters kept per draft position; sms: SMs to size
+    the launches for (-1: the library's default)."""
     B, d = H.shape
     Hr = W1.shape[0]
     M = W2.shape[0]
@@ -146,7 +148,7 @@ def router_topk(H, W1, b1, W2, b2, act, budget, pos, scores, cluster_ids, ws, st
         _ptr(H, BF16, "H"), B, d, _ptr(W1, BF16, "W1"), _ptr(b1, BF16, "b1"), Hr,
         _ptr(W2, BF16, "W2"), _ptr(b2, BF16, "b2"), M, ACT.get(act, act),
         bud.data_ptr(), bud.numel(), int(pos),
-        _ptr(scores, F32, "scores"), _ptr(cluster_ids, I32, "cluster_ids"),
+        _ptr(scores, F32, "scores"), _ptr(cluster_ids, I32, "cluster_ids"), int(sms),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _ptr(status, I32, "status"),
         _stream(stream)), "ds_router_topk")
 

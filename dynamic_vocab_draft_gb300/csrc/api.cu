@@ -67,7 +67,7 @@ extern "C" const char *ds_status_string(ds_status s)
     return "unknown status";
 }
 
-extern "C" int ds_version(void) { return 3; }
+extern "C" int ds_version(void) { return 4; }
 
 extern "C" size_t ds_workspace_bytes(int op, int B, int V, int M, int gamma, int hidden, int width)
 {

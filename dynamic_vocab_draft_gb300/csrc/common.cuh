@@ -239,21 +239,29 @@ __device__ __forceinline__ void st_stat(Stat *p, const Stat &a)
     q->m = a.m; q->s = a.s; q->key = a.key; q->v = a.v; q->j = a.j;
 }
 
+// Atomic add with acquire and release semantics at GPU scope: the calling thread's earlier
+// memory operations (and, through a barrier before it, those of its block) are ordered before
+// the add, and the values other threads released by their adds on the same counter are visible
+// to what the caller does after it.  No separate fence is needed on either side.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *counter, unsigned x)
+{
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(prev) : "l"(counter), "r"(x) : "memory");
+    return prev;
+}
+
 // "Am I the last block of this group to finish?"  Every block calls it once, after its
-// results are stored; the returning `true` block may read all of them.  The counter is
-// reset for the next launch by the last block.
+// results are stored; the returning `true` block may read all of them.  The barrier before
+// the add orders the block's stores before thread 0's release; the last block's acquire, and
+// the barrier after it, make every block's stores visible to all of its threads.  The last
+// block resets the counter; the next launch sees the reset (kernel boundary).
 __device__ __forceinline__ bool last_block_done(unsigned *counter, unsigned nblocks)
 {
     __shared__ bool is_last;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned prev = atomicAdd(counter, 1u);
-        is_last = (prev == nblocks - 1);
-        if (is_last) {
-            *counter = 0u;
-            __threadfence();
-        }
+        is_last = atom_add_acq_rel_gpu(counter, 1u) == nblocks - 1;
+        if (is_last) *counter = 0u;
     }
     __syncthreads();
     return is_last;

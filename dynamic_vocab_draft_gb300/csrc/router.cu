@@ -90,7 +90,6 @@ gemv_rows_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restr
 #pragma unroll
         for (int bt = 1; bt < BT; ++bt) if (lane == bt) a = acc[bt];
         y[size_t(b0 + lane) * N + i] = act_fn(a + bf16_to_f32(bias[i]), act);
-        if (topk_k > 0) __threadfence();
     }
     }
     if (topk_k > 0 && last_block_done(&counters[blockIdx.y], gridDim.x)) {
@@ -312,7 +311,6 @@ gemv1_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict_
         const float acc = warp_sum(a0 + a1);
         if (lane == 0) {
             y[i] = act_fn(acc + bf16_to_f32(bias[i]), act);
-            if (topk_k > 0) __threadfence();
         }
     }
     if (topk_k > 0 && last_block_done(counter, gridDim.x)) {
@@ -321,8 +319,8 @@ gemv1_kernel(const uint16_t *__restrict__ A, int N, int K, const XT *__restrict_
     }
 }
 
-constexpr int kGemv1Blocks = 64;       // a later position's router: four 256-thread blocks on each of
-                                       // the 16 SMs the batch-1 head leaves free
+constexpr int kGemv1PerSm = 4;         // a later position's router: four 256-thread blocks on each
+constexpr int kGemv1SideSms = 16;      // SM the batch-1 head leaves free (by default 16)
 
 // One block per row: the top-k of scores[b][0..M).
 __global__ void __launch_bounds__(kTopkThreads)
@@ -415,9 +413,10 @@ RouterTcWs router_tc_layout(int B, int Hr)
 // SMs free for it, and must fit there.
 constexpr int kRouterSideSms = 8;
 constexpr int kRouterMinUnits = 8;
-int router_grid(int pos, int units, int sms)
+// side: the caller's SM count for the launch (<= 0: the default above)
+int router_grid(int pos, int units, int sms, int side)
 {
-    int g = pos == 1 ? (units + kRouterMinUnits - 1) / kRouterMinUnits : kRouterSideSms;
+    int g = side > 0 ? side : pos == 1 ? (units + kRouterMinUnits - 1) / kRouterMinUnits : kRouterSideSms;
     if (g > sms) g = sms;
     if (g > tc::kMaxGrid) g = tc::kMaxGrid;
     if (g > units) g = units;
@@ -456,8 +455,8 @@ namespace {
 // ds_router_topk, and at B = 1 optionally the list's table (list_out.table non-null).
 ds_status router_topk(const uint16_t *H, int B, int d, const uint16_t *W1, const uint16_t *b1, int Hr,
                       const uint16_t *W2, const uint16_t *b2, int M, int act, const int32_t *budget, int n_budget,
-                      int pos, float *scores, int32_t *cluster_ids, void *ws, size_t ws_bytes, int32_t *dev_status,
-                      cudaStream_t stream, ListOut list_out)
+                      int pos, float *scores, int32_t *cluster_ids, int side, void *ws, size_t ws_bytes,
+                      int32_t *dev_status, cudaStream_t stream, ListOut list_out)
 {
     ds::NvtxRange range("ds_router_topk");
     if (!H || !W1 || !b1 || !W2 || !b2 || !budget || !scores || !cluster_ids)
@@ -478,9 +477,14 @@ ds_status router_topk(const uint16_t *H, int B, int d, const uint16_t *W1, const
     unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(ws) +
                                                       align256(size_t(B) * size_t(Hr) * sizeof(float)));
     if (B == 1) {
-        // the first position's router has the GPU to itself: one warp per weight row
+        // the first position's router has the GPU to itself: one warp per weight row; a later
+        // one runs kGemv1PerSm blocks on each SM the head beside it leaves free
         auto grid1 = [&](int rows) {
-            if (pos != 1) return kGemv1Blocks;
+            if (side > 0 || pos != 1) {
+                const int g = kGemv1PerSm * (side > 0 ? (side < sms ? side : sms) : kGemv1SideSms);
+                const int need = (rows + kGemvWarps - 1) / kGemvWarps;
+                return g < need ? g : need;
+            }
             const int g = (rows + kGemvWarps - 1) / kGemvWarps;
             return g < sms ? g : sms;
         };
@@ -502,13 +506,13 @@ ds_status router_topk(const uint16_t *H, int B, int d, const uint16_t *W1, const
         e1.n = Hr; e1.bias = b1; e1.hid2 = hid2; e1.Hr = Hr; e1.act = act;
         const tc::Operands op1{W1, H, d, B, dev_status, wait_budget()};
         const int u1 = ((Hr + tc::kRows - 1) / tc::kRows) * ((d + 127) / 128);
-        ds_status st = tc::launch_for(op1, e1, parts, tile_cnt, router_grid(pos, u1, sms), stream);
+        ds_status st = tc::launch_for(op1, e1, parts, tile_cnt, router_grid(pos, u1, sms, side), stream);
         if (st != DS_OK) return st;
         Layer2Ep e2;
         e2.n = M; e2.bias = b2; e2.scores = scores; e2.M = M; e2.B = B;
         const tc::Operands op2{W2, hid2, Hr, 2 * B, dev_status, wait_budget()};
         const int u2 = ((M + tc::kRows - 1) / tc::kRows) * ((Hr + 127) / 128);
-        st = tc::launch_for(op2, e2, parts, tile_cnt, router_grid(pos, u2, sms), stream);
+        st = tc::launch_for(op2, e2, parts, tile_cnt, router_grid(pos, u2, sms, side), stream);
         if (st != DS_OK) return st;
         topk_rows_kernel<<<B, kTopkThreads, 0, stream>>>(scores, M, k, cluster_ids);
         DS_TRY_LAUNCH();
@@ -526,13 +530,13 @@ extern "C" ds_status ds_router_topk(const uint16_t *H, int B, int d,
                                     const uint16_t *W1, const uint16_t *b1, int Hr,
                                     const uint16_t *W2, const uint16_t *b2, int M, int act,
                                     const int32_t *budget, int n_budget, int pos,
-                                    float *scores, int32_t *cluster_ids,
+                                    float *scores, int32_t *cluster_ids, int sms,
                                     void *ws, size_t ws_bytes, int32_t *dev_status,
                                     cudaStream_t stream)
 {
     ListOut none{};
     return router_topk(H, B, d, W1, b1, Hr, W2, b2, M, act, budget, n_budget, pos, scores, cluster_ids,
-                       ws, ws_bytes, dev_status, stream, none);
+                       sms, ws, ws_bytes, dev_status, stream, none);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -585,7 +589,7 @@ extern "C" size_t ds_router_workspace_bytes_h(ds_router_t r, int B)
 }
 
 extern "C" ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, int pos,
-                                      float *scores, int32_t *cluster_ids,
+                                      float *scores, int32_t *cluster_ids, int sms,
                                       void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream)
 {
     if (!r) return DS_ERR_INVALID_ARG;
@@ -594,7 +598,7 @@ extern "C" ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, i
     const size_t base = align256(ds_router_workspace_bytes(B, r->Hr));
     if (!scores) scores = reinterpret_cast<float *>(static_cast<char *>(ws) + base);
     return ds_router_topk(H, B, r->d, r->W1, r->b1, r->Hr, r->W2, r->b2, r->M, r->act,
-                          r->budget.data(), int(r->budget.size()), pos, scores, cluster_ids,
+                          r->budget.data(), int(r->budget.size()), pos, scores, cluster_ids, sms,
                           ws, base, dev_status, stream);
 }
 
@@ -604,7 +608,7 @@ extern "C" ds_status ds_router_topk_list_b1(ds_router_t r, const uint16_t *H, in
                                             const int32_t *csr_off, int V,
                                             float *scores, int32_t *cluster_ids,
                                             int32_t *cpos, int32_t *vs_offsets, int32_t *list_table,
-                                            int64_t capacity,
+                                            int64_t capacity, int sms,
                                             void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream)
 {
     if (!r || !csr_off || !cpos || !vs_offsets || !list_table || V < 1 || capacity < 0) return DS_ERR_INVALID_ARG;
@@ -614,5 +618,5 @@ extern "C" ds_status ds_router_topk_list_b1(ds_router_t r, const uint16_t *H, in
     lo.csr_off = csr_off; lo.V = V; lo.table = reinterpret_cast<int2 *>(list_table);
     lo.cpos = cpos; lo.vs_offsets = vs_offsets; lo.capacity = capacity; lo.status = dev_status;
     return router_topk(H, 1, r->d, r->W1, r->b1, r->Hr, r->W2, r->b2, r->M, r->act, r->budget.data(),
-                       int(r->budget.size()), pos, scores, cluster_ids, ws, ws_bytes, dev_status, stream, lo);
+                       int(r->budget.size()), pos, scores, cluster_ids, sms, ws, ws_bytes, dev_status, stream, lo);
 }

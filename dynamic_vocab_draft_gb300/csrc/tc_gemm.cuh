@@ -391,15 +391,14 @@ gemm_kernel(Operands op, Ep ep, float *__restrict__ parts, unsigned *__restrict_
             if (lane == 0) mbar_arrive(&acc_empty[buf]);      // the MMA may reuse this buffer
             if (!whole) {
                 // the last CTA of the tile adds the parts in k (= CTA) order
-                __threadfence();
                 epi_sync();
                 const int cf = cta_of(ts), cl = cta_of(ts + nks - 1);
                 if (tid == 0) {
                     int nparts = 1;                            // CTAs that own stages of tile t
                     for (int cc = cf; cc != cl; cc = next_owner(cc)) ++nparts;
-                    const unsigned prev = atomicAdd(&tile_cnt[t], 1u);
-                    s_last = prev == unsigned(nparts - 1);
-                    if (s_last) { tile_cnt[t] = 0u; __threadfence(); }
+                    // the epilogue barrier orders the warps' part stores before this release
+                    s_last = atom_add_acq_rel_gpu(&tile_cnt[t], 1u) == unsigned(nparts - 1);
+                    if (s_last) tile_cnt[t] = 0u;
                 }
                 epi_sync();
                 if (s_last) {

@@ -195,6 +195,25 @@ class _Common:
 
 
 
+# Batch 1: SMs a head leaves to the side stream, where the next position's router runs beside
+# it.  Fitted to measurements on GB300 (N SMs, HBM at about 6.7 TB/s): a head over L bytes of W
+# rows on n SMs takes about 9 us + L / (n / N x 6.7 TB/s); the router beside it, reading R bytes
+# of weights on s SMs at their share of the same HBM, about 21 us + R / (s / N x 6.7 TB/s).  The
+# choice is the s in 16, 24, 32, 40 that makes the slower of the two the fastest (the smaller s
+# on a tie): 16 beside Llama-size lists, more beside short lists, where the router would
+# otherwise hold up the next head (beyond 40 the head itself slows more than the router gains).
+SIDE_SMS_CHOICES = (16, 24, 32, 40)
+
+
+def side_sms_b1(list_bytes, router_bytes, sms):
+    bw = 6.7e6                                     # bytes per microsecond
+    def span(s):
+        head = 9.0 + list_bytes / ((sms - s) / sms * bw)
+        router = 21.0 + router_bytes / (s / sms * bw)
+        return max(head, router)
+    return min(SIDE_SMS_CHOICES, key=lambda s: (span(s), s))
+
+
 class ChainDrafter(_Common):
     """Chain drafting: B sequences, gamma draft positions, one shortlist per (sequence, position).
 
@@ -218,7 +237,7 @@ class ChainDrafter(_Common):
     TABLE_PREV_BYTES = 100e6
 
     def __init__(self, W, W1, b1, W2, b2, csr_off, csr_tok, *, B, gamma, budget, act, T, seed,
-                 union=None, prefetch_rows=0, list_table=None):
+                 union=None, prefetch_rows=0, list_table=None, side_sms=None):
         dev = W.device
         self.dev = dev
         self.W, self.W1, self.b1, self.W2, self.b2 = W, W1, b1, W2, b2
@@ -242,6 +261,19 @@ class ChainDrafter(_Common):
         ok = B == 1 and not self.union and not self.prefetch_rows
         self.table_pos = [bool(x) and ok for x in per_pos]
         self.table_mode = any(self.table_pos)
+        # SMs head t leaves free for the router of position t+1 beside it (the last head: none),
+        # and the SMs that router sizes its launches for (-1: the library's defaults)
+        self.head_free = [-1] * (gamma - 1) + [0]
+        if B == 1 and not self.union:
+            if side_sms is None:
+                nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+                cl = W.shape[0] / max(1, int(csr_off.numel()) - 1)           # mean cluster size
+                rb = 2.0 * (W1.shape[0] * W1.shape[1] + W2.shape[0] * W2.shape[1])
+                side_sms = [side_sms_b1(int(budget[t]) * cl * (2 * self.d + 8), rb, nsm) for t in range(gamma - 1)]
+            elif isinstance(side_sms, int):
+                side_sms = [side_sms] * (gamma - 1)
+            self.head_free = [int(x) for x in side_sms][:gamma - 1] + [0]
+        self.router_sms = [-1] + self.head_free[:gamma - 1]
         V, M = self.V, self.M
         cap = B * V
         i32 = dict(dtype=torch.int32, device=dev)
@@ -286,10 +318,10 @@ class ChainDrafter(_Common):
         if self.table_pos[t]:
             self.router.topk_list_b1(self.H[t], t + 1, self.csr_off, self.V, self.scores[t], self.cluster_ids[t],
                                      self.cpos[t], self.vs_offsets[t], self.list_table[t], self.logits.shape[1],
-                                     self.ws_router[t], self.status, stream)
+                                     self.ws_router[t], self.status, stream, sms=self.router_sms[t])
             return
         self.router.topk(self.H[t], t + 1, self.scores[t], self.cluster_ids[t], self.ws_router[t], self.status,
-                         stream)
+                         stream, sms=self.router_sms[t])
         un = (self.union_ids[t], self.union_cluster[t], self.union_count[t]) if self.union else (None,) * 3
         api.build_shortlist(self.csr_off, self.csr_tok, self.cluster_ids[t], self.vs_offsets[t],
                             self.vs_ids[t], self.cpos[t], self.ws_short[t], self.status,
@@ -299,7 +331,7 @@ class ChainDrafter(_Common):
 
     def head(self, t, stream=None):
         # the last position's head has the GPU to itself (no router runs beside it)
-        free = 0 if t == self.gamma - 1 else -1
+        free = self.head_free[t]
         if self.table_pos[t]:
             api.gathered_head_b1_table(self.H[t + 1], self.W, self.list_table[t], int(self.budget[t]), self.csr_tok,
                                        self.T, self.seed, t + 1, self.logits[t], self.tokens[t], self.token_idx[t],

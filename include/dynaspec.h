@@ -93,6 +93,12 @@ ds_status ds_vocab_index(const int32_t *csr_off, const int32_t *csr_tok, int M, 
  *                          which would not change the top-k)
  *   cluster_ids [B, k]     out: the k highest-scoring clusters of each row, ties to the lower
  *                          id, listed in ascending id
+ *   sms                    SMs to size the launches for: the ones a head running at the
+ *                          same time leaves free (its free_sms).  <= 0: the default -- every
+ *                          SM at pos 1 (nothing runs beside the first position's router),
+ *                          else 16 at B = 1 and 8 for 2 <= B <= 64.  B > 64 ignores it.  At
+ *                          B = 1 the results do not depend on it; for 2 <= B <= 64 the
+ *                          fp32 summation order of the scores does (split tiles).
  * Limits: 1 <= B <= 4096, d % 8 == 0, Hr % 8 == 0, 1 <= k <= M <= 8192.
  * ws: ds_router_workspace_bytes(B, Hr) bytes (the hidden layer and completion counters:
  *     zero it once before first use).
@@ -102,7 +108,7 @@ ds_status ds_router_topk(const uint16_t *H, int B, int d,
                          const uint16_t *W1, const uint16_t *b1, int Hr,
                          const uint16_t *W2, const uint16_t *b2, int M, int act,
                          const int32_t *budget, int n_budget, int pos,
-                         float *scores, int32_t *cluster_ids,
+                         float *scores, int32_t *cluster_ids, int sms,
                          void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
@@ -116,8 +122,8 @@ ds_status ds_router_topk(const uint16_t *H, int B, int d,
  *                          DS_ERR_UNSUPPORTED if it cannot be allocated.  *out is NULL on error.
  *   ds_router_destroy      releases the handle (NULL: no-op).  Not while a call using it is
  *                          being made on another host thread.
- *   ds_router_topk_h       ds_router_topk for draft position `pos` (1-based).  scores may be
- *                          NULL: the workspace then holds them.
+ *   ds_router_topk_h       ds_router_topk for draft position `pos` (1-based), sms as there.
+ *                          scores may be NULL: the workspace then holds them.
  *   ds_router_workspace_bytes_h  bytes of `ws` for B hidden states (the router call's
  *                          workspace followed by room for the scores); zero it once.
  * ------------------------------------------------------------------------------------- */
@@ -128,7 +134,7 @@ ds_status ds_router_create(ds_router_t *out, const uint16_t *W1, const uint16_t 
 ds_status ds_router_destroy(ds_router_t r);
 size_t ds_router_workspace_bytes_h(ds_router_t r, int B);
 ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, int pos,
-                           float *scores, int32_t *cluster_ids,
+                           float *scores, int32_t *cluster_ids, int sms,
                            void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 
 /* -------------------------------------------------------------------------------------
@@ -136,7 +142,7 @@ ds_status ds_router_topk_h(ds_router_t r, const uint16_t *H, int B, int pos,
  * selected clusters and the CSR, so instead of copying the tokens (ds_build_shortlist) the
  * router's top-k block writes a table of the selected clusters, and the head reads each listed
  * token from the CSR through it: one launch fewer per draft position, same results.
- *   ds_router_topk_list_b1  ds_router_topk_h at B = 1 for draft position pos, plus:
+ *   ds_router_topk_list_b1  ds_router_topk_h at B = 1 for draft position pos (sms as there), plus:
  *       list_table [2 (k+1)] int32 (out; 8-byte aligned): pairs {list start, CSR start} of the
  *                  k selected clusters in ascending id, then {list size, 0};
  *       cpos [M], vs_offsets [2] (out): as ds_build_shortlist writes them for one list;
@@ -155,7 +161,7 @@ ds_status ds_router_topk_list_b1(ds_router_t router, const uint16_t *H, int pos,
                                  const int32_t *csr_off, int V,
                                  float *scores, int32_t *cluster_ids,
                                  int32_t *cpos, int32_t *vs_offsets, int32_t *list_table, int64_t capacity,
-                                 void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
+                                 int sms, void *ws, size_t ws_bytes, int32_t *dev_status, cudaStream_t stream);
 ds_status ds_gathered_head_b1_table(const uint16_t *H, const uint16_t *W, int V, int d,
                                     const int32_t *list_table, int k, const int32_t *csr_tok,
                                     float T, uint64_t seed, int pos,

@@ -38,7 +38,7 @@ def test_status_strings(lib):
     for code in (0, 1, 2, 3, 4, 0x10, 0x20, 0x40, 0x30, 12345):
         s = lib.ds_status_string(code)
         assert isinstance(s, bytes) and s
-    assert lib.ds_version() == 3
+    assert lib.ds_version() == 4
 
 
 def test_workspace_queries(lib):
@@ -60,17 +60,17 @@ def test_host_argument_checks(lib):
     bptr = ctypes.cast(budget, ctypes.c_void_p)
     # router: NULL H; d not a multiple of 8; pos out of the budget table; k > M; no workspace
     assert lib.ds_router_topk(None, 1, 64, FAKE, FAKE, 64, FAKE, FAKE, 32, 0, bptr, 2, 1,
-                              FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
+                              FAKE, FAKE, -1, FAKE, 1 << 20, None, None) == 1
     assert lib.ds_router_topk(FAKE, 1, 60, FAKE, FAKE, 64, FAKE, FAKE, 32, 0, bptr, 2, 1,
-                              FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
+                              FAKE, FAKE, -1, FAKE, 1 << 20, None, None) == 1
     assert lib.ds_router_topk(FAKE, 1, 64, FAKE, FAKE, 64, FAKE, FAKE, 32, 0, bptr, 2, 3,
-                              FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
+                              FAKE, FAKE, -1, FAKE, 1 << 20, None, None) == 1
     assert lib.ds_router_topk(FAKE, 1, 64, FAKE, FAKE, 64, FAKE, FAKE, 3, 0, bptr, 2, 1,
-                              FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
+                              FAKE, FAKE, -1, FAKE, 1 << 20, None, None) == 1
     assert lib.ds_router_topk(FAKE, 1, 64, FAKE, FAKE, 64, FAKE, FAKE, 32, 7, bptr, 2, 1,
-                              FAKE, FAKE, FAKE, 1 << 20, None, None) == 1
+                              FAKE, FAKE, -1, FAKE, 1 << 20, None, None) == 1
     assert lib.ds_router_topk(FAKE, 1, 64, FAKE, FAKE, 64, FAKE, FAKE, 32, 0, bptr, 2, 1,
-                              FAKE, FAKE, None, 0, None, None) == 4
+                              FAKE, FAKE, -1, None, 0, None, None) == 4
     # shortlist: only some of the union outputs; k > M
     assert lib.ds_build_shortlist(FAKE, FAKE, 32, 4096, FAKE, 1, 4, FAKE, FAKE, 4096, FAKE,
                                   FAKE, None, None, FAKE, 1 << 20, None, None) == 1
@@ -172,9 +172,9 @@ def test_router_handle_host_side(lib):
         base = lib.ds_router_workspace_bytes(B, 512)
         assert lib.ds_router_workspace_bytes_h(h, B) == ((base + 255) // 256) * 256 + ((B * 32 * 4 + 255) // 256) * 256
     # NULL handle, too small a workspace, position outside the table: refused before any launch
-    assert lib.ds_router_topk_h(None, FAKE, 1, 1, None, FAKE, FAKE, 1 << 20, None, None) == 1
-    assert lib.ds_router_topk_h(h, FAKE, 1, 1, None, FAKE, FAKE, 16, None, None) == 4
-    assert lib.ds_router_topk_h(h, FAKE, 1, 4, None, FAKE, FAKE, 1 << 20, None, None) == 1
+    assert lib.ds_router_topk_h(None, FAKE, 1, 1, None, FAKE, -1, FAKE, 1 << 20, None, None) == 1
+    assert lib.ds_router_topk_h(h, FAKE, 1, 1, None, FAKE, -1, FAKE, 16, None, None) == 4
+    assert lib.ds_router_topk_h(h, FAKE, 1, 4, None, FAKE, -1, FAKE, 1 << 20, None, None) == 1
     assert lib.ds_router_destroy(h) == 0
     assert lib.ds_router_destroy(None) == 0
 
@@ -183,3 +183,21 @@ def test_wait_budget_arguments(lib):
     assert lib.ds_set_wait_budget(-1) == 1
     assert lib.ds_set_wait_budget(1000) == 0
     assert lib.ds_set_wait_budget(0) == 0          # back to the default
+
+
+def test_batch1_side_sms_rule():
+    # The side-stream share at batch 1: 16 SMs beside Llama-size heads (every position of the
+    # 6-position budget), more beside the short lists of a 262,144-token vocabulary (5% and 10%
+    # of its 2,048 clusters), none of it beyond the largest choice.
+    from dynamic_vocab_draft_gb300.pipeline import SIDE_SMS_CHOICES, side_sms_b1
+    llama_router = 2.0 * (1024 * 4096 + 1024 * 1024)
+    for k in (320, 272, 224, 192, 160):
+        assert side_sms_b1(k * (128256 / 1024) * (2 * 4096 + 8), llama_router, 152) == 16
+    large_router = 2.0 * (1024 * 2560 + 2048 * 1024)
+    row = (262144 / 2048) * (2 * 2560 + 8)
+    assert side_sms_b1(102 * row, large_router, 152) == 40
+    assert side_sms_b1(205 * row, large_router, 152) == 24
+    assert side_sms_b1(410 * row, large_router, 152) == 16
+    assert side_sms_b1(1.0, 1e12, 152) == max(SIDE_SMS_CHOICES)
+    # a router with nothing to read never needs more than the smallest share
+    assert side_sms_b1(1e9, 0.0, 152) == 16

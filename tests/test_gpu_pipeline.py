@@ -151,6 +151,37 @@ def test_chain_b1_list_table_and_copied_list_agree(pkg, name, T):
             assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("name", ["llama_b1", "large_b1_f5"])
+def test_chain_b1_side_sms_agree(pkg, name):
+    # Batch 1 with the heads leaving 16, 40 or the modelled number of SMs to the routers beside
+    # them (and the routers sized for them): the same lists, logits, draws and verification bit
+    # for bit (per-row GEMV and top-k do not depend on the grid); the heads' row statistics fold
+    # a different number of block partials, so they agree to rounding.  The default matches the
+    # oracle.
+    inp = gu.chain_inputs(name)
+    gamma = inp["cfg"].gamma
+    outs = []
+    for side in (None, 16, 40):
+        d = make_chain(pkg, inp, 1.0, side_sms=side)
+        assert d.head_free[-1] == 0 and len(d.head_free) == gamma
+        assert d.router_sms == [-1] + d.head_free[:-1]
+        if side is not None:
+            assert d.head_free[:-1] == [side] * (gamma - 1)
+        d.step()
+        torch.cuda.synchronize()
+        d.check_status()
+        if side is None:
+            compare_chain(inp, d, 1.0, [0])
+        outs.append((d.out.clone(), d.logits.clone(), d.vs_offsets.clone(), d.scores.clone(), d.token_idx.clone(),
+                     d.row_max.clone(), d.row_sumexp.clone()))
+        del d
+    for other in outs[1:]:
+        for a, b in zip(outs[0][:5], other[:5]):
+            assert torch.equal(a, b)
+        assert torch.equal(outs[0][5], other[5])                  # the maximum is exact
+        torch.testing.assert_close(outs[0][6], other[6], rtol=1e-5, atol=0)
+
+
 def _aligned_chain_ref(inp, T, seqs, upto):
     """Target rows that agree with the oracle's draft rows at positions t < upto for the
     sequences `seqs` (z = draft logits on the list, -60 elsewhere), and the oracle's whole step

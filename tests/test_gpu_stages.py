@@ -63,13 +63,16 @@ def test_vocab_index(ds, name):
 
 
 # ---------------------------------------------------------------------------------------
-@pytest.mark.parametrize("name,B", [("tiny", 1), ("small_batched", 5), ("llama_b1", 1),
-                                    ("batched", 32), ("large_b1_f5", 1), ("large_b8_f10", 8),
-                                    ("large_b64_f100", 64), ("large_b64_f100", 2), ("large_b64_f100", 100),
-                                    ("large_b64_f100", 20), ("large_b64_f100", 40)])
-def test_router_topk(ds, name, B):
+@pytest.mark.parametrize("name,B,sms", [("tiny", 1, -1), ("small_batched", 5, -1), ("llama_b1", 1, -1),
+                                        ("batched", 32, -1), ("large_b1_f5", 1, -1), ("large_b8_f10", 8, -1),
+                                        ("large_b64_f100", 64, -1), ("large_b64_f100", 2, -1),
+                                        ("large_b64_f100", 100, -1), ("large_b64_f100", 20, -1),
+                                        ("large_b64_f100", 40, -1), ("llama_b1", 1, 40), ("large_b1_f5", 1, 3),
+                                        ("batched", 32, 16), ("small_batched", 5, 3), ("large_b64_f100", 64, 152)])
+def test_router_topk(ds, name, B, sms):
     # B = 1: CUDA-core GEMV; 2 <= B <= 64: tensor-core layers; B > 64: CUDA-core batched GEMV.
     # B larger than the configuration's batch stacks the hidden states of several positions.
+    # sms: the SMs the launches are sized for (-1: the library's default).
     inp = gu.chain_inputs(name)
     cfg = inp["cfg"]
     H = inp["H"]
@@ -83,7 +86,7 @@ def test_router_topk(ds, name, B):
         k = cfg.budget[pos - 1]
         ids = torch.empty(B, k, dtype=torch.int32, device=gu.dev())
         ds.router_topk(gu.bf16(Hrows), gu.bf16(inp["W1"]), gu.bf16(inp["b1"]), gu.bf16(inp["W2"]),
-                       gu.bf16(inp["b2"]), cfg.act, cfg.budget, pos, scores, ids, ws, st)
+                       gu.bf16(inp["b2"]), cfg.act, cfg.budget, pos, scores, ids, ws, st, sms=sms)
         torch.cuda.synchronize()
         assert_close(scores.cpu().numpy(), scores_ref, f"{name} router scores")
         g = ids.cpu().numpy()

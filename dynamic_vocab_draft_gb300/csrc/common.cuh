@@ -134,14 +134,22 @@ __device__ __forceinline__ float gumbel_from_word(uint32_t x)
     return -0.69314718055994531f * __log2f(neg_log_unit(u));
 }
 
-// Gumbel noise of full-vocabulary token v for draft position `pos`, head row `row`: counter
-// (v >> 2, pos, row, 0), word v & 3.
-__device__ __forceinline__ float gumbel(uint64_t seed, uint32_t v, uint32_t pos, uint32_t row)
+// The Philox block of shortlist entries 4q .. 4q+3 (j >> 2 = q; entry j's index in its list) for
+// draft position `pos`, head row `row`: counter (q, pos, row, 0), key = the seed's halves.
+__device__ __forceinline__ uint4 gumbel_block(uint64_t seed, uint32_t q, uint32_t pos, uint32_t row)
 {
-    const uint4 w = philox4x32_10(make_uint4(v >> 2, pos, row, 0u), uint32_t(seed),
-                                  uint32_t(seed >> 32));
-    const uint32_t x = (v & 3u) == 0 ? w.x : (v & 3u) == 1 ? w.y : (v & 3u) == 2 ? w.z : w.w;
-    return gumbel_from_word(x);
+    return philox4x32_10(make_uint4(q, pos, row, 0u), uint32_t(seed), uint32_t(seed >> 32));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &w, uint32_t i)
+{
+    return i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
+}
+
+// Gumbel noise of shortlist entry j: word j & 3 of its block.
+__device__ __forceinline__ float gumbel(uint64_t seed, uint32_t j, uint32_t pos, uint32_t row)
+{
+    return gumbel_from_word(word_of(gumbel_block(seed, j >> 2, pos, row), j & 3u));
 }
 
 // ---------------------------------------------------------------------------------------

@@ -156,7 +156,7 @@ head_gemv_kernel(HeadArgs a, Stat *__restrict__ partials, unsigned *__restrict__
         const int my_j = jb + lane * stride;
         const bool my_ok = my_j < n && my_v >= 0 && my_v < a.V;
         float my_gum = 0.f, my_acc = 0.f;
-        if (a.T > 0.f && my_ok) my_gum = gumbel(a.seed, uint32_t(my_v), uint32_t(a.pos), uint32_t(b));
+        if (a.T > 0.f && my_ok) my_gum = gumbel(a.seed, uint32_t(my_j), uint32_t(a.pos), uint32_t(b));
         const int nrows = min(32, (n - jb + stride - 1) / stride);
         // ids of the next batch, one batch ahead
         const int nj = my_j + 32 * stride;
@@ -301,8 +301,11 @@ head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *_
     const int32_t *ids = a.vs_ids + off;
     Stat st = stat_empty();
     for (int ch = blockIdx.x; ch < nch; ch += gridDim.x) {
-        const int j0 = ch * kRsChunk + threadIdx.x * kRsPer;
-        // the independent noise computations of a thread's elements overlap
+        const int j0 = ch * kRsChunk + threadIdx.x * kRsPer;   // a multiple of 4
+        // the thread's four entries share one Philox block
+        static_assert(kRsPer == 4 && kRsChunk % 4 == 0, "one noise block per thread and chunk");
+        uint4 wq = make_uint4(0u, 0u, 0u, 0u);
+        if (a.T > 0.f && j0 < n) wq = gumbel_block(a.seed, uint32_t(j0) >> 2, uint32_t(a.pos), uint32_t(r));
 #pragma unroll
         for (int e = 0; e < kRsPer; ++e) {
             const int j = j0 + e;
@@ -310,7 +313,7 @@ head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *_
                 const float lj = l[j];
                 const int v = ids[j];
                 const float x = lj * a.inv_te;
-                const float key = a.T > 0.f ? x + gumbel(a.seed, uint32_t(v), uint32_t(a.pos), uint32_t(r)) : lj;
+                const float key = a.T > 0.f ? x + gumbel_from_word(word_of(wq, uint32_t(e))) : lj;
                 stat_add(st, x, key, v, j);
             }
         }

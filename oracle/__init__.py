@@ -104,8 +104,9 @@ def philox4x32_10(ctr, key) -> np.ndarray:
     return out
 
 
-def gumbel_uniform(seed: int, v: int, pos: int, row: int) -> float:
-    return float(lib().orc_gumbel_uniform(seed, v, pos, row))
+def gumbel_uniform(seed: int, j: int, pos: int, row: int) -> float:
+    """The draft draw's uniform for entry j of a shortlist (its index in list order)."""
+    return float(lib().orc_gumbel_uniform(seed, j, pos, row))
 
 
 _ACT = {"relu": 0, "gelu": 1}

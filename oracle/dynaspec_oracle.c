@@ -100,18 +100,19 @@ void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint3
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* The drafter's Gumbel uniform for full-vocabulary token v at draft position pos, head row
- * `row` (the pages name no generator; reading): counter (v >> 2, pos, row, 0), key = the
- * two 32-bit halves of `seed`, word v & 3, mapped to (2*(w >> 9) + 1) * 2^-24, which lies
- * strictly inside (0, 1) and is exact in fp32.  Indexing by the full-vocabulary id makes the
- * draw independent of the shortlist's order. */
-double orc_gumbel_uniform(uint64_t seed, int64_t v, int pos, int row)
+/* The drafter's Gumbel uniform for entry j of the shortlist (its index in the list's order:
+ * selected clusters ascending, each cluster's tokens in CSR order) at draft position pos, head
+ * row `row` (the pages name no generator; reading): counter (j >> 2, pos, row, 0), key = the
+ * two 32-bit halves of `seed`, word j & 3, mapped to (2*(w >> 9) + 1) * 2^-24, which lies
+ * strictly inside (0, 1) and is exact in fp32.  Four consecutive entries share one Philox
+ * block; the list's order is fixed, so the same list always gets the same draws. */
+double orc_gumbel_uniform(uint64_t seed, int64_t j, int pos, int row)
 {
-    uint32_t ctr[4] = {(uint32_t)((uint64_t)v >> 2), (uint32_t)pos, (uint32_t)row, 0u};
+    uint32_t ctr[4] = {(uint32_t)((uint64_t)j >> 2), (uint32_t)pos, (uint32_t)row, 0u};
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t w[4];
     orc_philox4x32_10(ctr, key, w);
-    uint32_t x = w[v & 3];
+    uint32_t x = w[j & 3];
     return (2.0 * (double)(x >> 9) + 1.0) * (1.0 / 16777216.0);
 }
 
@@ -238,7 +239,7 @@ void orc_head(const uint16_t *H, int R, int d, const uint16_t *W, const int32_t 
 /* ------------------------------------------------------------------------------------ */
 /* Draft token from the shortlist logits, mapped back to a full-vocabulary id.            */
 /*   T = 0: x = S[argmax_j l_j], ties to the lower full-vocabulary id.                     */
-/*   T > 0: x = S[argmax_j (l_j / T + g_j)], g_j = -log(-log u(S_j)) (Gumbel-max, an exact */
+/*   T > 0: x = S[argmax_j (l_j / T + g_j)], g_j = -log(-log u(j))  (Gumbel-max, an exact */
 /*          draw from softmax(l / T) over the shortlist), ties to the lower id.            */
 /* Also returns the softmax statistics of l / T_eff (T_eff = T, or 1 when T = 0):          */
 /* m = max_j l_j / T_eff and s = sum_j exp(l_j / T_eff - m).  Returns the token id and     */
@@ -257,7 +258,7 @@ int32_t orc_draft_sample(const double *l, const int32_t *S, int64_t n, double T,
     for (int64_t j = 0; j < n; ++j) {
         double key = l[j];
         if (T > 0.0) {
-            double u = orc_gumbel_uniform(seed, S[j], pos, row);
+            double u = orc_gumbel_uniform(seed, j, pos, row);
             key = l[j] / T - log(-log(u));
         }
         float k32 = f32(key);

@@ -48,7 +48,7 @@ def topk_same_or_excused(gpu_ids, scores, k) -> bool:
 def draft_key(l, S, j, T, seed, pos, row):
     if T == 0.0:
         return float(l[j])
-    return float(l[j]) / T - math.log(-math.log(oracle.gumbel_uniform(seed, int(S[j]), pos, row)))
+    return float(l[j]) / T - math.log(-math.log(oracle.gumbel_uniform(seed, int(j), pos, row)))
 
 
 def token_same_or_excused(gpu_idx, ref_idx, l, S, T, seed, pos, row) -> bool:

@@ -98,7 +98,7 @@ def test_gumbel_uniform_range_and_uniformity():
     hist, _ = np.histogram(us, bins=40, range=(0, 1))
     _, pval = scipy_stats.chisquare(hist)
     assert pval > 1e-4
-    # the token id, position and row all move the draw
+    # the list index, position and row all move the draw
     a = oracle.gumbel_uniform(seed, 11, 3, 1)
     assert a != oracle.gumbel_uniform(seed, 11, 4, 1)
     assert a != oracle.gumbel_uniform(seed, 11, 3, 2)

@@ -299,22 +299,53 @@ head_rowstats_kernel(HeadArgs a, int G, Stat *__restrict__ partials, unsigned *_
     if (int(blockIdx.x) >= nblk) return;                   // uniform over the block
     const float *l = a.logits + int64_t(off) * G + int64_t(gi) * n;
     const int32_t *ids = a.vs_ids + off;
-    Stat st = stat_empty();
-    for (int ch = blockIdx.x; ch < nch; ch += gridDim.x) {
-        const int j0 = ch * kRsChunk + threadIdx.x * kRsPer;   // a multiple of 4
-        // the thread's four entries share one Philox block
-        static_assert(kRsPer == 4 && kRsChunk % 4 == 0, "one noise block per thread and chunk");
-        uint4 wq = make_uint4(0u, 0u, 0u, 0u);
-        if (a.T > 0.f && j0 < n) wq = gumbel_block(a.seed, uint32_t(j0) >> 2, uint32_t(a.pos), uint32_t(r));
+    static_assert(kRsPer % 4 == 0, "whole noise blocks per thread and chunk");
+    // a thread's entries: 16-byte loads of each array where both rows are aligned
+    const bool vec = ((reinterpret_cast<uintptr_t>(l) | reinterpret_cast<uintptr_t>(ids)) & 15u) == 0;
+    auto load = [&](int ch, float (&lv)[kRsPer], int (&iv)[kRsPer]) {
+        const int j0 = ch * kRsChunk + threadIdx.x * kRsPer;
+        if (vec && j0 + kRsPer <= n) {
 #pragma unroll
-        for (int e = 0; e < kRsPer; ++e) {
-            const int j = j0 + e;
-            if (j < n) {
-                const float lj = l[j];
-                const int v = ids[j];
-                const float x = lj * a.inv_te;
-                const float key = a.T > 0.f ? x + gumbel_from_word(word_of(wq, uint32_t(e))) : lj;
-                stat_add(st, x, key, v, j);
+            for (int q = 0; q < kRsPer / 4; ++q) {
+                const float4 f = *reinterpret_cast<const float4 *>(l + j0 + 4 * q);
+                const int4 t = *reinterpret_cast<const int4 *>(ids + j0 + 4 * q);
+                lv[4 * q] = f.x; lv[4 * q + 1] = f.y; lv[4 * q + 2] = f.z; lv[4 * q + 3] = f.w;
+                iv[4 * q] = t.x; iv[4 * q + 1] = t.y; iv[4 * q + 2] = t.z; iv[4 * q + 3] = t.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < kRsPer; ++e) {
+                lv[e] = j0 + e < n ? l[j0 + e] : 0.f;
+                iv[e] = j0 + e < n ? ids[j0 + e] : 0;
+            }
+        }
+    };
+    Stat st = stat_empty();
+    // the next chunk's loads are in flight while this one is folded
+    float lv[kRsPer];
+    int iv[kRsPer];
+    load(blockIdx.x, lv, iv);
+    for (int ch = blockIdx.x; ch < nch; ch += gridDim.x) {
+        float lc[kRsPer];
+        int ic[kRsPer];
+#pragma unroll
+        for (int e = 0; e < kRsPer; ++e) { lc[e] = lv[e]; ic[e] = iv[e]; }
+        if (ch + int(gridDim.x) < nch) load(ch + int(gridDim.x), lv, iv);
+        const int j0 = ch * kRsChunk + threadIdx.x * kRsPer;   // a multiple of 4
+#pragma unroll
+        for (int q = 0; q < kRsPer / 4; ++q) {
+            // four consecutive entries share one Philox block
+            const int jq = j0 + 4 * q;
+            uint4 wq = make_uint4(0u, 0u, 0u, 0u);
+            if (a.T > 0.f && jq < n) wq = gumbel_block(a.seed, uint32_t(jq) >> 2, uint32_t(a.pos), uint32_t(r));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = jq + e;
+                if (j < n) {
+                    const float x = lc[4 * q + e] * a.inv_te;
+                    const float key = a.T > 0.f ? x + gumbel_from_word(word_of(wq, uint32_t(e))) : lc[4 * q + e];
+                    stat_add(st, x, key, ic[4 * q + e], j);
+                }
             }
         }
     }
@@ -467,6 +498,7 @@ extern "C" ds_status ds_gathered_head(const uint16_t *H, int B, int G,
     const int chunks = (V + kRsChunk - 1) / kRsChunk;
     int gx = int((long long)sms * kRsBlocksPerSm / rows);
     gx = gx < 1 ? 1 : gx > chunks ? chunks : gx;
+    if (gx > kGvMaxBlocks) gx = kGvMaxBlocks;             // the partials a row has room for
     head_rowstats_kernel<<<dim3(gx, unsigned(rows)), 256, 0, stream>>>(a, G, partials, counters);
     DS_TRY_LAUNCH();
     return DS_OK;

@@ -582,6 +582,12 @@ constexpr int kWalkThreads = 1024;
 constexpr int kWalkMaxM = 8192;
 constexpr int kWalkMaxCluster = 8;              // CTAs per sequence (portable cluster size)
 constexpr int kWalkU = 4;                       // elements per thread whose loads a pass issues together
+// A list of up to kWalkSlots x (CTAs x kWalkThreads) entries keeps the residual in the cluster's
+// shared memory (two buffers of kWalkSlots x kWalkThreads floats per CTA): entry j lives in CTA
+// (j / kWalkThreads) % CL, slot j / (kWalkThreads * CL), at slot * kWalkThreads + j % kWalkThreads,
+// which is the entry a thread's own passes touch.  Longer lists keep it in global memory.
+constexpr int kWalkSlots = 16;
+constexpr size_t kWalkSmem = size_t(2) * kWalkSlots * kWalkThreads * sizeof(float);
 
 struct WalkState {                 // what the walk leaves for the correction draw
     int mode;                      // 0: decided (greedy); 1: draw from p of `row`; 2: residual
@@ -671,83 +677,65 @@ __device__ __forceinline__ RowStat rowstat_butterfly(const RowStat &mine, int la
     return rowstat_merge(lo_s, hi_s);
 }
 
-// Fixed-order block reduction (warp trees, then warp 0 over the warp results); the result is
-// returned to every thread.
-__device__ RowStat block_rowstat(RowStat st, RowStat *ws)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        st = rowstat_butterfly(st, lane, o);
-    }
-    __syncthreads();
-    if (lane == 0) ws[warp] = st;
-    __syncthreads();
-    if (warp == 0) {
-        RowStat c = lane < nw ? ws[lane] : rowstat_empty();
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            c = rowstat_butterfly(c, lane, o);
-        }
-        if (lane == 0) ws[32] = c;
-    }
-    __syncthreads();
-    return ws[32];
-}
-
-// Cluster-wide reductions.  Every CTA reduces its own threads, publishes the result in its
-// shared memory, and after a cluster barrier each CTA's first warp reads all CTAs' results at
-// once (lane r from rank r) and merges them in a fixed lane tree, so every thread of the
-// cluster holds the same bits and takes the same decisions.  Two
-// publication slots alternate: a CTA rewrites a slot only after the barrier of the next
-// reduction, which every other CTA reaches only once it has finished reading that slot.
+// Cluster-wide reductions, with one CTA barrier and one cluster barrier each.  Every warp
+// reduces its lanes (a butterfly, so all lanes hold the same bits); the CTA's first warp
+// reduces the warp results the same way and publishes the CTA's result in its shared memory;
+// after the cluster barrier every warp of every CTA reads all CTAs' results at once (lane r
+// from rank r) and merges them in the same fixed lane tree, so every thread of the cluster
+// holds the same bits and takes the same decisions.  Two publication slots alternate: a CTA
+// rewrites a slot only after the barrier of the next reduction, which every other CTA reaches
+// only once all its warps have read that slot.  The warp results need one buffer: the first
+// warp reads them before the cluster barrier, and they are rewritten only after it.
 struct ClusterRed {
     RowStat stat[2];
     float sum[2];
-    int k;                                       // reductions so far (per thread, uniform)
+    RowStat wstat[32];                           // this CTA's warp results
+    float wsum[32];
 };
 
-__device__ RowStat cluster_rowstat(RowStat st, RowStat *red, ClusterRed &cr, int &k)
+__device__ __forceinline__ RowStat rowstat_tree(RowStat c, int lane, int width)
 {
-    cg::cluster_group cl = cg::this_cluster();
-    const RowStat mine = block_rowstat(st, red);
-    const int slot = k & 1;
-    if (threadIdx.x == 0) cr.stat[slot] = mine;
-    cl.sync();
-    if (threadIdx.x < 32) {
-        const unsigned lane = threadIdx.x;
-        RowStat m = lane < cl.num_blocks() ? cl.map_shared_rank(&cr, lane)->stat[slot] : rowstat_empty();
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            m = rowstat_butterfly(m, lane, o);
-        }
-        if (lane == 0) red[32] = m;
-    }
-    __syncthreads();
-    const RowStat out = red[32];
-    ++k;
-    return out;
+    for (int o = 1; o < width; o <<= 1) c = rowstat_butterfly(c, lane, o);
+    return c;
 }
 
-__device__ float cluster_sum(float x, float *scratch, ClusterRed &cr, int &k)
+__device__ RowStat cluster_rowstat(RowStat st, ClusterRed &cr, int &k)
 {
     cg::cluster_group cl = cg::this_cluster();
-    const float mine = block_sum(x, scratch);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int slot = k & 1;
-    if (threadIdx.x == 0) cr.sum[slot] = mine;
-    cl.sync();
-    if (threadIdx.x < 32) {
-        const unsigned lane = threadIdx.x;
-        float s = lane < cl.num_blocks() ? cl.map_shared_rank(&cr, lane)->sum[slot] : 0.f;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-        if (lane == 0) scratch[32] = s;
+    st = rowstat_tree(st, lane, 32);
+    if (lane == 0) cr.wstat[warp] = st;
+    __syncthreads();
+    if (warp == 0) {
+        const RowStat c = rowstat_tree(lane < nw ? cr.wstat[lane] : rowstat_empty(), lane, 32);
+        if (lane == 0) cr.stat[slot] = c;
     }
-    __syncthreads();
-    const float out = scratch[32];
-    __syncthreads();
+    cl.sync();
+    const int nb = int(cl.num_blocks());
+    RowStat m = lane < nb ? cl.map_shared_rank(&cr, lane)->stat[slot] : rowstat_empty();
+    m = rowstat_tree(m, lane, 32);
     ++k;
-    return out;
+    return m;
+}
+
+__device__ float cluster_sum(float x, ClusterRed &cr, int &k)
+{
+    cg::cluster_group cl = cg::this_cluster();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int slot = k & 1;
+    x = warp_sum(x);
+    if (lane == 0) cr.wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        const float c = warp_sum(lane < nw ? cr.wsum[lane] : 0.f);
+        if (lane == 0) cr.sum[slot] = c;
+    }
+    cl.sync();
+    const int nb = int(cl.num_blocks());
+    float t = lane < nb ? cl.map_shared_rank(&cr, lane)->sum[slot] : 0.f;
+    ++k;
+    return warp_sum(t);
 }
 
 // One thread-block cluster per sequence (grid = B clusters of CL CTAs): every pass over the
@@ -756,11 +744,10 @@ __global__ void __launch_bounds__(kWalkThreads)
 tree_walk_kernel(TreeArgs a)
 {
     __shared__ int s_cpos[kWalkMaxM];           // cpos of the children's list
-    __shared__ RowStat s_red[33];
-    __shared__ float fscr[33];
+    extern __shared__ float s_rbuf[];            // [2][kWalkSlots * kWalkThreads]: the residual
     __shared__ ClusterRed s_cr;
     __shared__ int s_kids[64];
-    __shared__ int s_nkids, s_accept;
+    __shared__ int s_nkids;
     __shared__ int s_cj[64];                     // per child: list index of its token (-1: none)
     __shared__ float s_cu[64], s_cq[64], s_cqm[64], s_cqs[64];   // its uniform, q(x), q's max / sum-exp
     cg::cluster_group cl = cg::this_cluster();
@@ -815,7 +802,7 @@ tree_walk_kernel(TreeArgs a)
                 }
             }
         }
-        const RowStat row = cluster_rowstat(st, s_red, s_cr, nred);
+        const RowStat row = cluster_rowstat(st, s_cr, nred);
         if (a.T == 0.f) {
             const int am = row.aid;
             int next = -1;
@@ -836,9 +823,24 @@ tree_walk_kernel(TreeArgs a)
         int nb = off[b + 1] - lo;
         if (lo < 0 || nb < 0 || nb > a.V) { if (tid == 0) set_status(a.status, DS_DEV_BAD_INDEX); nb = 0; }
         const int32_t *ids = a.vs_ids + size_t(dep) * a.vs_stride + lo;
-        float *r = a.rbuf + (size_t(b) * 2 + cb) * a.V;
+        // where r lives: the cluster's shared memory when the list fits, else the global buffers
+        const bool in_smem = nb <= kWalkSlots * GT;
+        auto rbase = [&](int buf) -> float * {
+            return in_smem ? s_rbuf + size_t(buf) * kWalkSlots * kWalkThreads : a.rbuf + (size_t(b) * 2 + buf) * a.V;
+        };
+        // this thread's element j = j0 + e * GT (j0 = gt + it * kWalkU * GT) at index ri of a buffer
+        auto rindex = [&](int j, int slot) { return in_smem ? slot * kWalkThreads + tid : j; };
+        // r[j] of any entry, after a cluster barrier that followed its write
+        auto rread = [&](int buf, int j) -> float {
+            if (!in_smem) return __ldcg(rbase(buf) + j);
+            const int blk = j / kWalkThreads;
+            const float *own = cl.map_shared_rank(rbase(buf), blk % CL);
+            return own[(blk / CL) * kWalkThreads + (j - blk * kWalkThreads)];
+        };
+        cb = 0;
+        float *r = rbase(cb);
         float on = 0.f;
-        for (int j0 = gt; j0 < nb; j0 += kWalkU * GT) {
+        for (int j0 = gt, it = 0; j0 < nb; j0 += kWalkU * GT, ++it) {
             int vv[kWalkU];
             float zv[kWalkU];
 #pragma unroll
@@ -850,7 +852,7 @@ tree_walk_kernel(TreeArgs a)
                 const int j = j0 + e * GT;
                 if (j < nb) {
                     const float pj = (vv[e] >= 0 && vv[e] < a.V) ? __expf(zv[e] * a.inv_te - row.m) / row.s : 0.f;
-                    r[j] = pj;
+                    r[rindex(j, it * kWalkU + e)] = pj;
                     on += pj;
                 }
             }
@@ -882,8 +884,15 @@ tree_walk_kernel(TreeArgs a)
                 s_cq[tid] = j >= 0 ? __expf(ql[j] * a.inv_te - qm) / qs : 0.f;
             }
         }
+        // the children's draft rows on this thread's entries, into L2 for the rejection passes
+        if ((tid & 31) == 0)
+            for (int k = 0; k < nk; ++k) {
+                const float *ql = a.q_logits + size_t(dep) * a.q_stride + int64_t(lo) * a.Wd +
+                                  int64_t(s_kids[k] - dep * a.Wd) * nb;
+                for (int j = gt; j < nb; j += GT) prefetch_l2(ql + j);
+            }
         const float O = row.o / row.s;
-        float R = O + cluster_sum(on, fscr, s_cr, nred);   // (its barriers also publish s_c*)
+        float R = O + cluster_sum(on, s_cr, nred);   // (its barriers also publish s_c*)
         int next = -1;
         for (int k = 0; k < nk; ++k) {
             const int n = s_kids[k];
@@ -896,31 +905,30 @@ tree_walk_kernel(TreeArgs a)
             } else {
                 RowStat q = rowstat_empty();
                 for (int j = gt; j < nb; j += GT) rowstat_add(q, ql[j], ql[j] * a.inv_te, false, j);
-                q = cluster_rowstat(q, s_red, s_cr, nred);
+                q = cluster_rowstat(q, s_cr, nred);
                 qm = q.m; qs = q.s;
             }
-            if (tid == 0) {                      // every CTA takes the same test on the same data
+            // every thread takes the same test on the same data
+            int acc = 0;
+            {
                 const int j = s_cj[k];
-                int acc = 0;
                 if (j < 0) {
-                    set_status(a.status, DS_DEV_BAD_INDEX);
+                    if (tid == 0) set_status(a.status, DS_DEV_BAD_INDEX);
                 } else {
                     const float q = a.q_max ? s_cq[k] : __expf(ql[j] * a.inv_te - qm) / qs;
-                    acc = s_cu[k] * q < __ldcg(&r[j]) / R;
+                    acc = s_cu[k] * q < rread(cb, j) / R;
                 }
-                s_accept = acc;
             }
-            __syncthreads();
-            if (s_accept) { next = n; break; }
+            if (acc) { next = n; break; }
             // rejected: r <- max(r - R q, 0) into the other buffer, kept if it has mass
-            float *rn = a.rbuf + (size_t(b) * 2 + (cb ^ 1)) * a.V;
+            float *rn = rbase(cb ^ 1);
             float part = 0.f;
-            for (int j0 = gt; j0 < nb; j0 += kWalkU * GT) {
+            for (int j0 = gt, it = 0; j0 < nb; j0 += kWalkU * GT, ++it) {
                 float rv[kWalkU], lv[kWalkU];
 #pragma unroll
                 for (int e = 0; e < kWalkU; ++e) {
                     const int j = j0 + e * GT;
-                    rv[e] = j < nb ? r[j] : 0.f;
+                    rv[e] = j < nb ? (in_smem ? r[rindex(j, it * kWalkU + e)] : __ldcg(r + j)) : 0.f;
                     lv[e] = j < nb ? ql[j] : 0.f;
                 }
 #pragma unroll
@@ -928,13 +936,24 @@ tree_walk_kernel(TreeArgs a)
                     const int j = j0 + e * GT;
                     if (j < nb) {
                         const float w = fmaxf(rv[e] - R * (__expf(lv[e] * a.inv_te - qm) / qs), 0.f);
-                        rn[j] = w;
+                        rn[rindex(j, it * kWalkU + e)] = w;
                         part += w;
                     }
                 }
             }
-            const float Rn = O + cluster_sum(part, fscr, s_cr, nred);
+            const float Rn = O + cluster_sum(part, s_cr, nred);
             if (Rn > 0.f) { cb ^= 1; r = rn; R = Rn; }
+        }
+        if (next < 0 && in_smem) {
+            // the correction draw reads the residual from the global buffer
+            float *g = a.rbuf + size_t(b) * 2 * a.V;
+            for (int j0 = gt, it = 0; j0 < nb; j0 += kWalkU * GT, ++it)
+#pragma unroll
+                for (int e = 0; e < kWalkU; ++e) {
+                    const int j = j0 + e * GT;
+                    if (j < nb) g[j] = r[rindex(j, it * kWalkU + e)];
+                }
+            cb = 0;
         }
         if (next >= 0) {
             if (lead) a.path[size_t(b) * a.D + A] = next;
@@ -1149,10 +1168,12 @@ extern "C" ds_status ds_verify_tree(const float *p_logits, int B, int D, int Wd,
     // one cluster of CL CTAs per sequence, CL = 8, 4, 2 or 1 so that the clusters fit the GPU
     int CL = kWalkMaxCluster;
     while (CL > 1 && long(B) * CL > sms) CL >>= 1;
+    static std::atomic<unsigned long long> walk_smem_set{0};
+    if (!smem_limit_once(tree_walk_kernel, kWalkSmem, walk_smem_set)) return DS_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(B * CL));
     cfg.blockDim = dim3(kWalkThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = kWalkSmem;             // the residual, when the list fits
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -896,6 +896,36 @@ def test_verify_tree_full_size(ds, T):
             assert (acc_ref >= 1).all() and (acc_ref < D).all()
 
 
+def test_verify_tree_long_lists(ds):
+    # 40 sequences (clusters of two CTAs: the walk keeps a list of up to 32,768 entries in the
+    # cluster's shared memory) with lists around and above that size, so both the shared-memory
+    # residual and the global one are walked, in the same call, against the oracle.
+    cfg = wl.config("tree")
+    B, D, Wd, V, M = 40, 2, 4, cfg.V, cfg.M
+    N = D * Wd
+    csr_off, csr_tok = wl.cluster_partition(cfg, 0)
+    parent = wl.tree_parents(D, Wd)
+    rng = np.random.default_rng(11)
+    budget = (400, 262)
+    ids = [np.sort(np.stack([rng.choice(M, budget[k], replace=False) for _ in range(B)]), axis=1)
+           for k in range(D)]
+    S = [[oracle.shortlist(csr_off, csr_tok, ids[k][b]) for k in range(D)] for b in range(B)]
+    sizes = np.array([[S[b][k].size for k in range(D)] for b in range(B)])
+    assert (sizes > 32768).any() and (sizes <= 32768).any()
+    qfp = [[(rng.standard_normal(S[b][n // Wd].size) * 2.0).astype(np.float32) for n in range(N)]
+           for b in range(B)]
+    didx = np.array([[int(np.argmax(qfp[b][n])) for n in range(N)] for b in range(B)])
+    u_node = rng.random((B, N)).astype(np.float32)
+    u_res = rng.random((B, D + 1)).astype(np.float32)
+    z0 = (rng.standard_normal((B, 1 + N, V)) * 3.0).astype(np.float32)
+    for mode in ("independent", "aligned"):
+        z = z0 if mode == "independent" else _align_targets(z0, parent, S, qfp, D, Wd)
+        acc_ref = _run_tree_verify(ds, V, M, csr_off, csr_tok, parent, D, Wd, ids, S, qfp, didx, z,
+                                   u_node, u_res, 0.8, with_stats=True)
+        if mode == "aligned":
+            assert acc_ref.sum() >= B
+
+
 # ---------------------------------------------------------------------------------------
 # Device-side errors: an id the kernels cannot use sets DS_DEV_BAD_INDEX (0x10) in the status
 # word; nothing faults and the other rows of the call are still computed.

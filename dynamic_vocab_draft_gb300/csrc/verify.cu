@@ -581,7 +581,7 @@ verify_residual_kernel(ChainArgs a)
 constexpr int kWalkThreads = 1024;
 constexpr int kWalkMaxM = 8192;
 constexpr int kWalkMaxCluster = 8;              // CTAs per sequence (portable cluster size)
-constexpr int kWalkU = 4;                       // elements per thread whose loads a pass issues together
+constexpr int kWalkU = 6;                       // elements per thread whose loads a pass issues together
 // A list of up to kWalkSlots x (CTAs x kWalkThreads) entries keeps the residual in the cluster's
 // shared memory (two buffers of kWalkSlots x kWalkThreads floats per CTA): entry j lives in CTA
 // (j / kWalkThreads) % CL, slot j / (kWalkThreads * CL), at slot * kWalkThreads + j % kWalkThreads,

@@ -102,6 +102,7 @@ def compare_chain(inp, d, T, seqs, ref=None, z=None):
     ("batched", None, [0, 13, 31]),
     ("large_b1_f5", None, None), ("large_b1_f100", None, None), ("large_b8_f10", None, [0, 7]),
     ("large_b64_f10", None, [0, 21, 42, 63]),
+    ("large_b8_f40", None, [0, 5]),          # lists of 40% of a 262,144-token vocabulary
 ])
 def test_chain_step_matches_oracle(pkg, name, T, seqs):
     inp = gu.chain_inputs(name)

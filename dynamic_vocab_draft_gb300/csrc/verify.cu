@@ -36,8 +36,9 @@ constexpr int kVThreads = 256;
 constexpr int kVPerBig = 32, kVPerSmall = 8;
 constexpr int kVChunkMin = kVThreads * kVPerSmall;   // sizes the workspace
 constexpr int kMaxGamma = 32;
-// Residual chunks: 2048 elements (8 per thread) under the same rule, else 1024.
-constexpr int kRPerBig = 8, kRPerSmall = 4;
+// Residual chunks: 2048 elements (8 per thread) under the same rule, else 512 (few sequences:
+// more, shorter blocks for the dependent lookups of the draw).
+constexpr int kRPerBig = 8, kRPerSmall = 2;
 constexpr int kRChunkMin = kVThreads * kRPerSmall;
 
 struct PStat { float m, s, amax; int aid; };   // target-row chunk: max, sum-exp, argmax

@@ -896,22 +896,23 @@ def test_verify_tree_full_size(ds, T):
             assert (acc_ref >= 1).all() and (acc_ref < D).all()
 
 
-def test_verify_tree_long_lists(ds):
+@pytest.mark.parametrize("B,budget,cap", [(40, (400, 262), 32768), (80, (200, 131), 16384)])
+def test_verify_tree_long_lists(ds, B, budget, cap):
     # 40 sequences (clusters of two CTAs: the walk keeps a list of up to 32,768 entries in the
-    # cluster's shared memory) with lists around and above that size, so both the shared-memory
-    # residual and the global one are walked, in the same call, against the oracle.
+    # cluster's shared memory) or 80 (one CTA each: 16,384) with lists around and above that
+    # size, so both the shared-memory residual and the global one are walked, in the same call,
+    # against the oracle.
     cfg = wl.config("tree")
-    B, D, Wd, V, M = 40, 2, 4, cfg.V, cfg.M
+    D, Wd, V, M = 2, 4, cfg.V, cfg.M
     N = D * Wd
     csr_off, csr_tok = wl.cluster_partition(cfg, 0)
     parent = wl.tree_parents(D, Wd)
     rng = np.random.default_rng(11)
-    budget = (400, 262)
     ids = [np.sort(np.stack([rng.choice(M, budget[k], replace=False) for _ in range(B)]), axis=1)
            for k in range(D)]
     S = [[oracle.shortlist(csr_off, csr_tok, ids[k][b]) for k in range(D)] for b in range(B)]
     sizes = np.array([[S[b][k].size for k in range(D)] for b in range(B)])
-    assert (sizes > 32768).any() and (sizes <= 32768).any()
+    assert (sizes > cap).any() and (sizes <= cap).any()
     qfp = [[(rng.standard_normal(S[b][n // Wd].size) * 2.0).astype(np.float32) for n in range(N)]
            for b in range(B)]
     didx = np.array([[int(np.argmax(qfp[b][n])) for n in range(N)] for b in range(B)])
